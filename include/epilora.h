@@ -1,0 +1,207 @@
+/*
+ * epilora.h — C ABI of the multi-tenant LoRA linear layer of an LLM decode step
+ * on NVIDIA GB300 (sm_103a).
+ *
+ *   Y[t,:] = bf16( dequant( Q(X)[t,:] . Q(W)^T ) + mask[t] * (x_t . A[idx_t]^T) . B[idx_t]^T )
+ *
+ * The operation is the one defined on the EpiLoRA page ("Fusing Many LoRA
+ * Adapters into Low-Precision GEMMs for Serving and RL"):
+ *   - §Background and motivation › The cost of the separate adapter path:
+ *     shrink h = x A^T, expand h B^T added to the projection's output;
+ *   - §Design › Multi-adapter kernels › K1 and K2: per-token activation
+ *     quantization for the low-precision base GEMM, h from the bf16
+ *     activations, the GEMM epilogue applies the scales then adds h B^T;
+ *   - §Design › Multi-adapter kernels › The decode path: the shrink is
+ *     launched first, the GEMM as its programmatic dependent, waiting for h
+ *     only before its epilogue;
+ * and on the PreFT page ("PreFT: Prefill-only finetuning for efficient
+ * inference", Core claim): the adapter applies to prefill tokens only, which
+ * is the per-token mask.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every data pointer is a DEVICE pointer (cudaMalloc'd or equivalent) owned
+ *    by the caller. The library allocates nothing and keeps no state between
+ *    calls besides cached kernel attributes and the driver entry point used
+ *    to encode TMA descriptors.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call
+ *    only enqueues work; it never synchronizes.
+ *  - Layouts are row-major with the innermost dimension contiguous:
+ *      X   bf16  [M, ldx]     (K used)            activations
+ *      Xq  FP8:  uint8 [M, K] E4M3 codes;  NVFP4: uint8 [M, K/2] packed E2M1
+ *          (element 2i in the low nibble of byte i)
+ *      x_scale        fp32 [M]                     FP8 per-token scale
+ *      x_block_scale  uint8 [M, K/16] E4M3         NVFP4 per-16-block scale
+ *      x_global_scale fp32 scalar (device)         NVFP4 encode multiplier g_x
+ *      Wq  FP8: uint8 [N, K];  NVFP4: uint8 [N, K/2]
+ *      w_scale        fp32 [N]                     FP8 per-output-channel scale
+ *      w_block_scale  uint8 [N, K/16];  w_global_scale fp32 scalar (device)
+ *      A   bf16 [L, r, K]   (h = x A_l^T)
+ *      B   bf16 [L, N, r]   (delta = h B_l^T)
+ *      idx int32 [M]   adapter slot of each token; idx < 0 = no adapter
+ *      mask uint8 [M]  0 = adapter skipped for this token; NULL = all ones
+ *      S   fp32 [M, r]  shrink output (workspace)
+ *      Y   bf16 [M, ldy] (N used)
+ *  - Constraints (checked on the host before any launch; violation returns
+ *    EPILORA_ERR_INVALID_ARG and enqueues nothing): M >= 0 (M == 0 is a
+ *    no-op), K % 32 == 0 and K >= 32, N % 16 == 0 and N >= 16,
+ *    r in {16, 32, 64, 128}, L >= 1, ldx >= K and ldx % 8 == 0,
+ *    for NVFP4 GEMMs K % 256 == 0 (the block-scale rows must be 16-byte
+ *    multiples for the tensor-memory-accelerator copies),
+ *    ldy >= N and ldy % 8 == 0, every data pointer 16-byte aligned, the
+ *    NVFP4 global scales non-NULL.
+ *  - Device-detected conditions are written to the optional `status_dev`
+ *    (int32 on the device, caller-owned; the first error wins through an
+ *    atomic compare-and-swap of 0): an adapter index idx >= L makes that
+ *    token "no adapter" and records EPILORA_ERR_INVALID_ARG; a non-positive
+ *    or non-finite NVFP4 global scale records EPILORA_ERR_INVALID_ARG; a
+ *    bounded wait inside a kernel that ran out records EPILORA_ERR_TIMEOUT
+ *    (the kernel then releases its resources and returns; its outputs are
+ *    undefined). Kernels never trap.
+ *  - Results are deterministic: every reduction is summed in a fixed order
+ *    (no floating-point atomics), so the same inputs at the same M give
+ *    bitwise-identical outputs.
+ *  - Errors from the CUDA runtime at launch are returned as EPILORA_ERR_CUDA.
+ */
+#ifndef EPILORA_H_
+#define EPILORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EPILORA_API __attribute__((visibility("default")))
+#else
+#define EPILORA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EPILORA_OK = 0,
+  EPILORA_ERR_INVALID_ARG = -1,
+  EPILORA_ERR_UNSUPPORTED = -2,
+  EPILORA_ERR_CUDA = -3,
+  EPILORA_ERR_TIMEOUT = -4,
+  EPILORA_ERR_WORKSPACE = -5
+} epilora_status;
+
+typedef enum { EPILORA_FMT_FP8_E4M3 = 0, EPILORA_FMT_NVFP4 = 1 } epilora_format;
+
+/* Smallest per-token amax used by the FP8 quantizer: an all-zero token gets
+ * scale 1e-12f / 448 and all-zero codes. */
+#define EPILORA_FP8_AMAX_FLOOR 1e-12f
+
+/* Version of this ABI (bumped on any signature change). */
+EPILORA_API int epilora_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+EPILORA_API const char* epilora_status_string(int status);
+
+/*
+ * Per-token activation quantizer (S1 / S1').
+ * Defined by: EpiLoRA page, §Design › Multi-adapter kernels › K1 and K2
+ * (activations are quantized one time per layer, with one scale per token,
+ * for the low-precision base GEMM), and its Introduction / Related work for
+ * the block-scaled 4-bit NVFP4 format.
+ *
+ * FP8:   s_t = fl32(max(amax_t, EPILORA_FP8_AMAX_FLOOR) / 448)  (IEEE division)
+ *        Xq[t,k] = E4M3_rn_satfinite(fl32(X[t,k] / s_t));  x_scale[t] = s_t
+ *        (x_block_scale, x_global_scale ignored; may be NULL)
+ * NVFP4: per 16-element block b of token t, with g = *x_global_scale:
+ *        sb = E4M3_rn_satfinite(fl32(fl32(amax_b / 6) * g));
+ *        sb == 0 -> the block's codes are 0, else
+ *        code = E2M1_rn_satfinite(fl32(X * fl32(g / sb)));
+ *        x_block_scale[t,b] = sb (E4M3 byte)          (x_scale ignored)
+ * Applied to a weight matrix (M := N rows) this also produces the FP8
+ * per-output-channel weight scales and the NVFP4 weight codes.
+ * Codes and scales are bit-exact functions of the inputs.
+ */
+EPILORA_API int epilora_quant_act(int fmt, const void* X, int M, int K, int ldx,
+                      void* Xq, float* x_scale, uint8_t* x_block_scale,
+                      const float* x_global_scale, int* status_dev, void* stream);
+
+/*
+ * NVFP4 encode multiplier of a whole bf16 tensor of n elements:
+ *   *g_out = fl32(448 * 6 / max(amax, EPILORA_FP8_AMAX_FLOOR)).
+ * A load-time (weights) or calibration (activations) helper; the EpiLoRA
+ * page only says NVFP4 has an fp32 global scale. g_out is a device float.
+ */
+EPILORA_API int epilora_nvfp4_global_scale(const void* T, size_t n, float* g_out, void* stream);
+
+/*
+ * Multi-adapter shrink (down-projection) (S2).
+ * Defined by: EpiLoRA page, §Background and motivation › The cost of the
+ * separate adapter path (h = x A^T) and §Design › Multi-adapter kernels ›
+ * K1 and K2 (h from the bf16 activations); mask from the PreFT page.
+ *   S[t, j] = sum_k X[t,k] * A[idx_t, j, k]   (fp32 accumulate, fixed order)
+ * for tokens with idx_t in [0, L) and (mask == NULL or mask[t] != 0);
+ * S[t, :] = 0 for every other token. Launched as an ordinary kernel (it
+ * waits for X); it allows a dependent kernel to launch at once.
+ */
+EPILORA_API int epilora_lora_shrink(const void* X, int M, int K, int ldx,
+                        const void* A, int L, int r,
+                        const int32_t* idx, const uint8_t* mask,
+                        float* S, int* status_dev, void* stream);
+
+/*
+ * Low-precision base GEMM with the multi-adapter LoRA epilogue (S3 + S5, S4).
+ * Defined by: EpiLoRA page, §Design › Multi-adapter kernels › K1 and K2
+ * (the epilogue applies the scales and adds h_l B_l^T for the rows of each
+ * adapter) and › The decode path (launched as the shrink's dependent; waits
+ * for h only before its epilogue).
+ *   FP8:   Y[t,n] = bf16( (sum_k Xq[t,k] Wq[n,k]) * x_scale[t] * w_scale[n] + d[t,n] )
+ *   NVFP4: Y[t,n] = bf16( (sum_k (Xq*sbx)[t,k] (Wq*sbw)[n,k]) / (g_x * g_w) + d[t,n] )
+ *   d[t,n] = sum_j S[t,j] * B[idx_t, n, j] for active tokens (as in the
+ *            shrink), else 0; with S == NULL there is no adapter term.
+ * pdl_dependent = 1 launches the kernel with programmatic stream
+ * serialization: it may start while the previous kernel on the stream (the
+ * shrink) is still running, streams W, and executes the grid-dependency wait
+ * just before reading S. pdl_dependent = 0 is an ordinary launch.
+ * Xq/x_scale/x_block_scale must already be complete when the previous kernel
+ * on the stream started (e.g. written by epilora_quant_act before the
+ * shrink).
+ */
+EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
+                               const void* Xq, const float* x_scale,
+                               const uint8_t* x_block_scale, const float* x_global_scale,
+                               const void* Wq, const float* w_scale,
+                               const uint8_t* w_block_scale, const float* w_global_scale,
+                               const float* S, const void* B, int L, int r,
+                               const int32_t* idx, const uint8_t* mask,
+                               void* Y, int ldy, int pdl_dependent,
+                               int* status_dev, void* stream);
+
+/*
+ * Bytes of device workspace epilora_layer_forward needs for (fmt, M, K, r):
+ * quantized activations, their scales and S, each 256-byte aligned.
+ */
+EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
+
+/*
+ * Fused one-call layer (the decode path of the EpiLoRA page, §Design ›
+ * Multi-adapter kernels › The decode path): enqueues
+ *   epilora_quant_act -> epilora_lora_shrink -> epilora_gemm_lora_epilogue
+ * (the GEMM as the shrink's programmatic dependent) using `workspace`
+ * (>= epilora_workspace_bytes, 256-byte aligned) for Xq, scales and S.
+ * A == NULL or B == NULL computes the base layer only. Graph-capturable: it
+ * makes no allocation and no synchronizing call.
+ */
+EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K,
+                          const void* X, int ldx,
+                          const void* Wq, const float* w_scale,
+                          const uint8_t* w_block_scale, const float* w_global_scale,
+                          const float* x_global_scale,
+                          const void* A, const void* B, int L, int r,
+                          const int32_t* idx, const uint8_t* mask,
+                          void* Y, int ldy,
+                          void* workspace, size_t workspace_bytes,
+                          int* status_dev, void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* EPILORA_H_ */

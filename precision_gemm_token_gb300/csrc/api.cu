@@ -1,0 +1,258 @@
+// C ABI of the multi-tenant LoRA layer: argument validation, workspace layout,
+// TMA descriptor encoding and the fused decode-path launch sequence.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace epi {
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static std::atomic<EncodeTiledFn> cached{nullptr};
+  EncodeTiledFn fn = cached.load(std::memory_order_acquire);
+  if (fn != nullptr) return fn;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || p == nullptr)
+    return nullptr;
+  fn = reinterpret_cast<EncodeTiledFn>(p);
+  cached.store(fn, std::memory_order_release);
+  return fn;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline bool fmt_ok(int fmt) { return fmt == EPILORA_FMT_FP8_E4M3 || fmt == EPILORA_FMT_NVFP4; }
+inline bool rank_ok(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
+inline bool k_ok(int K) { return K >= 32 && K % 32 == 0; }
+inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+bool quant_args_ok(int fmt, const void* X, int M, int K, int ldx, const void* Xq, const float* x_scale,
+                   const uint8_t* x_block_scale, const float* x_global_scale) {
+  if (!fmt_ok(fmt) || M < 0 || !k_ok(K) || ldx < K || ldx % 8 != 0) return false;
+  if (M == 0) return true;
+  if (X == nullptr || Xq == nullptr || !al16(X) || !al16(Xq)) return false;
+  if (fmt == EPILORA_FMT_FP8_E4M3) return x_scale != nullptr && al4(x_scale);
+  return x_block_scale != nullptr && al16(x_block_scale) && x_global_scale != nullptr && al4(x_global_scale);
+}
+
+bool shrink_args_ok(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
+                    const uint8_t* mask, const float* S) {
+  if (M < 0 || !k_ok(K) || ldx < K || ldx % 8 != 0 || L < 1 || !rank_ok(r)) return false;
+  if (M == 0) return true;
+  if (X == nullptr || A == nullptr || idx == nullptr || S == nullptr) return false;
+  if (!al16(X) || !al16(A) || !al16(S) || !al4(idx)) return false;
+  (void)mask;
+  return true;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int gemm_smem_bytes(int stage_bytes, int stages, int red_bytes) {
+  return 1024 + stages * stage_bytes + red_bytes + 4096;
+}
+
+int make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols_bytes, uint64_t pitch_bytes,
+                   uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return EPILORA_ERR_CUDA;
+  if (rows == 0 || cols_bytes == 0 || pitch_bytes % 16 != 0 || !al16(base)) return EPILORA_ERR_INVALID_ARG;
+  std::memset(map, 0, sizeof(*map));
+  cuuint64_t dims[2] = {cols_bytes, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? EPILORA_OK : EPILORA_ERR_CUDA;
+}
+
+static int gemm_validate(int fmt, int M, int N, int K, const void* Xq, const float* x_scale,
+                         const uint8_t* x_block_scale, const float* x_global_scale, const void* Wq,
+                         const float* w_scale, const uint8_t* w_block_scale, const float* w_global_scale,
+                         const float* S, const void* B, int L, int r, const int32_t* idx, const void* Y, int ldy) {
+  if (!fmt_ok(fmt) || M < 0 || N < 16 || N % 16 != 0 || !k_ok(K) || ldy < N || ldy % 8 != 0)
+    return EPILORA_ERR_INVALID_ARG;
+  if (fmt == EPILORA_FMT_NVFP4 && K % 256 != 0) return EPILORA_ERR_UNSUPPORTED;
+  if (M == 0) return EPILORA_OK;
+  if (Xq == nullptr || Wq == nullptr || Y == nullptr || !al16(Xq) || !al16(Wq) || !al16(Y))
+    return EPILORA_ERR_INVALID_ARG;
+  if (fmt == EPILORA_FMT_FP8_E4M3) {
+    if (x_scale == nullptr || w_scale == nullptr || !al4(x_scale) || !al4(w_scale)) return EPILORA_ERR_INVALID_ARG;
+  } else {
+    if (x_block_scale == nullptr || w_block_scale == nullptr || x_global_scale == nullptr ||
+        w_global_scale == nullptr || !al16(x_block_scale) || !al16(w_block_scale) || !al4(x_global_scale) ||
+        !al4(w_global_scale))
+      return EPILORA_ERR_INVALID_ARG;
+  }
+  if (S != nullptr) {
+    if (B == nullptr || idx == nullptr || L < 1 || !rank_ok(r) || !al16(S) || !al16(B) || !al4(idx))
+      return EPILORA_ERR_INVALID_ARG;
+  }
+  return EPILORA_OK;
+}
+
+}  // namespace epi
+
+using namespace epi;
+
+extern "C" {
+
+EPILORA_API int epilora_abi_version(void) { return 1; }
+
+EPILORA_API const char* epilora_status_string(int status) {
+  switch (status) {
+    case EPILORA_OK: return "EPILORA_OK";
+    case EPILORA_ERR_INVALID_ARG: return "EPILORA_ERR_INVALID_ARG";
+    case EPILORA_ERR_UNSUPPORTED: return "EPILORA_ERR_UNSUPPORTED";
+    case EPILORA_ERR_CUDA: return "EPILORA_ERR_CUDA";
+    case EPILORA_ERR_TIMEOUT: return "EPILORA_ERR_TIMEOUT";
+    case EPILORA_ERR_WORKSPACE: return "EPILORA_ERR_WORKSPACE";
+    default: return "EPILORA_UNKNOWN_STATUS";
+  }
+}
+
+EPILORA_API int epilora_quant_act(int fmt, const void* X, int M, int K, int ldx, void* Xq, float* x_scale,
+                                  uint8_t* x_block_scale, const float* x_global_scale, int* status_dev,
+                                  void* stream) {
+  if (!quant_args_ok(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale)) return EPILORA_ERR_INVALID_ARG;
+  return launch_quant(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale, status_dev,
+                      static_cast<cudaStream_t>(stream));
+}
+
+EPILORA_API int epilora_nvfp4_global_scale(const void* T, size_t n, float* g_out, void* stream) {
+  if (T == nullptr || g_out == nullptr || n == 0 || !al16(T) || !al4(g_out)) return EPILORA_ERR_INVALID_ARG;
+  return launch_global_scale(T, n, g_out, static_cast<cudaStream_t>(stream));
+}
+
+EPILORA_API int epilora_lora_shrink(const void* X, int M, int K, int ldx, const void* A, int L, int r,
+                                    const int32_t* idx, const uint8_t* mask, float* S, int* status_dev,
+                                    void* stream) {
+  if (!shrink_args_ok(X, M, K, ldx, A, L, r, idx, mask, S)) return EPILORA_ERR_INVALID_ARG;
+  return launch_shrink(X, M, K, ldx, A, L, r, idx, mask, S, status_dev, static_cast<cudaStream_t>(stream));
+}
+
+EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K, const void* Xq, const float* x_scale,
+                                           const uint8_t* x_block_scale, const float* x_global_scale,
+                                           const void* Wq, const float* w_scale, const uint8_t* w_block_scale,
+                                           const float* w_global_scale, const float* S, const void* B, int L,
+                                           int r, const int32_t* idx, const uint8_t* mask, void* Y, int ldy,
+                                           int pdl_dependent, int* status_dev, void* stream) {
+  int rc = gemm_validate(fmt, M, N, K, Xq, x_scale, x_block_scale, x_global_scale, Wq, w_scale, w_block_scale,
+                         w_global_scale, S, B, L, r, idx, Y, ldy);
+  if (rc != EPILORA_OK || M == 0) return rc;
+  GemmArgs a{};
+  a.fmt = fmt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.Xq = Xq;
+  a.x_scale = x_scale;
+  a.x_block_scale = x_block_scale;
+  a.x_global_scale = x_global_scale;
+  a.Wq = Wq;
+  a.w_scale = w_scale;
+  a.w_block_scale = w_block_scale;
+  a.w_global_scale = w_global_scale;
+  a.S = S;
+  a.B = B;
+  a.L = S != nullptr ? L : 1;
+  a.r = S != nullptr ? r : 16;
+  a.idx = idx;
+  a.mask = mask;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.pdl_dependent = pdl_dependent ? 1 : 0;
+  a.status_dev = status_dev;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return fmt == EPILORA_FMT_FP8_E4M3 ? launch_gemm_fp8(a) : launch_gemm_nvfp4(a);
+}
+
+EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
+  if (!fmt_ok(fmt) || M < 0 || K < 0 || r < 0) return 0;
+  const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
+  size_t bytes = 0;
+  if (fmt == EPILORA_FMT_FP8_E4M3) {
+    bytes += round256(m * k);          // Xq
+    bytes += round256(m * 4);          // x_scale
+  } else {
+    bytes += round256(m * k / 2);      // packed Xq
+    bytes += round256(m * k / 16);     // block scales
+  }
+  bytes += round256(m * static_cast<size_t>(r) * 4);   // S
+  return bytes;
+}
+
+EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* X, int ldx, const void* Wq,
+                                      const float* w_scale, const uint8_t* w_block_scale,
+                                      const float* w_global_scale, const float* x_global_scale, const void* A,
+                                      const void* B, int L, int r, const int32_t* idx, const uint8_t* mask,
+                                      void* Y, int ldy, void* workspace, size_t workspace_bytes, int* status_dev,
+                                      void* stream) {
+  const bool adapters = A != nullptr && B != nullptr;
+  if (!fmt_ok(fmt) || M < 0 || !k_ok(K) || ldx < K || ldx % 8 != 0) return EPILORA_ERR_INVALID_ARG;
+  if (adapters && (L < 1 || !rank_ok(r) || idx == nullptr)) return EPILORA_ERR_INVALID_ARG;
+  if (fmt == EPILORA_FMT_NVFP4 && (x_global_scale == nullptr || K % 256 != 0))
+    return x_global_scale == nullptr ? EPILORA_ERR_INVALID_ARG : EPILORA_ERR_UNSUPPORTED;
+  if (M == 0) return EPILORA_OK;
+  const int rr = adapters ? r : 0;
+  const size_t need = epilora_workspace_bytes(fmt, M, K, rr);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return EPILORA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
+  void* Xq = ws;
+  float* x_scale = nullptr;
+  uint8_t* x_block_scale = nullptr;
+  float* S = nullptr;
+  size_t off;
+  if (fmt == EPILORA_FMT_FP8_E4M3) {
+    off = round256(m * k);
+    x_scale = reinterpret_cast<float*>(ws + off);
+    off += round256(m * 4);
+  } else {
+    off = round256(m * k / 2);
+    x_block_scale = ws + off;
+    off += round256(m * k / 16);
+  }
+  if (adapters) S = reinterpret_cast<float*>(ws + off);
+
+  int rc = gemm_validate(fmt, M, N, K, Xq, x_scale, x_block_scale, x_global_scale, Wq, w_scale, w_block_scale,
+                         w_global_scale, S, B, L, r, idx, Y, ldy);
+  if (rc != EPILORA_OK) return rc;
+  if (adapters && !shrink_args_ok(X, M, K, ldx, A, L, r, idx, mask, S)) return EPILORA_ERR_INVALID_ARG;
+  if (!quant_args_ok(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale)) return EPILORA_ERR_INVALID_ARG;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = launch_quant(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale, status_dev, st);
+  if (rc != EPILORA_OK) return rc;
+  if (adapters) {
+    rc = launch_shrink(X, M, K, ldx, A, L, r, idx, mask, S, status_dev, st);
+    if (rc != EPILORA_OK) return rc;
+  }
+  return epilora_gemm_lora_epilogue(fmt, M, N, K, Xq, x_scale, x_block_scale, x_global_scale, Wq, w_scale,
+                                    w_block_scale, w_global_scale, S, B, L, r, idx, mask, Y, ldy,
+                                    adapters ? 1 : 0, status_dev, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Shared definitions of the CUDA library (not part of the public ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/epilora.h"
+
+namespace epi {
+
+constexpr float kE4M3Max = 448.0f;
+constexpr float kE2M1Max = 6.0f;
+constexpr float kAmaxFloor = EPILORA_FP8_AMAX_FLOOR;
+constexpr int kNvfp4Block = 16;
+// Wall-clock limit of any spin-wait inside a kernel (legitimate waits last
+// microseconds). After it runs out the kernel records EPILORA_ERR_TIMEOUT.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// First error wins (0 = OK).
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
+// host-side launch helpers shared by the translation units
+// ---------------------------------------------------------------------------
+struct GemmArgs {
+  int fmt;
+  int M, N, K;
+  const void* Xq;
+  const float* x_scale;
+  const uint8_t* x_block_scale;
+  const float* x_global_scale;
+  const void* Wq;
+  const float* w_scale;
+  const uint8_t* w_block_scale;
+  const float* w_global_scale;
+  const float* S;
+  const void* B;
+  int L, r;
+  const int32_t* idx;
+  const uint8_t* mask;
+  void* Y;
+  int ldy;
+  int pdl_dependent;
+  int* status_dev;
+  cudaStream_t stream;
+};
+
+int launch_quant(int fmt, const void* X, int M, int K, int ldx, void* Xq, float* x_scale,
+                 uint8_t* x_block_scale, const float* x_global_scale, int* status_dev, cudaStream_t stream);
+int launch_global_scale(const void* T, size_t n, float* g_out, cudaStream_t stream);
+int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
+                  const uint8_t* mask, float* S, int* status_dev, cudaStream_t stream);
+int launch_gemm_fp8(const GemmArgs& a);
+int launch_gemm_nvfp4(const GemmArgs& a);
+
+// Encodes a 2D tiled TMA descriptor for a row-major uint8 matrix
+// [rows, cols_bytes] with row pitch `pitch_bytes`, box [box_rows, box_cols].
+int make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols_bytes, uint64_t pitch_bytes,
+                   uint32_t box_rows, uint32_t box_cols, bool swizzle128);
+
+int num_sms();
+
+}  // namespace epi

@@ -1,0 +1,113 @@
+"""Tensor-level helpers over the C ABI: allocate outputs with torch on the
+inputs' device, call the binding, raise on a non-OK status. No arithmetic of
+the layer happens here; every step runs in libepilora.so's kernels."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _binding as E
+
+
+def _u8(shape, dev):
+    return torch.empty(shape, dtype=torch.uint8, device=dev)
+
+
+@dataclass
+class QuantWeight:
+    fmt: int
+    codes: torch.Tensor                         # uint8 [N, K] (FP8) or [N, K/2] (NVFP4)
+    scale: Optional[torch.Tensor] = None        # fp32 [N] (FP8)
+    block_scale: Optional[torch.Tensor] = None  # uint8 [N, K/16] (NVFP4)
+    global_scale: Optional[torch.Tensor] = None  # fp32 [1] (NVFP4)
+
+    @property
+    def N(self):
+        return self.codes.shape[0]
+
+
+def nvfp4_global_scale(T: torch.Tensor, stream=None) -> torch.Tensor:
+    g = torch.empty(1, dtype=torch.float32, device=T.device)
+    E.check(E.epilora_nvfp4_global_scale(T, T.numel(), g, stream), "epilora_nvfp4_global_scale")
+    return g
+
+
+def quant_act(X: torch.Tensor, fmt: int, global_scale: Optional[torch.Tensor] = None, status=None, stream=None):
+    """X bf16 [M, K] -> (codes, scale or block scale)."""
+    M, K = X.shape
+    dev = X.device
+    if fmt == E.FMT_FP8:
+        q, s = _u8((M, K), dev), torch.empty(M, dtype=torch.float32, device=dev)
+        E.check(E.epilora_quant_act(fmt, X, M, K, X.stride(0), q, s, None, None, status, stream), "quant_act")
+        return q, s
+    q, sb = _u8((M, K // 2), dev), _u8((M, K // 16), dev)
+    E.check(E.epilora_quant_act(fmt, X, M, K, X.stride(0), q, None, sb, global_scale, status, stream), "quant_act")
+    return q, sb
+
+
+def quantize_weight(W: torch.Tensor, fmt: int, stream=None) -> QuantWeight:
+    """Load-time quantization of a bf16 weight [N, K] with the same kernels:
+    FP8 per-output-channel scales, or NVFP4 with g_w from W's amax."""
+    if fmt == E.FMT_FP8:
+        q, s = quant_act(W, fmt, stream=stream)
+        return QuantWeight(fmt, q, scale=s)
+    g = nvfp4_global_scale(W, stream)
+    q, sb = quant_act(W, fmt, global_scale=g, stream=stream)
+    return QuantWeight(fmt, q, block_scale=sb, global_scale=g)
+
+
+def lora_shrink(X, A, idx, mask=None, status=None, stream=None) -> torch.Tensor:
+    M, K = X.shape
+    L, r, _ = A.shape
+    S = torch.empty((M, r), dtype=torch.float32, device=X.device)
+    E.check(E.epilora_lora_shrink(X, M, K, X.stride(0), A, L, r, idx, mask, S, status, stream), "lora_shrink")
+    return S
+
+
+def gemm_lora_epilogue(Xq, x_scale, w: QuantWeight, M, K, S=None, B=None, idx=None, mask=None,
+                       x_global_scale=None, pdl_dependent=False, status=None, stream=None, Y=None):
+    N = w.N
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=w.codes.device)
+    L, r = (B.shape[0], B.shape[2]) if B is not None else (1, 16)
+    if w.fmt == E.FMT_FP8:
+        rc = E.epilora_gemm_lora_epilogue(w.fmt, M, N, K, Xq, x_scale, None, None, w.codes, w.scale, None, None,
+                                          S, B, L, r, idx, mask, Y, Y.stride(0), pdl_dependent, status, stream)
+    else:
+        rc = E.epilora_gemm_lora_epilogue(w.fmt, M, N, K, Xq, None, x_scale, x_global_scale, w.codes, None,
+                                          w.block_scale, w.global_scale, S, B, L, r, idx, mask, Y, Y.stride(0),
+                                          pdl_dependent, status, stream)
+    E.check(rc, "gemm_lora_epilogue")
+    return Y
+
+
+class LayerWorkspace:
+    """Caller-owned workspace for epilora_layer_forward (grown on demand)."""
+
+    def __init__(self, device):
+        self.device = torch.device(device)
+        self.buf = torch.empty(0, dtype=torch.uint8, device=self.device)
+
+    def get(self, fmt, M, K, r) -> torch.Tensor:
+        need = E.epilora_workspace_bytes(fmt, M, K, r)
+        if self.buf.numel() < need:
+            self.buf = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+def layer_forward(X, w: QuantWeight, A=None, B=None, idx=None, mask=None, x_global_scale=None,
+                  workspace: Optional[LayerWorkspace] = None, status=None, stream=None, Y=None):
+    M, K = X.shape
+    N = w.N
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    L, r = (A.shape[0], A.shape[1]) if A is not None else (1, 16)
+    ws = workspace or LayerWorkspace(X.device)
+    buf = ws.get(w.fmt, M, K, r if A is not None else 0)
+    rc = E.epilora_layer_forward(w.fmt, M, N, K, X, X.stride(0), w.codes, w.scale, w.block_scale, w.global_scale,
+                                 x_global_scale, A, B, L, r, idx, mask, Y, Y.stride(0), buf, buf.numel(), status,
+                                 stream)
+    E.check(rc, "layer_forward")
+    return Y

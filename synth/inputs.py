@@ -4,8 +4,9 @@ Value laws (per projection, drawn in fp32 and rounded to bf16 where the
 layer's input is bf16):
 
 * activations X ~ N(0, 1)                      -> bf16 [M, K]
-* raw weights W ~ N(0, 0.02^2)                 -> fp32 [N, K] (quantized later
-  by whichever side consumes them; this module does not quantize)
+* weights W ~ N(0, 0.02^2)                     -> bf16 [N, K], the unquantized
+  checkpoint (quantized at load time by whichever side consumes it; this
+  module does not quantize)
 * adapter down-projections A ~ N(0, 1/K)       -> bf16 [L, r, K]
 * adapter up-projections   B ~ N(0, 0.01^2)    -> bf16 [L, N, r]
 * token -> adapter slot index: uniform, one-per-tenant, or truncated
@@ -47,7 +48,7 @@ B_STD = 0.01
 @dataclass
 class ProjectionInputs:
     X: torch.Tensor          # bf16 [M, K]
-    W: torch.Tensor          # fp32 [N, K] raw weights (not quantized)
+    W: torch.Tensor          # bf16 [N, K] unquantized weights
     A: torch.Tensor          # bf16 [L, r, K]
     B: torch.Tensor          # bf16 [L, N, r]
     idx: torch.Tensor        # int32 [M]; -1 = no adapter
@@ -131,12 +132,13 @@ def make_projection(M: int, K: int, N: int, L: int, r: int, *, seed: int = 0,
         A = rng.standard_normal((L, r, K), dtype=np.float32) * np.float32(1.0 / np.sqrt(K))
         B = rng.standard_normal((L, N, r), dtype=np.float32) * np.float32(b_std)
         t = lambda a: torch.from_numpy(a).to(device)  # noqa: E731
-        Xt, Wt, At, Bt = t(X).to(torch.bfloat16), t(W), t(A).to(torch.bfloat16), t(B).to(torch.bfloat16)
+        Xt, Wt = t(X).to(torch.bfloat16), t(W).to(torch.bfloat16)
+        At, Bt = t(A).to(torch.bfloat16), t(B).to(torch.bfloat16)
     elif gen == "torch":
         g = torch.Generator(device=device)
         g.manual_seed(int(seed) * 7919 + 17)
         Xt = (torch.randn((M, K), generator=g, device=device) * x_std).to(torch.bfloat16)
-        Wt = torch.randn((N, K), generator=g, device=device) * w_std
+        Wt = (torch.randn((N, K), generator=g, device=device) * w_std).to(torch.bfloat16)
         At = (torch.randn((L, r, K), generator=g, device=device) * (1.0 / np.sqrt(K))).to(torch.bfloat16)
         Bt = (torch.randn((L, N, r), generator=g, device=device) * b_std).to(torch.bfloat16)
     else:

@@ -1,0 +1,190 @@
+"""GPU layer (quantizer -> shrink -> tcgen05 GEMM with the LoRA epilogue as
+the shrink's programmatic dependent) vs the oracle, on FP8 and NVFP4 bases.
+
+Shapes span several 128-row weight tiles, every token-tile width (16..256
+columns), ragged token and weight tails, split-K clusters of 1..8 CTAs, and
+the degenerate cases: no adapter, zero B, mask 0, out-of-range index."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import epilora_oracle as O
+from oracle import fpformats as F
+from precision_gemm_token_gb300 import tensors as T
+from synth import make_projection
+
+from .gpu_util import (FP8, NVFP4, assert_y_close, ensure_lib, np32, npu8, same_codes_e2m1_packed,
+                       same_codes_e4m3, status_buf, tight_bound)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def run_case(fmt, M, K, N, L, r, seed=0, idx_mode="uniform", mask_mode="all", n_decode=0, zero_w=False,
+             use_adapter=True):
+    """Run GPU and oracle on the same inputs; returns (Y_gpu np, ref dict, bound, inputs)."""
+    p = make_projection(M, K, N, L, r, seed=seed, idx_mode=idx_mode, mask_mode=mask_mode, n_decode=n_decode)
+    W = torch.zeros_like(p.W) if zero_w else p.W
+    Xg, Wg = p.X.cuda(), W.cuda()
+    w = T.quantize_weight(Wg, fmt)
+    x, Wn = p.X.float().numpy(), W.float().numpy()
+    A, B = p.A.float().numpy(), p.B.float().numpy()
+    idx, mask = p.idx.numpy(), p.mask.numpy()
+    gx = None
+    if fmt == FP8:
+        wq, sw = O.quant_fp8_rows(Wn)
+        assert same_codes_e4m3(npu8(w.codes), wq).all() and (np32(w.scale) == sw).all()
+        ref = O.layer_fp8(x, wq, sw, A, B, idx, mask) if use_adapter else O.layer_fp8(
+            x, wq, sw, A, np.zeros_like(B), idx, mask)
+        xv = F.e4m3_decode(ref["xq"]) * ref["sx"][:, None].astype(np.float64)
+        wv = F.e4m3_decode(wq) * sw[:, None].astype(np.float64)
+    else:
+        gw = O.nvfp4_global_scale(Wn)
+        wq, sbw = O.quant_nvfp4_rows(Wn, gw)
+        assert np32(w.global_scale)[0] == gw
+        assert (npu8(w.block_scale) == sbw).all() and same_codes_e2m1_packed(npu8(w.codes), wq).all()
+        gxv = O.nvfp4_global_scale(x)
+        gx = torch.tensor([gxv], dtype=torch.float32, device="cuda")
+        Bref = B if use_adapter else np.zeros_like(B)
+        ref = O.layer_nvfp4(x, gxv, wq, sbw, gw, A, Bref, idx, mask)
+        xv = O.dequant_nvfp4_rows(ref["xq"], ref["sbx"], gxv)
+        wv = O.dequant_nvfp4_rows(wq, sbw, gw)
+    st = status_buf()
+    if use_adapter:
+        Y = T.layer_forward(Xg, w, p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda(), x_global_scale=gx, status=st)
+    else:
+        Y = T.layer_forward(Xg, w, x_global_scale=gx, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    bound = tight_bound(ref, xv, wv, B if use_adapter else np.zeros_like(B), idx, mask)
+    return np32(Y), ref, bound, (p, w, gx)
+
+
+SHAPES = [
+    # M, K, N, L, r        (token tile / split-K it exercises)
+    (4, 512, 1024, 4, 16),      # the small parity workload: BT 16, 2-CTA cluster split
+    (1, 512, 1024, 1, 64),      # single token
+    (4, 256, 1024, 4, 16),      # one K stage per CTA
+    (16, 1024, 2048, 8, 32),    # 4-CTA clusters
+    (17, 512, 144, 4, 16),      # ragged tokens (BT 32) and a partial 16-row weight tile
+    (31, 2048, 256, 2, 128),    # 8-CTA clusters, rank 128
+    (32, 4096, 512, 32, 64),    # one token per tenant
+    (33, 512, 272, 4, 16),      # BT 64, ragged weight tile
+    (100, 512, 384, 5, 32),     # BT 128, no split
+    (130, 256, 256, 3, 16),     # BT 256
+    (300, 512, 272, 7, 64),     # two 256-token tiles, ragged both ways
+]
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+@pytest.mark.parametrize("M,K,N,L,r", SHAPES)
+def test_layer_matches_oracle(fmt, M, K, N, L, r):
+    if fmt == NVFP4 and K % 256:
+        pytest.skip("NVFP4 GEMM needs K % 256 == 0")
+    y, ref, bound, _ = run_case(fmt, M, K, N, L, r, seed=M * 7 + N)
+    assert_y_close(y, ref, bound, what=(fmt, M, K, N))
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+def test_layer_mask_prefill_chunk(fmt):
+    y, ref, bound, _ = run_case(fmt, 40, 512, 256, 6, 16, seed=5, idx_mode="zipf", mask_mode="prefill_chunk",
+                                n_decode=8)
+    assert_y_close(y, ref, bound)
+
+
+def test_fp8_integer_codes_exact():
+    """Rows whose amax is 448 quantize with scale 1; with small-integer values
+    the codes are those integers, the fp32 accumulation is exact and Y must be
+    the bf16 rounding of the exact integer result."""
+    rng = np.random.default_rng(11)
+    M, K, N = 20, 512, 384
+    x = rng.integers(-2, 3, (M, K)).astype(np.float32)
+    w = rng.integers(-2, 3, (N, K)).astype(np.float32)
+    x[:, 0] = 448.0          # the 448s meet small values only: |Y| < 2^12
+    w[:, 1] = 448.0
+    X = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    W = torch.from_numpy(w).to(torch.bfloat16).cuda()
+    wt = T.quantize_weight(W, FP8)
+    assert (np32(wt.scale) == 1.0).all()
+    Y = T.layer_forward(X, wt)
+    exact = x.astype(np.int64) @ w.astype(np.int64).T
+    want = torch.from_numpy(exact.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    assert (np32(Y) == want).all()
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+def test_no_adapter_cases_are_bit_exact_base(fmt):
+    p = make_projection(24, 512, 512, 4, 16, seed=7)
+    X, W = p.X.cuda(), p.W.cuda()
+    w = T.quantize_weight(W, fmt)
+    gx = T.nvfp4_global_scale(X) if fmt == NVFP4 else None
+    A, B, idx, mask = p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda()
+    base = T.layer_forward(X, w, x_global_scale=gx)
+    for Yc in (T.layer_forward(X, w, A, torch.zeros_like(B), idx, mask, x_global_scale=gx),
+               T.layer_forward(X, w, A, B, idx, torch.zeros_like(mask), x_global_scale=gx),
+               T.layer_forward(X, w, A, B, torch.full_like(idx, -1), mask, x_global_scale=gx)):
+        assert torch.equal(Yc.float(), base.float())
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+def test_permutation_and_determinism(fmt):
+    p = make_projection(29, 1024, 640, 5, 32, seed=8, mask_mode="random")
+    X, W = p.X.cuda(), p.W.cuda()
+    w = T.quantize_weight(W, fmt)
+    gx = T.nvfp4_global_scale(X) if fmt == NVFP4 else None
+    A, B, idx, mask = p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda()
+    Y1 = T.layer_forward(X, w, A, B, idx, mask, x_global_scale=gx)
+    Y2 = T.layer_forward(X, w, A, B, idx, mask, x_global_scale=gx)
+    assert torch.equal(Y1, Y2)
+    perm = torch.randperm(29, generator=torch.Generator().manual_seed(1)).cuda()
+    Yp = T.layer_forward(X[perm].contiguous(), w, A, B, idx[perm].contiguous(), mask[perm].contiguous(),
+                         x_global_scale=gx)
+    assert torch.equal(Yp, Y1[perm])
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+def test_adapter_contribution_with_zero_base(fmt):
+    """All-zero weights: Y is bf16 of the adapter term alone."""
+    y, ref, _, _ = run_case(fmt, 16, 1024, 512, 4, 64, seed=9, zero_w=True)
+    d = ref["delta"]
+    assert np.linalg.norm(y - d) / np.linalg.norm(d) <= 1e-2
+
+
+def test_gemm_with_h_given_matches_fused():
+    """The standalone GEMM (S already in memory, ordinary launch) equals the
+    fused decode path bit for bit."""
+    p = make_projection(8, 1024, 512, 4, 32, seed=10)
+    X, W = p.X.cuda(), p.W.cuda()
+    w = T.quantize_weight(W, FP8)
+    A, B, idx, mask = p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda()
+    Yf = T.layer_forward(X, w, A, B, idx, mask)
+    Xq, sx = T.quant_act(X, FP8)
+    S = T.lora_shrink(X, A, idx, mask)
+    torch.cuda.synchronize()
+    Yg = T.gemm_lora_epilogue(Xq, sx, w, 8, 1024, S=S, B=B, idx=idx, mask=mask, pdl_dependent=False)
+    assert torch.equal(Yf, Yg)
+
+
+def test_out_of_range_index_in_gemm():
+    p = make_projection(6, 512, 256, 3, 16, seed=12)
+    idx = p.idx.clone()
+    idx[2] = 5
+    st = status_buf()
+    X, W = p.X.cuda(), p.W.cuda()
+    w = T.quantize_weight(W, FP8)
+    Y = T.layer_forward(X, w, p.A.cuda(), p.B.cuda(), idx.cuda(), p.mask.cuda(), status=st)
+    base = T.layer_forward(X, w)
+    torch.cuda.synchronize()
+    assert int(st.item()) == -1
+    assert torch.equal(Y[2], base[2])
+
+
+def test_empty_batch_is_a_noop():
+    w = T.quantize_weight(torch.randn(256, 512, device="cuda").to(torch.bfloat16), FP8)
+    X = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
+    Y = T.layer_forward(X, w)
+    assert Y.shape == (0, 256)

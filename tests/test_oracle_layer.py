@@ -169,7 +169,7 @@ def test_nvfp4_base_integer_codes_exact():
 def _small_layer(seed=0, M=6, K=64, N=48, L=3, r=8):
     p = make_projection(M, K, N, L, r, seed=seed)
     x = p.X.float().numpy()
-    w = p.W.numpy()
+    w = p.W.float().numpy()
     wq, sw = O.quant_fp8_rows(w)
     return p, x, wq, sw
 
@@ -239,7 +239,7 @@ def test_layer_bruteforce_loops_fp8():
 
 def test_layer_nvfp4_matches_dequantized_product():
     p = make_projection(4, 64, 32, 2, 4, seed=3)
-    x, w = p.X.float().numpy(), p.W.numpy()
+    x, w = p.X.float().numpy(), p.W.float().numpy()
     gw, gx = O.nvfp4_global_scale(w), O.nvfp4_global_scale(x)
     wq, sbw = O.quant_nvfp4_rows(w, gw)
     A, B = p.A.float().numpy(), p.B.float().numpy()
