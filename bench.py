@@ -1,0 +1,496 @@
+"""Benchmark of the multi-tenant LoRA decode layer on GB300 (one JSON line).
+
+A "step" is one Llama-3.1-8B-shaped decoder layer's four projections (qkv,
+o, gate_up, down), each a full pass of the hot path through the C ABI's fused
+entry (per-token quantizer -> multi-adapter shrink -> tcgen05 GEMM with the
+LoRA epilogue launched as the shrink's programmatic dependent), replayed as
+one CUDA graph. The L2 cache is flushed between steps (a write of twice its
+size) outside the timed events.
+
+Default workload: M = 1 decode token, one tenant with a rank-64 adapter, FP8
+E4M3 weights with per-channel scales and per-token FP8 activations. The
+32-tenant line (M = 32, one distinct rank-64 adapter per token) is measured in
+the same run and reported as tokens/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 8b_m1_fp8|8b_m32_fp8|8b_m1_nvfp4|...]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the layer needs no exchange between GPUs); rank 0 prints the line with the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+# The oracle baseline runs single-threaded so that "cores" is exact.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused FP8/NVFP4+LoRA layer µs @M=1, tokens/s @32 tenants, % HBM roofline"
+PROJ8B = (("qkv", 4096, 6144), ("o", 4096, 4096), ("gate_up", 4096, 28672), ("down", 14336, 4096))
+
+WORKLOADS = {
+    # name: (M, fmt, L, r, idx_mode, description)
+    "8b_m1_fp8": (1, 0, 1, 64, "single",
+                  "Llama-3.1-8B decode layer (qkv 4096->6144, o 4096->4096, gate_up 4096->28672, "
+                  "down 14336->4096), M=1, one tenant rank-64 bf16 adapter, FP8 E4M3 per-channel weights, "
+                  "per-token FP8 activations"),
+    "8b_m32_fp8": (32, 0, 32, 64, "per_token",
+                   "Llama-3.1-8B decode layer, M=32 tokens, 32 tenants each with a distinct rank-64 adapter, FP8"),
+    "8b_m1_nvfp4": (1, 1, 128, 64, "zipf",
+                    "Llama-3.1-8B decode layer, M=1, NVFP4 weights/activations, 128 resident rank-64 adapters"),
+    "8b_m32_nvfp4": (32, 1, 128, 64, "zipf",
+                     "Llama-3.1-8B decode layer, M=32, NVFP4, 128 resident rank-64 adapters, Zipf(1.1) indices"),
+}
+
+
+def csrc_sha256() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "precision_gemm_token_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()
+
+
+def read_profile_traffic(workload: str):
+    """dram bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"gemm_gate_up_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    s = re.search(r"csrc_sha256:\s*([0-9a-f]+)", txt)
+    if not m or not s or s.group(1) != csrc_sha256():
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only: one barrier and one max-reduction)
+# ----------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("EPILORA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def algorithmic_bytes(M, K, N, fmt, r, n_distinct, with_adapter=True):
+    """Bytes a perfect kernel must move for one projection (see the design
+    notes): weight codes + weight scales + bf16 X + bf16 Y + per distinct
+    active adapter its A (r x K) and B slice (N x r) in bf16 + S written and
+    read once (fp32) + quantized activations written and read once."""
+    wbytes = N * K if fmt == 0 else N * K // 2 + N * K // 16
+    wscale = N * 4 if fmt == 0 else 4
+    xq = M * K if fmt == 0 else M * K // 2 + M * K // 16
+    b = wbytes + wscale + M * K * 2 + M * N * 2 + 2 * xq
+    if with_adapter:
+        b += n_distinct * (r * K * 2 + N * r * 2) + 2 * M * r * 4
+    return b
+
+
+def gemm_kernel_bytes(M, K, N, fmt, r, n_distinct):
+    """Algorithmic bytes of one GEMM-with-epilogue launch: W codes and scales,
+    quantized X, S, the tile slices of B of the distinct active adapters, Y."""
+    wbytes = N * K if fmt == 0 else N * K // 2 + N * K // 16
+    wscale = N * 4 if fmt == 0 else 4
+    xq = M * K + M * 4 if fmt == 0 else M * K // 2 + M * K // 16
+    return wbytes + wscale + xq + M * r * 4 + n_distinct * N * r * 2 + M * N * 2
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import precision_gemm_token_gb300 as E
+    from precision_gemm_token_gb300 import tensors as T
+    from synth import make_projection
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        E.build()
+    barrier(world)
+    E.load()
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peaks = json.load(open(pk))
+
+    def make_layer(workload, seed):
+        M, fmt, L, r, idx_mode, _ = WORKLOADS[workload]
+        projs = []
+        for i, (name, K, N) in enumerate(PROJ8B):
+            p = make_projection(M, K, N, L, r, seed=seed + i, idx_mode=idx_mode, device=str(dev))
+            w = T.quantize_weight(p.W, fmt)
+            del p.W
+            gx = T.nvfp4_global_scale(p.X) if fmt == 1 else None
+            ws = T.LayerWorkspace(dev)
+            ws.get(fmt, M, K, r)
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            projs.append(dict(name=name, K=K, N=N, p=p, w=w, gx=gx, ws=ws, Y=Y, st=torch.zeros(1, dtype=torch.int32,
+                                                                                                 device=dev)))
+        torch.cuda.synchronize()
+        return projs
+
+    def layer(projs, stream=None):
+        for q in projs:
+            p = q["p"]
+            T.layer_forward(p.X, q["w"], p.A, p.B, p.idx, p.mask, x_global_scale=q["gx"], workspace=q["ws"],
+                            status=q["st"], stream=stream, Y=q["Y"])
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+
+    def time_graph(projs, steps, warmup, sampler=None):
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            layer(projs, s)           # warm the kernels' attributes before capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            layer(projs, s)
+        for _ in range(warmup):
+            flush.fill_(1)
+            g.replay()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        t_wall = time.perf_counter()
+        for a, b in evs:
+            flush.fill_(1)
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        clocks = sampler.stop() if sampler else None
+        barrier(world)
+        per = [a.elapsed_time(b) for a, b in evs]
+        for q in projs:
+            if int(q["st"].item()) != 0:
+                raise RuntimeError(f"device status {int(q['st'].item())} in {q['name']}")
+        return float(np.mean(per)), float(np.median(per)), t_wall, clocks
+
+    workload = args.workload
+    M, fmt, L, r, idx_mode, desc = WORKLOADS[workload]
+    projs = make_layer(workload, seed=100)
+    sampler = ClockSampler(local)
+    ms_mean, ms_med, t_wall, clocks = time_graph(projs, args.steps, args.warmup, sampler)
+    ms_max = max_over_ranks(ms_mean, world, dev)
+    value_us = ms_max * 1000.0
+
+    # 32-tenant tokens/s (same format)
+    t32 = None
+    if not args.skip_tenants:
+        w32 = "8b_m32_fp8" if fmt == 0 else "8b_m32_nvfp4"
+        projs32 = make_layer(w32, seed=200)
+        ms32, _, _, _ = time_graph(projs32, max(args.steps // 2, 3), args.warmup)
+        ms32 = max_over_ranks(ms32, world, dev)
+        nd32 = WORKLOADS[w32][2] if WORKLOADS[w32][4] == "per_token" else len(set(projs32[0]["p"].idx.tolist()))
+        bytes32 = sum(algorithmic_bytes(32, K, N, fmt, WORKLOADS[w32][3], nd32) for _, K, N in PROJ8B)
+        t32 = {"workload": WORKLOADS[w32][5], "layer_us": ms32 * 1000, "tokens_per_s": world * 32 / (ms32 / 1000),
+               "hbm_gbs": bytes32 / (ms32 / 1000) / 1e9,
+               "hbm_frac_of_measured": bytes32 / (ms32 / 1000) / 1e9 / peaks.get("hbm_gbs", 6800.0)}
+        del projs32
+        torch.cuda.empty_cache()
+
+    # dominant kernel (gate_up GEMM with the LoRA epilogue) timed alone with
+    # its S already in memory, L2 flushed before each launch
+    q = projs[2]
+    p = q["p"]
+    Xq, xs = T.quant_act(p.X, fmt, global_scale=q["gx"])
+    S = T.lora_shrink(p.X, p.A, p.idx, p.mask)
+    torch.cuda.synchronize()
+    kern = lambda: T.gemm_lora_epilogue(Xq, xs, q["w"], M, q["K"], S=S, B=p.B, idx=p.idx, mask=p.mask,  # noqa
+                                        x_global_scale=q["gx"], Y=q["Y"])
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        kern()
+    ke = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in ke:
+        flush.fill_(1)
+        a.record()
+        kern()
+        b.record()
+    torch.cuda.synchronize()
+    k_ms = float(np.mean([a.elapsed_time(b) for a, b in ke]))
+    n_distinct = len(set(int(i) for i in p.idx.tolist() if i >= 0))
+    kbytes = gemm_kernel_bytes(M, q["K"], q["N"], fmt, r, n_distinct)
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    achieved = kbytes / (k_ms / 1000) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": read_profile_traffic(workload),
+                "kernel": f"gemm_lora_kernel gate_up {q['K']}->{q['N']} M={M}", "kernel_us": round(k_ms * 1000, 2),
+                "algorithmic_bytes": kbytes, "peak_source": peak_src}
+
+    layer_bytes = sum(algorithmic_bytes(M, K, N, fmt, r, max(n_distinct, 1)) for _, K, N in PROJ8B)
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if not args.skip_e2e:
+        hx = [torch.empty_like(q["p"].X, device="cpu").pin_memory() for q in projs]
+        for h, q in zip(hx, projs):
+            h.copy_(q["p"].X.cpu())
+        hy = [torch.empty_like(q["Y"], device="cpu").pin_memory() for q in projs]
+        h2d = sum(h.numel() * h.element_size() for h in hx)
+        d2h = sum(h.numel() * h.element_size() for h in hy)
+        st = torch.cuda.current_stream()
+        for _ in range(args.warmup):
+            layer(projs)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for h, q in zip(hx, projs):
+                q["p"].X.copy_(h, non_blocking=True)
+            layer(projs, st)
+            for h, q in zip(hy, projs):
+                h.copy_(q["Y"], non_blocking=True)
+            torch.cuda.synchronize()
+            times.append(time.perf_counter() - t0)
+        e2e_us = max_over_ranks(float(np.mean(times)) * 1e6, world, dev)
+        e2e = {"value": round(e2e_us, 2), "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "how": "eager C-ABI calls per projection from Python (no graph), pinned host X in, Y out"}
+
+    line = {
+        "metric": METRIC, "value": round(value_us, 3), "unit": "us", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3" if fmt == 0 else "nvfp4_e2m1", "data": "synthetic",
+        "config": {"workload": desc, "M": M, "rank": r, "tenants": L if idx_mode != "single" else 1,
+                   "parallelism": f"replicas{world}", "cuda_graph": True,
+                   "l2": "flushed between steps (write of 2x L2 outside the timed events)",
+                   "timed": "CUDA events around each graph replay of the 4 projections"},
+        "tokens_per_s": round(world * M / (ms_max / 1000), 1),
+        "layer_hbm_gbs": round(layer_bytes / (ms_max / 1000) / 1e9, 1),
+        "layer_hbm_frac_of_measured": round(layer_bytes / (ms_max / 1000) / 1e9 / peak, 4),
+        "roofline": roofline,
+        "tenants32": t32,
+        "e2e": e2e,
+        "gpu_launches": args.steps * 3 * len(PROJ8B),
+        "clocks": clocks,
+        "median_ms_per_step": round(ms_med, 5),
+    }
+    if rank == 0 and not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(workload, args.cpu_seconds)
+    return line
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host (cpu baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_prepare(workload, cols_per_proj, seed=100):
+    """Inputs of one layer step restricted to a column sample of every
+    projection (full K and M), with the weights quantized by the oracle."""
+    from oracle import epilora_oracle as O
+    from synth import make_projection
+
+    M, fmt, L, r, idx_mode, _ = WORKLOADS[workload]
+    out = []
+    for i, (name, K, N) in enumerate(PROJ8B):
+        ncol = min(cols_per_proj, N)
+        Ls = L if idx_mode == "per_token" else min(L, 4)
+        p = make_projection(M, K, ncol, Ls, r, seed=seed + i, idx_mode=idx_mode if idx_mode != "zipf" else "uniform")
+        x, Wn = p.X.float().numpy(), p.W.float().numpy()
+        d = dict(name=name, N=N, ncol=ncol, x=x, A=p.A.float().numpy(), B=p.B.float().numpy(), idx=p.idx.numpy(),
+                 mask=p.mask.numpy())
+        if fmt == 0:
+            d["wq"], d["sw"] = O.quant_fp8_rows(Wn)
+        else:
+            d["gw"] = O.nvfp4_global_scale(Wn)
+            d["wq"], d["sbw"] = O.quant_nvfp4_rows(Wn, d["gw"])
+            d["gx"] = O.nvfp4_global_scale(x)
+        out.append(d)
+    return out
+
+
+def oracle_step(workload, sample):
+    """One timed oracle pass over the sample; returns (us per full layer
+    extrapolated by N / sampled columns, detail)."""
+    from oracle import epilora_oracle as O
+
+    fmt = WORKLOADS[workload][1]
+    total, detail = 0.0, []
+    for d in sample:
+        t0 = time.perf_counter()
+        if fmt == 0:
+            O.layer_fp8(d["x"], d["wq"], d["sw"], d["A"], d["B"], d["idx"], d["mask"])
+        else:
+            O.layer_nvfp4(d["x"], d["gx"], d["wq"], d["sbw"], d["gw"], d["A"], d["B"], d["idx"], d["mask"])
+        dt = time.perf_counter() - t0
+        total += dt * d["N"] / d["ncol"]
+        detail.append(f"{d['name']}: {d['ncol']}/{d['N']} cols {dt:.3f}s")
+    return total * 1e6, detail
+
+
+def cpu_baseline(workload, seconds_target=10.0):
+    """The oracle, single-threaded, on a sample sized to ~seconds_target of
+    timed work."""
+    probe_us, _ = oracle_step(workload, oracle_prepare(workload, 128))
+    per_col_us = probe_us / sum(N for _, _, N in PROJ8B)
+    cols = int(min(max(128, seconds_target * 1e6 / max(per_col_us, 1e-3) / 4), 28672))
+    us, detail = oracle_step(workload, oracle_prepare(workload, cols))
+    return {"value": round(us, 1), "unit": "us", "cores": 1, "kind": "oracle",
+            "sample": f"{cols} output columns of each projection at full K and M, extrapolated by N/cols; "
+                      + "; ".join(detail)}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: rank 0 only, on the host cores, each
+    step a column sample of the same workload sized so that the whole run
+    stays within about two minutes."""
+    if rank != 0:
+        return None
+    workload = args.workload
+    M, fmt, L, r, idx_mode, desc = WORKLOADS[workload]
+    probe_us, _ = oracle_step(workload, oracle_prepare(workload, 32))
+    per_col_s = probe_us / 1e6 / sum(N for _, _, N in PROJ8B)
+    budget = 120.0 / (args.steps + args.warmup)
+    cols = int(min(max(16, budget / max(per_col_s, 1e-9) / 4), 4096))
+    sample = oracle_prepare(workload, cols)
+    for _ in range(args.warmup):
+        oracle_step(workload, sample)
+    per = [oracle_step(workload, sample)[0] for _ in range(args.steps)]
+    value = sum(per) / len(per)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "us", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value / 1000, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "M": M, "rank": r, "tenants": L if idx_mode != "single" else 1,
+                   "parallelism": "host oracle, rank 0 only"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": 1, "kind": "oracle",
+                         "sample": f"{cols} output columns per projection per step at full K and M, "
+                                   f"extrapolated by N/cols"},
+        "e2e": {"value": round(value, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="8b_m1_fp8", choices=sorted(WORKLOADS))
+    ap.add_argument("--skip-tenants", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
