@@ -176,16 +176,27 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
 
 /*
  * Bytes of device workspace epilora_layer_forward needs for (fmt, M, K, r):
- * quantized activations, their scales and S, each 256-byte aligned.
+ * a 256-byte block of two uint32 counters, the quantized activations, their
+ * scales and S (r = 0: no adapters), each 256-byte aligned.
  */
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
 
 /*
  * Fused one-call layer (the decode path of the EpiLoRA page, §Design ›
- * Multi-adapter kernels › The decode path): enqueues
- *   epilora_quant_act -> epilora_lora_shrink -> epilora_gemm_lora_epilogue
- * (the GEMM as the shrink's programmatic dependent) using `workspace`
- * (>= epilora_workspace_bytes, 256-byte aligned) for Xq, scales and S.
+ * Multi-adapter kernels › The decode path): enqueues two kernels,
+ *   1. the shrink grid of epilora_lora_shrink plus one quantizer CTA per token
+ *      (the arithmetic of epilora_quant_act), launched as a programmatic
+ *      dependent of the previous kernel on the stream: it waits for that
+ *      kernel's completion before reading anything, and
+ *   2. the GEMM of epilora_gemm_lora_epilogue as its programmatic dependent:
+ *      it streams W immediately, waits (bounded) for the quantizer CTAs'
+ *      completion counter before loading the quantized activations, and for
+ *      the whole shrink grid only before reading S in its epilogue;
+ * using `workspace` (>= epilora_workspace_bytes, 256-byte aligned) for the
+ * counters, Xq, scales and S. The first 256 bytes of the workspace must be
+ * zero before its first use; every completed call leaves them zero again
+ * (after a call that reported EPILORA_ERR_TIMEOUT, re-zero them). Calls that
+ * share a workspace must be ordered on one stream.
  * A == NULL or B == NULL computes the base layer only. Graph-capturable: it
  * makes no allocation and no synchronizing call.
  */

@@ -32,17 +32,21 @@ def _inputs_mtime() -> float:
     return max(os.path.getmtime(f) for f in files if os.path.isfile(f))
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every CUDA translation unit and link libepilora.so; returns its path."""
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _inputs_mtime():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str | None = None) -> str:
+    """Compile every CUDA translation unit and link libepilora.so; returns its
+    path. `extra_flags` (e.g. -D tuning macros) with `out_dir` build a variant
+    of the library elsewhere without touching the in-tree one."""
+    build_dir = out_dir or BUILD_DIR
+    lib_path = os.path.join(build_dir, "libepilora.so")
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _inputs_mtime():
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     common = ARCH_FLAGS + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
-                           "-I", os.path.join(ROOT, "include")]
+                           "-I", os.path.join(ROOT, "include")] + list(extra_flags)
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
@@ -53,13 +57,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc] + ARCH_FLAGS + ["-shared", "-o", tmp] + objs
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

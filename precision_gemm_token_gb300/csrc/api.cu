@@ -33,6 +33,7 @@ inline bool fmt_ok(int fmt) { return fmt == EPILORA_FMT_FP8_E4M3 || fmt == EPILO
 inline bool rank_ok(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
 inline bool k_ok(int K) { return K >= 32 && K % 32 == 0; }
 inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+constexpr size_t kWorkspaceCounterBytes = 256;
 
 bool quant_args_ok(int fmt, const void* X, int M, int K, int ldx, const void* Xq, const float* x_scale,
                    const uint8_t* x_block_scale, const float* x_global_scale) {
@@ -85,6 +86,40 @@ int make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t c
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? EPILORA_OK : EPILORA_ERR_CUDA;
+}
+
+int make_tma_2d_swz(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols_bytes, uint64_t pitch_bytes,
+                    uint32_t box_rows, uint32_t box_cols, int swizzle_span) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return EPILORA_ERR_CUDA;
+  if (rows == 0 || cols_bytes == 0 || pitch_bytes % 16 != 0 || !al16(base) ||
+      box_cols > static_cast<uint32_t>(swizzle_span))
+    return EPILORA_ERR_INVALID_ARG;
+  const CUtensorMapSwizzle swz = swizzle_span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : swizzle_span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : swizzle_span == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
+  std::memset(map, 0, sizeof(*map));
+  cuuint64_t dims[2] = {cols_bytes, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? EPILORA_OK : EPILORA_ERR_CUDA;
+}
+
+int prefer_max_shared(const void* func, int* done_flags) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return EPILORA_ERR_CUDA;
+  if (!done_flags[dev]) {
+    if (cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+        cudaSuccess)
+      return EPILORA_ERR_CUDA;
+    done_flags[dev] = 1;
+  }
+  return EPILORA_OK;
 }
 
 static int gemm_validate(int fmt, int M, int N, int K, const void* Xq, const float* x_scale,
@@ -191,7 +226,8 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K, const v
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   if (!fmt_ok(fmt) || M < 0 || K < 0 || r < 0) return 0;
   const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
-  size_t bytes = 0;
+  if (M == 0) return 0;
+  size_t bytes = kWorkspaceCounterBytes;   // two uint32 counters, zero between calls
   if (fmt == EPILORA_FMT_FP8_E4M3) {
     bytes += round256(m * k);          // Xq
     bytes += round256(m * 4);          // x_scale
@@ -221,17 +257,18 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
     return EPILORA_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
-  void* Xq = ws;
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws);      // [0] rows quantized, [1] GEMM CTAs done
+  size_t off = kWorkspaceCounterBytes;
+  void* Xq = ws + off;
   float* x_scale = nullptr;
   uint8_t* x_block_scale = nullptr;
   float* S = nullptr;
-  size_t off;
   if (fmt == EPILORA_FMT_FP8_E4M3) {
-    off = round256(m * k);
+    off += round256(m * k);
     x_scale = reinterpret_cast<float*>(ws + off);
     off += round256(m * 4);
   } else {
-    off = round256(m * k / 2);
+    off += round256(m * k / 2);
     x_block_scale = ws + off;
     off += round256(m * k / 16);
   }
@@ -243,16 +280,42 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
   if (adapters && !shrink_args_ok(X, M, K, ldx, A, L, r, idx, mask, S)) return EPILORA_ERR_INVALID_ARG;
   if (!quant_args_ok(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale)) return EPILORA_ERR_INVALID_ARG;
 
+  // The shrink grid (plus one quantizer CTA per token) is launched normally;
+  // the GEMM is its programmatic dependent: it streams W at once, loads the
+  // quantized activations after the quantizer CTAs' counter reaches M, and
+  // reads S after the whole shrink grid completed.
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  rc = launch_quant(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale, status_dev, st);
+  rc = launch_shrink_quant(X, M, K, ldx, A, adapters ? L : 1, adapters ? r : 0, idx, mask, S, fmt, Xq, x_scale,
+                           x_block_scale, x_global_scale, &counters[0], status_dev, st);
   if (rc != EPILORA_OK) return rc;
-  if (adapters) {
-    rc = launch_shrink(X, M, K, ldx, A, L, r, idx, mask, S, status_dev, st);
-    if (rc != EPILORA_OK) return rc;
-  }
-  return epilora_gemm_lora_epilogue(fmt, M, N, K, Xq, x_scale, x_block_scale, x_global_scale, Wq, w_scale,
-                                    w_block_scale, w_global_scale, S, B, L, r, idx, mask, Y, ldy,
-                                    adapters ? 1 : 0, status_dev, stream);
+  GemmArgs a{};
+  a.fmt = fmt;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.Xq = Xq;
+  a.x_scale = x_scale;
+  a.x_block_scale = x_block_scale;
+  a.x_global_scale = x_global_scale;
+  a.Wq = Wq;
+  a.w_scale = w_scale;
+  a.w_block_scale = w_block_scale;
+  a.w_global_scale = w_global_scale;
+  a.S = S;
+  a.B = B;
+  a.L = adapters ? L : 1;
+  a.r = adapters ? r : 16;
+  a.idx = idx;
+  a.mask = mask;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.pdl_dependent = 1;
+  a.status_dev = status_dev;
+  a.stream = st;
+  a.x_ready = &counters[0];
+  a.x_ready_target = static_cast<uint32_t>(M);
+  a.done_ctr = &counters[1];
+  return fmt == EPILORA_FMT_FP8_E4M3 ? launch_gemm_fp8(a) : launch_gemm_nvfp4(a);
 }
 
 }  // extern "C"

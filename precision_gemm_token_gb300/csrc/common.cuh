@@ -51,6 +51,11 @@ struct GemmArgs {
   int pdl_dependent;
   int* status_dev;
   cudaStream_t stream;
+  // fused decode path: Xq / scales are produced by quantizer CTAs running
+  // concurrently in the shrink's grid; see launch_shrink_quant
+  const uint32_t* x_ready = nullptr;
+  uint32_t x_ready_target = 0;
+  uint32_t* done_ctr = nullptr;
 };
 
 int launch_quant(int fmt, const void* X, int M, int K, int ldx, void* Xq, float* x_scale,
@@ -58,6 +63,13 @@ int launch_quant(int fmt, const void* X, int M, int K, int ldx, void* Xq, float*
 int launch_global_scale(const void* T, size_t n, float* g_out, cudaStream_t stream);
 int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
                   const uint8_t* mask, float* S, int* status_dev, cudaStream_t stream);
+// Shrink grid with one extra quantizer CTA per token: S as launch_shrink, and
+// Xq / scales as launch_quant; each quantizer CTA increments *x_ready (release)
+// after its row is written. Launched as a programmatic dependent of the
+// previous kernel on the stream, which it waits for before reading anything.
+int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
+                        const uint8_t* mask, float* S, int fmt, void* Xq, float* x_scale, uint8_t* x_block_scale,
+                        const float* x_global_scale, uint32_t* x_ready, int* status_dev, cudaStream_t stream);
 int launch_gemm_fp8(const GemmArgs& a);
 int launch_gemm_nvfp4(const GemmArgs& a);
 
@@ -65,6 +77,15 @@ int launch_gemm_nvfp4(const GemmArgs& a);
 // [rows, cols_bytes] with row pitch `pitch_bytes`, box [box_rows, box_cols].
 int make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols_bytes, uint64_t pitch_bytes,
                    uint32_t box_rows, uint32_t box_cols, bool swizzle128);
+
+// As make_tma_2d_u8 with the box's inner extent swizzled over `swizzle_span`
+// bytes (32, 64 or 128; the inner box extent must not exceed it).
+int make_tma_2d_swz(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols_bytes, uint64_t pitch_bytes,
+                    uint32_t box_rows, uint32_t box_cols, int swizzle_span);
+
+// Once per device: prefer the largest shared-memory carveout for a small
+// kernel, so that the SMs it lands on keep room for the GEMM's CTAs beside it.
+int prefer_max_shared(const void* func, int* done_flags);
 
 int num_sms();
 

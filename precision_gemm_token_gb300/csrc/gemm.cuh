@@ -4,13 +4,14 @@
 // EpiLoRA, "Fusing Many LoRA Adapters into Low-Precision GEMMs for Serving and
 // RL":
 //  * §Design › Multi-adapter kernels › K1 and K2 — the GEMM's epilogue applies
-//    the weight and activation scales and then adds h_l B_l^T for the rows of
-//    each adapter, reading only the tile's slice of B_l;
+//    the weight and activation scales and then adds h_l B_l^T for each group
+//    of rows that shares an adapter, reading only the tile's slice of B_l;
 //  * › The decode path — the GEMM runs as the shrink's programmatic dependent:
-//    it streams its weights while the shrink runs and waits for h only before
-//    its epilogue; it prefetches B;
+//    it streams its weights while the shrink runs (extra thread blocks of the
+//    shrink quantize the activations) and waits for h only before its
+//    epilogue; it prefetches B;
 //  * › When the overlap hides the adapter — exposure grows when the GEMM has
-//    more CTAs than SMs, so the decode grid is sized to one wave.
+//    more CTAs than SMs, so decode grids are sized to stay resident.
 //
 // GB300 design (not the pages' Triton kernel):
 //  * swap-AB: weight rows are the MMA's M = 128 side (TMEM lanes), tokens the
@@ -18,15 +19,27 @@
 //    tokens still issues full-height MMAs while W streams;
 //  * one elected thread issues tcgen05.mma (kind::f8f6f4 for E4M3, or
 //    kind::mxf4nvf4 block-scaled with UE4M3 scales for NVFP4) on 128-byte
-//    swizzled K-major tiles that TMA writes into a multi-stage ring;
-//    the accumulator lives in TMEM;
+//    swizzled K-major tiles that TMA writes into a multi-stage ring; a stage
+//    holds KA 128-byte K atoms of every row; the accumulator lives in TMEM;
+//  * the producer fills the ring with weight tiles as soon as the CTA starts;
+//    when the activations are quantized by a concurrently running kernel it
+//    waits (bounded) on that kernel's completion counter only before its first
+//    activation load;
+//  * every weight tile starts its K loop at its own offset, so the CTAs
+//    streaming W at the same time do not all read the same column slice;
 //  * few output tiles (decode): the K dimension is split over a thread-block
-//    cluster of KS CTAs; each CTA's fp32 partial tile is reduced through
-//    distributed shared memory in rank order (deterministic, no atomics),
-//    each CTA finishing 128/KS rows;
-//  * epilogue warps prefetch the tile's B_l slices into L2 at kernel start,
-//    read TMEM after the main loop, then execute griddepcontrol.wait (the
-//    shrink's completion) before reading S.
+//    cluster of KS CTAs; each CTA stores its fp32 partial rows straight into
+//    the shared memory of the CTA that owns them (distributed shared memory),
+//    and every owner sums the KS partials in rank order (deterministic, no
+//    atomics), each CTA finishing 128/KS rows;
+//  * decode tiles whose tokens use several adapters stream the B_l slices of
+//    the tile (one 128-byte-swizzled TMA box per adapter) through the same
+//    ring right behind the weights; the epilogue warps consume them group by
+//    group into an fp32 output tile in shared memory, so the up-projection's
+//    bytes keep HBM busy instead of being fetched one token at a time;
+//  * the epilogue warps are idle during the main loop: they prefetch B into
+//    L2 and load their first B row, execute griddepcontrol.wait (the shrink's
+//    completion) and stage S in shared memory before the accumulator is ready.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator
 // and MMA issuer (all 32 lanes re-lay NVFP4 scale factors), warps 2..5 =
@@ -39,14 +52,18 @@ namespace epi {
 
 constexpr int kGemmThreads = 192;
 constexpr int kTileN = 128;          // weight rows per tile (MMA M)
-constexpr int kStageKBytes = 128;    // bytes of K per stage and row (one 128-B swizzle atom)
+constexpr int kAtomBytes = 128;      // bytes of K per 128-B swizzle atom
 constexpr int kMaxRank = 128;
+constexpr int kEpiBarrier = 1;       // named barrier of the 4 epilogue warps
+constexpr int kMaxSplit = 8;         // largest cluster along K
+constexpr int kDecodeBT = 32;        // token tiles up to this width use the decode epilogue
 
 struct GemmParams {
   CUtensorMap tmW;    // uint8 [N, Kbytes], box 128 x 128 B, 128-B swizzle
   CUtensorMap tmX;    // uint8 [M, Kbytes], box BT x 128 B, 128-B swizzle
-  CUtensorMap tmSW;   // NVFP4: uint8 [N, K/16], box 128 x 16 B
-  CUtensorMap tmSX;   // NVFP4: uint8 [M, K/16], box BT x 16 B
+  CUtensorMap tmSW;   // NVFP4: uint8 [N, K/16], box 128 x 16*KA B
+  CUtensorMap tmSX;   // NVFP4: uint8 [M, K/16], box BT x 16*KA B
+  CUtensorMap tmB;    // streamed B: uint8 [L*N, 2r], box (128/KS) rows x min(2r, 128) B, swizzled
   const float* x_scale;
   const float* w_scale;
   const float* x_gs;
@@ -57,72 +74,197 @@ struct GemmParams {
   const uint8_t* mask;
   __nv_bfloat16* Y;
   int* status;
+  // Set when the quantized activations are produced by a kernel that runs
+  // concurrently (the shrink's quantizer CTAs): the GEMM waits until
+  // *x_ready >= x_ready_target before loading them; the last GEMM CTA to
+  // finish (counted in *done_ctr) resets both counters to 0.
+  const uint32_t* x_ready;
+  uint32_t x_ready_target;
+  uint32_t* done_ctr;
   int M, N, K, L, r, ldy;
-  int num_kb;         // stages of K in total
+  int num_kb;         // K stages in total (KA atoms each)
   int ks;             // cluster size along K (1 = no split)
   int stages;         // depth of the smem ring
+  int rotate;         // 1: per-tile rotation of the K loop start
+  int stream_b;       // 1: tiles with >= 2 adapter groups stream B through the ring
+  int b_box_bytes;    // inner box bytes of tmB (32, 64 or 128 = its swizzle span)
+  int b_atoms;        // tmB boxes per group (2 when 2r = 256)
+  int b_group_bytes;  // ring bytes of one group's boxes (1024-byte aligned)
+  int b_groups_per_slot;
 };
 
-template <int FMT, int BT>
+template <int FMT, int BT, int KA>
 struct GemmCfg {
   static constexpr bool kFP4 = (FMT == EPILORA_FMT_NVFP4);
-  static constexpr int kWBytes = kTileN * kStageKBytes;           // 16 KB
-  static constexpr int kXBytes = BT * kStageKBytes;               // multiple of 1 KB
-  static constexpr int kSfAtomsB = (BT + 127) / 128;              // scale atoms per K=64 step for tokens
-  static constexpr int kSfABytes = kFP4 ? 4 * 512 : 0;            // 4 K-steps x 512-B atom
-  static constexpr int kSfBBytes = kFP4 ? 4 * 512 * kSfAtomsB : 0;
-  static constexpr int kSfWRaw = kFP4 ? kTileN * 16 : 0;          // TMA box of W scales
-  static constexpr int kSfXRaw = kFP4 ? BT * 16 : 0;              // TMA box of X scales
-  static constexpr int kStageRaw = kWBytes + kXBytes + kSfABytes + kSfBBytes + kSfWRaw + kSfXRaw;
+  static constexpr bool kDecode = BT <= kDecodeBT;
+  static constexpr int kWAtom = kTileN * kAtomBytes;              // 16 KB
+  static constexpr int kXAtom = BT * kAtomBytes;                  // multiple of 1 KB
+  static constexpr int kWBytes = KA * kWAtom;
+  static constexpr int kXBytes = KA * kXAtom;
+  static constexpr int kKSteps = 4 * KA;                          // MMAs per stage (32 bytes of K each)
+  static constexpr int kSfAtomsB = (BT + 127) / 128;              // scale atoms per K step for tokens
+  static constexpr int kSfABytes = kFP4 ? kKSteps * 512 : 0;      // one 512-B atom per K step
+  static constexpr int kSfBBytes = kFP4 ? kKSteps * 512 * kSfAtomsB : 0;
+  static constexpr int kSfRow = 16 * KA;                          // scale bytes per row and stage
+  static constexpr int kSfWRaw = kFP4 ? kTileN * kSfRow : 0;      // TMA box of W scales
+  static constexpr int kSfXRaw = kFP4 ? BT * kSfRow : 0;          // TMA box of X scales
+  static constexpr int kSfXRawPad = (kSfXRaw + 1023) / 1024 * 1024;
+  static constexpr int kStageRaw = kWBytes + kXBytes + kSfABytes + kSfBBytes + kSfWRaw + kSfXRawPad;
   static constexpr int kStageBytes = (kStageRaw + 1023) / 1024 * 1024;
   static constexpr int kStageTx = kWBytes + kXBytes + kSfWRaw + kSfXRaw;   // bytes TMA delivers per stage
   // TMEM: accumulator columns [0, BT); NVFP4 scale columns after it, two slots.
-  static constexpr int kSfColsA = 16;                             // 4 K-steps x 4 columns
-  static constexpr int kSfColsB = 16 * kSfAtomsB;
+  static constexpr int kSfColsA = 4 * kKSteps;
+  static constexpr int kSfColsB = 4 * kKSteps * kSfAtomsB;
   static constexpr int kSfSlotCols = kSfColsA + kSfColsB;
   static constexpr int kTmemNeed = BT + (kFP4 ? 2 * kSfSlotCols : 0);
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
   static constexpr uint32_t kIdesc = kFP4 ? idesc_mxf4nvf4(kTileN, BT) : idesc_f8f6f4_e4m3(kTileN, BT);
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 256, "token tile");
+  static_assert(KA == 1 || KA == 2 || KA == 4, "atoms per stage");
   static_assert(kTmemNeed <= 512, "TMEM");
 };
 
-// bytes of dynamic shared memory beyond the stage ring
-template <int BT>
-__host__ __device__ constexpr int gemm_misc_bytes() { return 4096; }
+constexpr int kGemmMiscBytes = 4096;
 
+// Split-K reduction buffer: partial rows from every rank of the cluster,
+// [rank][token][row within the owner's slice], fp32.
+__host__ __device__ constexpr int gemm_red_rows(int ks) { return (kTileN + ks - 1) / ks; }
 template <int BT>
-__host__ __device__ constexpr int gemm_red_bytes(int ks) { return ks > 1 ? kTileN * BT * 4 : 0; }
+__host__ __device__ constexpr int gemm_red_bytes(int ks) {
+  return ks > 1 ? ks * BT * gemm_red_rows(ks) * 4 : 0;
+}
+// Decode-tile region: S rows [BT][r] fp32, output tile [BT][128/ks] fp32,
+// token order by adapter group [BT], group starts [BT+1], group adapters [BT],
+// group of each ordered token [BT].
+__host__ __device__ constexpr int gemm_decode_bytes(int BT, int r, int ks) {
+  return BT > kDecodeBT ? 0 : (BT * r * 4 + BT * gemm_red_rows(ks) * 4 + (4 * BT + 4) * 4 + 15) / 16 * 16;
+}
 
-template <int FMT, int BT>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_lora_kernel(const __grid_constant__ GemmParams p) {
-  using C = GemmCfg<FMT, BT>;
+// Optional per-CTA phase timestamps (built only with -DEPILORA_GEMM_TRACE, for
+// tuning): entry, ring primed, first stage landed, last stage landed,
+// accumulator ready, S readable, epilogue done, SM id.
+#ifdef EPILORA_GEMM_TRACE
+constexpr int kTraceCtas = 8192;
+static __device__ unsigned long long g_gemm_trace[kTraceCtas][8];
+#define EPI_TRACE(slot, value)                                                                     \
+  do {                                                                                             \
+    const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);          \
+    if (cta_ < kTraceCtas) g_gemm_trace[cta_][slot] = (value);                                     \
+  } while (0)
+#else
+#define EPI_TRACE(slot, value) \
+  do {                         \
+  } while (0)
+#endif
+
+// Named barrier of the epilogue warps that also ORs a flag over them.
+__device__ __forceinline__ bool epi_bar_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(kEpiBarrier)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ float dot_srow_brow(const float4* srow, const uint32_t (&brow)[kMaxRank / 2], int r,
+                                               bool srow_in_smem) {
+  float d = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kMaxRank / 4; ++c) {
+    if (c < r / 4) {
+      const float4 s4 = srow_in_smem ? srow[c] : __ldcg(srow + c);
+      d = fmaf(s4.x, bf16_lo(brow[2 * c]), d);
+      d = fmaf(s4.y, bf16_hi(brow[2 * c]), d);
+      d = fmaf(s4.z, bf16_lo(brow[2 * c + 1]), d);
+      d = fmaf(s4.w, bf16_hi(brow[2 * c + 1]), d);
+    }
+  }
+  return d;
+}
+
+template <int FMT, int BT, int KA>
+__global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid_constant__ GemmParams p) {
+  using C = GemmCfg<FMT, BT, KA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stages = p.stages;
+  const int ks = p.ks;
   uint8_t* red_buf = smem + static_cast<size_t>(stages) * C::kStageBytes;
-  uint8_t* misc = red_buf + gemm_red_bytes<BT>(p.ks);
+  uint8_t* misc = red_buf + gemm_red_bytes<BT>(ks);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(misc);
   uint64_t* empty_bar = full_bar + stages;
   uint64_t* acc_bar = empty_bar + stages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* ngroups_s = reinterpret_cast<int*>(tmem_slot + 2);
   float* meta_sx = reinterpret_cast<float*>(tmem_slot + 4);
   int* meta_idx = reinterpret_cast<int*>(meta_sx + BT);       // adapter slot, -1 = none
+  // decode region (BT <= kDecodeBT)
+  const int RR = gemm_red_rows(ks);           // rows owned per rank (last rank: fewer)
+  float* s_stage = reinterpret_cast<float*>(misc + kGemmMiscBytes);   // [token][r]
+  float* y_tile = s_stage + BT * p.r;                                 // [token][RR]
+  int* g_order = reinterpret_cast<int*>(y_tile + BT * RR);            // tokens sorted by group
+  int* g_start = g_order + BT;                                        // [group + 1]
+  int* g_adapter = g_start + BT + 1;                                  // adapter of each group
+  int* g_of = g_adapter + BT;                                         // group of g_order[k]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ks = p.ks;
   const int rank = ks > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int t0 = blockIdx.y * BT;
   const int n0 = blockIdx.z * kTileN;
   const int kb_begin = (p.num_kb * rank) / ks;
   const int kb_end = (p.num_kb * (rank + 1)) / ks;
   const int nkb = kb_end - kb_begin;
+  const int tv = min(BT, p.M - t0);           // valid token columns of this tile
+  const int row_lo = ks > 1 ? RR * rank : 0;
+  const int row_hi = ks > 1 ? min(kTileN, RR * (rank + 1)) : kTileN;
+  const int R = row_hi - row_lo;
+  const int et = threadIdx.x - 64;            // epilogue thread 0..127
+  // K-loop rotation of this weight tile (fixed per weight tile and the same
+  // for every token tile: results stay deterministic and independent of the
+  // tokens' positions)
+  const int rot = p.rotate ? static_cast<int>((blockIdx.z * 5u) % static_cast<unsigned>(nkb)) : 0;
+
+  auto stage_kb = [&](int i) {
+    int kb = i + rot;
+    if (kb >= nkb) kb -= nkb;
+    return kb + kb_begin;
+  };
+  // TMA loads of ring slot s for loop iteration i: weights (+ their scales)
+  auto issue_w = [&](int i, int s) {
+    uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
+    const int kb = stage_kb(i);
+    mbar_arrive_expect_tx(&full_bar[s], C::kStageTx);
+#pragma unroll
+    for (int a = 0; a < KA; ++a)
+      tma_load_2d(st + a * C::kWAtom, &p.tmW, &full_bar[s], (kb * KA + a) * kAtomBytes, n0);
+    if (C::kFP4)
+      tma_load_2d(st + C::kWBytes + C::kXBytes + C::kSfABytes + C::kSfBBytes, &p.tmSW, &full_bar[s],
+                  kb * C::kSfRow, n0);
+  };
+  // ... and activations (+ their scales)
+  auto issue_x = [&](int i, int s) {
+    uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
+    const int kb = stage_kb(i);
+#pragma unroll
+    for (int a = 0; a < KA; ++a)
+      tma_load_2d(st + C::kWBytes + a * C::kXAtom, &p.tmX, &full_bar[s], (kb * KA + a) * kAtomBytes, t0);
+    if (C::kFP4)
+      tma_load_2d(st + C::kWBytes + C::kXBytes + C::kSfABytes + C::kSfBBytes + C::kSfWRaw, &p.tmSX, &full_bar[s],
+                  kb * C::kSfRow, t0);
+  };
 
   // ---------------------------------------------------------------- setup
+  const int prologue = nkb < stages ? nkb : stages;
   if (warp == 0 && lane == 0) {
+    EPI_TRACE(0, globaltimer_ns());
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
@@ -130,25 +272,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_lora_kernel(const __grid
     mbar_init(acc_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
-    tma_prefetch_desc(&p.tmW);
-    tma_prefetch_desc(&p.tmX);
-    if (C::kFP4) {
-      tma_prefetch_desc(&p.tmSW);
-      tma_prefetch_desc(&p.tmSX);
+    // the ring starts empty: stream weights into it before anything else
+    for (int i = 0; i < prologue; ++i) issue_w(i, i);
+    if (p.x_ready != nullptr) {
+      // the activations are being quantized right now by the shrink's
+      // quantizer CTAs (all resident: this grid launched after every CTA of
+      // that grid had started): wait for their completion count
+      bool ok = ld_acquire_gpu_u32(p.x_ready) >= p.x_ready_target;
+      if (!ok) {
+        const uint64_t tstart = globaltimer_ns();
+        while (!ok) {
+          __nanosleep(64);
+          ok = ld_acquire_gpu_u32(p.x_ready) >= p.x_ready_target;
+          if (!ok && globaltimer_ns() - tstart > kWaitLimitNs) break;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_status(p.status, EPILORA_ERR_TIMEOUT);
+      }
+      fence_proxy_async_global();   // the TMA reads below see the quantizers' writes
     }
+    // (after a timeout the loads are still issued so that every stage
+    // completes; the abort flag discards the result)
+    for (int i = 0; i < prologue; ++i) issue_x(i, i);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
   if (warp >= 2) {
-    const int et = threadIdx.x - 64;
+    // token metadata (its loads overlap the first weight loads)
     for (int i = et; i < BT; i += 128) {
       const int t = t0 + i;
       float sx = 0.0f;
       int l = -1;
       if (t < p.M) {
-        if (!C::kFP4) sx = p.x_scale[t];
+        if (!C::kFP4 && p.x_ready == nullptr) sx = p.x_scale[t];
         if (p.S != nullptr) {
           const int li = p.idx[t];
           const bool on = li >= 0 && li < p.L && (p.mask == nullptr || p.mask[t] != 0);
@@ -159,39 +319,131 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_lora_kernel(const __grid
       meta_sx[i] = sx;
       meta_idx[i] = l;
     }
+    asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
+    if (C::kDecode) {
+      if (warp == 2) {
+        // adapter groups of the tile (lane t = token t, BT <= 32), numbered in
+        // order of first appearance, and the tokens sorted by group (stable)
+        const unsigned full = 0xffffffffu;
+        const int l = lane < tv ? meta_idx[lane] : -1;
+        const unsigned act = __ballot_sync(full, l >= 0);
+        const unsigned same = __match_any_sync(full, l);       // lanes holding the same adapter
+        const int leader = __ffs(same) - 1;                    // its first token
+        const bool is_leader = l >= 0 && leader == lane;
+        const unsigned leaders = __ballot_sync(full, is_leader);
+        const int gid = __popc(leaders & ((1u << leader) - 1u));
+        const int cnt = is_leader ? __popc(same) : 0;
+        int incl = cnt;                                        // inclusive scan of group sizes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(full, incl, o);
+          if (lane >= o) incl += n;
+        }
+        const int start = __shfl_sync(full, incl - cnt, leader);
+        if (l >= 0) {
+          const int pos = start + __popc(same & ((1u << lane) - 1u));
+          g_order[pos] = lane;
+          g_of[pos] = gid;
+        }
+        if (is_leader) {
+          g_adapter[gid] = l;
+          g_start[gid] = start;
+        }
+        if (lane == 0) {
+          g_start[__popc(leaders)] = __popc(act);
+          *ngroups_s = __popc(leaders);
+        }
+      }
+    } else if (et == 0) {
+      *ngroups_s = 0;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) EPI_TRACE(1, globaltimer_ns());
+  // every CTA of the cluster has started once this phase completes (its wait
+  // comes before the first store into a peer's shared memory)
+  if (ks > 1) cluster_arrive_relaxed();
+  // stream the tile's B slices through the ring (decode tiles, >= 2 groups)
+  const int ngroups = *ngroups_s;
+  const bool sb = C::kDecode && p.stream_b && ngroups >= 2 && p.S != nullptr;
+  const int gps = p.b_groups_per_slot;
+  const int n_bslots = sb ? (ngroups + gps - 1) / gps : 0;    // ring loads carrying B slices
+  const int n_loads = nkb + n_bslots;
+
+  // epilogue state carried from the main-loop phase into the epilogue phase
+  int cached_key = -1;
+  uint32_t brow[kMaxRank / 2];
+
+  auto load_brow = [&](int l, int mm) {
+    const uint4* bsrc =
+        reinterpret_cast<const uint4*>(p.B + (static_cast<size_t>(l) * p.N + n0 + mm) * p.r);
+#pragma unroll
+    for (int c = 0; c < kMaxRank / 8; ++c) {
+      if (c < p.r / 8) {
+        const uint4 v = __ldg(bsrc + c);
+        brow[4 * c + 0] = v.x;
+        brow[4 * c + 1] = v.y;
+        brow[4 * c + 2] = v.z;
+        brow[4 * c + 3] = v.w;
+      }
+    }
+    cached_key = l * kTileN + mm;
+  };
 
   // ---------------------------------------------------------------- roles
   if (warp == 0) {
     // ===== TMA producer =====
-    if (lane == 0) {
-      uint32_t issued_mask = 0, parity_mask = 0;   // per stage: a fill was issued / its phase parity
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % stages;
-        const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
-        if (*abort_flag) break;
-        if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, kWaitLimitNs)) {
-          *abort_flag = 1;
-          record_status(p.status, EPILORA_ERR_TIMEOUT);
-          break;
-        }
-        uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
-        const int kb = kb_begin + i;
-        mbar_arrive_expect_tx(&full_bar[s], C::kStageTx);
-        tma_load_2d(st, &p.tmW, &full_bar[s], kb * kStageKBytes, n0);
-        tma_load_2d(st + C::kWBytes, &p.tmX, &full_bar[s], kb * kStageKBytes, t0);
-        if (C::kFP4) {
-          uint8_t* raw = st + C::kWBytes + C::kXBytes + C::kSfABytes + C::kSfBBytes;
-          tma_load_2d(raw, &p.tmSW, &full_bar[s], kb * 16, n0);
-          tma_load_2d(raw + C::kSfWRaw, &p.tmSX, &full_bar[s], kb * 16, t0);
-        }
-        issued_mask |= 1u << s;
-        parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
+    uint32_t issued_mask = (prologue >= 32) ? 0xffffffffu : ((1u << prologue) - 1u);
+    uint32_t parity_mask = 0;
+    bool stop = false;
+    // one ring load: W/X stage (i < nkb) or the B slice of group i - nkb
+    auto produce = [&](int i) {
+      const int s = i % stages;
+      const uint32_t ph = static_cast<uint32_t>(i / stages) & 1u;
+      if (*abort_flag) {
+        stop = true;
+        return;
       }
+      if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, kWaitLimitNs)) {
+        *abort_flag = 1;
+        record_status(p.status, EPILORA_ERR_TIMEOUT);
+        stop = true;
+        return;
+      }
+      if (i < nkb) {
+        issue_w(i, s);
+        issue_x(i, s);
+      } else {
+        // groups [g0, g1) of this slot: rows [n0 + row_lo, + RR) of each
+        // group's adapter, one box per 128 B of the row
+        uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
+        const int g0 = (i - nkb) * gps;
+        const int g1 = min(ngroups, g0 + gps);
+        mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>((g1 - g0) * RR * p.b_box_bytes * p.b_atoms));
+        for (int g = g0; g < g1; ++g) {
+          const int y = g_adapter[g] * p.N + n0 + row_lo;
+          for (int a = 0; a < p.b_atoms; ++a)
+            tma_load_2d(st + (g - g0) * p.b_group_bytes + a * RR * p.b_box_bytes, &p.tmB, &full_bar[s],
+                        a * p.b_box_bytes, y);
+        }
+      }
+      issued_mask |= 1u << s;
+      parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
+    };
+    if (lane == 0)
+      for (int i = prologue; i < nkb && !stop; ++i) produce(i);
+    __syncwarp();
+    // The B slices are freed by the epilogue warps, which first pass the
+    // cluster barrier: arrive on its second phase before producing them.
+    if (ks > 1) {
+      cluster_wait();
+      cluster_arrive();
+    }
+    if (lane == 0) {
+      for (int i = (prologue > nkb ? prologue : nkb); i < n_loads && !stop; ++i) produce(i);
       if (*abort_flag) {
         // do not leave with copies in flight: wait for every issued fill
         for (int s = 0; s < stages; ++s)
@@ -215,21 +467,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_lora_kernel(const __grid
         }
         break;
       }
+      if (lane == 0 && i == 0) EPI_TRACE(2, globaltimer_ns());
+      if (lane == 0 && i == nkb - 1) EPI_TRACE(3, globaltimer_ns());
       uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
       const uint32_t w_addr = smem_u32(st);
       const uint32_t x_addr = smem_u32(st + C::kWBytes);
+      uint8_t* sfa = st + C::kWBytes + C::kXBytes;
+      uint8_t* sfb = sfa + C::kSfABytes;
       if (C::kFP4) {
-        // Re-lay the canonical [rows][16 scale bytes] TMA boxes into 512-B
-        // atoms per K=64 step: line r0 (16 B) = the 4 scale bytes of rows
-        // r0, r0+32, r0+64, r0+96 (4 bytes each).
-        uint8_t* sfa = st + C::kWBytes + C::kXBytes;
-        uint8_t* sfb = sfa + C::kSfABytes;
+        // Re-lay the canonical [rows][16*KA scale bytes] TMA boxes into one
+        // 512-B atom per K=64 step: line r0 (16 B) = the 4 scale bytes of
+        // rows r0, r0+32, r0+64, r0+96.
         const uint8_t* raw_w = sfb + C::kSfBBytes;
         const uint8_t* raw_x = raw_w + C::kSfWRaw;
-        {
+#pragma unroll
+        for (int a = 0; a < KA; ++a) {
           uint4 v[4];
 #pragma unroll
-          for (int r1 = 0; r1 < 4; ++r1) v[r1] = *reinterpret_cast<const uint4*>(raw_w + (lane + 32 * r1) * 16);
+          for (int r1 = 0; r1 < 4; ++r1)
+            v[r1] = *reinterpret_cast<const uint4*>(raw_w + (lane + 32 * r1) * C::kSfRow + 16 * a);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             uint4 o;
@@ -237,25 +493,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_lora_kernel(const __grid
             o.y = (&v[1].x)[kk];
             o.z = (&v[2].x)[kk];
             o.w = (&v[3].x)[kk];
-            *reinterpret_cast<uint4*>(sfa + kk * 512 + lane * 16) = o;
-          }
-        }
-#pragma unroll
-        for (int a = 0; a < C::kSfAtomsB; ++a) {
-          uint4 v[4];
-#pragma unroll
-          for (int r1 = 0; r1 < 4; ++r1) {
-            const int row = 128 * a + 32 * r1 + lane;
-            v[r1] = row < BT ? *reinterpret_cast<const uint4*>(raw_x + row * 16) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sfa + (a * 4 + kk) * 512 + lane * 16) = o;
           }
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            uint4 o;
-            o.x = (&v[0].x)[kk];
-            o.y = (&v[1].x)[kk];
-            o.z = (&v[2].x)[kk];
-            o.w = (&v[3].x)[kk];
-            *reinterpret_cast<uint4*>(sfb + (kk * C::kSfAtomsB + a) * 512 + lane * 16) = o;
+          for (int b = 0; b < C::kSfAtomsB; ++b) {
+#pragma unroll
+            for (int r1 = 0; r1 < 4; ++r1) {
+              const int row = 128 * b + 32 * r1 + lane;
+              v[r1] = row < BT ? *reinterpret_cast<const uint4*>(raw_x + row * C::kSfRow + 16 * a)
+                               : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              uint4 o;
+              o.x = (&v[0].x)[kk];
+              o.y = (&v[1].x)[kk];
+              o.z = (&v[2].x)[kk];
+              o.w = (&v[3].x)[kk];
+              *reinterpret_cast<uint4*>(sfb + ((a * 4 + kk) * C::kSfAtomsB + b) * 512 + lane * 16) = o;
+            }
           }
         }
         fence_proxy_async_smem();
@@ -265,23 +521,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_lora_kernel(const __grid
         tc_fence_after();
         const uint32_t slot_col = static_cast<uint32_t>(BT + (i & 1) * C::kSfSlotCols);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t adesc = make_smem_desc(w_addr + kk * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bdesc = make_smem_desc(x_addr + kk * 32, 16, 1024, kSwizzle128B);
-          const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
-          if (C::kFP4) {
-            const uint32_t sfa_addr = smem_u32(st + C::kWBytes + C::kXBytes) + kk * 512;
-            const uint32_t sfb_addr = smem_u32(st + C::kWBytes + C::kXBytes + C::kSfABytes) + kk * C::kSfAtomsB * 512;
-            const uint32_t sfa_col = slot_col + kk * 4;
-            const uint32_t sfb_col = slot_col + C::kSfColsA + kk * 4 * C::kSfAtomsB;
-            tc_cp_32x128b_warpx4(tmem_base + sfa_col, make_smem_desc(sfa_addr, 16, 128, kSwizzleNone));
+        for (int a = 0; a < KA; ++a) {
 #pragma unroll
-            for (int a = 0; a < C::kSfAtomsB; ++a)
-              tc_cp_32x128b_warpx4(tmem_base + sfb_col + 4 * a,
-                                   make_smem_desc(sfb_addr + a * 512, 16, 128, kSwizzleNone));
-            mma_mxf4nvf4(tmem_base, adesc, bdesc, C::kIdesc, tmem_base + sfa_col, tmem_base + sfb_col, accum);
-          } else {
-            mma_f8f6f4(tmem_base, adesc, bdesc, C::kIdesc, accum);
+          for (int kk = 0; kk < 4; ++kk) {
+            const int j = a * 4 + kk;                       // K step within the stage
+            const uint64_t adesc = make_smem_desc(w_addr + a * C::kWAtom + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bdesc = make_smem_desc(x_addr + a * C::kXAtom + kk * 32, 16, 1024, kSwizzle128B);
+            const uint32_t accum = (i > 0 || j > 0) ? 1u : 0u;
+            if (C::kFP4) {
+              const uint32_t sfa_addr = smem_u32(sfa) + j * 512;
+              const uint32_t sfb_addr = smem_u32(sfb) + j * C::kSfAtomsB * 512;
+              const uint32_t sfa_col = slot_col + j * 4;
+              const uint32_t sfb_col = slot_col + C::kSfColsA + j * 4 * C::kSfAtomsB;
+              tc_cp_32x128b_warpx4(tmem_base + sfa_col, make_smem_desc(sfa_addr, 16, 128, kSwizzleNone));
+#pragma unroll
+              for (int b = 0; b < C::kSfAtomsB; ++b)
+                tc_cp_32x128b_warpx4(tmem_base + sfb_col + 4 * b,
+                                     make_smem_desc(sfb_addr + b * 512, 16, 128, kSwizzleNone));
+              mma_mxf4nvf4(tmem_base, adesc, bdesc, C::kIdesc, tmem_base + sfa_col, tmem_base + sfb_col, accum);
+            } else {
+              mma_f8f6f4(tmem_base, adesc, bdesc, C::kIdesc, accum);
+            }
           }
         }
         tc_commit(&empty_bar[s]);   // frees the stage once these MMAs have read it
@@ -290,160 +550,289 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_lora_kernel(const __grid
     }
     if (lane == 0) tc_commit(acc_bar);   // accumulator complete (or drained after an abort)
     __syncwarp();
+    if (ks > 1) {
+      cluster_wait();      // first phase (armed after setup)
+      cluster_arrive();    // second phase: nothing of this warp is still to land in a peer
+    }
   } else {
-    // ===== epilogue warps: prefetch B slices, then wait for the accumulator =====
-    const int et = threadIdx.x - 64;   // 0..127
-    const int q = warp & 3;            // TMEM lane quadrant of this warp
-    const int m = q * 32 + lane;       // tile row owned in the unsplit case
-    const int row_lo = (kTileN * rank) / ks, row_hi = (kTileN * (rank + 1)) / ks;
-    if (et == 0 && p.S != nullptr) {
+    // ===== epilogue warps, main-loop phase =====
+    if (p.S != nullptr && !sb) {
+      // L2 prefetch of the tile's B slices, first B row into registers
       const int rows = min(row_hi, p.N - n0) - row_lo;
-      if (rows > 0) {
-        int prev = -1;
-        for (int i = 0; i < BT; ++i) {
-          const int l = meta_idx[i];
-          if (l >= 0 && l != prev) {
-            prefetch_l2_bulk(p.B + (static_cast<size_t>(l) * p.N + n0 + row_lo) * p.r,
-                             static_cast<uint32_t>(rows * p.r * 2));
-            prev = l;
-          }
+      int first_l = -1;
+      int prev = -1;
+      for (int i = 0; i < BT; ++i) {
+        const int l = meta_idx[i];
+        if (l >= 0 && first_l < 0) first_l = l;
+        if (et == 0 && rows > 0 && l >= 0 && l != prev) {
+          prefetch_l2_bulk(p.B + (static_cast<size_t>(l) * p.N + n0 + row_lo) * p.r,
+                           static_cast<uint32_t>(rows * p.r * 2));
+          prev = l;
         }
       }
+      const int mm = ks == 1 ? ((warp & 3) * 32 + lane) : row_lo + (R > 0 ? et % R : 0);
+      if (first_l >= 0 && n0 + mm < p.N && mm < row_hi) load_brow(first_l, mm);
     }
-    bool ok = mbar_wait_bounded(acc_bar, 0, kWaitLimitNs);
+    // The shrink's completion (normally well before the main loop ends): from
+    // here on S is visible. Also orders this grid after the whole primary grid.
+    pdl_wait_primary();
+    if (C::kDecode && p.S != nullptr) {
+      // S rows of this tile's tokens into shared memory
+      const float4* src = reinterpret_cast<const float4*>(p.S + static_cast<size_t>(t0) * p.r);
+      float4* dst = reinterpret_cast<float4*>(s_stage);
+      for (int i = et; i < tv * p.r / 4; i += 128) dst[i] = __ldcg(src + i);
+    }
+    if (!C::kFP4 && p.x_ready != nullptr) {
+      // per-token scales written by the quantizer CTAs before they counted
+      // their rows ready (observe the count with acquire, then read)
+      const uint64_t tstart = globaltimer_ns();
+      while (ld_acquire_gpu_u32(p.x_ready) < p.x_ready_target) {
+        if (globaltimer_ns() - tstart > kWaitLimitNs) {
+          *abort_flag = 1;
+          record_status(p.status, EPILORA_ERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+      for (int i = et; i < BT; i += 128) meta_sx[i] = (t0 + i < p.M) ? __ldcg(p.x_scale + t0 + i) : 0.0f;
+    }
+    asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
+    const bool ok = mbar_wait_bounded(acc_bar, 0, kWaitLimitNs);
+    if (et == 0) EPI_TRACE(4, globaltimer_ns());
     if (!ok) {
       *abort_flag = 1;
       record_status(p.status, EPILORA_ERR_TIMEOUT);
     }
     tc_fence_after();
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    if (ks > 1 && ok) {
-      // stage this CTA's fp32 partial tile for the cluster reduction: red[t][m]
-      float* red = reinterpret_cast<float*>(red_buf);
+    if (ks > 1) {
+      // every CTA of the cluster has started (the phase armed after setup)
+      cluster_wait();
+      if (ok) {
+        // scatter this CTA's fp32 partial rows into their owners' buffers:
+        // owner d, slot [rank][token][row - row_lo(d)]
+        const int q = warp & 3;
+        const int m = q * 32 + lane;
+        const int d = m / RR;
+        const uint32_t dst = map_to_cta(smem_u32(red_buf), static_cast<uint32_t>(d)) +
+                             static_cast<uint32_t>(((rank * BT) * RR + (m - d * RR)) * 4);
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BT / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(lane_base + c * 16, v);
-        tmem_ld_wait();
+        for (int c = 0; c < BT / 16; ++c) {
+          if (c * 16 >= tv) break;
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(lane_base + c * 16, v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) red[(c * 16 + j) * kTileN + m] = __uint_as_float(v[j]);
+          for (int j = 0; j < 16; ++j)
+            if (c * 16 + j < tv) st_dsmem_f32(dst + static_cast<uint32_t>((c * 16 + j) * RR * 4), __uint_as_float(v[j]));
+        }
       }
     }
   }
 
+  // The main loop is done: the next kernel on the stream (the next layer
+  // call's shrink grid) may become resident now; it waits for this grid's
+  // completion before it reads anything this grid writes.
+  pdl_allow_dependents();
+
   // ---------------------------------------------------------------- epilogue
-  // Per element (tile row mm, token column tl) with its fp32 accumulator:
-  //   y = acc * scales + [token has an adapter] * sum_j S[t, j] * B[l, n, j]
-  // B rows are cached in registers while consecutive tokens share an adapter.
-  auto finish = [&](int mm, int tl, float acc, int& cached_key, uint32_t (&brow)[kMaxRank / 2], float alpha,
-                    float sw) {
+  const float alpha = C::kFP4 ? 1.0f / (*p.x_gs * *p.w_gs) : 1.0f;
+  // base value of element (tile row mm, token column tl) from its fp32 sum
+  auto base_value = [&](int mm, int tl, float acc, float sw) {
+    return C::kFP4 ? acc * alpha : (acc * meta_sx[tl]) * sw;
+  };
+  // y = base + [token has an adapter] * S[t] . B[l, n]  (B row cached in
+  // registers while consecutive elements share (row, adapter))
+  auto finish = [&](int mm, int tl, float acc, float sw) {
     const int n = n0 + mm;
     const int t = t0 + tl;
     if (n >= p.N || t >= p.M) return;
-    float y = C::kFP4 ? acc * alpha : (acc * meta_sx[tl]) * sw;
+    float y = base_value(mm, tl, acc, sw);
     const int l = meta_idx[tl];
     if (l >= 0) {
-      const int key = l * kTileN + mm;
-      if (key != cached_key) {
-        const uint4* bsrc = reinterpret_cast<const uint4*>(p.B + (static_cast<size_t>(l) * p.N + n) * p.r);
-#pragma unroll
-        for (int c = 0; c < kMaxRank / 8; ++c) {
-          if (c < p.r / 8) {
-            const uint4 v = __ldg(bsrc + c);
-            brow[4 * c + 0] = v.x;
-            brow[4 * c + 1] = v.y;
-            brow[4 * c + 2] = v.z;
-            brow[4 * c + 3] = v.w;
-          }
-        }
-        cached_key = key;
-      }
-      const float4* srow = reinterpret_cast<const float4*>(p.S + static_cast<size_t>(t) * p.r);
-      float d = 0.0f;
-#pragma unroll
-      for (int c = 0; c < kMaxRank / 4; ++c) {
-        if (c < p.r / 4) {
-          const float4 s4 = __ldcg(srow + c);
-          d = fmaf(s4.x, bf16_lo(brow[2 * c]), d);
-          d = fmaf(s4.y, bf16_hi(brow[2 * c]), d);
-          d = fmaf(s4.z, bf16_lo(brow[2 * c + 1]), d);
-          d = fmaf(s4.w, bf16_hi(brow[2 * c + 1]), d);
-        }
-      }
-      y += d;
+      if (l * kTileN + mm != cached_key) load_brow(l, mm);
+      const float4* srow = C::kDecode ? reinterpret_cast<const float4*>(s_stage + tl * p.r)
+                                      : reinterpret_cast<const float4*>(p.S + static_cast<size_t>(t) * p.r);
+      y += dot_srow_brow(srow, brow, p.r, C::kDecode);
     }
     p.Y[static_cast<size_t>(t) * p.ldy + n] = __float2bfloat16_rn(y);
   };
 
-  const int aborted = __shfl_sync(0xffffffffu, *abort_flag, 0);   // warp-uniform
-  if (ks == 1) {
-    if (warp >= 2 && !aborted) {
+  if (ks > 1 && warp >= 2) {
+    // all partial rows have landed in their owners' shared memory (the
+    // producer and MMA warps arrived on this phase already)
+    cluster_arrive();
+    cluster_wait();
+  }
+  // the 4 epilogue warps agree on whether to produce output (the sections
+  // below contain their named barrier, which all four must reach)
+  if (warp >= 2 && !epi_bar_any(*abort_flag != 0)) {
+    if (et == 0) EPI_TRACE(5, globaltimer_ns());
+    const float* red = reinterpret_cast<const float*>(red_buf);
+    if (sb) {
+      // ---- streamed-B epilogue (decode tile with >= 2 adapter groups) ----
+      // 1) base values into the shared output tile y_tile[token][row]
+      if (ks == 1) {
+        const int q = warp & 3;
+        const int m = q * 32 + lane;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const float sw = (!C::kFP4 && n0 + m < p.N) ? p.w_scale[n0 + m] : 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < BT / 16; ++c) {
+          if (c * 16 >= tv) break;
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(lane_base + c * 16, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c * 16 + j < tv) y_tile[(c * 16 + j) * RR + m] = base_value(m, c * 16 + j, __uint_as_float(v[j]), sw);
+        }
+      } else {
+        for (int e = et; e < R * tv; e += 128) {
+          const int i = e % R, tl = e / R;
+          float acc = 0.0f;
+#pragma unroll
+          for (int s = 0; s < kMaxSplit; ++s)
+            if (s < ks) acc += red[(s * BT + tl) * RR + i];     // rank order: deterministic
+          const int mm = row_lo + i;
+          const float sw = (!C::kFP4 && n0 + mm < p.N) ? p.w_scale[n0 + mm] : 0.0f;
+          y_tile[tl * RR + i] = base_value(mm, tl, acc, sw);
+        }
+      }
+      asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
+      // 2) ring slots of B slices (several adapter groups each): thread ->
+      //    row i, the slot's tokens strided by 128 / R (R divides 128)
+      const int i = et % R;
+      const int tstep = 128 / R;
+      const int tsl = et / R;
+      const int sw_span = p.b_box_bytes;                   // 32, 64 or 128: swizzle span
+      const int sw_mask = sw_span / 16 - 1;
+      const int sw_shift = sw_span == 128 ? 0 : sw_span == 64 ? 1 : 2;   // row >> shift = (row * span) / 128
+      for (int j = 0; j < n_bslots; ++j) {
+        const int li = nkb + j;
+        const int s = li % stages;
+        const uint32_t ph = static_cast<uint32_t>(li / stages) & 1u;
+        // every thread waits itself (TMA data visibility); the outcome is
+        // made uniform over the 4 epilogue warps before anyone leaves
+        const bool late = !mbar_wait_bounded(&full_bar[s], ph, kWaitLimitNs);
+        if (epi_bar_any(late)) {
+          *abort_flag = 1;
+          record_status(p.status, EPILORA_ERR_TIMEOUT);
+          break;
+        }
+        const uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
+        // y[t][i] += S[t] . B_g[row i], B's row read 16 bytes at a time from
+        // the swizzled box (chunk c of row i lives at chunk c ^ f(i))
+        const int chunks_per_atom = sw_span / 16;
+        const int xr = (i >> sw_shift) & sw_mask;
+        const int g0 = j * gps;
+        const int g1 = min(ngroups, g0 + gps);
+        for (int k = g_start[g0] + tsl; k < g_start[g1]; k += tstep) {
+          const int tl = g_order[k];
+          const uint8_t* gb = st + (g_of[k] - g0) * p.b_group_bytes;
+          const float4* srow = reinterpret_cast<const float4*>(s_stage + tl * p.r);
+          float d = 0.0f;
+          for (int c = 0; c < p.r / 8; ++c) {
+            const int a = c / chunks_per_atom, cc = c % chunks_per_atom;
+            const uint4 v = *reinterpret_cast<const uint4*>(gb + a * RR * sw_span + i * sw_span + ((cc ^ xr) * 16));
+            const float4 s0 = srow[2 * c], s1 = srow[2 * c + 1];
+            d = fmaf(s0.x, bf16_lo(v.x), d);
+            d = fmaf(s0.y, bf16_hi(v.x), d);
+            d = fmaf(s0.z, bf16_lo(v.y), d);
+            d = fmaf(s0.w, bf16_hi(v.y), d);
+            d = fmaf(s1.x, bf16_lo(v.z), d);
+            d = fmaf(s1.y, bf16_hi(v.z), d);
+            d = fmaf(s1.z, bf16_lo(v.w), d);
+            d = fmaf(s1.w, bf16_hi(v.w), d);
+          }
+          y_tile[tl * RR + i] += d;
+        }
+        asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
+        if (et == 0) mbar_arrive(&empty_bar[s]);          // slot free for the producer
+      }
+      // 3) the output tile
+      for (int e = et; e < R * tv; e += 128) {
+        const int ii = e % R, tl = e / R;
+        const int n = n0 + row_lo + ii;
+        if (n < p.N) p.Y[static_cast<size_t>(t0 + tl) * p.ldy + n] = __float2bfloat16_rn(y_tile[tl * RR + ii]);
+      }
+    } else if (ks == 1) {
       const int q = warp & 3;
       const int m = q * 32 + lane;
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      const float alpha = C::kFP4 ? 1.0f / (*p.x_gs * *p.w_gs) : 1.0f;
       const float sw = (!C::kFP4 && n0 + m < p.N) ? p.w_scale[n0 + m] : 0.0f;
-      if (p.S != nullptr) pdl_wait_primary();   // the shrink has completed: S is visible
-      int cached_key = -1;
-      uint32_t brow[kMaxRank / 2];
 #pragma unroll 1
       for (int c = 0; c < BT / 16; ++c) {
+        if (c * 16 >= tv) break;
         uint32_t v[16];
         tmem_ld_32x32b_x16(lane_base + c * 16, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) finish(m, c * 16 + j, __uint_as_float(v[j]), cached_key, brow, alpha, sw);
+        for (int j = 0; j < 16; ++j) finish(m, c * 16 + j, __uint_as_float(v[j]), sw);
       }
-    }
-  } else {
-    // partials of every CTA of the cluster are in their shared memory
-    cluster_arrive();
-    cluster_wait();
-    if (warp >= 2 && !__shfl_sync(0xffffffffu, *abort_flag, 0)) {
-      const int et = threadIdx.x - 64;
-      const int row_lo = (kTileN * rank) / ks, row_hi = (kTileN * (rank + 1)) / ks;
-      const int R = row_hi - row_lo;
-      const float alpha = C::kFP4 ? 1.0f / (*p.x_gs * *p.w_gs) : 1.0f;
-      const uint32_t red_addr = smem_u32(red_buf);
-      if (p.S != nullptr) pdl_wait_primary();
-      int cached_key = -1;
-      uint32_t brow[kMaxRank / 2];
+    } else {
       int sw_row = -1;
       float sw = 0.0f;
 #pragma unroll 1
-      for (int e = et; e < R * BT; e += 128) {
-        const int mm = row_lo + e % R;
-        const int tl = e / R;
-        const uint32_t off = static_cast<uint32_t>((tl * kTileN + mm) * 4);
+      for (int e = et; e < R * tv; e += 128) {
+        const int i = e % R, tl = e / R;
+        const int mm = row_lo + i;
         float acc = 0.0f;
-        for (int s = 0; s < ks; ++s) acc += ld_dsmem_f32(map_to_cta(red_addr + off, static_cast<uint32_t>(s)));
+#pragma unroll
+        for (int s = 0; s < kMaxSplit; ++s)
+          if (s < ks) acc += red[(s * BT + tl) * RR + i];     // rank order: deterministic
         if (!C::kFP4 && mm != sw_row) {
           sw = (n0 + mm < p.N) ? p.w_scale[n0 + mm] : 0.0f;
           sw_row = mm;
         }
-        finish(mm, tl, acc, cached_key, brow, alpha, sw);
+        finish(mm, tl, acc, sw);
       }
     }
-    // peers may still be reading this CTA's partials
-    cluster_arrive();
-    cluster_wait();
   }
 
   // ---------------------------------------------------------------- teardown
+  if (ks > 1 && warp < 2) cluster_wait();   // second phase, for the producer and MMA warps
+  if (threadIdx.x == 64) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    EPI_TRACE(6, globaltimer_ns());
+    EPI_TRACE(7, smid);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  if (threadIdx.x == 0 && p.done_ctr != nullptr) {
+    // the last CTA of the grid re-arms the counters for the next launch on
+    // the stream (every CTA has passed its wait on x_ready by now)
+    const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
+    __threadfence();
+    if (atomicAdd(p.done_ctr, 1u) == total - 1u) {
+      *const_cast<uint32_t*>(p.x_ready) = 0u;
+      *p.done_ctr = 0u;
+      __threadfence();
+    }
+  }
 }
 
 // Host side ------------------------------------------------------------------
 int gemm_smem_bytes(int stage_bytes, int stages, int red_bytes);
 
-template <int FMT, int BT>
+#ifndef EPILORA_GEMM_ROTATE
+#define EPILORA_GEMM_ROTATE 1
+#endif
+#ifndef EPILORA_GEMM_RESIDENT
+#define EPILORA_GEMM_RESIDENT 2      // CTAs per SM a large decode grid is sized for
+#endif
+#ifndef EPILORA_GEMM_STREAM_B
+#define EPILORA_GEMM_STREAM_B 1
+#endif
+
+template <int FMT, int BT, int KA>
 int launch_gemm_tiled(const GemmArgs& a) {
-  using C = GemmCfg<FMT, BT>;
+  using C = GemmCfg<FMT, BT, KA>;
   const bool fp4 = C::kFP4;
   const int kbytes = fp4 ? a.K / 2 : a.K;
   GemmParams p{};
@@ -457,46 +846,76 @@ int launch_gemm_tiled(const GemmArgs& a) {
   p.mask = a.mask;
   p.Y = static_cast<__nv_bfloat16*>(a.Y);
   p.status = a.status_dev;
+  p.x_ready = a.x_ready;
+  p.x_ready_target = a.x_ready_target;
+  p.done_ctr = a.done_ctr;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
   p.L = a.L;
   p.r = a.r;
   p.ldy = a.ldy;
-  p.num_kb = (kbytes + kStageKBytes - 1) / kStageKBytes;
+  p.num_kb = (kbytes + KA * kAtomBytes - 1) / (KA * kAtomBytes);
+  p.rotate = EPILORA_GEMM_ROTATE;
 
-  int rc = make_tma_2d_u8(&p.tmW, a.Wq, a.N, kbytes, kbytes, kTileN, kStageKBytes, true);
+  int rc = make_tma_2d_u8(&p.tmW, a.Wq, a.N, kbytes, kbytes, kTileN, kAtomBytes, true);
   if (rc != EPILORA_OK) return rc;
-  rc = make_tma_2d_u8(&p.tmX, a.Xq, a.M, kbytes, kbytes, BT, kStageKBytes, true);
+  rc = make_tma_2d_u8(&p.tmX, a.Xq, a.M, kbytes, kbytes, BT, kAtomBytes, true);
   if (rc != EPILORA_OK) return rc;
   if (fp4) {
-    rc = make_tma_2d_u8(&p.tmSW, a.w_block_scale, a.N, a.K / 16, a.K / 16, kTileN, 16, false);
+    rc = make_tma_2d_u8(&p.tmSW, a.w_block_scale, a.N, a.K / 16, a.K / 16, kTileN, C::kSfRow, false);
     if (rc != EPILORA_OK) return rc;
-    rc = make_tma_2d_u8(&p.tmSX, a.x_block_scale, a.M, a.K / 16, a.K / 16, BT, 16, false);
+    rc = make_tma_2d_u8(&p.tmSX, a.x_block_scale, a.M, a.K / 16, a.K / 16, BT, C::kSfRow, false);
     if (rc != EPILORA_OK) return rc;
   }
 
+  // Decode grids: split K over clusters of 2/4/8 CTAs while the grid stays
+  // resident (EPILORA_GEMM_RESIDENT CTAs per SM); a grid larger than the SM
+  // count gets the shared memory of that many CTAs per SM.
+  const int sms = num_sms();
   const int n_tiles = (a.N + kTileN - 1) / kTileN;
   const int t_tiles = (a.M + BT - 1) / BT;
   const long tiles = static_cast<long>(n_tiles) * t_tiles;
   int ks = 1;
   if (BT <= 64) {
-    const long fit = num_sms() / tiles;
-    ks = static_cast<int>(fit < 1 ? 1 : fit > 8 ? 8 : fit);
     const int max_by_k = p.num_kb / 2 > 0 ? p.num_kb / 2 : 1;
-    if (ks > max_by_k) ks = max_by_k;
+    for (int cand = 2; cand <= kMaxSplit; cand *= 2)
+      if (tiles * cand <= static_cast<long>(sms) * EPILORA_GEMM_RESIDENT && cand <= max_by_k) ks = cand;
   }
   p.ks = ks;
-  const int red = gemm_red_bytes<BT>(ks);
-  const int budget = 200 * 1024;
-  int stages = (budget - 1024 - red - gemm_misc_bytes<BT>()) / C::kStageBytes;
-  if (stages > 16) stages = 16;
-  if (stages > p.num_kb / ks + 1) stages = p.num_kb / ks + 1;   // no deeper than the K loop needs
-  if (stages < 2) stages = 2;
-  p.stages = stages;
-  const int smem = gemm_smem_bytes(C::kStageBytes, stages, red) ;
+  const int RR = gemm_red_rows(ks);
 
-  auto kern = gemm_lora_kernel<FMT, BT>;
+  // streamed B (decode tiles): one TMA box of the tile's rows per adapter,
+  // its inner extent the row of B (2r bytes, in atoms of at most 128 B)
+  const int brow_bytes = 2 * a.r;
+  p.b_box_bytes = brow_bytes >= 128 ? 128 : brow_bytes;
+  p.b_atoms = brow_bytes > 128 ? brow_bytes / 128 : 1;
+  p.stream_b = 0;
+  p.b_group_bytes = (RR * brow_bytes + 1023) / 1024 * 1024;
+  p.b_groups_per_slot = C::kStageBytes / p.b_group_bytes;
+  if (p.b_groups_per_slot > BT) p.b_groups_per_slot = BT;
+  if (C::kDecode && a.S != nullptr && EPILORA_GEMM_STREAM_B && p.b_groups_per_slot >= 1) {
+    const uint64_t rows = static_cast<uint64_t>(a.L) * static_cast<uint64_t>(a.N);
+    rc = make_tma_2d_swz(&p.tmB, a.B, rows, brow_bytes, brow_bytes, RR, p.b_box_bytes, p.b_box_bytes);
+    if (rc != EPILORA_OK) return rc;
+    p.stream_b = 1;
+  }
+
+  const long ctas = tiles * ks;
+  const int budget = ctas > sms ? (227 * 1024) / EPILORA_GEMM_RESIDENT - 2048 : 200 * 1024;
+  const int red = gemm_red_bytes<BT>(ks);
+  const int dec = gemm_decode_bytes(BT, a.r, ks);
+  int stages = (budget - 1024 - red - kGemmMiscBytes - dec) / C::kStageBytes;
+  if (stages > 16) stages = 16;
+  const int per_cta = (p.num_kb + ks - 1) / ks;
+  if (stages > per_cta && !p.stream_b) stages = per_cta;     // no deeper than the K loop needs
+  if (stages < 2 && p.stream_b) stages = 2;
+  if (stages < 1) stages = 1;
+  p.stages = stages;
+  const int smem = gemm_smem_bytes(C::kStageBytes, stages, red) + dec;
+  if (smem > 227 * 1024) return EPILORA_ERR_UNSUPPORTED;
+
+  auto kern = gemm_lora_kernel<FMT, BT, KA>;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -532,13 +951,22 @@ int launch_gemm_tiled(const GemmArgs& a) {
   return EPILORA_OK;
 }
 
+#ifndef EPILORA_GEMM_KA
+#define EPILORA_GEMM_KA 2
+#endif
+
 template <int FMT>
 int launch_gemm_by_m(const GemmArgs& a) {
-  if (a.M <= 16) return launch_gemm_tiled<FMT, 16>(a);
-  if (a.M <= 32) return launch_gemm_tiled<FMT, 32>(a);
-  if (a.M <= 64) return launch_gemm_tiled<FMT, 64>(a);
-  if (a.M <= 128) return launch_gemm_tiled<FMT, 128>(a);
-  return launch_gemm_tiled<FMT, 256>(a);
+  constexpr int KA = EPILORA_GEMM_KA;
+  constexpr int KA256 = (FMT == EPILORA_FMT_NVFP4 && KA > 2) ? 2 : KA;   // TMEM budget of NVFP4 scales
+  // NVFP4 decode stages carry scale boxes too: one atom per stage keeps
+  // three or more stages in flight at two CTAs per SM
+  constexpr int KAD = FMT == EPILORA_FMT_NVFP4 ? 1 : KA;
+  if (a.M <= 16) return launch_gemm_tiled<FMT, 16, KAD>(a);
+  if (a.M <= 32) return launch_gemm_tiled<FMT, 32, KAD>(a);
+  if (a.M <= 64) return launch_gemm_tiled<FMT, 64, KA>(a);
+  if (a.M <= 128) return launch_gemm_tiled<FMT, 128, KA>(a);
+  return launch_gemm_tiled<FMT, 256, KA256>(a);
 }
 
 }  // namespace epi

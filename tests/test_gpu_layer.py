@@ -188,3 +188,48 @@ def test_empty_batch_is_a_noop():
     X = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
     Y = T.layer_forward(X, w)
     assert Y.shape == (0, 256)
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+def test_back_to_back_calls_share_workspace_and_replay_in_a_graph(fmt):
+    """Consecutive fused calls (each a programmatic dependent of the one
+    before) that share one workspace, eagerly and captured in a CUDA graph,
+    give bitwise the results of isolated calls."""
+    shapes = [(1, 4096, 1024, 1, 64), (3, 2048, 4096, 2, 16), (1, 4096, 6144, 1, 64), (17, 1024, 512, 4, 32)]
+    cases = []
+    for i, (M, K, N, L, r) in enumerate(shapes):
+        p = make_projection(M, K, N, L, r, seed=40 + i)
+        X, W = p.X.cuda(), p.W.cuda()
+        w = T.quantize_weight(W, fmt)
+        gx = T.nvfp4_global_scale(X) if fmt == NVFP4 else None
+        args = (X, w, p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda(), gx)
+        ref = T.layer_forward(*args[:6], x_global_scale=gx)       # own workspace
+        torch.cuda.synchronize()
+        cases.append((args, ref))
+    ws = T.LayerWorkspace("cuda")
+    for M, K, N, L, r in shapes:
+        ws.get(fmt, M, K, r)
+    outs = [torch.empty_like(ref) for _, ref in cases]
+
+    def run(stream=None):
+        for (args, _), Y in zip(cases, outs):
+            T.layer_forward(*args[:6], x_global_scale=args[6], workspace=ws, Y=Y, stream=stream)
+
+    run()
+    torch.cuda.synchronize()
+    for (_, ref), Y in zip(cases, outs):
+        assert torch.equal(Y, ref)
+    for Y in outs:
+        Y.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run(s)
+    for _ in range(2):
+        for Y in outs:
+            Y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for (_, ref), Y in zip(cases, outs):
+            assert torch.equal(Y, ref)

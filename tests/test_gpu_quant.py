@@ -25,7 +25,7 @@ def _bf16_rows(rng, M, K, std=1.0):
 
 
 @pytest.mark.parametrize("M,K,std", [(4, 512, 1.0), (1, 4096, 1.0), (33, 14336, 3.0), (7, 32, 1e-3),
-                                     (64, 1024, 100.0)])
+                                     (64, 1024, 100.0), (2, 40960, 1.0)])
 def test_fp8_quant_bit_exact(M, K, std):
     rng = np.random.default_rng(M * 1000 + K)
     X = _bf16_rows(rng, M, K, std)
