@@ -211,6 +211,45 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K,
                           void* workspace, size_t workspace_bytes,
                           int* status_dev, void* stream);
 
+/*
+ * epilora_layer_forward without a caller workspace. The EpiLoRA page has no
+ * counterpart of this entry point: it serves callers that cannot hand the
+ * library device memory, such as a plain C host with no device allocator of
+ * its own, or code at a point where entering an allocator is not allowed (an
+ * allocator's own hook, a section that must not call cudaMalloc).
+ *
+ * It allocates nothing. Its scratch is a fixed array of
+ * EPILORA_NOALLOC_SCRATCH_BYTES bytes of static device storage inside the
+ * library, one per device. The first call on a device (the device current
+ * at the call) looks up that array's address with cudaGetSymbolAddress; make
+ * that first call before any stream capture. Arguments, layout, results and
+ * status codes are those of epilora_layer_forward without the workspace.
+ *
+ * Returns EPILORA_ERR_WORKSPACE, having enqueued nothing, when
+ * epilora_workspace_bytes(fmt, M, K, A && B ? r : 0) exceeds
+ * EPILORA_NOALLOC_SCRATCH_BYTES (8 MiB: e.g. FP8 with M * K up to about 7.9
+ * million elements at r = 64); EPILORA_ERR_CUDA if the address lookup fails.
+ * Otherwise each call first clears the scratch's 256-byte counter block on
+ * `stream` (only that block needs a starting value; the rest is written
+ * before it is read), then enqueues what epilora_layer_forward enqueues.
+ * Argument errors found by epilora_layer_forward are reported after that
+ * clearing has been enqueued; nothing else is.
+ *
+ * All calls on one device share the one scratch array: calls that overlap in
+ * time (on different streams, or from host threads that do not order their
+ * streams) race on it and produce wrong results. Order them on one stream.
+ */
+#define EPILORA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+EPILORA_API int epilora_layer_forward_noalloc(int fmt, int M, int N, int K,
+                          const void* X, int ldx,
+                          const void* Wq, const float* w_scale,
+                          const uint8_t* w_block_scale, const float* w_global_scale,
+                          const float* x_global_scale,
+                          const void* A, const void* B, int L, int r,
+                          const int32_t* idx, const uint8_t* mask,
+                          void* Y, int ldy,
+                          int* status_dev, void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -38,6 +38,8 @@ SIGNATURES = {
     "epilora_workspace_bytes": (_sz, [_c_int, _c_int, _c_int, _c_int]),
     "epilora_layer_forward": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _sz, _vp, _vp]),
+    "epilora_layer_forward_noalloc": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp,
+                                               _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp]),
 }
 
 _lib = None
@@ -138,3 +140,11 @@ def epilora_layer_forward(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_gl
                                         _p(w_global_scale), _p(x_global_scale), _p(A), _p(B), L, r, _p(idx),
                                         _p(mask), _p(Y), ldy, _p(workspace), workspace_bytes, _p(status_dev),
                                         _stream(stream))
+
+
+def epilora_layer_forward_noalloc(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale,
+                                  x_global_scale, A, B, L, r, idx, mask, Y, ldy, status_dev=None,
+                                  stream=None) -> int:
+    return load().epilora_layer_forward_noalloc(fmt, M, N, K, _p(X), ldx, _p(Wq), _p(w_scale), _p(w_block_scale),
+                                                _p(w_global_scale), _p(x_global_scale), _p(A), _p(B), L, r,
+                                                _p(idx), _p(mask), _p(Y), ldy, _p(status_dev), _stream(stream))
