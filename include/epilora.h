@@ -176,27 +176,30 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
 
 /*
  * Bytes of device workspace epilora_layer_forward needs for (fmt, M, K, r):
- * a 256-byte block of two uint32 counters, the quantized activations, their
- * scales and S (r = 0: no adapters), each 256-byte aligned.
+ * the quantized activations, their scales and S (r = 0: no adapters; for a
+ * few tokens S is held as up to ceil(K / 4096) partial sums over K slices,
+ * capped at 8), each region 256-byte aligned. Returns 0 for M == 0 or
+ * invalid arguments.
  */
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
 
 /*
  * Fused one-call layer (the decode path of the EpiLoRA page, §Design ›
  * Multi-adapter kernels › The decode path): enqueues two kernels,
- *   1. the shrink grid of epilora_lora_shrink plus one quantizer CTA per token
- *      (the arithmetic of epilora_quant_act), launched as a programmatic
- *      dependent of the previous kernel on the stream: it waits for that
- *      kernel's completion before reading anything, and
+ *   1. the shrink grid of epilora_lora_shrink (for a few tokens split over
+ *      K slices) plus quantizer CTAs (the arithmetic of epilora_quant_act),
+ *      launched as a programmatic dependent of the previous kernel on the
+ *      stream: it lets the GEMM launch at once, then waits for that kernel's
+ *      completion before reading anything, and
  *   2. the GEMM of epilora_gemm_lora_epilogue as its programmatic dependent:
- *      it streams W immediately, waits (bounded) for the quantizer CTAs'
- *      completion counter before loading the quantized activations, and for
- *      the whole shrink grid only before reading S in its epilogue;
- * using `workspace` (>= epilora_workspace_bytes, 256-byte aligned) for the
- * counters, Xq, scales and S. The first 256 bytes of the workspace must be
- * zero before its first use; every completed call leaves them zero again
- * (after a call that reported EPILORA_ERR_TIMEOUT, re-zero them). Calls that
- * share a workspace must be ordered on one stream.
+ *      it starts streaming Wq (and w_block_scale) as soon as it is resident,
+ *      and reads everything else only after the shrink grid has completed;
+ * using `workspace` (>= epilora_workspace_bytes, 256-byte aligned, no
+ * initial value needed) for Xq, scales and S. Calls that share a workspace
+ * must be ordered on one stream.
+ * Because the GEMM may start while the kernel that precedes this call on the
+ * stream is still running, that kernel must not write Wq or w_block_scale
+ * (every other input, X included, may be its output).
  * A == NULL or B == NULL computes the base layer only. Graph-capturable: it
  * makes no allocation and no synchronizing call.
  */
@@ -229,11 +232,8 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K,
  * epilora_workspace_bytes(fmt, M, K, A && B ? r : 0) exceeds
  * EPILORA_NOALLOC_SCRATCH_BYTES (8 MiB: e.g. FP8 with M * K up to about 7.9
  * million elements at r = 64); EPILORA_ERR_CUDA if the address lookup fails.
- * Otherwise each call first clears the scratch's 256-byte counter block on
- * `stream` (only that block needs a starting value; the rest is written
- * before it is read), then enqueues what epilora_layer_forward enqueues.
- * Argument errors found by epilora_layer_forward are reported after that
- * clearing has been enqueued; nothing else is.
+ * Otherwise it enqueues what epilora_layer_forward enqueues (the scratch
+ * needs no starting value: every byte is written before it is read).
  *
  * All calls on one device share the one scratch array: calls that overlap in
  * time (on different streams, or from host threads that do not order their

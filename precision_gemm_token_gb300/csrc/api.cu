@@ -33,7 +33,6 @@ inline bool fmt_ok(int fmt) { return fmt == EPILORA_FMT_FP8_E4M3 || fmt == EPILO
 inline bool rank_ok(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
 inline bool k_ok(int K) { return K >= 32 && K % 32 == 0; }
 inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
-constexpr size_t kWorkspaceCounterBytes = 256;
 
 bool quant_args_ok(int fmt, const void* X, int M, int K, int ldx, const void* Xq, const float* x_scale,
                    const uint8_t* x_block_scale, const float* x_global_scale) {
@@ -227,7 +226,7 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   if (!fmt_ok(fmt) || M < 0 || K < 0 || r < 0) return 0;
   const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
   if (M == 0) return 0;
-  size_t bytes = kWorkspaceCounterBytes;   // two uint32 counters, zero between calls
+  size_t bytes = 0;
   if (fmt == EPILORA_FMT_FP8_E4M3) {
     bytes += round256(m * k);          // Xq
     bytes += round256(m * 4);          // x_scale
@@ -235,7 +234,8 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
     bytes += round256(m * k / 2);      // packed Xq
     bytes += round256(m * k / 16);     // block scales
   }
-  bytes += round256(m * static_cast<size_t>(r) * 4);   // S
+  // S, or the partial sums of a shrink split over K slices
+  bytes += round256(m * static_cast<size_t>(r) * 4 * static_cast<size_t>(r > 0 ? shrink_parts_max(K) : 1));
   return bytes;
 }
 
@@ -257,8 +257,7 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
     return EPILORA_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
-  uint32_t* counters = reinterpret_cast<uint32_t*>(ws);      // [0] rows quantized, [1] GEMM CTAs done
-  size_t off = kWorkspaceCounterBytes;
+  size_t off = 0;
   void* Xq = ws + off;
   float* x_scale = nullptr;
   uint8_t* x_block_scale = nullptr;
@@ -280,13 +279,14 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
   if (adapters && !shrink_args_ok(X, M, K, ldx, A, L, r, idx, mask, S)) return EPILORA_ERR_INVALID_ARG;
   if (!quant_args_ok(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale)) return EPILORA_ERR_INVALID_ARG;
 
-  // The shrink grid (plus one quantizer CTA per token) is launched normally;
-  // the GEMM is its programmatic dependent: it streams W at once, loads the
-  // quantized activations after the quantizer CTAs' counter reaches M, and
-  // reads S after the whole shrink grid completed.
+  // The shrink grid (with the quantizer CTAs) is a programmatic dependent of
+  // the previous kernel on the stream and releases the GEMM at once; the GEMM
+  // streams W immediately and reads everything the shrink grid writes (and
+  // the token metadata) only after that grid has completed.
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  rc = launch_shrink_quant(X, M, K, ldx, A, adapters ? L : 1, adapters ? r : 0, idx, mask, S, fmt, Xq, x_scale,
-                           x_block_scale, x_global_scale, &counters[0], status_dev, st);
+  const int parts = adapters ? shrink_parts(M, K, r) : shrink_parts(M, K, 0);
+  rc = launch_shrink_quant(X, M, K, ldx, A, adapters ? L : 1, adapters ? r : 0, idx, mask, S, parts, fmt, Xq,
+                           x_scale, x_block_scale, x_global_scale, status_dev, st);
   if (rc != EPILORA_OK) return rc;
   GemmArgs a{};
   a.fmt = fmt;
@@ -312,9 +312,8 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
   a.pdl_dependent = 1;
   a.status_dev = status_dev;
   a.stream = st;
-  a.x_ready = &counters[0];
-  a.x_ready_target = static_cast<uint32_t>(M);
-  a.done_ctr = &counters[1];
+  a.fused = 1;
+  a.s_parts = parts;
   return fmt == EPILORA_FMT_FP8_E4M3 ? launch_gemm_fp8(a) : launch_gemm_nvfp4(a);
 }
 

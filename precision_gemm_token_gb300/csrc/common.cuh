@@ -51,11 +51,10 @@ struct GemmArgs {
   int pdl_dependent;
   int* status_dev;
   cudaStream_t stream;
-  // fused decode path: Xq / scales are produced by quantizer CTAs running
-  // concurrently in the shrink's grid; see launch_shrink_quant
-  const uint32_t* x_ready = nullptr;
-  uint32_t x_ready_target = 0;
-  uint32_t* done_ctr = nullptr;
+  // fused layer call: Xq, its scales, idx and mask come from the primary
+  // grid (launch_shrink_quant), S as s_parts partial arrays [s_parts][M][r]
+  int fused = 0;
+  int s_parts = 1;
 };
 
 int launch_quant(int fmt, const void* X, int M, int K, int ldx, void* Xq, float* x_scale,
@@ -63,13 +62,18 @@ int launch_quant(int fmt, const void* X, int M, int K, int ldx, void* Xq, float*
 int launch_global_scale(const void* T, size_t n, float* g_out, cudaStream_t stream);
 int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
                   const uint8_t* mask, float* S, int* status_dev, cudaStream_t stream);
-// Shrink grid with one extra quantizer CTA per token: S as launch_shrink, and
-// Xq / scales as launch_quant; each quantizer CTA increments *x_ready (release)
-// after its row is written. Launched as a programmatic dependent of the
-// previous kernel on the stream, which it waits for before reading anything.
+// Shrink grid with extra quantizer CTAs: Xq / scales as launch_quant, and S
+// as `s_parts` partial arrays [s_parts][M][r] over consecutive K slices (their
+// sum in part order is S; s_parts == 1 gives S itself). Launched as a
+// programmatic dependent of the previous kernel on the stream: it releases its
+// own dependent at once and waits for that kernel before reading anything.
 int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
-                        const uint8_t* mask, float* S, int fmt, void* Xq, float* x_scale, uint8_t* x_block_scale,
-                        const float* x_global_scale, uint32_t* x_ready, int* status_dev, cudaStream_t stream);
+                        const uint8_t* mask, float* S, int s_parts, int fmt, void* Xq, float* x_scale,
+                        uint8_t* x_block_scale, const float* x_global_scale, int* status_dev, cudaStream_t stream);
+// Number of K slices launch_shrink_quant uses for (M, K, r) (1 when M > 32),
+// and the largest it can use for K (sizes the workspace).
+int shrink_parts(int M, int K, int r);
+int shrink_parts_max(int K);
 int launch_gemm_fp8(const GemmArgs& a);
 int launch_gemm_nvfp4(const GemmArgs& a);
 

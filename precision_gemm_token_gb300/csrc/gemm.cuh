@@ -22,9 +22,10 @@
 //    swizzled K-major tiles that TMA writes into a multi-stage ring; a stage
 //    holds KA 128-byte K atoms of every row; the accumulator lives in TMEM;
 //  * the producer fills the ring with weight tiles as soon as the CTA starts;
-//    when the activations are quantized by a concurrently running kernel it
-//    waits (bounded) on that kernel's completion counter only before its first
-//    activation load;
+//    in the fused layer call it waits for the shrink grid (which quantizes the
+//    activations) only before its first activation load, so a GEMM that
+//    becomes resident while the previous layer call's GEMM drains streams
+//    its weights at once;
 //  * every weight tile starts its K loop at its own offset, so the CTAs
 //    streaming W at the same time do not all read the same column slice;
 //  * few output tiles (decode): the K dimension is split over a thread-block
@@ -74,13 +75,14 @@ struct GemmParams {
   const uint8_t* mask;
   __nv_bfloat16* Y;
   int* status;
-  // Set when the quantized activations are produced by a kernel that runs
-  // concurrently (the shrink's quantizer CTAs): the GEMM waits until
-  // *x_ready >= x_ready_target before loading them; the last GEMM CTA to
-  // finish (counted in *done_ctr) resets both counters to 0.
-  const uint32_t* x_ready;
-  uint32_t x_ready_target;
-  uint32_t* done_ctr;
+  // 1: the quantized activations, their scales, idx and mask are written by
+  // the primary grid (the fused shrink grid): the producer streams weights
+  // first and executes griddepcontrol.wait before the first activation load,
+  // the epilogue warps before reading any token metadata.
+  int fused;
+  // S is the sum of s_parts partial arrays [s_parts][M][r] (split K of the
+  // shrink), added in part order
+  int s_parts;
   int M, N, K, L, r, ldy;
   int num_kb;         // K stages in total (KA atoms each)
   int ks;             // cluster size along K (1 = no split)
@@ -91,6 +93,7 @@ struct GemmParams {
   int b_atoms;        // tmB boxes per group (2 when 2r = 256)
   int b_group_bytes;  // ring bytes of one group's boxes (1024-byte aligned)
   int b_groups_per_slot;
+  int trace_slot;     // tuning builds only: which trace buffer this launch fills
 };
 
 template <int FMT, int BT, int KA>
@@ -145,12 +148,17 @@ __host__ __device__ constexpr int gemm_decode_bytes(int BT, int r, int ks) {
 // tuning): entry, ring primed, first stage landed, last stage landed,
 // accumulator ready, S readable, epilogue done, SM id.
 #ifdef EPILORA_GEMM_TRACE
-constexpr int kTraceCtas = 8192;
-static __device__ unsigned long long g_gemm_trace[kTraceCtas][8];
+constexpr int kTraceSlots = 8;       // consecutive launches, round robin
+constexpr int kTraceCtas = 2048;
+static __device__ unsigned long long g_gemm_trace[kTraceSlots][kTraceCtas][8];
+inline int& gemm_trace_launches() {
+  static int n = 0;
+  return n;
+}
 #define EPI_TRACE(slot, value)                                                                     \
   do {                                                                                             \
     const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);          \
-    if (cta_ < kTraceCtas) g_gemm_trace[cta_][slot] = (value);                                     \
+    if (cta_ < kTraceCtas) g_gemm_trace[p.trace_slot][cta_][slot] = (value);                       \
   } while (0)
 #else
 #define EPI_TRACE(slot, value) \
@@ -274,27 +282,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     fence_mbarrier_init();
     // the ring starts empty: stream weights into it before anything else
     for (int i = 0; i < prologue; ++i) issue_w(i, i);
-    if (p.x_ready != nullptr) {
-      // the activations are being quantized right now by the shrink's
-      // quantizer CTAs (all resident: this grid launched after every CTA of
-      // that grid had started): wait for their completion count
-      bool ok = ld_acquire_gpu_u32(p.x_ready) >= p.x_ready_target;
-      if (!ok) {
-        const uint64_t tstart = globaltimer_ns();
-        while (!ok) {
-          __nanosleep(64);
-          ok = ld_acquire_gpu_u32(p.x_ready) >= p.x_ready_target;
-          if (!ok && globaltimer_ns() - tstart > kWaitLimitNs) break;
-        }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        record_status(p.status, EPILORA_ERR_TIMEOUT);
-      }
-      fence_proxy_async_global();   // the TMA reads below see the quantizers' writes
+    if (p.fused) {
+      // the shrink grid quantizes the activations: its completion (and that
+      // of everything before it) makes them visible
+      pdl_wait_primary();
+      fence_proxy_async_global();
     }
-    // (after a timeout the loads are still issued so that every stage
-    // completes; the abort flag discards the result)
     for (int i = 0; i < prologue; ++i) issue_x(i, i);
   }
   if (warp == 1) {
@@ -302,13 +295,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     tmem_relinquish();
   }
   if (warp >= 2) {
-    // token metadata (its loads overlap the first weight loads)
+    // token metadata (its loads overlap the first weight loads); in the fused
+    // call it is read once the shrink grid has completed
+    if (p.fused) pdl_wait_primary();
     for (int i = et; i < BT; i += 128) {
       const int t = t0 + i;
       float sx = 0.0f;
       int l = -1;
       if (t < p.M) {
-        if (!C::kFP4 && p.x_ready == nullptr) sx = p.x_scale[t];
+        if (!C::kFP4) sx = p.x_scale[t];
         if (p.S != nullptr) {
           const int li = p.idx[t];
           const bool on = li >= 0 && li < p.L && (p.mask == nullptr || p.mask[t] != 0);
@@ -376,6 +371,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   // epilogue state carried from the main-loop phase into the epilogue phase
   int cached_key = -1;
   uint32_t brow[kMaxRank / 2];
+  float sw_pre = 0.0f;      // FP8: scale of this thread's weight row
+  float alpha_pre = 1.0f;   // NVFP4: 1 / (g_x * g_w)
 
   auto load_brow = [&](int l, int mm) {
     const uint4* bsrc =
@@ -577,24 +574,30 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     // here on S is visible. Also orders this grid after the whole primary grid.
     pdl_wait_primary();
     if (C::kDecode && p.S != nullptr) {
-      // S rows of this tile's tokens into shared memory
+      // S rows of this tile's tokens into shared memory (partials of a split
+      // shrink added in part order)
+      const size_t part = static_cast<size_t>(p.M) * p.r / 4;
       const float4* src = reinterpret_cast<const float4*>(p.S + static_cast<size_t>(t0) * p.r);
       float4* dst = reinterpret_cast<float4*>(s_stage);
-      for (int i = et; i < tv * p.r / 4; i += 128) dst[i] = __ldcg(src + i);
-    }
-    if (!C::kFP4 && p.x_ready != nullptr) {
-      // per-token scales written by the quantizer CTAs before they counted
-      // their rows ready (observe the count with acquire, then read)
-      const uint64_t tstart = globaltimer_ns();
-      while (ld_acquire_gpu_u32(p.x_ready) < p.x_ready_target) {
-        if (globaltimer_ns() - tstart > kWaitLimitNs) {
-          *abort_flag = 1;
-          record_status(p.status, EPILORA_ERR_TIMEOUT);
-          break;
+      for (int i = et; i < tv * p.r / 4; i += 128) {
+        float4 v = __ldcg(src + i);
+        for (int q = 1; q < p.s_parts; ++q) {
+          const float4 w = __ldcg(src + q * part + i);
+          v.x += w.x;
+          v.y += w.y;
+          v.z += w.z;
+          v.w += w.w;
         }
-        __nanosleep(64);
+        dst[i] = v;
       }
-      for (int i = et; i < BT; i += 128) meta_sx[i] = (t0 + i < p.M) ? __ldcg(p.x_scale + t0 + i) : 0.0f;
+    }
+    // this thread's weight-row scale and the NVFP4 dequantization factor,
+    // loaded while the main loop runs
+    if (!C::kFP4) {
+      const int mrow = ks == 1 ? (warp & 3) * 32 + lane : row_lo + (R > 0 ? et % R : 0);
+      sw_pre = n0 + mrow < p.N ? __ldg(p.w_scale + n0 + mrow) : 0.0f;
+    } else {
+      alpha_pre = 1.0f / (*p.x_gs * *p.w_gs);
     }
     asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
     const bool ok = mbar_wait_bounded(acc_bar, 0, kWaitLimitNs);
@@ -636,7 +639,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   pdl_allow_dependents();
 
   // ---------------------------------------------------------------- epilogue
-  const float alpha = C::kFP4 ? 1.0f / (*p.x_gs * *p.w_gs) : 1.0f;
+  const float alpha = alpha_pre;
   // base value of element (tile row mm, token column tl) from its fp32 sum
   auto base_value = [&](int mm, int tl, float acc, float sw) {
     return C::kFP4 ? acc * alpha : (acc * meta_sx[tl]) * sw;
@@ -676,7 +679,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         const int q = warp & 3;
         const int m = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        const float sw = (!C::kFP4 && n0 + m < p.N) ? p.w_scale[n0 + m] : 0.0f;
+        const float sw = sw_pre;
 #pragma unroll 1
         for (int c = 0; c < BT / 16; ++c) {
           if (c * 16 >= tv) break;
@@ -695,8 +698,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
           for (int s = 0; s < kMaxSplit; ++s)
             if (s < ks) acc += red[(s * BT + tl) * RR + i];     // rank order: deterministic
           const int mm = row_lo + i;
-          const float sw = (!C::kFP4 && n0 + mm < p.N) ? p.w_scale[n0 + mm] : 0.0f;
-          y_tile[tl * RR + i] = base_value(mm, tl, acc, sw);
+          y_tile[tl * RR + i] = base_value(mm, tl, acc, sw_pre);   // i == et % R: this thread's row
         }
       }
       asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
@@ -760,7 +762,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       const int q = warp & 3;
       const int m = q * 32 + lane;
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      const float sw = (!C::kFP4 && n0 + m < p.N) ? p.w_scale[n0 + m] : 0.0f;
+      const float sw = sw_pre;
 #pragma unroll 1
       for (int c = 0; c < BT / 16; ++c) {
         if (c * 16 >= tv) break;
@@ -771,21 +773,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         for (int j = 0; j < 16; ++j) finish(m, c * 16 + j, __uint_as_float(v[j]), sw);
       }
     } else {
-      int sw_row = -1;
-      float sw = 0.0f;
 #pragma unroll 1
       for (int e = et; e < R * tv; e += 128) {
-        const int i = e % R, tl = e / R;
+        const int i = e % R, tl = e / R;     // i == et % R: this thread's row
         const int mm = row_lo + i;
         float acc = 0.0f;
 #pragma unroll
         for (int s = 0; s < kMaxSplit; ++s)
           if (s < ks) acc += red[(s * BT + tl) * RR + i];     // rank order: deterministic
-        if (!C::kFP4 && mm != sw_row) {
-          sw = (n0 + mm < p.N) ? p.w_scale[n0 + mm] : 0.0f;
-          sw_row = mm;
-        }
-        finish(mm, tl, acc, sw);
+        finish(mm, tl, acc, sw_pre);
       }
     }
   }
@@ -803,17 +799,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
-  }
-  if (threadIdx.x == 0 && p.done_ctr != nullptr) {
-    // the last CTA of the grid re-arms the counters for the next launch on
-    // the stream (every CTA has passed its wait on x_ready by now)
-    const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
-    __threadfence();
-    if (atomicAdd(p.done_ctr, 1u) == total - 1u) {
-      *const_cast<uint32_t*>(p.x_ready) = 0u;
-      *p.done_ctr = 0u;
-      __threadfence();
-    }
   }
 }
 
@@ -846,9 +831,11 @@ int launch_gemm_tiled(const GemmArgs& a) {
   p.mask = a.mask;
   p.Y = static_cast<__nv_bfloat16*>(a.Y);
   p.status = a.status_dev;
-  p.x_ready = a.x_ready;
-  p.x_ready_target = a.x_ready_target;
-  p.done_ctr = a.done_ctr;
+  p.fused = a.fused;
+#ifdef EPILORA_GEMM_TRACE
+  p.trace_slot = gemm_trace_launches()++ % kTraceSlots;
+#endif
+  p.s_parts = a.s_parts < 1 ? 1 : a.s_parts;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
@@ -909,7 +896,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   if (stages > 16) stages = 16;
   const int per_cta = (p.num_kb + ks - 1) / ks;
   if (stages > per_cta && !p.stream_b) stages = per_cta;     // no deeper than the K loop needs
-  if (stages < 2 && p.stream_b) stages = 2;
+  if (stages < 2) p.stream_b = 0;        // B slots need a ring of two or more
   if (stages < 1) stages = 1;
   p.stages = stages;
   const int smem = gemm_smem_bytes(C::kStageBytes, stages, red) + dec;
@@ -962,8 +949,10 @@ int launch_gemm_by_m(const GemmArgs& a) {
   // NVFP4 decode stages carry scale boxes too: one atom per stage keeps
   // three or more stages in flight at two CTAs per SM
   constexpr int KAD = FMT == EPILORA_FMT_NVFP4 ? 1 : KA;
+  // 32-token decode tiles also keep output-tile and S buffers: one atom per
+  // stage leaves room for three or more stages
   if (a.M <= 16) return launch_gemm_tiled<FMT, 16, KAD>(a);
-  if (a.M <= 32) return launch_gemm_tiled<FMT, 32, KAD>(a);
+  if (a.M <= 32) return launch_gemm_tiled<FMT, 32, 1>(a);
   if (a.M <= 64) return launch_gemm_tiled<FMT, 64, KA>(a);
   if (a.M <= 128) return launch_gemm_tiled<FMT, 128, KA>(a);
   return launch_gemm_tiled<FMT, 256, KA256>(a);

@@ -7,8 +7,7 @@
 // call cudaMalloc). For them this entry point allocates nothing: its scratch
 // is a fixed array of static device storage, one instance per device (each
 // device's module image holds its own), whose address is looked up once per
-// device. It then enqueues exactly what epilora_layer_forward enqueues, after
-// clearing the scratch's counter block on the same stream.
+// device. It then enqueues exactly what epilora_layer_forward enqueues.
 #include <mutex>
 
 #include "common.cuh"
@@ -17,10 +16,9 @@ namespace epi {
 namespace {
 
 constexpr size_t kScratchBytes = EPILORA_NOALLOC_SCRATCH_BYTES;
-constexpr size_t kCounterBytes = 256;   // leading counter block of the layer workspace
 constexpr int kMaxDevices = 64;
 
-// Static device storage: zero at module load, never freed.
+// Static device storage, never freed; every byte is written before it is read.
 __device__ __align__(256) unsigned char g_layer_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
@@ -63,8 +61,6 @@ EPILORA_API int epilora_layer_forward_noalloc(int fmt, int M, int N, int K, cons
   if (need > epi::kScratchBytes) return EPILORA_ERR_WORKSPACE;
   void* scratch = epi::scratch_for_current_device();
   if (scratch == nullptr) return EPILORA_ERR_CUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, epi::kCounterBytes, st) != cudaSuccess) return EPILORA_ERR_CUDA;
   return epilora_layer_forward(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale, x_global_scale, A,
                                B, L, r, idx, mask, Y, ldy, scratch, epi::kScratchBytes, status_dev, stream);
 }

@@ -89,17 +89,44 @@ __device__ __forceinline__ void quant_row_fp8(const __nv_bfloat16* __restrict__ 
     out[c] = quant8_e4m3(__ldg(row + c), s);
 }
 
+// amax over a whole row by one CTA, loads kept in flight (nothing held).
+__device__ __forceinline__ float row_amax_bf16(const __nv_bfloat16* __restrict__ xrow, int K, float* red) {
+  const uint4* row = reinterpret_cast<const uint4*>(xrow);
+  const int nch = K / 8;
+  float amax = 0.0f;
+#pragma unroll 8
+  for (int c = static_cast<int>(threadIdx.x); c < nch; c += static_cast<int>(blockDim.x)) {
+    float x[8];
+    unpack8(__ldg(row + c), x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  }
+  return block_max(amax, red);
+}
+
+// E4M3 codes of the row's elements [k0, k1) (multiples of 8) with scale s.
+__device__ __forceinline__ void quant_slice_fp8(const __nv_bfloat16* __restrict__ xrow, int k0, int k1,
+                                                uint8_t* __restrict__ qrow, float s) {
+  const uint4* row = reinterpret_cast<const uint4*>(xrow);
+  uint2* out = reinterpret_cast<uint2*>(qrow);
+#pragma unroll 4
+  for (int c = k0 / 8 + static_cast<int>(threadIdx.x); c < k1 / 8; c += static_cast<int>(blockDim.x))
+    out[c] = quant8_e4m3(__ldg(row + c), s);
+}
+
 // One CTA quantizes one row to NVFP4: per 16-element block b,
 // sb = E4M3(fl32(fl32(amax_b / 6) * g)), codes = E2M1(fl32(x * fl32(g / sb))).
-// Returns false if the global scale g is not a positive finite number (the
-// row is then written as zeros).
+// Blocks [b0, b1) of the row (all of it by default). Returns false if the
+// global scale g is not a positive finite number (those blocks are then
+// written as zeros).
 __device__ __forceinline__ bool quant_row_nvfp4(const __nv_bfloat16* __restrict__ xrow, int K,
-                                                uint8_t* __restrict__ qrow, uint8_t* __restrict__ srow, float g) {
+                                                uint8_t* __restrict__ qrow, uint8_t* __restrict__ srow, float g,
+                                                int b0 = 0, int b1 = -1) {
   const bool g_ok = (g > 0.0f) && isfinite(g);
   const uint4* row = reinterpret_cast<const uint4*>(xrow);
   uint2* out = reinterpret_cast<uint2*>(qrow);
-  const int nb = K / kNvfp4Block;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+  const int nb = b1 < 0 ? K / kNvfp4Block : b1;
+  for (int b = b0 + static_cast<int>(threadIdx.x); b < nb; b += blockDim.x) {
     float x[16];
     {
       float a[8], c[8];

@@ -39,67 +39,102 @@ __device__ __forceinline__ float dot8(const uint4& xv, const uint4& av, float ac
   return acc;
 }
 
+#ifdef EPILORA_GEMM_TRACE
+// tuning builds only: per launch (round robin over 8), earliest entry,
+// earliest return from the dependency wait, latest quantizer exit, latest
+// rank-CTA exit
+static __device__ unsigned long long g_shrink_trace[8][4];
+int g_shrink_trace_launches = 0;
+#define SHRINK_TRACE_MIN(i) atomicMin(&g_shrink_trace[tslot][i], globaltimer_ns())
+#define SHRINK_TRACE_MAX(i) atomicMax(&g_shrink_trace[tslot][i], globaltimer_ns())
+#else
+#define SHRINK_TRACE_MIN(i) \
+  do {                      \
+  } while (0)
+#define SHRINK_TRACE_MAX(i) \
+  do {                      \
+  } while (0)
+#endif
+
 struct QuantSide {          // quantizer CTAs of the fused grid (fmt < 0: none)
   int fmt;
   uint8_t* Xq;
   float* x_scale;
   uint8_t* x_block_scale;
   const float* x_global_scale;
-  uint32_t* x_ready;
 };
 
+// grid (M, [parts quantizer CTAs +] (r / 4) * parts rank CTAs); CTA (t, y):
+// quantizer slice y of token t, or ranks 4 * (g % (r / 4)) .. + 3 of token t
+// over K slice g / (r / 4), g = y - parts. Slices are `kslice` elements
+// (a multiple of 256); partial sums go to S[part][t][:].
 __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bfloat16* __restrict__ X, int K,
                                                                     int ldx, const __nv_bfloat16* __restrict__ A,
                                                                     int L, int r, const int32_t* __restrict__ idx,
                                                                     const uint8_t* __restrict__ mask,
                                                                     float* __restrict__ S, int* status,
-                                                                    QuantSide qs) {
-  // When this grid is itself a programmatic dependent (of the previous layer
-  // call on the stream) its CTAs are already resident: wait here for that
-  // kernel's completion; x and the workspace are only valid from now on
-  // (no-op for an ordinary launch). Then let the dependent GEMM start
-  // streaming its weights; it waits for this grid's completion only before
-  // its epilogue. Waiting first keeps consecutive calls ordered, so calls may
-  // share a workspace.
-  pdl_wait_primary();
+                                                                    QuantSide qs, int parts, int kslice, int tslot) {
+  // Let the dependent GEMM launch at once: before it reads anything this grid
+  // writes it waits for this grid's completion, and until then it only
+  // streams weights. Then, when this grid is itself a programmatic dependent
+  // (of the previous call's GEMM), wait for that grid's completion: x, idx,
+  // mask and the workspace are only valid from here on (no-op for an
+  // ordinary launch).
+  if (threadIdx.x == 0) SHRINK_TRACE_MIN(0);
   pdl_allow_dependents();
+  pdl_wait_primary();
+  if (threadIdx.x == 0) SHRINK_TRACE_MIN(1);
   __shared__ float red[kShrinkThreads / 32][kRanksPerCta];
 
   const size_t t = blockIdx.x;
   int gy = static_cast<int>(blockIdx.y);
   if (qs.fmt >= 0) {
-    if (gy == 0) {
-      // quantizer CTA of token t
+    if (gy < parts) {
+      // quantizer CTA: slice gy of token t
       const __nv_bfloat16* xrow = X + t * static_cast<size_t>(ldx);
+      const int k0 = gy * kslice;
+      const int k1 = min(K, k0 + kslice);
       if (qs.fmt == EPILORA_FMT_FP8_E4M3) {
-        quant_row_fp8<kShrinkQuantChunks>(xrow, K, qs.Xq + t * static_cast<size_t>(K), qs.x_scale + t, &red[0][0]);
+        if (parts == 1) {
+          quant_row_fp8<kShrinkQuantChunks>(xrow, K, qs.Xq + t * static_cast<size_t>(K), qs.x_scale + t,
+                                            &red[0][0]);
+        } else {
+          // every slice CTA takes the whole row's amax (the same exact max)
+          const float amax = row_amax_bf16(xrow, K, &red[0][0]);
+          const float sc = __fdiv_rn(fmaxf(amax, kAmaxFloor), kE4M3Max);
+          if (gy == 0 && threadIdx.x == 0) qs.x_scale[t] = sc;
+          if (k0 < k1) quant_slice_fp8(xrow, k0, k1, qs.Xq + t * static_cast<size_t>(K), sc);
+        }
       } else {
         const bool ok = quant_row_nvfp4(xrow, K, qs.Xq + t * static_cast<size_t>(K / 2),
                                         qs.x_block_scale + t * static_cast<size_t>(K / kNvfp4Block),
-                                        *qs.x_global_scale);
-        if (!ok && threadIdx.x == 0) record_status(status, EPILORA_ERR_INVALID_ARG);
+                                        *qs.x_global_scale, k0 / kNvfp4Block, k1 / kNvfp4Block);
+        if (!ok && gy == 0 && threadIdx.x == 0) record_status(status, EPILORA_ERR_INVALID_ARG);
       }
-      fence_proxy_async_global();   // the GEMM reads these codes with TMA (async proxy)
-      __threadfence();              // this thread's codes are visible GPU-wide ...
       __syncthreads();
-      if (threadIdx.x == 0) atomicAdd(qs.x_ready, 1u);   // ... before the row counts as ready
+      if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
       return;
     }
-    gy -= 1;
+    gy -= parts;
   }
 
-  const int j0 = gy * kRanksPerCta;
+  const int groups = r / kRanksPerCta;
+  if (groups == 0) return;
+  const int part = gy / groups;
+  const int j0 = (gy - part * groups) * kRanksPerCta;
   const int l = idx[t];
   bool act = (l >= 0) && (mask == nullptr || mask[t] != 0);
   if (l >= L) {
     if (gy == 0 && threadIdx.x == 0) record_status(status, EPILORA_ERR_INVALID_ARG);
     act = false;
   }
-  float* srow = S + t * static_cast<size_t>(r) + j0;
+  float* srow = S + (static_cast<size_t>(part) * gridDim.x + t) * static_cast<size_t>(r) + j0;
   if (!act) {
     if (threadIdx.x < kRanksPerCta) srow[threadIdx.x] = 0.0f;
     return;
   }
+  const int c0 = part * kslice / 8;
+  const int c1 = min(K, (part + 1) * kslice) / 8;
   const int nch = K / 8;
   const uint4* xr = reinterpret_cast<const uint4*>(X + t * static_cast<size_t>(ldx));
   const uint4* ar = reinterpret_cast<const uint4*>(A + (static_cast<size_t>(l) * r + j0) * static_cast<size_t>(K));
@@ -109,7 +144,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   for (int j = 0; j < kRanksPerCta; ++j) acc[j] = 0.0f;
 
 #pragma unroll 2
-  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+  for (int c = c0 + static_cast<int>(threadIdx.x); c < c1; c += blockDim.x) {
     const uint4 xv = __ldg(xr + c);
     uint4 av[kRanksPerCta];
 #pragma unroll
@@ -128,41 +163,80 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   }
   __syncthreads();
   if (threadIdx.x < kRanksPerCta) {
-    float s = 0.0f;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) s += red[w][threadIdx.x];
-    srow[threadIdx.x] = s;
+    float sum = 0.0f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) sum += red[w][threadIdx.x];
+    srow[threadIdx.x] = sum;
+    if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
   }
+}
+
+constexpr int kShrinkSliceTarget = 4096;   // elements of K per slice when splitting
+constexpr int kShrinkMaxParts = 8;
+
+int kslice_for(int K, int parts) {
+  const int per = (K + parts - 1) / parts;
+  return (per + 255) / 256 * 256;
 }
 
 int shrink_carveout_done[64] = {0};
 
+int trace_slot_next() {
+#ifdef EPILORA_GEMM_TRACE
+  return g_shrink_trace_launches++ % 8;
+#else
+  return 0;
+#endif
+}
+
 }  // namespace
+
+int shrink_parts_max(int K) {
+  const int p = (K + kShrinkSliceTarget - 1) / kShrinkSliceTarget;
+  return p < 1 ? 1 : p > kShrinkMaxParts ? kShrinkMaxParts : p;
+}
+
+int shrink_parts(int M, int K, int r) {
+  // split K only while the grid stays small (decode): a token's chain of
+  // dependent loads then shortens without adding a wave of CTAs
+  if (M > 32) return 1;
+  const int per_part = M * (r / kRanksPerCta + 1);
+  int cap = num_sms() / (per_part > 0 ? per_part : 1);
+  if (cap < 1) cap = 1;
+  int p = shrink_parts_max(K);
+  if (p > cap) p = cap;
+  // every slice non-empty
+  while (p > 1 && kslice_for(K, p) * (p - 1) >= K) --p;
+  return p;
+}
 
 int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
                   const uint8_t* mask, float* S, int* status_dev, cudaStream_t stream) {
   if (M == 0) return EPILORA_OK;
   if (prefer_max_shared(reinterpret_cast<const void*>(shrink_kernel), shrink_carveout_done) != EPILORA_OK)
     return EPILORA_ERR_CUDA;
-  QuantSide qs{-1, nullptr, nullptr, nullptr, nullptr, nullptr};
+  QuantSide qs{-1, nullptr, nullptr, nullptr, nullptr};
   dim3 grid(M, r / kRanksPerCta);
   shrink_kernel<<<grid, kShrinkThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), K, ldx,
                                                       static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S,
-                                                      status_dev, qs);
+                                                      status_dev, qs, 1, K, trace_slot_next());
   return cudaGetLastError() == cudaSuccess ? EPILORA_OK : EPILORA_ERR_CUDA;
 }
 
 int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
-                        const uint8_t* mask, float* S, int fmt, void* Xq, float* x_scale, uint8_t* x_block_scale,
-                        const float* x_global_scale, uint32_t* x_ready, int* status_dev, cudaStream_t stream) {
+                        const uint8_t* mask, float* S, int s_parts, int fmt, void* Xq, float* x_scale,
+                        uint8_t* x_block_scale, const float* x_global_scale, int* status_dev, cudaStream_t stream) {
   if (M == 0) return EPILORA_OK;
+  if (s_parts < 1 || s_parts > shrink_parts_max(K) || (s_parts > 1 && kslice_for(K, s_parts) * (s_parts - 1) >= K))
+    return EPILORA_ERR_INVALID_ARG;
   if (prefer_max_shared(reinterpret_cast<const void*>(shrink_kernel), shrink_carveout_done) != EPILORA_OK)
     return EPILORA_ERR_CUDA;
-  QuantSide qs{fmt, static_cast<uint8_t*>(Xq), x_scale, x_block_scale, x_global_scale, x_ready};
+  QuantSide qs{fmt, static_cast<uint8_t*>(Xq), x_scale, x_block_scale, x_global_scale};
+  const int kslice = s_parts == 1 ? K : kslice_for(K, s_parts);
   // launched as a programmatic dependent of whatever precedes it on the
   // stream: its CTAs become resident early and wait (griddepcontrol.wait)
   // for that kernel's completion before touching x or the workspace
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(M, r / kRanksPerCta + 1);
+  cfg.gridDim = dim3(M, s_parts + (r / kRanksPerCta) * s_parts);
   cfg.blockDim = dim3(kShrinkThreads, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -171,9 +245,27 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, shrink_kernel, static_cast<const __nv_bfloat16*>(X), K, ldx,
-                         static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S, status_dev, qs) != cudaSuccess)
+                         static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S, status_dev, qs, s_parts,
+                         kslice, trace_slot_next()) != cudaSuccess)
     return EPILORA_ERR_CUDA;
   return EPILORA_OK;
 }
 
 }  // namespace epi
+
+#ifdef EPILORA_GEMM_TRACE
+// tuning builds only: copy (and reset) the shrink launches' timestamps
+extern "C" EPILORA_API int epilora_debug_shrink_trace(void* host_out, int clear) {
+  if (cudaMemcpyFromSymbol(host_out, epi::g_shrink_trace, sizeof(epi::g_shrink_trace)) != cudaSuccess) return -3;
+  if (clear) {
+    static unsigned long long init[8][4];
+    for (auto& row : init) {
+      row[0] = row[1] = ~0ull;
+      row[2] = row[3] = 0ull;
+    }
+    if (cudaMemcpyToSymbol(epi::g_shrink_trace, init, sizeof(init)) != cudaSuccess) return -3;
+    epi::g_shrink_trace_launches = 0;
+  }
+  return 0;
+}
+#endif

@@ -93,8 +93,7 @@ class LayerWorkspace:
     def get(self, fmt, M, K, r) -> torch.Tensor:
         need = E.epilora_workspace_bytes(fmt, M, K, r)
         if self.buf.numel() < need:
-            # zero-filled: the leading counter block must start at zero
-            self.buf = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
+            self.buf = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
         return self.buf
 
 

@@ -147,9 +147,12 @@ def test_permutation_and_determinism(fmt):
 
 
 @pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
-def test_adapter_contribution_with_zero_base(fmt):
+@pytest.mark.parametrize("M,K,N,L,r", [(16, 1024, 512, 4, 64),
+                                       (2, 14336, 256, 2, 64),     # shrink split over 4 K slices
+                                       (1, 8192, 256, 1, 128)])    # 2 K slices, rank 128
+def test_adapter_contribution_with_zero_base(fmt, M, K, N, L, r):
     """All-zero weights: Y is bf16 of the adapter term alone."""
-    y, ref, _, _ = run_case(fmt, 16, 1024, 512, 4, 64, seed=9, zero_w=True)
+    y, ref, _, _ = run_case(fmt, M, K, N, L, r, seed=9, zero_w=True)
     d = ref["delta"]
     assert np.linalg.norm(y - d) / np.linalg.norm(d) <= 1e-2
 
@@ -195,7 +198,8 @@ def test_back_to_back_calls_share_workspace_and_replay_in_a_graph(fmt):
     """Consecutive fused calls (each a programmatic dependent of the one
     before) that share one workspace, eagerly and captured in a CUDA graph,
     give bitwise the results of isolated calls."""
-    shapes = [(1, 4096, 1024, 1, 64), (3, 2048, 4096, 2, 16), (1, 4096, 6144, 1, 64), (17, 1024, 512, 4, 32)]
+    shapes = [(1, 4096, 1024, 1, 64), (3, 2048, 4096, 2, 16), (1, 14336, 1024, 1, 64), (1, 4096, 6144, 1, 64),
+              (17, 1024, 512, 4, 32)]
     cases = []
     for i, (M, K, N, L, r) in enumerate(shapes):
         p = make_projection(M, K, N, L, r, seed=40 + i)
