@@ -177,7 +177,7 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
 /*
  * Bytes of device workspace epilora_layer_forward needs for (fmt, M, K, r):
  * the quantized activations, their scales and S (r = 0: no adapters; for a
- * few tokens S is held as up to ceil(K / 4096) partial sums over K slices,
+ * few tokens S is held as up to ceil(K / 1024) partial sums over K slices,
  * capped at 8), each region 256-byte aligned. Returns 0 for M == 0 or
  * invalid arguments.
  */

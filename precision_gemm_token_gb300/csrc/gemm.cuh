@@ -49,6 +49,31 @@
 #include "common.cuh"
 #include "ptx.cuh"
 
+#ifndef EPILORA_GEMM_FUSED_MODE
+// fused call, order of the producer's first steps: 0 = weight stages and L2
+// prefetch, then wait for the shrink grid; 1 = wait first; 2 = weight stages,
+// wait, then L2 prefetch
+#define EPILORA_GEMM_FUSED_MODE 2
+#endif
+#ifndef EPILORA_GEMM_EARLY_TRIGGER
+#define EPILORA_GEMM_EARLY_TRIGGER 1  // release the next kernel on the stream after the main loop
+#endif
+#ifndef EPILORA_GEMM_SB_MIN_GROUPS
+// decode tiles with at least this many adapter groups stream their B slices
+// through the TMA ring (behind the weights) instead of loading B rows with
+// ordinary loads, which queue behind the weight stream
+#define EPILORA_GEMM_SB_MIN_GROUPS 1
+#endif
+#ifndef EPILORA_GEMM_PREWAIT_STAGES
+#define EPILORA_GEMM_PREWAIT_STAGES 16  // weight stages a fused call issues before its wait
+#endif
+#ifndef EPILORA_GEMM_B_L2
+#define EPILORA_GEMM_B_L2 0             // prefetch streamed B slices into L2 after set-up
+#endif
+#ifndef EPILORA_GEMM_L2_AHEAD_MB
+#define EPILORA_GEMM_L2_AHEAD_MB 32  // weight bytes a fused call may prefetch into L2 after its wait
+#endif
+
 namespace epi {
 
 constexpr int kGemmThreads = 192;
@@ -94,6 +119,7 @@ struct GemmParams {
   int b_group_bytes;  // ring bytes of one group's boxes (1024-byte aligned)
   int b_groups_per_slot;
   int trace_slot;     // tuning builds only: which trace buffer this launch fills
+  int l2_ahead;       // fused call: weight stages past the ring to prefetch into L2 while waiting
 };
 
 template <int FMT, int BT, int KA>
@@ -150,7 +176,7 @@ __host__ __device__ constexpr int gemm_decode_bytes(int BT, int r, int ks) {
 #ifdef EPILORA_GEMM_TRACE
 constexpr int kTraceSlots = 8;       // consecutive launches, round robin
 constexpr int kTraceCtas = 2048;
-static __device__ unsigned long long g_gemm_trace[kTraceSlots][kTraceCtas][8];
+static __device__ unsigned long long g_gemm_trace[kTraceSlots][kTraceCtas][12];
 inline int& gemm_trace_launches() {
   static int n = 0;
   return n;
@@ -165,6 +191,12 @@ inline int& gemm_trace_launches() {
   do {                         \
   } while (0)
 #endif
+// timestamp taken once `dep` is available (tuning builds)
+#define EPI_TRACE_AFTER(slot, dep)                      \
+  do {                                                  \
+    asm volatile("" ::"f"(static_cast<float>(dep)));    \
+    EPI_TRACE(slot, globaltimer_ns());                  \
+  } while (0)
 
 // Named barrier of the epilogue warps that also ORs a flag over them.
 __device__ __forceinline__ bool epi_bar_any(bool v) {
@@ -208,7 +240,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(misc);
   uint64_t* empty_bar = full_bar + stages;
   uint64_t* acc_bar = empty_bar + stages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  uint64_t* meta_bar = acc_bar + 1;           // token metadata and adapter groups are in shared memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* ngroups_s = reinterpret_cast<int*>(tmem_slot + 2);
   float* meta_sx = reinterpret_cast<float*>(tmem_slot + 4);
@@ -278,15 +311,39 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(acc_bar, 1);
+    mbar_init(meta_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     // the ring starts empty: stream weights into it before anything else
-    for (int i = 0; i < prologue; ++i) issue_w(i, i);
-    if (p.fused) {
-      // the shrink grid quantizes the activations: its completion (and that
-      // of everything before it) makes them visible
+    auto l2_ahead = [&]() {
+      // the next weight stages go to L2 now and come back from there later
+      const int ahead_end = min(nkb, prologue + p.l2_ahead);
+      for (int i = prologue; i < ahead_end; ++i) {
+        const int kb = stage_kb(i);
+#pragma unroll
+        for (int a = 0; a < KA; ++a) tma_prefetch_l2_2d(&p.tmW, (kb * KA + a) * kAtomBytes, n0);
+        if (C::kFP4) tma_prefetch_l2_2d(&p.tmSW, kb * C::kSfRow, n0);
+      }
+    };
+    if (p.fused && EPILORA_GEMM_FUSED_MODE == 1) {
       pdl_wait_primary();
       fence_proxy_async_global();
+    }
+    // before the wait only the first EPILORA_GEMM_PREWAIT_STAGES stages (a
+    // deep queue of weight reads would delay the shrink grid's own loads)
+    const int prewait = p.fused && EPILORA_GEMM_FUSED_MODE != 1 ? min(prologue, EPILORA_GEMM_PREWAIT_STAGES)
+                                                                  : prologue;
+    for (int i = 0; i < prewait; ++i) issue_w(i, i);
+    if (p.fused) {
+      if (EPILORA_GEMM_FUSED_MODE == 0) l2_ahead();
+      if (EPILORA_GEMM_FUSED_MODE != 1) {
+        // the shrink grid quantizes the activations: its completion (and
+        // that of everything before it) makes them visible
+        pdl_wait_primary();
+        fence_proxy_async_global();
+      }
+      for (int i = prewait; i < prologue; ++i) issue_w(i, i);
+      if (EPILORA_GEMM_FUSED_MODE != 0) l2_ahead();
     }
     for (int i = 0; i < prologue; ++i) issue_x(i, i);
   }
@@ -294,10 +351,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 2) {
-    // token metadata (its loads overlap the first weight loads); in the fused
-    // call it is read once the shrink grid has completed
-    if (p.fused) pdl_wait_primary();
+  // Token metadata of the tile (scales, adapter slots) and, for decode tiles,
+  // the adapter groups: by the four epilogue warps. In the fused call it is
+  // read in the main-loop phase, once the shrink grid has completed (set-up
+  // then needs no global loads); otherwise during set-up.
+  auto build_meta = [&]() {
     for (int i = et; i < BT; i += 128) {
       const int t = t0 + i;
       float sx = 0.0f;
@@ -352,7 +410,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     } else if (et == 0) {
       *ngroups_s = 0;
     }
-  }
+    asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");   // groups visible to all four warps
+  };
+  if (warp >= 2 && !p.fused) build_meta();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -361,12 +421,20 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   // every CTA of the cluster has started once this phase completes (its wait
   // comes before the first store into a peer's shared memory)
   if (ks > 1) cluster_arrive_relaxed();
-  // stream the tile's B slices through the ring (decode tiles, >= 2 groups)
-  const int ngroups = *ngroups_s;
-  const bool sb = C::kDecode && p.stream_b && ngroups >= 2 && p.S != nullptr;
+  // Decode tiles stream their B slices through the ring, behind the weights.
+  // The group count is known to the epilogue warps once they have built the
+  // metadata, and to the producer once meta_bar has completed.
+  int ngroups = 0;
+  bool sb = false;
   const int gps = p.b_groups_per_slot;
-  const int n_bslots = sb ? (ngroups + gps - 1) / gps : 0;    // ring loads carrying B slices
-  const int n_loads = nkb + n_bslots;
+  int n_bslots = 0;       // ring loads carrying B slices
+  int n_loads = nkb;
+  auto set_groups = [&]() {
+    ngroups = *ngroups_s;
+    sb = C::kDecode && p.stream_b && ngroups >= EPILORA_GEMM_SB_MIN_GROUPS && p.S != nullptr;
+    n_bslots = sb ? (ngroups + gps - 1) / gps : 0;
+    n_loads = nkb + n_bslots;
+  };
 
   // epilogue state carried from the main-loop phase into the epilogue phase
   int cached_key = -1;
@@ -380,7 +448,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
 #pragma unroll
     for (int c = 0; c < kMaxRank / 8; ++c) {
       if (c < p.r / 8) {
-        const uint4 v = __ldg(bsrc + c);
+        const uint4 v = ldg_nc_v4_now(bsrc + c);
         brow[4 * c + 0] = v.x;
         brow[4 * c + 1] = v.y;
         brow[4 * c + 2] = v.z;
@@ -440,6 +508,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       cluster_arrive();
     }
     if (lane == 0) {
+      if (!stop && !mbar_wait_bounded(meta_bar, 0, kWaitLimitNs)) {
+        *abort_flag = 1;
+        record_status(p.status, EPILORA_ERR_TIMEOUT);
+        stop = true;
+      }
+      if (!stop) set_groups();
       for (int i = (prologue > nkb ? prologue : nkb); i < n_loads && !stop; ++i) produce(i);
       if (*abort_flag) {
         // do not leave with copies in flight: wait for every issued fill
@@ -553,6 +627,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     }
   } else {
     // ===== epilogue warps, main-loop phase =====
+    if (p.fused) {
+      // the shrink grid (quantized activations, scales, S) has completed
+      pdl_wait_primary();
+      build_meta();
+    }
+    set_groups();
+    if (et == 0) mbar_arrive(meta_bar);   // the producer may now stream B slices
     if (p.S != nullptr && !sb) {
       // L2 prefetch of the tile's B slices, first B row into registers
       const int rows = min(row_hi, p.N - n0) - row_lo;
@@ -595,7 +676,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     // loaded while the main loop runs
     if (!C::kFP4) {
       const int mrow = ks == 1 ? (warp & 3) * 32 + lane : row_lo + (R > 0 ? et % R : 0);
-      sw_pre = n0 + mrow < p.N ? __ldg(p.w_scale + n0 + mrow) : 0.0f;
+      sw_pre = n0 + mrow < p.N ? ldg_nc_f32_now(p.w_scale + n0 + mrow) : 0.0f;
     } else {
       alpha_pre = 1.0f / (*p.x_gs * *p.w_gs);
     }
@@ -636,7 +717,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   // The main loop is done: the next kernel on the stream (the next layer
   // call's shrink grid) may become resident now; it waits for this grid's
   // completion before it reads anything this grid writes.
-  pdl_allow_dependents();
+  if (EPILORA_GEMM_EARLY_TRIGGER) pdl_allow_dependents();
 
   // ---------------------------------------------------------------- epilogue
   const float alpha = alpha_pre;
@@ -651,14 +732,18 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     const int t = t0 + tl;
     if (n >= p.N || t >= p.M) return;
     float y = base_value(mm, tl, acc, sw);
+    if (et == 0 && tl == 0) EPI_TRACE_AFTER(8, y);
     const int l = meta_idx[tl];
     if (l >= 0) {
       if (l * kTileN + mm != cached_key) load_brow(l, mm);
+      if (et == 0 && tl == 0) EPI_TRACE_AFTER(9, __uint_as_float(brow[0] | brow[31]));
       const float4* srow = C::kDecode ? reinterpret_cast<const float4*>(s_stage + tl * p.r)
                                       : reinterpret_cast<const float4*>(p.S + static_cast<size_t>(t) * p.r);
       y += dot_srow_brow(srow, brow, p.r, C::kDecode);
     }
+    if (et == 0 && tl == 0) EPI_TRACE_AFTER(10, y);
     p.Y[static_cast<size_t>(t) * p.ldy + n] = __float2bfloat16_rn(y);
+    if (et == 0 && tl == 0) EPI_TRACE(7, globaltimer_ns());
   };
 
   if (ks > 1 && warp >= 2) {
@@ -667,10 +752,16 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     cluster_arrive();
     cluster_wait();
   }
+#ifdef EPILORA_GEMM_TRACE
+  long long epi_clk0 = 0;
+#endif
   // the 4 epilogue warps agree on whether to produce output (the sections
   // below contain their named barrier, which all four must reach)
   if (warp >= 2 && !epi_bar_any(*abort_flag != 0)) {
     if (et == 0) EPI_TRACE(5, globaltimer_ns());
+#ifdef EPILORA_GEMM_TRACE
+    epi_clk0 = clock64();
+#endif
     const float* red = reinterpret_cast<const float*>(red_buf);
     if (sb) {
       // ---- streamed-B epilogue (decode tile with >= 2 adapter groups) ----
@@ -769,8 +860,21 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         uint32_t v[16];
         tmem_ld_32x32b_x16(lane_base + c * 16, v);
         tmem_ld_wait();
+        if (C::kDecode) {
+          // valid token columns to this thread's row of the output tile;
+          // only they are finished below (a loop with a run-time bound, so
+          // that no work is spent on the tile's empty columns)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) finish(m, c * 16 + j, __uint_as_float(v[j]), sw);
+          for (int j = 0; j < 16; ++j)
+            if (c * 16 + j < tv) y_tile[(c * 16 + j) * RR + m] = __uint_as_float(v[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) finish(m, c * 16 + j, __uint_as_float(v[j]), sw);
+        }
+      }
+      if (C::kDecode) {
+#pragma unroll 1
+        for (int tl = 0; tl < tv; ++tl) finish(m, tl, y_tile[tl * RR + m], sw);
       }
     } else {
 #pragma unroll 1
@@ -792,7 +896,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     unsigned smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     EPI_TRACE(6, globaltimer_ns());
-    EPI_TRACE(7, smid);
+    (void)smid;
+#ifdef EPILORA_GEMM_TRACE
+    if (!*abort_flag) EPI_TRACE(11, static_cast<unsigned long long>(clock64() - epi_clk0));
+#endif
   }
   tc_fence_before();
   __syncthreads();
@@ -899,6 +1006,16 @@ int launch_gemm_tiled(const GemmArgs& a) {
   if (stages < 2) p.stream_b = 0;        // B slots need a ring of two or more
   if (stages < 1) stages = 1;
   p.stages = stages;
+  // fused call: prefetch into L2 (while the shrink grid runs) up to about
+  // EPILORA_GEMM_L2_AHEAD_MB of weight stages beyond the ring, over the grid
+  {
+    const long budget_bytes = static_cast<long>(EPILORA_GEMM_L2_AHEAD_MB) << 20;
+    const long per_stage_grid = ctas * static_cast<long>(C::kWBytes + C::kSfWRaw);
+    long ahead = per_stage_grid > 0 ? budget_bytes / per_stage_grid : 0;
+    const long left = per_cta - stages;
+    if (ahead > left) ahead = left;
+    p.l2_ahead = a.fused && ahead > 0 ? static_cast<int>(ahead) : 0;
+  }
   const int smem = gemm_smem_bytes(C::kStageBytes, stages, red) + dec;
   if (smem > 227 * 1024) return EPILORA_ERR_UNSUPPORTED;
 

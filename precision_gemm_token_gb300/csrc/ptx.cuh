@@ -87,6 +87,29 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Bring the box of a tiled tensor map at (x, y) into L2 (no shared memory
+// involved; x * element size is a multiple of 16 bytes at every call site).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+               : "memory");
+}
+
+// Read-only 16-byte load that the compiler keeps where it is written (it is
+// not sunk towards its first use): used to start loads early.
+__device__ __forceinline__ uint4 ldg_nc_v4_now(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ float ldg_nc_f32_now(const float* ptr) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+  return v;
+}
+
 // Bring [ptr, ptr + bytes) into L2 (bytes a multiple of 16, ptr 16-B aligned).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)

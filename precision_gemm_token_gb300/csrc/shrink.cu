@@ -64,6 +64,38 @@ struct QuantSide {          // quantizer CTAs of the fused grid (fmt < 0: none)
   const float* x_global_scale;
 };
 
+// Before the dependency wait: bring this CTA's inputs into L2 (its slice of
+// x, and for a rank CTA its A rows of the token's adapter) so that the loads
+// after the wait do not queue behind the weight stream of the GEMM that is
+// starting meanwhile. Only hints: the index read here may still change (the
+// previous kernel may write it); the loads after the wait re-read it.
+__device__ __forceinline__ void prefetch_inputs(const __nv_bfloat16* X, int K, int ldx, const __nv_bfloat16* A,
+                                                int L, int r, const int32_t* idx, int qparts, int kslice) {
+  const size_t t = blockIdx.x;
+  int gy = static_cast<int>(blockIdx.y);
+  const int parts = qparts > 0 ? qparts : 1;
+  if (qparts > 0 && gy < qparts) {
+    const int k0 = gy * kslice, k1 = min(K, k0 + kslice);
+    if (k1 > k0) prefetch_l2_bulk(X + t * static_cast<size_t>(ldx) + k0, static_cast<uint32_t>((k1 - k0) * 2));
+    return;
+  }
+  gy -= qparts;
+  const int groups = r / kRanksPerCta;
+  if (groups == 0) return;
+  const int part = gy / groups;
+  const int j0 = (gy - part * groups) * kRanksPerCta;
+  const int k0 = part * kslice, k1 = min(K, (part + 1) * kslice);
+  if (k1 <= k0) return;
+  int l;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(l) : "l"(idx + t));
+  if (l < 0 || l >= L) return;
+  prefetch_l2_bulk(X + t * static_cast<size_t>(ldx) + k0, static_cast<uint32_t>((k1 - k0) * 2));
+  for (int j = 0; j < kRanksPerCta; ++j)
+    prefetch_l2_bulk(A + (static_cast<size_t>(l) * r + j0 + j) * static_cast<size_t>(K) + k0,
+                     static_cast<uint32_t>((k1 - k0) * 2));
+  (void)parts;
+}
+
 // grid (M, [parts quantizer CTAs +] (r / 4) * parts rank CTAs); CTA (t, y):
 // quantizer slice y of token t, or ranks 4 * (g % (r / 4)) .. + 3 of token t
 // over K slice g / (r / 4), g = y - parts. Slices are `kslice` elements
@@ -81,6 +113,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   // mask and the workspace are only valid from here on (no-op for an
   // ordinary launch).
   if (threadIdx.x == 0) SHRINK_TRACE_MIN(0);
+  if (threadIdx.x == 0) prefetch_inputs(X, K, ldx, A, L, r, idx, qs.fmt >= 0 ? parts : 0, kslice);
   pdl_allow_dependents();
   pdl_wait_primary();
   if (threadIdx.x == 0) SHRINK_TRACE_MIN(1);
@@ -170,7 +203,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   }
 }
 
-constexpr int kShrinkSliceTarget = 4096;   // elements of K per slice when splitting
+constexpr int kShrinkSliceTarget = 1024;   // elements of K per slice when splitting
 constexpr int kShrinkMaxParts = 8;
 
 int kslice_for(int K, int parts) {

@@ -59,12 +59,13 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    # Xq, scales, then S with room for ceil(K / 4096) partial sums (at most 8)
+    # Xq, scales, then S with room for ceil(K / 1024) partial sums (at most 8)
     assert E.epilora_workspace_bytes(0, 4, 512, 16) == r256(4 * 512) + r256(16) + r256(4 * 16 * 4)
     assert E.epilora_workspace_bytes(1, 4, 512, 16) == r256(4 * 256) + r256(4 * 32) + r256(4 * 16 * 4)
     assert E.epilora_workspace_bytes(0, 4, 512, 0) == r256(4 * 512) + r256(16)
-    assert E.epilora_workspace_bytes(0, 2, 14336, 64) == r256(2 * 14336) + r256(8) + r256(2 * 64 * 4 * 4)
+    assert E.epilora_workspace_bytes(0, 2, 14336, 64) == r256(2 * 14336) + r256(8) + r256(2 * 64 * 4 * 8)
     assert E.epilora_workspace_bytes(0, 1, 40960, 16) == r256(40960) + r256(4) + r256(16 * 4 * 8)
+    assert E.epilora_workspace_bytes(0, 3, 4096, 32) == r256(3 * 4096) + r256(12) + r256(3 * 32 * 4 * 4)
     assert E.epilora_workspace_bytes(0, 0, 512, 16) == 0
     assert E.epilora_workspace_bytes(7, 4, 512, 16) == 0
 
