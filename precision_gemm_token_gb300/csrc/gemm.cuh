@@ -176,7 +176,7 @@ __host__ __device__ constexpr int gemm_decode_bytes(int BT, int r, int ks) {
 #ifdef EPILORA_GEMM_TRACE
 constexpr int kTraceSlots = 8;       // consecutive launches, round robin
 constexpr int kTraceCtas = 2048;
-static __device__ unsigned long long g_gemm_trace[kTraceSlots][kTraceCtas][12];
+static __device__ unsigned long long g_gemm_trace[kTraceSlots][kTraceCtas][16];
 inline int& gemm_trace_launches() {
   static int n = 0;
   return n;
@@ -226,6 +226,30 @@ __device__ __forceinline__ float dot_srow_brow(const float4* srow, const uint32_
     }
   }
   return d;
+}
+
+// S[t] . B_g[row] for a B row of NC 16-byte chunks held in a swizzled ring
+// box (chunk c in atom c >> cpa_log, at position (c & mask) ^ xr), S in
+// shared memory; loads independent, two accumulators.
+template <int NC>
+__device__ __forceinline__ float dot_b_row(const uint8_t* gb, int atom_stride, int cpa_log, int mask, int xr,
+                                           const float4* srow) {
+  float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(gb + (c >> cpa_log) * atom_stride + (((c & mask) ^ xr) << 4));
+    const float4 s0 = srow[2 * c], s1 = srow[2 * c + 1];
+    float& d = (c & 1) ? d1 : d0;
+    d = fmaf(s0.x, bf16_lo(v.x), d);
+    d = fmaf(s0.y, bf16_hi(v.x), d);
+    d = fmaf(s0.z, bf16_lo(v.y), d);
+    d = fmaf(s0.w, bf16_hi(v.y), d);
+    d = fmaf(s1.x, bf16_lo(v.z), d);
+    d = fmaf(s1.y, bf16_hi(v.z), d);
+    d = fmaf(s1.z, bf16_lo(v.w), d);
+    d = fmaf(s1.w, bf16_hi(v.w), d);
+  }
+  return d0 + d1;
 }
 
 template <int FMT, int BT, int KA>
@@ -514,6 +538,16 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         stop = true;
       }
       if (!stop) set_groups();
+      EPI_TRACE(15, globaltimer_ns());
+      if (EPILORA_GEMM_B_L2 == 2 && sb && !stop) {
+        // the weights are all requested: the B slices go to L2 behind them,
+        // so that their ring loads below find them there
+        const int rows = min(row_hi, p.N - n0) - row_lo;
+        if (rows > 0)
+          for (int g = 0; g < ngroups; ++g)
+            prefetch_l2_bulk(p.B + (static_cast<size_t>(g_adapter[g]) * p.N + n0 + row_lo) * p.r,
+                             static_cast<uint32_t>(rows * p.r * 2));
+      }
       for (int i = (prologue > nkb ? prologue : nkb); i < n_loads && !stop; ++i) produce(i);
       if (*abort_flag) {
         // do not leave with copies in flight: wait for every issued fill
@@ -801,6 +835,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       const int sw_span = p.b_box_bytes;                   // 32, 64 or 128: swizzle span
       const int sw_mask = sw_span / 16 - 1;
       const int sw_shift = sw_span == 128 ? 0 : sw_span == 64 ? 1 : 2;   // row >> shift = (row * span) / 128
+      const int cpa_log = 3 - sw_shift;                    // log2 of the 16-byte chunks per atom
+      const int nchunk = p.r / 8;                          // 16-byte chunks of a B row
+      const int atom_stride = RR * sw_span;                // bytes between a group's atoms
       for (int j = 0; j < n_bslots; ++j) {
         const int li = nkb + j;
         const int s = li % stages;
@@ -808,41 +845,52 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         // every thread waits itself (TMA data visibility); the outcome is
         // made uniform over the 4 epilogue warps before anyone leaves
         const bool late = !mbar_wait_bounded(&full_bar[s], ph, kWaitLimitNs);
+        if (et == 0 && j == 0) EPI_TRACE(12, globaltimer_ns());
+        if (et == 0 && j == n_bslots - 1) EPI_TRACE(13, globaltimer_ns());
+#ifdef EPILORA_GEMM_TRACE
+        const long long ck0 = clock64();
+#endif
         if (epi_bar_any(late)) {
           *abort_flag = 1;
           record_status(p.status, EPILORA_ERR_TIMEOUT);
           break;
         }
+#ifdef EPILORA_GEMM_TRACE
+        const long long ck1 = clock64();
+#endif
         const uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
         // y[t][i] += S[t] . B_g[row i], B's row read 16 bytes at a time from
         // the swizzled box (chunk c of row i lives at chunk c ^ f(i))
-        const int chunks_per_atom = sw_span / 16;
         const int xr = (i >> sw_shift) & sw_mask;
         const int g0 = j * gps;
         const int g1 = min(ngroups, g0 + gps);
         for (int k = g_start[g0] + tsl; k < g_start[g1]; k += tstep) {
           const int tl = g_order[k];
-          const uint8_t* gb = st + (g_of[k] - g0) * p.b_group_bytes;
+          const uint8_t* gb = st + (g_of[k] - g0) * p.b_group_bytes + i * sw_span;
           const float4* srow = reinterpret_cast<const float4*>(s_stage + tl * p.r);
-          float d = 0.0f;
-          for (int c = 0; c < p.r / 8; ++c) {
-            const int a = c / chunks_per_atom, cc = c % chunks_per_atom;
-            const uint4 v = *reinterpret_cast<const uint4*>(gb + a * RR * sw_span + i * sw_span + ((cc ^ xr) * 16));
-            const float4 s0 = srow[2 * c], s1 = srow[2 * c + 1];
-            d = fmaf(s0.x, bf16_lo(v.x), d);
-            d = fmaf(s0.y, bf16_hi(v.x), d);
-            d = fmaf(s0.z, bf16_lo(v.y), d);
-            d = fmaf(s0.w, bf16_hi(v.y), d);
-            d = fmaf(s1.x, bf16_lo(v.z), d);
-            d = fmaf(s1.y, bf16_hi(v.z), d);
-            d = fmaf(s1.z, bf16_lo(v.w), d);
-            d = fmaf(s1.w, bf16_hi(v.w), d);
+          float d;
+          switch (nchunk) {   // rank 16 / 32 / 64 / 128: a loop without guards per chunk
+            case 2: d = dot_b_row<2>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
+            case 4: d = dot_b_row<4>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
+            case 8: d = dot_b_row<8>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
+            default: d = dot_b_row<16>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
           }
           y_tile[tl * RR + i] += d;
         }
+#ifdef EPILORA_GEMM_TRACE
+        const long long ck2 = clock64();
+#endif
         asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
+#ifdef EPILORA_GEMM_TRACE
+        if (et == 0 && j == 0) {
+          EPI_TRACE(8, static_cast<unsigned long long>(ck1 - ck0));
+          EPI_TRACE(9, static_cast<unsigned long long>(ck2 - ck1));
+          EPI_TRACE(10, static_cast<unsigned long long>(clock64() - ck2));
+        }
+#endif
         if (et == 0) mbar_arrive(&empty_bar[s]);          // slot free for the producer
       }
+      if (et == 0) EPI_TRACE(14, globaltimer_ns());
       // 3) the output tile
       for (int e = et; e < R * tv; e += 128) {
         const int ii = e % R, tl = e / R;

@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
                                                                     int L, int r, const int32_t* __restrict__ idx,
                                                                     const uint8_t* __restrict__ mask,
                                                                     float* __restrict__ S, int* status,
-                                                                    QuantSide qs, int parts, int kslice, int tslot) {
+                                                                    QuantSide qs, int parts, int kslice, int tslot,
+                                                                    int early_release) {
   // Let the dependent GEMM launch at once: before it reads anything this grid
   // writes it waits for this grid's completion, and until then it only
   // streams weights. Then, when this grid is itself a programmatic dependent
@@ -114,7 +115,10 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   // ordinary launch).
   if (threadIdx.x == 0) SHRINK_TRACE_MIN(0);
   if (threadIdx.x == 0) prefetch_inputs(X, K, ldx, A, L, r, idx, qs.fmt >= 0 ? parts : 0, kslice);
-  pdl_allow_dependents();
+  // A grid that fits beside the GEMM's CTAs releases it at once; a larger one
+  // keeps the SMs to itself and releases it as its CTAs finish (its A stream
+  // is then not starved of CTA slots by a GEMM still waiting for it).
+  if (early_release) pdl_allow_dependents();
   pdl_wait_primary();
   if (threadIdx.x == 0) SHRINK_TRACE_MIN(1);
   __shared__ float red[kShrinkThreads / 32][kRanksPerCta];
@@ -233,10 +237,15 @@ int shrink_parts(int M, int K, int r) {
   // dependent loads then shortens without adding a wave of CTAs
   if (M > 32) return 1;
   const int per_part = M * (r / kRanksPerCta + 1);
-  int cap = num_sms() / (per_part > 0 ? per_part : 1);
-  if (cap < 1) cap = 1;
   int p = shrink_parts_max(K);
-  if (p > cap) p = cap;
+  if (per_part <= num_sms()) {
+    // small grid, released at once and run beside the GEMM's CTAs: at most
+    // one slice set per SM
+    const int cap = num_sms() / per_part;
+    if (p > cap) p = cap;
+  }
+  // (a larger grid runs before the GEMM's CTAs arrive: more, shorter CTAs
+  // keep more loads in flight)
   // every slice non-empty
   while (p > 1 && kslice_for(K, p) * (p - 1) >= K) --p;
   return p;
@@ -251,7 +260,7 @@ int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, in
   dim3 grid(M, r / kRanksPerCta);
   shrink_kernel<<<grid, kShrinkThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), K, ldx,
                                                       static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S,
-                                                      status_dev, qs, 1, K, trace_slot_next());
+                                                      status_dev, qs, 1, K, trace_slot_next(), 1);
   return cudaGetLastError() == cudaSuccess ? EPILORA_OK : EPILORA_ERR_CUDA;
 }
 
@@ -279,7 +288,8 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, shrink_kernel, static_cast<const __nv_bfloat16*>(X), K, ldx,
                          static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S, status_dev, qs, s_parts,
-                         kslice, trace_slot_next()) != cudaSuccess)
+                         kslice, trace_slot_next(),
+                         static_cast<int>(cfg.gridDim.x * cfg.gridDim.y) <= num_sms() ? 1 : 0) != cudaSuccess)
     return EPILORA_ERR_CUDA;
   return EPILORA_OK;
 }
