@@ -236,6 +236,8 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   }
   // S, or the partial sums of a shrink split over K slices
   bytes += round256(m * static_cast<size_t>(r) * 4 * static_cast<size_t>(r > 0 ? shrink_parts_max(K) : 1));
+  // more than one decode tile of tokens with adapters: the adapter-sorted row order
+  if (r > 0 && M > 32) bytes += round256(m * 4);
   return bytes;
 }
 
@@ -271,7 +273,12 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
     x_block_scale = ws + off;
     off += round256(m * k / 16);
   }
-  if (adapters) S = reinterpret_cast<float*>(ws + off);
+  int32_t* perm = nullptr;
+  if (adapters) {
+    S = reinterpret_cast<float*>(ws + off);
+    off += round256(m * static_cast<size_t>(r) * 4 * static_cast<size_t>(shrink_parts_max(K)));
+    if (M > 32) perm = reinterpret_cast<int32_t*>(ws + off);
+  }
 
   int rc = gemm_validate(fmt, M, N, K, Xq, x_scale, x_block_scale, x_global_scale, Wq, w_scale, w_block_scale,
                          w_global_scale, S, B, L, r, idx, Y, ldy);
@@ -286,7 +293,7 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int parts = adapters ? shrink_parts(M, K, r) : shrink_parts(M, K, 0);
   rc = launch_shrink_quant(X, M, K, ldx, A, adapters ? L : 1, adapters ? r : 0, idx, mask, S, parts, fmt, Xq,
-                           x_scale, x_block_scale, x_global_scale, status_dev, st);
+                           x_scale, x_block_scale, x_global_scale, perm, status_dev, st);
   if (rc != EPILORA_OK) return rc;
   GemmArgs a{};
   a.fmt = fmt;
@@ -314,6 +321,7 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
   a.stream = st;
   a.fused = 1;
   a.s_parts = parts;
+  a.perm = perm;
   return fmt == EPILORA_FMT_FP8_E4M3 ? launch_gemm_fp8(a) : launch_gemm_nvfp4(a);
 }
 

@@ -55,6 +55,9 @@ struct GemmArgs {
   // grid (launch_shrink_quant), S as s_parts partial arrays [s_parts][M][r]
   int fused = 0;
   int s_parts = 1;
+  // fused call, more than one decode tile of tokens: rows of Xq / x_scale /
+  // x_block_scale are in adapter-sorted order, perm[row] = token
+  const int32_t* perm = nullptr;
 };
 
 int launch_quant(int fmt, const void* X, int M, int K, int ldx, void* Xq, float* x_scale,
@@ -67,9 +70,13 @@ int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, in
 // sum in part order is S; s_parts == 1 gives S itself). Launched as a
 // programmatic dependent of the previous kernel on the stream: it releases its
 // own dependent at once and waits for that kernel before reading anything.
+// perm != nullptr (s_parts == 1 only): the quantized rows and their scales are
+// written in adapter-sorted order (key idx[t] if the token carries an adapter,
+// else L; ties by token), and perm[row] = token.
 int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
                         const uint8_t* mask, float* S, int s_parts, int fmt, void* Xq, float* x_scale,
-                        uint8_t* x_block_scale, const float* x_global_scale, int* status_dev, cudaStream_t stream);
+                        uint8_t* x_block_scale, const float* x_global_scale, int32_t* perm, int* status_dev,
+                        cudaStream_t stream);
 // Number of K slices launch_shrink_quant uses for (M, K, r) (1 when M > 32),
 // and the largest it can use for K (sizes the workspace).
 int shrink_parts(int M, int K, int r);

@@ -46,6 +46,8 @@
 // and MMA issuer (all 32 lanes re-lay NVFP4 scale factors), warps 2..5 =
 // epilogue (warp w reads TMEM lane quadrant w % 4).
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -105,6 +107,8 @@ struct GemmParams {
   // first and executes griddepcontrol.wait before the first activation load,
   // the epilogue warps before reading any token metadata.
   int fused;
+  const int32_t* perm;  // rows of Xq / x_scale are in this token order (perm[row] = token), or identity if null
+  int stage_s;          // non-decode tiles: S of the tile's tokens is staged in the ring after the main loop
   // S is the sum of s_parts partial arrays [s_parts][M][r] (split K of the
   // shrink), added in part order
   int s_parts;
@@ -212,20 +216,38 @@ __device__ __forceinline__ bool epi_bar_any(bool v) {
   return r != 0;
 }
 
+// S[t] . B[l, n] with the B row in registers: R4 float4 chunks of S (from
+// shared or global memory), no per-chunk guards, two accumulators.
+template <int R4, bool kSmem>
+__device__ __forceinline__ float dot_srow_brow_n(const float4* srow, const uint32_t (&brow)[kMaxRank / 2]) {
+  float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+  for (int c = 0; c < R4; ++c) {
+    const float4 s4 = kSmem ? srow[c] : __ldcg(srow + c);
+    float& d = (c & 1) ? d1 : d0;
+    d = fmaf(s4.x, bf16_lo(brow[2 * c]), d);
+    d = fmaf(s4.y, bf16_hi(brow[2 * c]), d);
+    d = fmaf(s4.z, bf16_lo(brow[2 * c + 1]), d);
+    d = fmaf(s4.w, bf16_hi(brow[2 * c + 1]), d);
+  }
+  return d0 + d1;
+}
 __device__ __forceinline__ float dot_srow_brow(const float4* srow, const uint32_t (&brow)[kMaxRank / 2], int r,
                                                bool srow_in_smem) {
-  float d = 0.0f;
-#pragma unroll
-  for (int c = 0; c < kMaxRank / 4; ++c) {
-    if (c < r / 4) {
-      const float4 s4 = srow_in_smem ? srow[c] : __ldcg(srow + c);
-      d = fmaf(s4.x, bf16_lo(brow[2 * c]), d);
-      d = fmaf(s4.y, bf16_hi(brow[2 * c]), d);
-      d = fmaf(s4.z, bf16_lo(brow[2 * c + 1]), d);
-      d = fmaf(s4.w, bf16_hi(brow[2 * c + 1]), d);
+  if (srow_in_smem) {
+    switch (r) {
+      case 16: return dot_srow_brow_n<4, true>(srow, brow);
+      case 32: return dot_srow_brow_n<8, true>(srow, brow);
+      case 64: return dot_srow_brow_n<16, true>(srow, brow);
+      default: return dot_srow_brow_n<32, true>(srow, brow);
     }
   }
-  return d;
+  switch (r) {
+    case 16: return dot_srow_brow_n<4, false>(srow, brow);
+    case 32: return dot_srow_brow_n<8, false>(srow, brow);
+    case 64: return dot_srow_brow_n<16, false>(srow, brow);
+    default: return dot_srow_brow_n<32, false>(srow, brow);
+  }
 }
 
 // S[t] . B_g[row] for a B row of NC 16-byte chunks held in a swizzled ring
@@ -270,6 +292,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   int* ngroups_s = reinterpret_cast<int*>(tmem_slot + 2);
   float* meta_sx = reinterpret_cast<float*>(tmem_slot + 4);
   int* meta_idx = reinterpret_cast<int*>(meta_sx + BT);       // adapter slot, -1 = none
+  int* meta_tok = meta_idx + BT;                               // token of each tile column (row of Y and S)
+  float* s_big = reinterpret_cast<float*>(smem);               // non-decode: S rows of the tile, after the main loop
   // decode region (BT <= kDecodeBT)
   const int RR = gemm_red_rows(ks);           // rows owned per rank (last rank: fewer)
   float* s_stage = reinterpret_cast<float*>(misc + kGemmMiscBytes);   // [token][r]
@@ -381,20 +405,23 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   // then needs no global loads); otherwise during set-up.
   auto build_meta = [&]() {
     for (int i = et; i < BT; i += 128) {
-      const int t = t0 + i;
+      const int row = t0 + i;             // row of the quantized activations
       float sx = 0.0f;
       int l = -1;
-      if (t < p.M) {
-        if (!C::kFP4) sx = p.x_scale[t];
+      int tok = row;
+      if (row < p.M) {
+        if (p.perm != nullptr) tok = p.perm[row];
+        if (!C::kFP4) sx = p.x_scale[row];
         if (p.S != nullptr) {
-          const int li = p.idx[t];
-          const bool on = li >= 0 && li < p.L && (p.mask == nullptr || p.mask[t] != 0);
+          const int li = p.idx[tok];
+          const bool on = li >= 0 && li < p.L && (p.mask == nullptr || p.mask[tok] != 0);
           if (li >= p.L) record_status(p.status, EPILORA_ERR_INVALID_ARG);
           l = on ? li : -1;
         }
       }
       meta_sx[i] = sx;
       meta_idx[i] = l;
+      meta_tok[i] = tok;
     }
     asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
     if (C::kDecode) {
@@ -746,6 +773,18 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         }
       }
     }
+    const bool all_ok = !epi_bar_any(!ok);    // uniform over the four warps (a barrier follows)
+    if (!C::kDecode && p.stage_s && all_ok) {
+      // every stage has been consumed: the ring now holds the S rows of this
+      // tile's tokens (one read of each from L2 instead of one per element)
+      const int n4 = p.r / 4;
+      float4* dst = reinterpret_cast<float4*>(s_big);
+      for (int k = et; k < tv * n4; k += 128) {
+        const int tl = k / n4;
+        dst[k] = __ldcg(reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r) + (k - tl * n4));
+      }
+      asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
+    }
   }
 
   // The main loop is done: the next kernel on the stream (the next layer
@@ -771,12 +810,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     if (l >= 0) {
       if (l * kTileN + mm != cached_key) load_brow(l, mm);
       if (et == 0 && tl == 0) EPI_TRACE_AFTER(9, __uint_as_float(brow[0] | brow[31]));
-      const float4* srow = C::kDecode ? reinterpret_cast<const float4*>(s_stage + tl * p.r)
-                                      : reinterpret_cast<const float4*>(p.S + static_cast<size_t>(t) * p.r);
-      y += dot_srow_brow(srow, brow, p.r, C::kDecode);
+      const bool s_smem = C::kDecode || p.stage_s;
+      const float4* srow =
+          C::kDecode ? reinterpret_cast<const float4*>(s_stage + tl * p.r)
+          : p.stage_s ? reinterpret_cast<const float4*>(s_big + tl * p.r)
+                      : reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r);
+      y += dot_srow_brow(srow, brow, p.r, s_smem);
     }
     if (et == 0 && tl == 0) EPI_TRACE_AFTER(10, y);
-    p.Y[static_cast<size_t>(t) * p.ldy + n] = __float2bfloat16_rn(y);
+    p.Y[static_cast<size_t>(meta_tok[tl]) * p.ldy + n] = __float2bfloat16_rn(y);
     if (et == 0 && tl == 0) EPI_TRACE(7, globaltimer_ns());
   };
 
@@ -895,7 +937,60 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       for (int e = et; e < R * tv; e += 128) {
         const int ii = e % R, tl = e / R;
         const int n = n0 + row_lo + ii;
-        if (n < p.N) p.Y[static_cast<size_t>(t0 + tl) * p.ldy + n] = __float2bfloat16_rn(y_tile[tl * RR + ii]);
+        if (n < p.N) p.Y[static_cast<size_t>(meta_tok[tl]) * p.ldy + n] = __float2bfloat16_rn(y_tile[tl * RR + ii]);
+      }
+    } else if (ks == 1 && !C::kDecode && p.S != nullptr) {
+      // wide tiles: this thread's weight row m over the tile's token columns
+      // in order. The row of B is reloaded only when the adapter changes
+      // (adapter-sorted tokens make that rare) and the next adapter's row is
+      // prefetched into L2 at each change; S comes from shared memory.
+      const int q = warp & 3;
+      const int m = q * 32 + lane;
+      const int n = n0 + m;
+      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const float sw = sw_pre;
+      auto run = [&](auto r4c) {
+        constexpr int R4 = decltype(r4c)::value;     // float4 chunks of an S row
+        int cur_l = -1;
+#pragma unroll 1
+        for (int c = 0; c < BT / 16; ++c) {
+          if (c * 16 >= tv) break;
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(lane_base + c * 16, v);
+          tmem_ld_wait();
+          if (n < p.N) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int tl = c * 16 + j;
+              if (tl < tv) {
+                float y = base_value(m, tl, __uint_as_float(v[j]), sw);
+                const int l = meta_idx[tl];
+                if (l >= 0) {
+                  if (l != cur_l) {
+                    load_brow(l, m);
+                    cur_l = l;
+                    int k = tl + 1;
+                    while (k < tv && (meta_idx[k] == l || meta_idx[k] < 0)) ++k;
+                    if (k < tv)
+                      prefetch_l2_bulk(p.B + (static_cast<size_t>(meta_idx[k]) * p.N + n) * p.r,
+                                       static_cast<uint32_t>(p.r * 2));
+                  }
+                  y += p.stage_s ? dot_srow_brow_n<R4, true>(reinterpret_cast<const float4*>(s_big + tl * p.r), brow)
+                                 : dot_srow_brow_n<R4, false>(
+                                       reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r),
+                                       brow);
+                }
+                p.Y[static_cast<size_t>(meta_tok[tl]) * p.ldy + n] = __float2bfloat16_rn(y);
+              }
+            }
+          }
+        }
+      };
+      switch (p.r) {
+        case 16: run(std::integral_constant<int, 4>{}); break;
+        case 32: run(std::integral_constant<int, 8>{}); break;
+        case 64: run(std::integral_constant<int, 16>{}); break;
+        default: run(std::integral_constant<int, 32>{}); break;
       }
     } else if (ks == 1) {
       const int q = warp & 3;
@@ -987,6 +1082,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   p.Y = static_cast<__nv_bfloat16*>(a.Y);
   p.status = a.status_dev;
   p.fused = a.fused;
+  p.perm = a.perm;
 #ifdef EPILORA_GEMM_TRACE
   p.trace_slot = gemm_trace_launches()++ % kTraceSlots;
 #endif
@@ -1044,6 +1140,9 @@ int launch_gemm_tiled(const GemmArgs& a) {
   }
 
   const long ctas = tiles * ks;
+  // a grid larger than the GPU keeps EPILORA_GEMM_RESIDENT CTAs per SM: one
+  // CTA's epilogue then runs while the other's main loop keeps the weight
+  // stream (decode) or the tensor pipe (wide tiles) busy
   const int budget = ctas > sms ? (227 * 1024) / EPILORA_GEMM_RESIDENT - 2048 : 200 * 1024;
   const int red = gemm_red_bytes<BT>(ks);
   const int dec = gemm_decode_bytes(BT, a.r, ks);
@@ -1053,6 +1152,18 @@ int launch_gemm_tiled(const GemmArgs& a) {
   if (stages > per_cta && !p.stream_b) stages = per_cta;     // no deeper than the K loop needs
   if (stages < 2) p.stream_b = 0;        // B slots need a ring of two or more
   if (stages < 1) stages = 1;
+  // non-decode tiles stage S of their tokens in the ring once the main loop
+  // is over (one fp32 row of r per token column); deepen the ring if needed
+  p.stage_s = 0;
+  if (!C::kDecode && a.S != nullptr) {
+    const int need = BT * a.r * 4;
+    int st_need = (need + C::kStageBytes - 1) / C::kStageBytes;
+    if (st_need < stages) st_need = stages;
+    if (gemm_smem_bytes(C::kStageBytes, st_need, red) + dec <= budget) {
+      stages = st_need;
+      p.stage_s = 1;
+    }
+  }
   p.stages = stages;
   // fused call: prefetch into L2 (while the shrink grid runs) up to about
   // EPILORA_GEMM_L2_AHEAD_MB of weight stages beyond the ring, over the grid
@@ -1106,11 +1217,16 @@ int launch_gemm_tiled(const GemmArgs& a) {
 #ifndef EPILORA_GEMM_KA
 #define EPILORA_GEMM_KA 2
 #endif
+#ifndef EPILORA_GEMM_KA_WIDE
+#define EPILORA_GEMM_KA_WIDE 1
+#endif
 
 template <int FMT>
 int launch_gemm_by_m(const GemmArgs& a) {
   constexpr int KA = EPILORA_GEMM_KA;
-  constexpr int KA256 = (FMT == EPILORA_FMT_NVFP4 && KA > 2) ? 2 : KA;   // TMEM budget of NVFP4 scales
+  // wide token tiles: EPILORA_GEMM_KA_WIDE atoms per stage (a 256-token FP8
+  // stage is then 48 KB and the ring four deep)
+  constexpr int KAW = EPILORA_GEMM_KA_WIDE;
   // NVFP4 decode stages carry scale boxes too: one atom per stage keeps
   // three or more stages in flight at two CTAs per SM
   constexpr int KAD = FMT == EPILORA_FMT_NVFP4 ? 1 : KA;
@@ -1119,8 +1235,8 @@ int launch_gemm_by_m(const GemmArgs& a) {
   if (a.M <= 16) return launch_gemm_tiled<FMT, 16, KAD>(a);
   if (a.M <= 32) return launch_gemm_tiled<FMT, 32, 1>(a);
   if (a.M <= 64) return launch_gemm_tiled<FMT, 64, KA>(a);
-  if (a.M <= 128) return launch_gemm_tiled<FMT, 128, KA>(a);
-  return launch_gemm_tiled<FMT, 256, KA256>(a);
+  if (a.M <= 128) return launch_gemm_tiled<FMT, 128, KAW>(a);
+  return launch_gemm_tiled<FMT, 256, KAW>(a);
 }
 
 }  // namespace epi

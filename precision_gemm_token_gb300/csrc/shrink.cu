@@ -62,7 +62,36 @@ struct QuantSide {          // quantizer CTAs of the fused grid (fmt < 0: none)
   float* x_scale;
   uint8_t* x_block_scale;
   const float* x_global_scale;
+  int32_t* perm;            // non-null: rows are written in adapter-sorted order, perm[row] = token
 };
+
+// Sort key of token t for the adapter-sorted row order: its adapter slot if
+// it carries one (idx in [0, L), mask set), else L; ties keep token order.
+__device__ __forceinline__ int sort_key(const int32_t* idx, const uint8_t* mask, int L, int t) {
+  const int l = idx[t];
+  return (l >= 0 && l < L && (mask == nullptr || mask[t] != 0)) ? l : L;
+}
+
+// Row of token t in the sorted order: the number of tokens whose (key, index)
+// precedes its own (one CTA; every thread takes a strided share of the
+// tokens, then a fixed-order reduction).
+__device__ __forceinline__ int sorted_row(const int32_t* idx, const uint8_t* mask, int L, int M, int t,
+                                          int* red_i) {
+  const int key = sort_key(idx, mask, L, t);
+  int cnt = 0;
+  for (int u = threadIdx.x; u < M; u += blockDim.x) {
+    const int k = sort_key(idx, mask, L, u);
+    cnt += (k < key || (k == key && u < t)) ? 1 : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if ((threadIdx.x & 31) == 0) red_i[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  int total = 0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += red_i[w];
+  __syncthreads();
+  return total;
+}
 
 // Before the dependency wait: bring this CTA's inputs into L2 (its slice of
 // x, and for a rank CTA its A rows of the token's adapter) so that the loads
@@ -127,24 +156,31 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   int gy = static_cast<int>(blockIdx.y);
   if (qs.fmt >= 0) {
     if (gy < parts) {
-      // quantizer CTA: slice gy of token t
+      // quantizer CTA: slice gy of token t, written to row q (t, or its
+      // place in the adapter-sorted order)
+      size_t q = t;
+      if (qs.perm != nullptr) {
+        q = static_cast<size_t>(sorted_row(idx, mask, L, static_cast<int>(gridDim.x), static_cast<int>(t),
+                                           reinterpret_cast<int*>(&red[0][0])));
+        if (gy == 0 && threadIdx.x == 0) qs.perm[q] = static_cast<int32_t>(t);
+      }
       const __nv_bfloat16* xrow = X + t * static_cast<size_t>(ldx);
       const int k0 = gy * kslice;
       const int k1 = min(K, k0 + kslice);
       if (qs.fmt == EPILORA_FMT_FP8_E4M3) {
         if (parts == 1) {
-          quant_row_fp8<kShrinkQuantChunks>(xrow, K, qs.Xq + t * static_cast<size_t>(K), qs.x_scale + t,
+          quant_row_fp8<kShrinkQuantChunks>(xrow, K, qs.Xq + q * static_cast<size_t>(K), qs.x_scale + q,
                                             &red[0][0]);
         } else {
           // every slice CTA takes the whole row's amax (the same exact max)
           const float amax = row_amax_bf16(xrow, K, &red[0][0]);
           const float sc = __fdiv_rn(fmaxf(amax, kAmaxFloor), kE4M3Max);
-          if (gy == 0 && threadIdx.x == 0) qs.x_scale[t] = sc;
-          if (k0 < k1) quant_slice_fp8(xrow, k0, k1, qs.Xq + t * static_cast<size_t>(K), sc);
+          if (gy == 0 && threadIdx.x == 0) qs.x_scale[q] = sc;
+          if (k0 < k1) quant_slice_fp8(xrow, k0, k1, qs.Xq + q * static_cast<size_t>(K), sc);
         }
       } else {
-        const bool ok = quant_row_nvfp4(xrow, K, qs.Xq + t * static_cast<size_t>(K / 2),
-                                        qs.x_block_scale + t * static_cast<size_t>(K / kNvfp4Block),
+        const bool ok = quant_row_nvfp4(xrow, K, qs.Xq + q * static_cast<size_t>(K / 2),
+                                        qs.x_block_scale + q * static_cast<size_t>(K / kNvfp4Block),
                                         *qs.x_global_scale, k0 / kNvfp4Block, k1 / kNvfp4Block);
         if (!ok && gy == 0 && threadIdx.x == 0) record_status(status, EPILORA_ERR_INVALID_ARG);
       }
@@ -256,7 +292,7 @@ int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, in
   if (M == 0) return EPILORA_OK;
   if (prefer_max_shared(reinterpret_cast<const void*>(shrink_kernel), shrink_carveout_done) != EPILORA_OK)
     return EPILORA_ERR_CUDA;
-  QuantSide qs{-1, nullptr, nullptr, nullptr, nullptr};
+  QuantSide qs{-1, nullptr, nullptr, nullptr, nullptr, nullptr};
   dim3 grid(M, r / kRanksPerCta);
   shrink_kernel<<<grid, kShrinkThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), K, ldx,
                                                       static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S,
@@ -266,13 +302,15 @@ int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, in
 
 int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
                         const uint8_t* mask, float* S, int s_parts, int fmt, void* Xq, float* x_scale,
-                        uint8_t* x_block_scale, const float* x_global_scale, int* status_dev, cudaStream_t stream) {
+                        uint8_t* x_block_scale, const float* x_global_scale, int32_t* perm, int* status_dev,
+                        cudaStream_t stream) {
   if (M == 0) return EPILORA_OK;
   if (s_parts < 1 || s_parts > shrink_parts_max(K) || (s_parts > 1 && kslice_for(K, s_parts) * (s_parts - 1) >= K))
     return EPILORA_ERR_INVALID_ARG;
   if (prefer_max_shared(reinterpret_cast<const void*>(shrink_kernel), shrink_carveout_done) != EPILORA_OK)
     return EPILORA_ERR_CUDA;
-  QuantSide qs{fmt, static_cast<uint8_t*>(Xq), x_scale, x_block_scale, x_global_scale};
+  if (perm != nullptr && (s_parts != 1 || idx == nullptr)) return EPILORA_ERR_INVALID_ARG;
+  QuantSide qs{fmt, static_cast<uint8_t*>(Xq), x_scale, x_block_scale, x_global_scale, perm};
   const int kslice = s_parts == 1 ? K : kslice_for(K, s_parts);
   // launched as a programmatic dependent of whatever precedes it on the
   // stream: its CTAs become resident early and wait (griddepcontrol.wait)

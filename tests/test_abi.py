@@ -66,6 +66,9 @@ def test_workspace_bytes(lib):
     assert E.epilora_workspace_bytes(0, 2, 14336, 64) == r256(2 * 14336) + r256(8) + r256(2 * 64 * 4 * 8)
     assert E.epilora_workspace_bytes(0, 1, 40960, 16) == r256(40960) + r256(4) + r256(16 * 4 * 8)
     assert E.epilora_workspace_bytes(0, 3, 4096, 32) == r256(3 * 4096) + r256(12) + r256(3 * 32 * 4 * 4)
+    # more than 32 tokens with adapters: plus the adapter-sorted row order (int32 per token)
+    assert E.epilora_workspace_bytes(0, 64, 512, 16) == r256(64 * 512) + r256(256) + r256(64 * 16 * 4) + r256(256)
+    assert E.epilora_workspace_bytes(0, 64, 512, 0) == r256(64 * 512) + r256(256)
     assert E.epilora_workspace_bytes(0, 0, 512, 16) == 0
     assert E.epilora_workspace_bytes(7, 4, 512, 16) == 0
 

@@ -84,13 +84,29 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
     rows_t = torch.from_numpy(rows).cuda()
     buf = ws.buf
     off_xq = 0
+    # workspace: Xq, scales, S (room for min(8, ceil(K / 1024)) partial sums),
+    # and for more than 32 tokens the adapter-sorted row order: row q holds
+    # token perm[q]
+    xq_bytes = M * K if fmt == FP8 else M * K // 2
+    sc_bytes = 4 * M if fmt == FP8 else M * K // 16
+    off_perm = _r256(xq_bytes) + _r256(sc_bytes) + _r256(M * r * 4 * min(8, -(-K // 1024)))
+    if M > 32:
+        perm = buf[off_perm:off_perm + 4 * M].view(torch.int32).cpu().numpy()
+        assert np.array_equal(np.sort(perm), np.arange(M))
+        keys = np.where((idx_all >= 0) & (idx_all < L) & (mask_all != 0), idx_all, L)
+        assert np.array_equal(perm, np.lexsort((np.arange(M), keys)))
+        row_of = np.empty(M, dtype=np.int64)
+        row_of[perm] = np.arange(M)
+        qrows_t = torch.from_numpy(row_of[rows]).cuda()
+    else:
+        qrows_t = torch.from_numpy(rows).cuda()
     if fmt == FP8:
         wq, sw = O.quant_fp8_rows(Wn)
         assert same_codes_e4m3(npu8(w.codes[cols_t]), wq).all()
         assert (np32(w.scale[cols_t]) == sw).all()
         ref = O.layer_fp8(x, wq, sw, A_s, B_s, idx_s, mask)
-        xq_gpu = buf[off_xq:off_xq + M * K].view(M, K)[rows_t]
-        sx_gpu = buf[off_xq + _r256(M * K):off_xq + _r256(M * K) + 4 * M].view(torch.float32)[rows_t]
+        xq_gpu = buf[off_xq:off_xq + M * K].view(M, K)[qrows_t]
+        sx_gpu = buf[off_xq + _r256(M * K):off_xq + _r256(M * K) + 4 * M].view(torch.float32)[qrows_t]
         assert same_codes_e4m3(npu8(xq_gpu), ref["xq"]).all()
         assert (np32(sx_gpu) == ref["sx"]).all()
     else:
@@ -101,9 +117,9 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
         assert (npu8(w.block_scale[cols_t]) == sbw).all()
         assert same_codes_e2m1_packed(npu8(w.codes[cols_t]), wq).all()
         ref = O.layer_nvfp4(x, gx, wq, sbw, gw, A_s, B_s, idx_s, mask)
-        xq_gpu = buf[off_xq:off_xq + M * K // 2].view(M, K // 2)[rows_t]
+        xq_gpu = buf[off_xq:off_xq + M * K // 2].view(M, K // 2)[qrows_t]
         o2 = off_xq + _r256(M * K // 2)
-        sb_gpu = buf[o2:o2 + M * K // 16].view(M, K // 16)[rows_t]
+        sb_gpu = buf[o2:o2 + M * K // 16].view(M, K // 16)[qrows_t]
         assert same_codes_e2m1_packed(npu8(xq_gpu), ref["xq"]).all()
         assert (npu8(sb_gpu) == ref["sbx"]).all()
     # S of the same tokens from the standalone shrink (the fused call keeps it

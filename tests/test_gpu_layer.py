@@ -131,8 +131,9 @@ def test_no_adapter_cases_are_bit_exact_base(fmt):
 
 
 @pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
-def test_permutation_and_determinism(fmt):
-    p = make_projection(29, 1024, 640, 5, 32, seed=8, mask_mode="random")
+@pytest.mark.parametrize("M", [29, 300])   # one decode tile; several adapter-sorted wide tiles
+def test_permutation_and_determinism(fmt, M):
+    p = make_projection(M, 1024, 640, 5, 32, seed=8, mask_mode="random")
     X, W = p.X.cuda(), p.W.cuda()
     w = T.quantize_weight(W, fmt)
     gx = T.nvfp4_global_scale(X) if fmt == NVFP4 else None
@@ -140,7 +141,7 @@ def test_permutation_and_determinism(fmt):
     Y1 = T.layer_forward(X, w, A, B, idx, mask, x_global_scale=gx)
     Y2 = T.layer_forward(X, w, A, B, idx, mask, x_global_scale=gx)
     assert torch.equal(Y1, Y2)
-    perm = torch.randperm(29, generator=torch.Generator().manual_seed(1)).cuda()
+    perm = torch.randperm(M, generator=torch.Generator().manual_seed(1)).cuda()
     Yp = T.layer_forward(X[perm].contiguous(), w, A, B, idx[perm].contiguous(), mask[perm].contiguous(),
                          x_global_scale=gx)
     assert torch.equal(Yp, Y1[perm])
