@@ -40,6 +40,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused FP8/NVFP4+LoRA layer µs @M=1, tokens/s @32 tenants, % HBM roofline"
 PROJ8B = (("qkv", 4096, 6144), ("o", 4096, 4096), ("gate_up", 4096, 28672), ("down", 14336, 4096))
+PROJ70B = (("qkv", 8192, 10240), ("o", 8192, 8192), ("gate_up", 8192, 57344), ("down", 28672, 8192))
+# wide token tiles (tensor-bound): (name, projections, M, fmt, L, r, idx_mode, mask_mode, n_decode, description)
+LARGE_WORKLOADS = (
+    ("70b_prefill2048_fp8", PROJ70B, 2112, 0, 512, 16, "zipf", "prefill_chunk", 64,
+     "Llama-3.1-70B layer, 64 decode tokens (mask 0) + one 2048-token prefill chunk (mask 1, one adapter), "
+     "512 resident rank-16 adapters, Zipf(1.1) indices, FP8"),
+    ("8b_m512_nvfp4", PROJ8B, 512, 1, 128, 64, "zipf", "all", 0,
+     "Llama-3.1-8B layer, M=512, NVFP4, 128 resident rank-64 adapters, Zipf(1.1) indices"),
+)
 
 WORKLOADS = {
     # name: (M, fmt, L, r, idx_mode, description)
@@ -207,11 +216,16 @@ def run_ours(args, rank, world, local):
     if os.path.exists(pk):
         peaks = json.load(open(pk))
 
-    def make_layer(workload, seed):
-        M, fmt, L, r, idx_mode, _ = WORKLOADS[workload]
+    def make_layer(workload, seed, spec=None):
+        if spec is None:
+            M, fmt, L, r, idx_mode, _ = WORKLOADS[workload]
+            plist, mask_mode, n_decode = PROJ8B, "all", 0
+        else:
+            _, plist, M, fmt, L, r, idx_mode, mask_mode, n_decode, _ = spec
         projs = []
-        for i, (name, K, N) in enumerate(PROJ8B):
-            p = make_projection(M, K, N, L, r, seed=seed + i, idx_mode=idx_mode, device=str(dev))
+        for i, (name, K, N) in enumerate(plist):
+            p = make_projection(M, K, N, L, r, seed=seed + i, idx_mode=idx_mode, mask_mode=mask_mode,
+                                n_decode=n_decode, device=str(dev))
             w = T.quantize_weight(p.W, fmt)
             del p.W
             gx = T.nvfp4_global_scale(p.X) if fmt == 1 else None
@@ -230,7 +244,21 @@ def run_ours(args, rank, world, local):
                             status=q["st"], stream=stream, Y=q["Y"])
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+    flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+    clean_buf = torch.ones(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+    clean_out = torch.empty((), dtype=torch.int64, device=dev)
+
+    class _Flush:
+        """Write a buffer of twice the L2 size, then read another one: nothing
+        of the workload stays in L2, and the flush's own dirty lines are
+        written back before the timed events rather than inside them."""
+
+        @staticmethod
+        def fill_(v):
+            flush_buf.fill_(v)
+            torch.sum(clean_buf, dim=0, dtype=torch.int64, out=clean_out)
+
+    flush = _Flush()
 
     def time_graph(projs, steps, warmup, sampler=None):
         s = torch.cuda.Stream(device=dev)
@@ -291,6 +319,26 @@ def run_ours(args, rank, world, local):
         del projs32
         torch.cuda.empty_cache()
 
+    # wide token tiles: tensor-pipe fraction of the fused layer (FP8 peak =
+    # measured bf16 burst x 2, NVFP4 = x 6: the nominal dense ratios)
+    large = None
+    if not args.skip_large:
+        large = []
+        bf16 = peaks.get("bf16_tflops", 1900.0)
+        for spec in LARGE_WORKLOADS:
+            name, plist, Ml, fl, _, _, _, _, _, desc_l = spec
+            projs_l = make_layer(None, seed=300, spec=spec)
+            ms_l, _, _, _ = time_graph(projs_l, 5, args.warmup)
+            ms_l = max_over_ranks(ms_l, world, dev)
+            flops = sum(2.0 * Ml * N * K for _, K, N in plist)
+            peak_l = bf16 * (2.0 if fl == 0 else 6.0)
+            tf = flops / (ms_l / 1000) / 1e12
+            large.append({"workload": desc_l, "M": Ml, "layer_us": round(ms_l * 1000, 1), "tflops": round(tf, 1),
+                          "peak_tflops": round(peak_l, 1), "frac": round(tf / peak_l, 4),
+                          "peak_source": "measured bf16 burst x " + ("2 (FP8)" if fl == 0 else "6 (NVFP4)")})
+            del projs_l
+            torch.cuda.empty_cache()
+
     # dominant kernel (gate_up GEMM with the LoRA epilogue) timed alone with
     # its S already in memory, L2 flushed before each launch
     q = projs[2]
@@ -298,27 +346,21 @@ def run_ours(args, rank, world, local):
     Xq, xs = T.quant_act(p.X, fmt, global_scale=q["gx"])
     S = T.lora_shrink(p.X, p.A, p.idx, p.mask)
     torch.cuda.synchronize()
-    # one GEMM launch captured as a graph, so that host launch overhead never
-    # falls inside the event interval
-    ks_ = torch.cuda.Stream(device=dev)
-    ks_.wait_stream(torch.cuda.current_stream())
-    kern = lambda s: T.gemm_lora_epilogue(Xq, xs, q["w"], M, q["K"], S=S, B=p.B, idx=p.idx, mask=p.mask,  # noqa
-                                          x_global_scale=q["gx"], Y=q["Y"], stream=s)
-    with torch.cuda.stream(ks_):
-        kern(ks_)
-    torch.cuda.synchronize()
-    kg = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(kg, stream=ks_):
-        kern(ks_)
+    # eager launches on the current stream, each queued behind the L2 flush
+    # (a kernel of tens of microseconds): the host has submitted the start
+    # event and the GEMM before the flush ends, so the events bracket the
+    # GEMM's execution only
+    kern = lambda: T.gemm_lora_epilogue(Xq, xs, q["w"], M, q["K"], S=S, B=p.B, idx=p.idx, mask=p.mask,  # noqa
+                                        x_global_scale=q["gx"], Y=q["Y"])
     for _ in range(args.warmup):
         flush.fill_(1)
-        kg.replay()
+        kern()
     ke = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     torch.cuda.synchronize()
     for a, b in ke:
         flush.fill_(1)
         a.record()
-        kg.replay()
+        kern()
         b.record()
     torch.cuda.synchronize()
     k_ms = float(np.mean([a.elapsed_time(b) for a, b in ke]))
@@ -370,15 +412,17 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None, "dtype": "fp8_e4m3" if fmt == 0 else "nvfp4_e2m1", "data": "synthetic",
         "config": {"workload": desc, "M": M, "rank": r, "tenants": L if idx_mode != "single" else 1,
                    "parallelism": f"replicas{world}", "cuda_graph": True,
-                   "l2": "flushed between steps (write of 2x L2 outside the timed events)",
+                   "l2": "flushed between steps outside the timed events: write of a 2x-L2 buffer, then a read "
+                         "of another 2x-L2 buffer (the write's dirty lines leave L2 before the timed region)",
                    "timed": "CUDA events around each graph replay of the 4 projections"},
         "tokens_per_s": round(world * M / (ms_max / 1000), 1),
         "layer_hbm_gbs": round(layer_bytes / (ms_max / 1000) / 1e9, 1),
         "layer_hbm_frac_of_measured": round(layer_bytes / (ms_max / 1000) / 1e9 / peak, 4),
         "roofline": roofline,
         "tenants32": t32,
+        "large_m": large,
         "e2e": e2e,
-        "gpu_launches": args.steps * 3 * len(PROJ8B),
+        "gpu_launches": args.steps * 2 * len(PROJ8B),   # per projection: the shrink grid and the GEMM
         "clocks": clocks,
         "median_ms_per_step": round(ms_med, 5),
     }
@@ -510,6 +554,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="8b_m1_fp8", choices=sorted(WORKLOADS))
     ap.add_argument("--skip-tenants", action="store_true")
+    ap.add_argument("--skip-large", action="store_true", help="skip the wide-tile (tensor-bound) layers")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
