@@ -390,10 +390,17 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         pdl_wait_primary();
         fence_proxy_async_global();
       }
-      for (int i = prewait; i < prologue; ++i) issue_w(i, i);
+      // activations of the stages already requested first (the MMA waits
+      // for them), then the rest of the ring, then the L2 prefetch
+      for (int i = 0; i < prewait; ++i) issue_x(i, i);
+      for (int i = prewait; i < prologue; ++i) {
+        issue_w(i, i);
+        issue_x(i, i);
+      }
       if (EPILORA_GEMM_FUSED_MODE != 0) l2_ahead();
+    } else {
+      for (int i = 0; i < prologue; ++i) issue_x(i, i);
     }
-    for (int i = 0; i < prologue; ++i) issue_x(i, i);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
