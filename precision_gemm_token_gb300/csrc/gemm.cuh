@@ -69,6 +69,12 @@
 #ifndef EPILORA_GEMM_PREWAIT_STAGES
 #define EPILORA_GEMM_PREWAIT_STAGES 16  // weight stages a fused call issues before its wait
 #endif
+#ifndef EPILORA_GEMM_X_FIRST
+#define EPILORA_GEMM_X_FIRST 1          // fused call: activation loads right after the wait, before the L2 prefetch
+#endif
+#ifndef EPILORA_GEMM_B_EARLY
+#define EPILORA_GEMM_B_EARLY 1          // one-group decode tiles load their B slice into a buffer of its own
+#endif
 #ifndef EPILORA_GEMM_B_L2
 #define EPILORA_GEMM_B_L2 0             // prefetch streamed B slices into L2 after set-up
 #endif
@@ -122,6 +128,7 @@ struct GemmParams {
   int b_atoms;        // tmB boxes per group (2 when 2r = 256)
   int b_group_bytes;  // ring bytes of one group's boxes (1024-byte aligned)
   int b_groups_per_slot;
+  int b_early;        // 1: a decode tile with one adapter group loads its B slice at once into its own buffer
   int trace_slot;     // tuning builds only: which trace buffer this launch fills
   int l2_ahead;       // fused call: weight stages past the ring to prefetch into L2 while waiting
 };
@@ -287,7 +294,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   uint64_t* empty_bar = full_bar + stages;
   uint64_t* acc_bar = empty_bar + stages;
   uint64_t* meta_bar = acc_bar + 1;           // token metadata and adapter groups are in shared memory
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta_bar + 1);
+  uint64_t* b_bar = meta_bar + 1;             // the early B slice has landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* ngroups_s = reinterpret_cast<int*>(tmem_slot + 2);
   float* meta_sx = reinterpret_cast<float*>(tmem_slot + 4);
@@ -297,6 +305,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   // decode region (BT <= kDecodeBT)
   const int RR = gemm_red_rows(ks);           // rows owned per rank (last rank: fewer)
   float* s_stage = reinterpret_cast<float*>(misc + kGemmMiscBytes);   // [token][r]
+  // one-group decode tiles: the B slice of the group (1024-byte aligned for the swizzled box)
+  uint8_t* b_early_buf = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(misc + kGemmMiscBytes + gemm_decode_bytes(BT, p.r, ks)) + 1023) & ~uintptr_t(1023));
   float* y_tile = s_stage + BT * p.r;                                 // [token][RR]
   int* g_order = reinterpret_cast<int*>(y_tile + BT * RR);            // tokens sorted by group
   int* g_start = g_order + BT;                                        // [group + 1]
@@ -360,6 +371,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     }
     mbar_init(acc_bar, 1);
     mbar_init(meta_bar, 1);
+    mbar_init(b_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     // the ring starts empty: stream weights into it before anything else
@@ -390,14 +402,20 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         pdl_wait_primary();
         fence_proxy_async_global();
       }
-      // activations of the stages already requested first (the MMA waits
-      // for them), then the rest of the ring, then the L2 prefetch
-      for (int i = 0; i < prewait; ++i) issue_x(i, i);
-      for (int i = prewait; i < prologue; ++i) {
-        issue_w(i, i);
-        issue_x(i, i);
+      if (EPILORA_GEMM_X_FIRST) {
+        // activations of the stages already requested first (the MMA waits
+        // for them), then the rest of the ring, then the L2 prefetch
+        for (int i = 0; i < prewait; ++i) issue_x(i, i);
+        for (int i = prewait; i < prologue; ++i) {
+          issue_w(i, i);
+          issue_x(i, i);
+        }
+        if (EPILORA_GEMM_FUSED_MODE != 0) l2_ahead();
+      } else {
+        for (int i = prewait; i < prologue; ++i) issue_w(i, i);
+        if (EPILORA_GEMM_FUSED_MODE != 0) l2_ahead();
+        for (int i = 0; i < prologue; ++i) issue_x(i, i);
       }
-      if (EPILORA_GEMM_FUSED_MODE != 0) l2_ahead();
     } else {
       for (int i = 0; i < prologue; ++i) issue_x(i, i);
     }
@@ -487,10 +505,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   const int gps = p.b_groups_per_slot;
   int n_bslots = 0;       // ring loads carrying B slices
   int n_loads = nkb;
+  bool b_early_on = false;  // the tile's only group comes through b_early_buf instead of the ring
   auto set_groups = [&]() {
     ngroups = *ngroups_s;
     sb = C::kDecode && p.stream_b && ngroups >= EPILORA_GEMM_SB_MIN_GROUPS && p.S != nullptr;
-    n_bslots = sb ? (ngroups + gps - 1) / gps : 0;
+    b_early_on = sb && p.b_early && ngroups == 1;
+    n_bslots = sb && !b_early_on ? (ngroups + gps - 1) / gps : 0;
     n_loads = nkb + n_bslots;
   };
 
@@ -702,6 +722,14 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     }
     set_groups();
     if (et == 0) mbar_arrive(meta_bar);   // the producer may now stream B slices
+    if (b_early_on && et == 0) {
+      // a one-group tile's B slice goes to its own buffer now (the ring is
+      // busy with weight stages), so the epilogue finds it there
+      mbar_arrive_expect_tx(b_bar, static_cast<uint32_t>(RR * p.b_box_bytes * p.b_atoms));
+      const int y = g_adapter[0] * p.N + n0 + row_lo;
+      for (int a = 0; a < p.b_atoms; ++a)
+        tma_load_2d(b_early_buf + a * RR * p.b_box_bytes, &p.tmB, b_bar, a * p.b_box_bytes, y);
+    }
     if (p.S != nullptr && !sb) {
       // L2 prefetch of the tile's B slices, first B row into registers
       const int rows = min(row_hi, p.N - n0) - row_lo;
@@ -887,6 +915,30 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       const int cpa_log = 3 - sw_shift;                    // log2 of the 16-byte chunks per atom
       const int nchunk = p.r / 8;                          // 16-byte chunks of a B row
       const int atom_stride = RR * sw_span;                // bytes between a group's atoms
+      if (b_early_on) {
+        // the only group's slice is in its own buffer
+        const bool late = !mbar_wait_bounded(b_bar, 0, kWaitLimitNs);
+        if (!epi_bar_any(late)) {
+          const int xr = (i >> sw_shift) & sw_mask;
+          for (int k = g_start[0] + tsl; k < g_start[1]; k += tstep) {
+            const int tl = g_order[k];
+            const uint8_t* gb = b_early_buf + i * sw_span;
+            const float4* srow = reinterpret_cast<const float4*>(s_stage + tl * p.r);
+            float d;
+            switch (nchunk) {
+              case 2: d = dot_b_row<2>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
+              case 4: d = dot_b_row<4>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
+              case 8: d = dot_b_row<8>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
+              default: d = dot_b_row<16>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
+            }
+            y_tile[tl * RR + i] += d;
+          }
+          asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
+        } else {
+          *abort_flag = 1;
+          record_status(p.status, EPILORA_ERR_TIMEOUT);
+        }
+      }
       for (int j = 0; j < n_bslots; ++j) {
         const int li = nkb + j;
         const int s = li % stages;
@@ -1041,6 +1093,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   }
 
   // ---------------------------------------------------------------- teardown
+  if (b_early_on && et == 0 && *abort_flag) (void)mbar_wait_bounded(b_bar, 0, kWaitLimitNs);   // no copy in flight
   if (ks > 1 && warp < 2) cluster_wait();   // second phase, for the producer and MMA warps
   if (threadIdx.x == 64) {
     unsigned smid;
@@ -1159,6 +1212,15 @@ int launch_gemm_tiled(const GemmArgs& a) {
   if (stages > per_cta && !p.stream_b) stages = per_cta;     // no deeper than the K loop needs
   if (stages < 2) p.stream_b = 0;        // B slots need a ring of two or more
   if (stages < 1) stages = 1;
+  // one-group decode tiles: a buffer of its own for the B slice, if it fits
+  // beside the ring without giving up a stage
+  int early_bytes = 0;
+  p.b_early = 0;
+  if (p.stream_b && EPILORA_GEMM_B_EARLY) {
+    early_bytes = p.b_group_bytes + 1024;      // + alignment of the swizzled box
+    if (gemm_smem_bytes(C::kStageBytes, stages, red) + dec + early_bytes <= budget) p.b_early = 1;
+    else early_bytes = 0;
+  }
   // non-decode tiles stage S of their tokens in the ring once the main loop
   // is over (one fp32 row of r per token column); deepen the ring if needed
   p.stage_s = 0;
@@ -1182,7 +1244,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
     if (ahead > left) ahead = left;
     p.l2_ahead = a.fused && ahead > 0 ? static_cast<int>(ahead) : 0;
   }
-  const int smem = gemm_smem_bytes(C::kStageBytes, stages, red) + dec;
+  const int smem = gemm_smem_bytes(C::kStageBytes, stages, red) + dec + early_bytes;
   if (smem > 227 * 1024) return EPILORA_ERR_UNSUPPORTED;
 
   auto kern = gemm_lora_kernel<FMT, BT, KA>;
