@@ -319,6 +319,20 @@ def run_ours(args, rank, world, local):
         del projs32
         torch.cuda.empty_cache()
 
+    # the same decode layer with an NVFP4 base (M = 1, 128 resident adapters)
+    nv = None
+    if not args.skip_tenants and fmt == 0:
+        projs_nv = make_layer("8b_m1_nvfp4", seed=400)
+        ms_nv, _, _, _ = time_graph(projs_nv, max(args.steps // 2, 3), args.warmup)
+        ms_nv = max_over_ranks(ms_nv, world, dev)
+        nd_nv = len(set(int(i) for i in projs_nv[0]["p"].idx.tolist() if i >= 0))
+        bytes_nv = sum(algorithmic_bytes(1, K, N, 1, WORKLOADS["8b_m1_nvfp4"][3], nd_nv) for _, K, N in PROJ8B)
+        nv = {"workload": WORKLOADS["8b_m1_nvfp4"][5], "layer_us": round(ms_nv * 1000, 2),
+              "hbm_gbs": round(bytes_nv / (ms_nv / 1000) / 1e9, 1),
+              "hbm_frac_of_measured": round(bytes_nv / (ms_nv / 1000) / 1e9 / peaks.get("hbm_gbs", 6800.0), 4)}
+        del projs_nv
+        torch.cuda.empty_cache()
+
     # wide token tiles: tensor-pipe fraction of the fused layer (FP8 peak =
     # measured bf16 burst x 2, NVFP4 = x 6: the nominal dense ratios)
     large = None
@@ -420,6 +434,7 @@ def run_ours(args, rank, world, local):
         "layer_hbm_frac_of_measured": round(layer_bytes / (ms_max / 1000) / 1e9 / peak, 4),
         "roofline": roofline,
         "tenants32": t32,
+        "nvfp4_m1": nv,
         "large_m": large,
         "e2e": e2e,
         "gpu_launches": args.steps * 2 * len(PROJ8B),   # per projection: the shrink grid and the GEMM

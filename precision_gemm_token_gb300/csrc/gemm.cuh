@@ -1462,6 +1462,9 @@ int launch_gemm_tiled(const GemmArgs& a) {
 #ifndef EPILORA_GEMM_KA
 #define EPILORA_GEMM_KA 2
 #endif
+#ifndef EPILORA_GEMM_KA32
+#define EPILORA_GEMM_KA32 1           // atoms per stage of 32-token decode tiles
+#endif
 #ifndef EPILORA_GEMM_KA_WIDE
 #define EPILORA_GEMM_KA_WIDE 1
 #endif
@@ -1478,7 +1481,7 @@ int launch_gemm_by_m(const GemmArgs& a) {
   // 32-token decode tiles also keep output-tile and S buffers: one atom per
   // stage leaves room for three or more stages
   if (a.M <= 16) return launch_gemm_tiled<FMT, 16, KAD>(a);
-  if (a.M <= 32) return launch_gemm_tiled<FMT, 32, 1>(a);
+  if (a.M <= 32) return launch_gemm_tiled<FMT, 32, EPILORA_GEMM_KA32>(a);
   if (a.M <= 64) return launch_gemm_tiled<FMT, 64, KA>(a);
   if (a.M <= 128) return launch_gemm_tiled<FMT, 128, KAW>(a);
   return launch_gemm_tiled<FMT, 256, KAW>(a);
