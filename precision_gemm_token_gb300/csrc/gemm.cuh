@@ -141,6 +141,7 @@ struct GemmParams {
   int l2_ahead;       // fused call: weight stages past the ring to prefetch into L2 while waiting
   int tc_expand;      // wide tiles: one-adapter column chunks get their adapter term from tensor-core MMAs
   int tc_slots;       // B slices that fit in the ring beside the staged S (tensor-core expand)
+  int y_stage;        // wide tiles: ring byte offset of the per-warp output staging (-1: 2-byte stores)
 };
 
 template <int FMT, int BT, int KA>
@@ -326,6 +327,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   int* xslot_l = xplan + 1 + 3 * 16;
   uint32_t* xmask = reinterpret_cast<uint32_t*>(xslot_l + 4);
   float* s_big = reinterpret_cast<float*>(smem);               // non-decode: S rows of the tile, after the main loop
+  const int s_ld = p.r + 4;                                    // its row stride in floats (bank-conflict padding)
   // decode region (BT <= kDecodeBT)
   const int RR = gemm_red_rows(ks);           // rows owned per rank (last rank: fewer)
   float* s_stage = reinterpret_cast<float*>(misc + kGemmMiscBytes);   // [token][r]
@@ -972,10 +974,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       // every stage has been consumed: the ring now holds the S rows of this
       // tile's tokens (one read of each from L2 instead of one per element)
       const int n4 = p.r / 4;
-      float4* dst = reinterpret_cast<float4*>(s_big);
       for (int k = et; k < tv * n4; k += 128) {
         const int tl = k / n4;
-        dst[k] = __ldcg(reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r) + (k - tl * n4));
+        reinterpret_cast<float4*>(s_big + tl * s_ld)[k - tl * n4] =
+            __ldcg(reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r) + (k - tl * n4));
       }
       asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
     }
@@ -1007,13 +1009,49 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       const bool s_smem = C::kDecode || p.stage_s;
       const float4* srow =
           C::kDecode ? reinterpret_cast<const float4*>(s_stage + tl * p.r)
-          : p.stage_s ? reinterpret_cast<const float4*>(s_big + tl * p.r)
+          : p.stage_s ? reinterpret_cast<const float4*>(s_big + tl * s_ld)
                       : reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r);
       y += dot_srow_brow(srow, brow, p.r, s_smem);
     }
     if (et == 0 && tl == 0) EPI_TRACE_AFTER(10, y);
     p.Y[static_cast<size_t>(meta_tok[tl]) * p.ldy + n] = __float2bfloat16_rn(y);
     if (et == 0 && tl == 0) EPI_TRACE(7, globaltimer_ns());
+  };
+
+  // wide tiles: 16 token columns of this warp's 32 output rows go through a
+  // staging block in the (consumed) ring, [16 tokens][40] bf16 (rows padded
+  // against bank conflicts), and leave as 16-byte row segments, 8 token rows
+  // per store instruction instead of one
+  constexpr int kYsLd = 40;
+  auto y_stage_block = [&]() {
+    return reinterpret_cast<__nv_bfloat16*>(smem + p.y_stage) + (warp & 3) * 16 * kYsLd;
+  };
+  auto flush16 = [&](int c) {
+    const int q = warp & 3;
+    const __nv_bfloat16* ys = y_stage_block();
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = h * 8 + (lane >> 2);
+      const int tl = c * 16 + row;
+      const int n = n0 + q * 32 + (lane & 3) * 8;
+      if (tl < tv && n < p.N) {
+        const __nv_bfloat16* src = ys + row * kYsLd + (lane & 3) * 8;
+        __nv_bfloat16* dst = p.Y + static_cast<size_t>(meta_tok[tl]) * p.ldy + n;
+        if (n + 8 <= p.N) {
+          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        } else {
+          for (int e = 0; e < p.N - n; ++e) dst[e] = src[e];
+        }
+      }
+    }
+    __syncwarp();     // the block is free for the next chunk
+  };
+  auto emit16 = [&](int c, const float* yv) {
+    __nv_bfloat16* ys = y_stage_block();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ys[j * kYsLd + lane] = __float2bfloat16_rn(yv[j]);
+    flush16(c);
   };
 
   if (ks > 1 && warp >= 2) {
@@ -1158,22 +1196,139 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         if (n < p.N) p.Y[static_cast<size_t>(meta_tok[tl]) * p.ldy + n] = __float2bfloat16_rn(y_tile[tl * RR + ii]);
       }
     } else if (ks == 1 && !C::kDecode && p.S != nullptr) {
-      // wide tiles: this thread's weight row m over the tile's token columns
-      // in order. The row of B is reloaded only when the adapter changes
-      // (adapter-sorted tokens make that rare) and the next adapter's row is
-      // prefetched into L2 at each change; S comes from shared memory.
+      // wide tiles: the token columns in adapter-sorted chunks of 16. For
+      // ranks <= 32 every chunk takes its adapter term from TF32 tensor-core
+      // MMAs, one pass per adapter present in the chunk:
+      //   D[row][token] = sum_k B_l[row][k] * S[token][k]
+      // with the adapter rows (bf16, exact in TF32) as the A operand and S
+      // split into two TF32 halves (hi + lo, together exact to about 2^-22)
+      // as the B operand, fp32 accumulate. The m16n8 accumulator layout is
+      // the one tcgen05.ld.16x256b returns the base sums in, so base and
+      // adapter term meet in registers. Higher ranks go element by element
+      // on CUDA cores: this thread's weight row m, its B row reloaded when
+      // the adapter changes.
       const int q = warp & 3;
       const int m = q * 32 + lane;
       const int n = n0 + m;
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       const float sw = sw_pre;
+      const int g = lane >> 2, tq = lane & 3;     // MMA fragment coordinates
+      // weight-row scales of this thread's fragment rows q*32 + mt*16 + g + 8h
+      float swf[2][2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = n0 + q * 32 + mt * 16 + g + 8 * h;
+          swf[mt][h] = !C::kFP4 && row < p.N ? ldg_nc_f32_now(p.w_scale + row) : 0.0f;
+        }
+      // L2 prefetch of this warp's 32 B rows of the next adapter after column tl
+      auto prefetch_next = [&](int l, int tl) {
+        for (int base = tl + 1; base < tv; base += 32) {
+          const int k = base + lane;
+          const int lk = k < tv ? meta_idx[k] : -1;
+          const uint32_t hit = __ballot_sync(0xffffffffu, lk >= 0 && lk != l);
+          if (hit != 0u) {
+            const int rows = min(32, p.N - (n0 + q * 32));
+            if (lane == 0 && rows > 0)
+              prefetch_l2_bulk(p.B + (static_cast<size_t>(meta_idx[base + __ffs(hit) - 1]) * p.N + n0 + q * 32) * p.r,
+                               static_cast<uint32_t>(rows * p.r * 2));
+            break;
+          }
+        }
+      };
       auto run = [&](auto r4c) {
         constexpr int R4 = decltype(r4c)::value;     // float4 chunks of an S row
-        int cur_l = -1;
+        constexpr bool kMma = R4 <= 8;               // tensor-core chunks: rank <= 32
+        constexpr int KS = kMma ? R4 / 2 : 1;        // k-steps of 8
+        int cur_l = -1;                              // adapter of brow
+        int cur_la = -1;                             // adapter of the A fragments
+        uint32_t af[2 * KS][4];                      // [mt * KS + ks]
+        auto load_afrag = [&](int l) {
+          const uint16_t* bl = reinterpret_cast<const uint16_t*>(p.B) + static_cast<size_t>(l) * p.N * p.r;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int row = n0 + q * 32 + mt * 16 + g + 8 * h;
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const uint32_t b = row < p.N ? __ldg(bl + static_cast<size_t>(row) * p.r + ks * 8 + tq + 4 * e) : 0u;
+                  af[mt * KS + ks][h + 2 * e] = b << 16;     // bf16 -> fp32 (exact, also as TF32)
+                }
+            }
+        };
 #pragma unroll 1
         for (int c = 0; c < BT / 16; ++c) {
           if (c * 16 >= tv) break;
+          // the chunk's adapters (the same for every thread): none, one, or several
+          const int jl = c * 16 + (lane & 15);
+          const int lj = jl < tv ? meta_idx[jl] : -1;
+          const uint32_t actm = __ballot_sync(0xffffffffu, lj >= 0) & 0xffffu;
+          if (kMma && !tc_on && p.stage_s && p.y_stage >= 0) {
+            uint32_t va[2][8];
+            tmem_ld_16x256b_x2(lane_base + c * 16, va[0]);
+            tmem_ld_16x256b_x2(lane_base + (16u << 16) + c * 16, va[1]);
+            float d[2][2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d[mt][nt][i] = 0.0f;
+            // one pass per adapter of the chunk, S of the other columns zeroed:
+            // a column's sum is the same whichever chunk it falls in
+            uint32_t rem = actm;
+            while (rem != 0u) {
+              const int l = meta_idx[c * 16 + __ffs(rem) - 1];
+              const uint32_t cols = __ballot_sync(0xffffffffu, lj == l) & 0xffffu;
+              rem &= ~cols;
+              if (l != cur_la) {
+                load_afrag(l);
+                cur_la = l;
+                prefetch_next(l, c * 16 + 31 - __clz(cols));
+              }
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                  // S of token column c*16 + nt*8 + g, ranks ks*8 + tq and + 4
+                  const bool on = (cols >> (nt * 8 + g)) & 1u;
+                  const float* sp = s_big + (c * 16 + nt * 8 + g) * s_ld + ks * 8 + tq;
+                  const float s0 = on ? sp[0] : 0.0f, s1 = on ? sp[4] : 0.0f;
+                  const uint32_t h0 = f32_to_tf32(s0), h1 = f32_to_tf32(s1);
+                  const uint32_t l0 = f32_to_tf32(s0 - __uint_as_float(h0));
+                  const uint32_t l1 = f32_to_tf32(s1 - __uint_as_float(h1));
+#pragma unroll
+                  for (int mt = 0; mt < 2; ++mt) {
+                    mma_tf32_m16n8k8(d[mt][nt], af[mt * KS + ks], l0, l1);
+                    mma_tf32_m16n8k8(d[mt][nt], af[mt * KS + ks], h0, h1);
+                  }
+                }
+            }
+            tmem_ld_wait();
+            // element (mt, nt, i): row q*32 + mt*16 + g + 8*(i/2), column
+            // c*16 + nt*8 + 2*tq + i%2
+            __nv_bfloat16* ys = y_stage_block();
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int col = nt * 8 + 2 * tq + (i & 1);
+                  const float acc = __uint_as_float(va[mt][nt * 4 + i]);
+                  const float b = C::kFP4 ? acc * alpha : (acc * meta_sx[c * 16 + col]) * swf[mt][i >> 1];
+                  const float y = (actm >> col) & 1u ? b + d[mt][nt][i] : b;
+                  ys[col * kYsLd + mt * 16 + g + 8 * (i >> 1)] = __float2bfloat16_rn(y);
+                }
+            flush16(c);
+            continue;
+          }
           uint32_t v[16];
+          float yv[16] = {};
           tmem_ld_32x32b_x16(lane_base + c * 16, v);
           tmem_ld_wait();
           if (n < p.N) {
@@ -1188,20 +1343,22 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
                   if (l != cur_l) {
                     load_brow(l, m);
                     cur_l = l;
-                    int k = tl + 1;
-                    while (k < tv && (meta_idx[k] == l || meta_idx[k] < 0)) ++k;
-                    if (k < tv)
-                      prefetch_l2_bulk(p.B + (static_cast<size_t>(meta_idx[k]) * p.N + n) * p.r,
-                                       static_cast<uint32_t>(p.r * 2));
                   }
-                  y += p.stage_s ? dot_srow_brow_n<R4, true>(reinterpret_cast<const float4*>(s_big + tl * p.r), brow)
-                                 : dot_srow_brow_n<R4, false>(
-                                       reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r),
-                                       brow);
+                  const float4* srow = p.stage_s ? reinterpret_cast<const float4*>(s_big + tl * s_ld)
+                                                 : reinterpret_cast<const float4*>(
+                                                       p.S + static_cast<size_t>(meta_tok[tl]) * p.r);
+                  y += p.stage_s ? dot_srow_brow_n<R4, true>(srow, brow) : dot_srow_brow_n<R4, false>(srow, brow);
                 }
-                p.Y[static_cast<size_t>(meta_tok[tl]) * p.ldy + n] = __float2bfloat16_rn(y);
+                yv[j] = y;
               }
             }
+          }
+          if (p.y_stage >= 0) {
+            emit16(c, yv);
+          } else if (n < p.N) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c * 16 + j < tv) p.Y[static_cast<size_t>(meta_tok[c * 16 + j]) * p.ldy + n] = __float2bfloat16_rn(yv[j]);
           }
         }
       };
@@ -1216,12 +1373,22 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       const int m = q * 32 + lane;
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       const float sw = sw_pre;
+#ifdef EPILORA_GEMM_TRACE
+      long long ck_ld = 0, ck_fin = 0;
+#endif
 #pragma unroll 1
       for (int c = 0; c < BT / 16; ++c) {
         if (c * 16 >= tv) break;
         uint32_t v[16];
+#ifdef EPILORA_GEMM_TRACE
+        const long long ca = clock64();
+#endif
         tmem_ld_32x32b_x16(lane_base + c * 16, v);
         tmem_ld_wait();
+#ifdef EPILORA_GEMM_TRACE
+        const long long cb = clock64();
+        ck_ld += cb - ca;
+#endif
         if (C::kDecode) {
           // valid token columns to this thread's row of the output tile;
           // only they are finished below (a loop with a run-time bound, so
@@ -1229,11 +1396,25 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (c * 16 + j < tv) y_tile[(c * 16 + j) * RR + m] = __uint_as_float(v[j]);
+        } else if (p.y_stage >= 0) {
+          float yv[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) yv[j] = base_value(m, c * 16 + j, __uint_as_float(v[j]), sw);
+          emit16(c, yv);
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) finish(m, c * 16 + j, __uint_as_float(v[j]), sw);
         }
+#ifdef EPILORA_GEMM_TRACE
+        if (!C::kDecode) ck_fin += clock64() - cb;
+#endif
       }
+#ifdef EPILORA_GEMM_TRACE
+      if (et == 0 && !C::kDecode) {
+        EPI_TRACE(12, static_cast<unsigned long long>(ck_ld));
+        EPI_TRACE(13, static_cast<unsigned long long>(ck_fin));
+      }
+#endif
       if (C::kDecode) {
 #pragma unroll 1
         for (int tl = 0; tl < tv; ++tl) finish(m, tl, y_tile[tl * RR + m], sw);
@@ -1401,7 +1582,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
     }
   }
   if (!C::kDecode && a.S != nullptr && !p.tc_expand) {
-    const int need = BT * a.r * 4;
+    const int need = BT * (a.r + 4) * 4 + 5 * 1024;     // padded S rows + the output staging
     int st_need = (need + C::kStageBytes - 1) / C::kStageBytes;
     if (st_need < stages) st_need = stages;
     if (gemm_smem_bytes(C::kStageBytes, st_need, red) + dec <= budget) {
@@ -1410,6 +1591,13 @@ int launch_gemm_tiled(const GemmArgs& a) {
     }
   }
   p.stages = stages;
+  // wide tiles without split K: output rows leave through a 5 KB staging
+  // block placed after the staged S (16-byte stores need aligned rows)
+  p.y_stage = -1;
+  if (!C::kDecode && ks == 1 && !p.tc_expand && (reinterpret_cast<uintptr_t>(a.Y) & 15) == 0 && a.ldy % 8 == 0) {
+    const int off = p.stage_s ? (BT * (a.r + 4) * 4 + 127) / 128 * 128 : 0;
+    if (off + 5 * 1024 <= stages * C::kStageBytes) p.y_stage = off;
+  }
   // fused call: prefetch into L2 (while the shrink grid runs) up to about
   // EPILORA_GEMM_L2_AHEAD_MB of weight stages beyond the ring, over the grid
   {
@@ -1465,6 +1653,9 @@ int launch_gemm_tiled(const GemmArgs& a) {
 #ifndef EPILORA_GEMM_KA32
 #define EPILORA_GEMM_KA32 1           // atoms per stage of 32-token decode tiles
 #endif
+#ifndef EPILORA_GEMM_MAX_BT
+#define EPILORA_GEMM_MAX_BT 256       // widest token tile
+#endif
 #ifndef EPILORA_GEMM_KA_WIDE
 #define EPILORA_GEMM_KA_WIDE 1
 #endif
@@ -1483,7 +1674,7 @@ int launch_gemm_by_m(const GemmArgs& a) {
   if (a.M <= 16) return launch_gemm_tiled<FMT, 16, KAD>(a);
   if (a.M <= 32) return launch_gemm_tiled<FMT, 32, EPILORA_GEMM_KA32>(a);
   if (a.M <= 64) return launch_gemm_tiled<FMT, 64, KA>(a);
-  if (a.M <= 128) return launch_gemm_tiled<FMT, 128, KAW>(a);
+  if (a.M <= 128 || EPILORA_GEMM_MAX_BT <= 128) return launch_gemm_tiled<FMT, 128, KAW>(a);
   return launch_gemm_tiled<FMT, 256, KAW>(a);
 }
 

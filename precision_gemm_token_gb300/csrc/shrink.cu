@@ -144,9 +144,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   // ordinary launch).
   if (threadIdx.x == 0) SHRINK_TRACE_MIN(0);
   if (threadIdx.x == 0) prefetch_inputs(X, K, ldx, A, L, r, idx, qs.fmt >= 0 ? parts : 0, kslice);
-  // A grid that fits beside the GEMM's CTAs releases it at once; a larger one
-  // keeps the SMs to itself and releases it as its CTAs finish (its A stream
-  // is then not starved of CTA slots by a GEMM still waiting for it).
+  // early_release: the GEMM may launch as soon as every CTA of this grid has
+  // started (else as they exit)
   if (early_release) pdl_allow_dependents();
   pdl_wait_primary();
   if (threadIdx.x == 0) SHRINK_TRACE_MIN(1);
@@ -243,6 +242,10 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   }
 }
 
+#ifndef EPILORA_SHRINK_EARLY_ALL
+#define EPILORA_SHRINK_EARLY_ALL 0   // 1: grids of any size release the GEMM at CTA start
+#endif
+
 constexpr int kShrinkSliceTarget = 1024;   // elements of K per slice when splitting
 constexpr int kShrinkMaxParts = 8;
 
@@ -317,6 +320,13 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
   // for that kernel's completion before touching x or the workspace
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(M, s_parts + (r / kRanksPerCta) * s_parts);
+  // The GEMM is released at CTA start when the grid fits beside it, and for
+  // decode batches of any grid size: it then launches once the last CTA has
+  // started and streams weights under the shrink's tail. Wide batches
+  // release it at exit instead (their shrink is a small share of the layer,
+  // and an early GEMM only competes with it for HBM).
+  const int early_release =
+      EPILORA_SHRINK_EARLY_ALL || M <= 32 || static_cast<int>(cfg.gridDim.x * cfg.gridDim.y) <= num_sms() ? 1 : 0;
   cfg.blockDim = dim3(kShrinkThreads, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -327,7 +337,7 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
   if (cudaLaunchKernelEx(&cfg, shrink_kernel, static_cast<const __nv_bfloat16*>(X), K, ldx,
                          static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S, status_dev, qs, s_parts,
                          kslice, trace_slot_next(),
-                         static_cast<int>(cfg.gridDim.x * cfg.gridDim.y) <= num_sms() ? 1 : 0) != cudaSuccess)
+                         early_release) != cudaSuccess)
     return EPILORA_ERR_CUDA;
   return EPILORA_OK;
 }

@@ -96,6 +96,17 @@ def test_layer_mask_prefill_chunk(fmt):
     assert_y_close(y, ref, bound)
 
 
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+@pytest.mark.parametrize("r", [16, 32, 64])
+def test_wide_tiles_prefill_chunk_one_adapter_runs(fmt, r):
+    """Wide (256-token) tiles whose columns are long one-adapter runs, mask-0
+    decode tokens and a ragged last tile: the one-adapter, no-adapter and
+    mixed 16-column chunks of the wide epilogue."""
+    y, ref, bound, _ = run_case(fmt, 600, 512, 384, 64, r, seed=11 + r, idx_mode="zipf", mask_mode="prefill_chunk",
+                                n_decode=40)
+    assert_y_close(y, ref, bound, what=(fmt, r))
+
+
 def test_fp8_integer_codes_exact():
     """Rows whose amax is 448 quantize with scale 1; with small-integer values
     the codes are those integers, the fp32 accumulation is exact and Y must be
