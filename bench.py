@@ -561,6 +561,32 @@ def run_profile(args):
     print(json.dumps({"profile": args.workload, "kernel": f"gate_up {K}->{N} M={M}", "ok": True}))
 
 
+def run_profile_wide(args):
+    """A wide-tile fused layer call alone, for ncu: the Llama-3.1-70B gate_up
+    projection's 1/8 column slice (K 8192 -> N 7168) over the prefill-chunk
+    batch (64 mask-0 decode tokens + 2048 prefill tokens on one adapter, 512
+    resident rank-16 adapters, Zipf(1.1) indices, FP8), five layer_forward
+    calls (shrink grid + GEMM each)."""
+    import torch
+
+    import precision_gemm_token_gb300 as E
+    from precision_gemm_token_gb300 import tensors as T
+    from synth import make_projection
+
+    E.build()
+    E.load()
+    M, K, N = 2112, 8192, 57344 // 8
+    p = make_projection(M, K, N, 512, 16, seed=5, idx_mode="zipf", mask_mode="prefill_chunk", n_decode=64,
+                        device="cuda")
+    w = T.quantize_weight(p.W, 0)
+    ws = T.LayerWorkspace("cuda")
+    for _ in range(5):
+        T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, workspace=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": "70b_gate_up_slice_prefill2112_fp8", "kernel": f"gate_up {K}->{N} M={M}",
+                      "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -574,11 +600,15 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true", help="run the dominant kernel alone (for ncu)")
+    ap.add_argument("--profile-wide", action="store_true", help="run one wide-tile fused layer call alone (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.profile:
         run_profile(args)
+        return
+    if args.profile_wide:
+        run_profile_wide(args)
         return
     rank, world, local = dist_setup()
     if args.impl == "reference":
