@@ -141,6 +141,7 @@ struct GemmParams {
   int l2_ahead;       // fused call: weight stages past the ring to prefetch into L2 while waiting
   int tc_expand;      // wide tiles: one-adapter column chunks get their adapter term from tensor-core MMAs
   int tc_slots;       // B slices that fit in the ring beside the staged S (tensor-core expand)
+  int t_tiles, n_tiles;  // persistent wide kernel: token tiles, weight tiles
   int y_stage;        // wide tiles: ring byte offset of the per-warp output staging (-1: 2-byte stores)
 };
 
@@ -974,10 +975,19 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       // every stage has been consumed: the ring now holds the S rows of this
       // tile's tokens (one read of each from L2 instead of one per element)
       const int n4 = p.r / 4;
+      const size_t part = static_cast<size_t>(p.M) * p.r / 4;     // partial sums of a split shrink, in part order
       for (int k = et; k < tv * n4; k += 128) {
         const int tl = k / n4;
-        reinterpret_cast<float4*>(s_big + tl * s_ld)[k - tl * n4] =
-            __ldcg(reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r) + (k - tl * n4));
+        const float4* src = reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r) + (k - tl * n4);
+        float4 v = __ldcg(src);
+        for (int q = 1; q < p.s_parts; ++q) {
+          const float4 w = __ldcg(src + q * part);
+          v.x += w.x;
+          v.y += w.y;
+          v.z += w.z;
+          v.w += w.w;
+        }
+        reinterpret_cast<float4*>(s_big + tl * s_ld)[k - tl * n4] = v;
       }
       asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
     }
@@ -1590,6 +1600,8 @@ int launch_gemm_tiled(const GemmArgs& a) {
       p.stage_s = 1;
     }
   }
+  // wide tiles read a split shrink's partial sums only from the staged rows
+  if (!C::kDecode && a.S != nullptr && p.s_parts > 1 && !p.stage_s) return EPILORA_ERR_UNSUPPORTED;
   p.stages = stages;
   // wide tiles without split K: output rows leave through a 5 KB staging
   // block placed after the staged S (16-byte stores need aligned rows)
@@ -1653,12 +1665,21 @@ int launch_gemm_tiled(const GemmArgs& a) {
 #ifndef EPILORA_GEMM_KA32
 #define EPILORA_GEMM_KA32 1           // atoms per stage of 32-token decode tiles
 #endif
+#ifndef EPILORA_NV_BT256
+#define EPILORA_NV_BT256 0            // 1: NVFP4 wide batches in 256-token tiles too
+#endif
 #ifndef EPILORA_GEMM_MAX_BT
 #define EPILORA_GEMM_MAX_BT 256       // widest token tile
 #endif
 #ifndef EPILORA_GEMM_KA_WIDE
 #define EPILORA_GEMM_KA_WIDE 1
 #endif
+
+}  // namespace epi
+
+#include "gemm_wide.cuh"
+
+namespace epi {
 
 template <int FMT>
 int launch_gemm_by_m(const GemmArgs& a) {
@@ -1674,7 +1695,14 @@ int launch_gemm_by_m(const GemmArgs& a) {
   if (a.M <= 16) return launch_gemm_tiled<FMT, 16, KAD>(a);
   if (a.M <= 32) return launch_gemm_tiled<FMT, 32, EPILORA_GEMM_KA32>(a);
   if (a.M <= 64) return launch_gemm_tiled<FMT, 64, KA>(a);
-  if (a.M <= 128 || EPILORA_GEMM_MAX_BT <= 128) return launch_gemm_tiled<FMT, 128, KAW>(a);
+  // (NVFP4 stages of 256 tokens carry scale boxes too: at two CTAs per SM
+  // the ring would be one stage deep, so NVFP4 stays at 128-token tiles)
+  if (a.M <= 128 || EPILORA_GEMM_MAX_BT <= 128 || (FMT == EPILORA_FMT_NVFP4 && !EPILORA_NV_BT256))
+    return launch_gemm_tiled<FMT, 128, KAW>(a);
+  if constexpr (FMT == EPILORA_FMT_FP8_E4M3) {
+    const int rc = launch_gemm_wide<FMT>(a);     // persistent, two accumulators
+    if (rc != EPILORA_ERR_UNSUPPORTED) return rc;
+  }
   return launch_gemm_tiled<FMT, 256, KAW>(a);
 }
 

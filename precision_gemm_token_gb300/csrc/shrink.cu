@@ -125,82 +125,53 @@ __device__ __forceinline__ void prefetch_inputs(const __nv_bfloat16* X, int K, i
   (void)parts;
 }
 
-// grid (M, [parts quantizer CTAs +] (r / 4) * parts rank CTAs); CTA (t, y):
-// quantizer slice y of token t, or ranks 4 * (g % (r / 4)) .. + 3 of token t
-// over K slice g / (r / 4), g = y - parts. Slices are `kslice` elements
-// (a multiple of 256); partial sums go to S[part][t][:].
-__global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bfloat16* __restrict__ X, int K,
-                                                                    int ldx, const __nv_bfloat16* __restrict__ A,
-                                                                    int L, int r, const int32_t* __restrict__ idx,
-                                                                    const uint8_t* __restrict__ mask,
-                                                                    float* __restrict__ S, int* status,
-                                                                    QuantSide qs, int parts, int kslice, int tslot,
-                                                                    int early_release) {
-  // Let the dependent GEMM launch at once: before it reads anything this grid
-  // writes it waits for this grid's completion, and until then it only
-  // streams weights. Then, when this grid is itself a programmatic dependent
-  // (of the previous call's GEMM), wait for that grid's completion: x, idx,
-  // mask and the workspace are only valid from here on (no-op for an
-  // ordinary launch).
-  if (threadIdx.x == 0) SHRINK_TRACE_MIN(0);
-  if (threadIdx.x == 0) prefetch_inputs(X, K, ldx, A, L, r, idx, qs.fmt >= 0 ? parts : 0, kslice);
-  // early_release: the GEMM may launch as soon as every CTA of this grid has
-  // started (else as they exit)
-  if (early_release) pdl_allow_dependents();
-  pdl_wait_primary();
-  if (threadIdx.x == 0) SHRINK_TRACE_MIN(1);
-  __shared__ float red[kShrinkThreads / 32][kRanksPerCta];
-
-  const size_t t = blockIdx.x;
-  int gy = static_cast<int>(blockIdx.y);
-  if (qs.fmt >= 0) {
-    if (gy < parts) {
-      // quantizer CTA: slice gy of token t, written to row q (t, or its
-      // place in the adapter-sorted order)
-      size_t q = t;
-      if (qs.perm != nullptr) {
-        q = static_cast<size_t>(sorted_row(idx, mask, L, static_cast<int>(gridDim.x), static_cast<int>(t),
-                                           reinterpret_cast<int*>(&red[0][0])));
-        if (gy == 0 && threadIdx.x == 0) qs.perm[q] = static_cast<int32_t>(t);
-      }
-      const __nv_bfloat16* xrow = X + t * static_cast<size_t>(ldx);
-      const int k0 = gy * kslice;
-      const int k1 = min(K, k0 + kslice);
-      if (qs.fmt == EPILORA_FMT_FP8_E4M3) {
-        if (parts == 1) {
-          quant_row_fp8<kShrinkQuantChunks>(xrow, K, qs.Xq + q * static_cast<size_t>(K), qs.x_scale + q,
-                                            &red[0][0]);
-        } else {
-          // every slice CTA takes the whole row's amax (the same exact max)
-          const float amax = row_amax_bf16(xrow, K, &red[0][0]);
-          const float sc = __fdiv_rn(fmaxf(amax, kAmaxFloor), kE4M3Max);
-          if (gy == 0 && threadIdx.x == 0) qs.x_scale[q] = sc;
-          if (k0 < k1) quant_slice_fp8(xrow, k0, k1, qs.Xq + q * static_cast<size_t>(K), sc);
-        }
-      } else {
-        const bool ok = quant_row_nvfp4(xrow, K, qs.Xq + q * static_cast<size_t>(K / 2),
-                                        qs.x_block_scale + q * static_cast<size_t>(K / kNvfp4Block),
-                                        *qs.x_global_scale, k0 / kNvfp4Block, k1 / kNvfp4Block);
-        if (!ok && gy == 0 && threadIdx.x == 0) record_status(status, EPILORA_ERR_INVALID_ARG);
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
-      return;
-    }
-    gy -= parts;
+// Quantizer CTA of a fused grid: K slice gy of token t (of `parts`), written
+// to row q (t, or its place in the adapter-sorted order when qs.perm is set).
+__device__ __forceinline__ void quant_role(const __nv_bfloat16* __restrict__ X, int K, int ldx,
+                                           const int32_t* __restrict__ idx, const uint8_t* __restrict__ mask, int L,
+                                           int M, size_t t, int gy, int parts, int kslice, const QuantSide& qs,
+                                           int* status, float* red) {
+  size_t q = t;
+  if (qs.perm != nullptr) {
+    q = static_cast<size_t>(sorted_row(idx, mask, L, M, static_cast<int>(t), reinterpret_cast<int*>(red)));
+    if (gy == 0 && threadIdx.x == 0) qs.perm[q] = static_cast<int32_t>(t);
   }
+  const __nv_bfloat16* xrow = X + t * static_cast<size_t>(ldx);
+  const int k0 = gy * kslice;
+  const int k1 = min(K, k0 + kslice);
+  if (qs.fmt == EPILORA_FMT_FP8_E4M3) {
+    if (parts == 1) {
+      quant_row_fp8<kShrinkQuantChunks>(xrow, K, qs.Xq + q * static_cast<size_t>(K), qs.x_scale + q, red);
+    } else {
+      // every slice CTA takes the whole row's amax (the same exact max)
+      const float amax = row_amax_bf16(xrow, K, red);
+      const float sc = __fdiv_rn(fmaxf(amax, kAmaxFloor), kE4M3Max);
+      if (gy == 0 && threadIdx.x == 0) qs.x_scale[q] = sc;
+      if (k0 < k1) quant_slice_fp8(xrow, k0, k1, qs.Xq + q * static_cast<size_t>(K), sc);
+    }
+  } else {
+    const bool ok = quant_row_nvfp4(xrow, K, qs.Xq + q * static_cast<size_t>(K / 2),
+                                    qs.x_block_scale + q * static_cast<size_t>(K / kNvfp4Block),
+                                    *qs.x_global_scale, k0 / kNvfp4Block, k1 / kNvfp4Block);
+    if (!ok && gy == 0 && threadIdx.x == 0) record_status(status, EPILORA_ERR_INVALID_ARG);
+  }
+}
 
-  const int groups = r / kRanksPerCta;
-  if (groups == 0) return;
-  const int part = gy / groups;
-  const int j0 = (gy - part * groups) * kRanksPerCta;
+// Rank CTA: ranks j0 .. j0 + 3 of token t over K slice `part` (kslice
+// elements), written to S[part][t][j0 ..]; zeros for a token without an
+// active adapter. `red` holds (blockDim.x / 32) * 4 floats.
+__device__ __forceinline__ void rank_role(const __nv_bfloat16* __restrict__ X, int K, int ldx,
+                                          const __nv_bfloat16* __restrict__ A, int L, int r,
+                                          const int32_t* __restrict__ idx, const uint8_t* __restrict__ mask,
+                                          float* __restrict__ S, int* status, int M, size_t t, int j0, int part,
+                                          int kslice, bool report, float* red) {
   const int l = idx[t];
   bool act = (l >= 0) && (mask == nullptr || mask[t] != 0);
   if (l >= L) {
-    if (gy == 0 && threadIdx.x == 0) record_status(status, EPILORA_ERR_INVALID_ARG);
+    if (report && threadIdx.x == 0) record_status(status, EPILORA_ERR_INVALID_ARG);
     act = false;
   }
-  float* srow = S + (static_cast<size_t>(part) * gridDim.x + t) * static_cast<size_t>(r) + j0;
+  float* srow = S + (static_cast<size_t>(part) * M + t) * static_cast<size_t>(r) + j0;
   if (!act) {
     if (threadIdx.x < kRanksPerCta) srow[threadIdx.x] = 0.0f;
     return;
@@ -231,20 +202,217 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
     float v = acc[j];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) red[warp][j] = v;
+    if (lane == 0) red[warp * kRanksPerCta + j] = v;
   }
   __syncthreads();
   if (threadIdx.x < kRanksPerCta) {
     float sum = 0.0f;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) sum += red[w][threadIdx.x];
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) sum += red[w * kRanksPerCta + threadIdx.x];
     srow[threadIdx.x] = sum;
-    if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
   }
 }
 
+// grid (M, [parts quantizer CTAs +] (r / 4) * parts rank CTAs); CTA (t, y):
+// quantizer slice y of token t, or ranks 4 * (g % (r / 4)) .. + 3 of token t
+// over K slice g / (r / 4), g = y - parts. Slices are `kslice` elements
+// (a multiple of 256); partial sums go to S[part][t][:].
+__global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bfloat16* __restrict__ X, int K,
+                                                                    int ldx, const __nv_bfloat16* __restrict__ A,
+                                                                    int L, int r, const int32_t* __restrict__ idx,
+                                                                    const uint8_t* __restrict__ mask,
+                                                                    float* __restrict__ S, int* status,
+                                                                    QuantSide qs, int parts, int kslice, int tslot,
+                                                                    int early_release) {
+  // Let the dependent GEMM launch at once: before it reads anything this grid
+  // writes it waits for this grid's completion, and until then it only
+  // streams weights. Then, when this grid is itself a programmatic dependent
+  // (of the previous call's GEMM), wait for that grid's completion: x, idx,
+  // mask and the workspace are only valid from here on (no-op for an
+  // ordinary launch).
+  if (threadIdx.x == 0) SHRINK_TRACE_MIN(0);
+  if (threadIdx.x == 0) prefetch_inputs(X, K, ldx, A, L, r, idx, qs.fmt >= 0 ? parts : 0, kslice);
+  // early_release: the GEMM may launch as soon as every CTA of this grid has
+  // started (else as they exit)
+  if (early_release) pdl_allow_dependents();
+  pdl_wait_primary();
+  if (threadIdx.x == 0) SHRINK_TRACE_MIN(1);
+  __shared__ float red[kShrinkThreads / 32][kRanksPerCta];
+
+  const size_t t = blockIdx.x;
+  int gy = static_cast<int>(blockIdx.y);
+  if (qs.fmt >= 0) {
+    if (gy < parts) {
+      quant_role(X, K, ldx, idx, mask, L, static_cast<int>(gridDim.x), static_cast<int>(t), gy, parts, kslice, qs,
+                 status, &red[0][0]);
+      __syncthreads();
+      if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
+      return;
+    }
+    gy -= parts;
+  }
+
+  const int groups = r / kRanksPerCta;
+  if (groups == 0) return;
+  const int part = gy / groups;
+  rank_role(X, K, ldx, A, L, r, idx, mask, S, status, static_cast<int>(gridDim.x), t,
+            (gy - part * groups) * kRanksPerCta, part, kslice, gy == 0, &red[0][0]);
+  if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
+}
+
+#ifndef EPILORA_SHRINK_BLOCK
+#define EPILORA_SHRINK_BLOCK 1       // wide batches: token-block CTAs on the tensor cores
+#endif
 #ifndef EPILORA_SHRINK_EARLY_ALL
 #define EPILORA_SHRINK_EARLY_ALL 0   // 1: grids of any size release the GEMM at CTA start
 #endif
+
+// Wide batches (M > 32): tokens in blocks of 16 consecutive tokens. A block
+// whose active tokens carry at most kBlockAdapters distinct adapters (the
+// tokens of a prefill request share one and sit next to each other) is taken
+// by one CTA per K slice that computes all r ranks of S for it on the tensor
+// cores (m16n8k16 bf16 mma.sync: products of bf16 values are exact in fp32,
+// fp32 accumulate), reading a row of the adapter's A once per block instead
+// of once per token: one pass per adapter, the x rows of the other tokens
+// zeroed; the four warps take consecutive quarters of the slice and their
+// partial tiles are added in warp order. Any other block is taken token by
+// token by rank CTAs as in shrink_kernel (4 ranks over the whole K each,
+// written to part 0; its block CTAs zero the other parts).
+// Grid: M quantizer CTAs (token blockIdx.x), nblk * parts block CTAs (block,
+// part), M * r / 4 rank CTAs (token, rank group).
+constexpr int kBlockTokens = 16;
+constexpr int kBlockAdapters = 2;
+
+// distinct active adapters of tokens t0 .. t0 + 15 (< M), for a whole warp
+__device__ __forceinline__ int block_adapters(const int32_t* __restrict__ idx, const uint8_t* __restrict__ mask,
+                                              int L, int M, int t0) {
+  const int lane = threadIdx.x & 31;
+  const int t = t0 + (lane & 15);
+  int l = -1;
+  if (t < M) {
+    l = idx[t];
+    if (l < 0 || l >= L || (mask != nullptr && mask[t] == 0)) l = -1;
+  }
+  const unsigned same = __match_any_sync(0xffffffffu, l);
+  const bool first = __ffs(same) - 1 == lane;
+  return __popc(__ballot_sync(0xffffffffu, first && l >= 0));
+}
+
+__device__ __forceinline__ uint32_t ldg_b32(const __nv_bfloat16* p) {
+  return __ldg(reinterpret_cast<const unsigned int*>(p));
+}
+
+template <int NT>   // rank tiles of 8 (r / 8)
+__global__ void __launch_bounds__(kShrinkThreads) shrink_block_kernel(const __nv_bfloat16* __restrict__ X, int K,
+                                                                      int ldx, const __nv_bfloat16* __restrict__ A,
+                                                                      int L, int r, const int32_t* __restrict__ idx,
+                                                                      const uint8_t* __restrict__ mask,
+                                                                      float* __restrict__ S, int* status,
+                                                                      QuantSide qs, int M, int parts, int kslice,
+                                                                      int tslot, int early_release) {
+  if (early_release) pdl_allow_dependents();
+  pdl_wait_primary();
+  __shared__ float red[4][kBlockTokens * 8 * NT];
+  __shared__ int lsh[kBlockTokens];
+  if (blockIdx.x < static_cast<unsigned>(M)) {
+    if (qs.fmt >= 0)
+      quant_role(X, K, ldx, idx, mask, L, M, blockIdx.x, 0, 1, K, qs, status, &red[0][0]);
+    if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
+    return;
+  }
+  const int nblk = (M + kBlockTokens - 1) / kBlockTokens;
+  const int q = static_cast<int>(blockIdx.x) - M;
+  if (q >= nblk * parts) {
+    // rank CTA of a token in a block with many adapters
+    const int groups = r / kRanksPerCta;
+    const int u = q - nblk * parts;
+    const int t = u / groups;
+    if (block_adapters(idx, mask, L, M, (t / kBlockTokens) * kBlockTokens) <= kBlockAdapters) return;
+    rank_role(X, K, ldx, A, L, r, idx, mask, S, status, M, static_cast<size_t>(t), (u - t * groups) * kRanksPerCta, 0,
+              K, u - t * groups == 0, &red[0][0]);
+    return;
+  }
+  const int blk = q / parts;
+  const int part = q - blk * parts;
+  const int t0 = blk * kBlockTokens;
+  if (block_adapters(idx, mask, L, M, t0) > kBlockAdapters) {
+    // taken token by token (part 0): zero the other parts
+    if (part > 0)
+      for (int e = threadIdx.x; e < kBlockTokens * r; e += kShrinkThreads) {
+        const int t = t0 + e / r;
+        if (t < M) S[(static_cast<size_t>(part) * M + t) * r + (e % r)] = 0.0f;
+      }
+    return;
+  }
+  if (threadIdx.x < kBlockTokens) {
+    const int t = t0 + static_cast<int>(threadIdx.x);
+    int l = -1;
+    if (t < M) {
+      l = idx[t];
+      if (l >= L) {
+        if (part == 0) record_status(status, EPILORA_ERR_INVALID_ARG);
+        l = -1;
+      }
+      if (l >= 0 && mask != nullptr && mask[t] == 0) l = -1;
+    }
+    lsh[threadIdx.x] = l;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int k0 = part * kslice, k1 = min(K, k0 + kslice);
+  const int nsteps = (k1 - k0) / 16;
+  const int s0 = (nsteps * warp) / 4, s1 = (nsteps * (warp + 1)) / 4;
+  float c[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[nt][i] = 0.0f;
+  const int lj = lsh[lane & 15];
+  uint32_t rem = __ballot_sync(0xffffffffu, lj >= 0) & 0xffffu;
+  while (rem != 0u) {
+    const int l = lsh[__ffs(rem) - 1];
+    const uint32_t rows = __ballot_sync(0xffffffffu, lj == l) & 0xffffu;
+    rem &= ~rows;
+    const bool ona = (rows >> g) & 1u, onb = (rows >> (g + 8)) & 1u;
+    // rows of tokens outside the block's valid range are never "on"
+    const __nv_bfloat16* xa = X + static_cast<size_t>(ona ? t0 + g : 0) * ldx + 2 * tq;
+    const __nv_bfloat16* xb = X + static_cast<size_t>(onb ? t0 + g + 8 : 0) * ldx + 2 * tq;
+    const __nv_bfloat16* al = A + (static_cast<size_t>(l) * r + g) * K + 2 * tq;
+#pragma unroll 2
+    for (int st = s0; st < s1; ++st) {
+      const int k = k0 + st * 16;
+      uint32_t a[4];
+      a[0] = ona ? ldg_b32(xa + k) : 0u;
+      a[1] = onb ? ldg_b32(xb + k) : 0u;
+      a[2] = ona ? ldg_b32(xa + k + 8) : 0u;
+      a[3] = onb ? ldg_b32(xb + k + 8) : 0u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const __nv_bfloat16* ar = al + static_cast<size_t>(nt * 8) * K + k;
+        mma_bf16_m16n8k16(c[nt], a, ldg_b32(ar), ldg_b32(ar + 8));
+      }
+    }
+  }
+  // tile [token 0..15][rank 0..r): this warp's partial, then the warps' sum
+  // in warp order
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    red[warp][g * (8 * NT) + nt * 8 + 2 * tq] = c[nt][0];
+    red[warp][g * (8 * NT) + nt * 8 + 2 * tq + 1] = c[nt][1];
+    red[warp][(g + 8) * (8 * NT) + nt * 8 + 2 * tq] = c[nt][2];
+    red[warp][(g + 8) * (8 * NT) + nt * 8 + 2 * tq + 1] = c[nt][3];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < kBlockTokens * 8 * NT; e += kShrinkThreads) {
+    const int tl = e / (8 * NT);
+    const int t = t0 + tl;
+    if (t < M) {
+      const float v = ((red[0][e] + red[1][e]) + red[2][e]) + red[3][e];
+      S[(static_cast<size_t>(part) * M + t) * r + (e - tl * 8 * NT)] = v;
+    }
+  }
+  if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
+}
 
 constexpr int kShrinkSliceTarget = 1024;   // elements of K per slice when splitting
 constexpr int kShrinkMaxParts = 8;
@@ -272,9 +440,18 @@ int shrink_parts_max(int K) {
 }
 
 int shrink_parts(int M, int K, int r) {
+  if (M > 32 && !EPILORA_SHRINK_BLOCK) return 1;
+  if (M > 32) {
+    // token-block CTAs: K slices of about 2048 (ranks <= 64; rank 128 keeps
+    // one slice, the wide GEMM then reads S rows straight from memory)
+    if (r <= 0 || r > 64) return 1;
+    int p = (K + 2047) / 2048;
+    if (p > kShrinkMaxParts) p = kShrinkMaxParts;
+    while (p > 1 && kslice_for(K, p) * (p - 1) >= K) --p;
+    return p < 1 ? 1 : p;
+  }
   // split K only while the grid stays small (decode): a token's chain of
   // dependent loads then shortens without adding a wave of CTAs
-  if (M > 32) return 1;
   const int per_part = M * (r / kRanksPerCta + 1);
   int p = shrink_parts_max(K);
   if (per_part <= num_sms()) {
@@ -312,9 +489,43 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
     return EPILORA_ERR_INVALID_ARG;
   if (prefer_max_shared(reinterpret_cast<const void*>(shrink_kernel), shrink_carveout_done) != EPILORA_OK)
     return EPILORA_ERR_CUDA;
-  if (perm != nullptr && (s_parts != 1 || idx == nullptr)) return EPILORA_ERR_INVALID_ARG;
+  if (perm != nullptr && (M <= 32 || idx == nullptr || (s_parts != 1 && !EPILORA_SHRINK_BLOCK)))
+    return EPILORA_ERR_INVALID_ARG;
   QuantSide qs{fmt, static_cast<uint8_t*>(Xq), x_scale, x_block_scale, x_global_scale, perm};
   const int kslice = s_parts == 1 ? K : kslice_for(K, s_parts);
+  if (M > 32 && EPILORA_SHRINK_BLOCK) {
+    // wide batch: M quantizer CTAs, then token-block CTAs (block, K slice)
+    const int nblk = r > 0 ? (M + kBlockTokens - 1) / kBlockTokens : 0;
+    const long ctas = static_cast<long>(M) + static_cast<long>(nblk) * s_parts +
+                      (r > 0 ? static_cast<long>(M) * (r / kRanksPerCta) : 0L);
+    if (ctas > (1L << 30)) return EPILORA_ERR_INVALID_ARG;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(kShrinkThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int early = EPILORA_SHRINK_EARLY_ALL || ctas <= num_sms() ? 1 : 0;
+    const __nv_bfloat16* Xb = static_cast<const __nv_bfloat16*>(X);
+    const __nv_bfloat16* Ab = static_cast<const __nv_bfloat16*>(A);
+    const int ts = trace_slot_next();
+    cudaError_t e = cudaSuccess;
+    switch (r) {
+      case 0:
+      case 16: e = cudaLaunchKernelEx(&cfg, shrink_block_kernel<2>, Xb, K, ldx, Ab, L, r, idx, mask, S, status_dev, qs,
+                                      M, s_parts, kslice, ts, early); break;
+      case 32: e = cudaLaunchKernelEx(&cfg, shrink_block_kernel<4>, Xb, K, ldx, Ab, L, r, idx, mask, S, status_dev, qs,
+                                      M, s_parts, kslice, ts, early); break;
+      case 64: e = cudaLaunchKernelEx(&cfg, shrink_block_kernel<8>, Xb, K, ldx, Ab, L, r, idx, mask, S, status_dev, qs,
+                                      M, s_parts, kslice, ts, early); break;
+      default: e = cudaLaunchKernelEx(&cfg, shrink_block_kernel<16>, Xb, K, ldx, Ab, L, r, idx, mask, S, status_dev,
+                                      qs, M, s_parts, kslice, ts, early); break;
+    }
+    return e == cudaSuccess ? EPILORA_OK : EPILORA_ERR_CUDA;
+  }
   // launched as a programmatic dependent of whatever precedes it on the
   // stream: its CTAs become resident early and wait (griddepcontrol.wait)
   // for that kernel's completion before touching x or the workspace

@@ -107,6 +107,26 @@ def test_wide_tiles_prefill_chunk_one_adapter_runs(fmt, r):
     assert_y_close(y, ref, bound, what=(fmt, r))
 
 
+WIDE_PERSISTENT = [
+    # M, K, N, L, r, idx_mode, mask_mode     (more 256-token tiles than SMs: the
+    # persistent two-accumulator kernel for FP8)
+    (520, 256, 7168, 8, 16, "uniform", "all"),           # mixed-adapter chunks, ragged token tile
+    (520, 256, 7152, 64, 32, "zipf", "prefill_chunk"),   # one-adapter runs, mask-0 tokens, ragged weight tile
+    (1000, 512, 5120, 16, 64, "zipf", "all"),            # rank 64
+    (520, 256, 7168, 8, 0, "uniform", "all"),            # no adapter
+]
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+@pytest.mark.parametrize("M,K,N,L,r,idx_mode,mask_mode", WIDE_PERSISTENT)
+def test_wide_grids_larger_than_the_gpu(fmt, M, K, N, L, r, idx_mode, mask_mode):
+    use = r > 0
+    y, ref, bound, _ = run_case(fmt, M, K, N, L, r if use else 16, seed=3 + r, idx_mode=idx_mode,
+                                mask_mode=mask_mode, n_decode=24 if mask_mode == "prefill_chunk" else 0,
+                                use_adapter=use)
+    assert_y_close(y, ref, bound, what=(fmt, M, N, r))
+
+
 def test_fp8_integer_codes_exact():
     """Rows whose amax is 448 quantize with scale 1; with small-integer values
     the codes are those integers, the fp32 accumulation is exact and Y must be
