@@ -61,7 +61,7 @@ __device__ __forceinline__ void quant_row_fp8(const __nv_bfloat16* __restrict__ 
     const int c = static_cast<int>(threadIdx.x) + j * nt;
     v[j] = c < nch ? __ldg(row + c) : make_uint4(0, 0, 0, 0);
   }
-#pragma unroll 4
+#pragma unroll 8
   for (int c = static_cast<int>(threadIdx.x) + kRowRegChunks * nt; c < nch; c += nt) {
     float x[8];
     unpack8(__ldg(row + c), x);
@@ -84,7 +84,7 @@ __device__ __forceinline__ void quant_row_fp8(const __nv_bfloat16* __restrict__ 
     const int c = static_cast<int>(threadIdx.x) + j * nt;
     if (c < nch) out[c] = quant8_e4m3(v[j], s);
   }
-#pragma unroll 4
+#pragma unroll 8
   for (int c = static_cast<int>(threadIdx.x) + kRowRegChunks * nt; c < nch; c += nt)
     out[c] = quant8_e4m3(__ldg(row + c), s);
 }

@@ -43,7 +43,7 @@ __device__ __forceinline__ float dot8(const uint4& xv, const uint4& av, float ac
 // tuning builds only: per launch (round robin over 8), earliest entry,
 // earliest return from the dependency wait, latest quantizer exit, latest
 // rank-CTA exit
-static __device__ unsigned long long g_shrink_trace[8][4];
+static __device__ unsigned long long g_shrink_trace[8][8];
 int g_shrink_trace_launches = 0;
 #define SHRINK_TRACE_MIN(i) atomicMin(&g_shrink_trace[tslot][i], globaltimer_ns())
 #define SHRINK_TRACE_MAX(i) atomicMax(&g_shrink_trace[tslot][i], globaltimer_ns())
@@ -79,7 +79,27 @@ __device__ __forceinline__ int sorted_row(const int32_t* idx, const uint8_t* mas
                                           int* red_i) {
   const int key = sort_key(idx, mask, L, t);
   int cnt = 0;
-  for (int u = threadIdx.x; u < M; u += blockDim.x) {
+  int u0 = 0;
+  if ((reinterpret_cast<uintptr_t>(idx) & 15u) == 0 && (reinterpret_cast<uintptr_t>(mask) & 3u) == 0) {
+    // four tokens per load
+    const int n4 = M / 4;
+#pragma unroll 2
+    for (int v = threadIdx.x; v < n4; v += blockDim.x) {
+      const int4 iv = reinterpret_cast<const int4*>(idx)[v];
+      const uint32_t mv = mask != nullptr ? reinterpret_cast<const uint32_t*>(mask)[v] : 0x01010101u;
+      const int ls[4] = {iv.x, iv.y, iv.z, iv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int l = ls[e];
+        const int k = (l >= 0 && l < L && ((mv >> (8 * e)) & 0xFFu) != 0u) ? l : L;
+        const int u = 4 * v + e;
+        cnt += (k < key || (k == key && u < t)) ? 1 : 0;
+      }
+    }
+    u0 = n4 * 4;
+  }
+#pragma unroll 4
+  for (int u = u0 + threadIdx.x; u < M; u += blockDim.x) {
     const int k = sort_key(idx, mask, L, u);
     cnt += (k < key || (k == key && u < t)) ? 1 : 0;
   }
@@ -277,8 +297,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
 // partial tiles are added in warp order. Any other block is taken token by
 // token by rank CTAs as in shrink_kernel (4 ranks over the whole K each,
 // written to part 0; its block CTAs zero the other parts).
-// Grid: M quantizer CTAs (token blockIdx.x), nblk * parts block CTAs (block,
-// part), M * r / 4 rank CTAs (token, rank group).
+// Grid: nblk * parts block CTAs (block, part) first, then per token its
+// quantizer CTA and r / 4 rank CTAs.
 constexpr int kBlockTokens = 16;
 constexpr int kBlockAdapters = 2;
 
@@ -297,43 +317,43 @@ __device__ __forceinline__ int block_adapters(const int32_t* __restrict__ idx, c
   return __popc(__ballot_sync(0xffffffffu, first && l >= 0));
 }
 
-__device__ __forceinline__ uint32_t ldg_b32(const __nv_bfloat16* p) {
-  return __ldg(reinterpret_cast<const unsigned int*>(p));
-}
-
-template <int NT>   // rank tiles of 8 (r / 8)
-__global__ void __launch_bounds__(kShrinkThreads) shrink_block_kernel(const __nv_bfloat16* __restrict__ X, int K,
+__global__ void __launch_bounds__(kShrinkThreads, 6) shrink_block_kernel(const __nv_bfloat16* __restrict__ X, int K,
                                                                       int ldx, const __nv_bfloat16* __restrict__ A,
                                                                       int L, int r, const int32_t* __restrict__ idx,
                                                                       const uint8_t* __restrict__ mask,
                                                                       float* __restrict__ S, int* status,
                                                                       QuantSide qs, int M, int parts, int kslice,
                                                                       int tslot, int early_release) {
+  if (threadIdx.x == 0) SHRINK_TRACE_MIN(0);
   if (early_release) pdl_allow_dependents();
   pdl_wait_primary();
-  __shared__ float red[4][kBlockTokens * 8 * NT];
+  if (threadIdx.x == 0) SHRINK_TRACE_MIN(1);
+  extern __shared__ float red_dyn[];        // [4 warps][16 tokens][r] (at least 64 floats)
   __shared__ int lsh[kBlockTokens];
-  if (blockIdx.x < static_cast<unsigned>(M)) {
-    if (qs.fmt >= 0)
-      quant_role(X, K, ldx, idx, mask, L, M, blockIdx.x, 0, 1, K, qs, status, &red[0][0]);
-    if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
-    return;
-  }
-  const int nblk = (M + kBlockTokens - 1) / kBlockTokens;
-  const int q = static_cast<int>(blockIdx.x) - M;
+  const int nblk = r > 0 ? (M + kBlockTokens - 1) / kBlockTokens : 0;
+  const int q = static_cast<int>(blockIdx.x);
   if (q >= nblk * parts) {
-    // rank CTA of a token in a block with many adapters
+    // per token: its quantizer CTA, then its rank CTAs (a token of a block
+    // with many adapters)
     const int groups = r / kRanksPerCta;
     const int u = q - nblk * parts;
-    const int t = u / groups;
+    const int t = u / (1 + groups);
+    const int role = u - t * (1 + groups);
+    if (role == 0) {
+      if (qs.fmt >= 0) quant_role(X, K, ldx, idx, mask, L, M, static_cast<size_t>(t), 0, 1, K, qs, status, red_dyn);
+      if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
+      return;
+    }
     if (block_adapters(idx, mask, L, M, (t / kBlockTokens) * kBlockTokens) <= kBlockAdapters) return;
-    rank_role(X, K, ldx, A, L, r, idx, mask, S, status, M, static_cast<size_t>(t), (u - t * groups) * kRanksPerCta, 0,
-              K, u - t * groups == 0, &red[0][0]);
+    rank_role(X, K, ldx, A, L, r, idx, mask, S, status, M, static_cast<size_t>(t), (role - 1) * kRanksPerCta, 0, K,
+              role == 1, red_dyn);
+    if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
     return;
   }
   const int blk = q / parts;
   const int part = q - blk * parts;
   const int t0 = blk * kBlockTokens;
+  if (threadIdx.x == 0) SHRINK_TRACE_MIN(5);
   if (block_adapters(idx, mask, L, M, t0) > kBlockAdapters) {
     // taken token by token (part 0): zero the other parts
     if (part > 0)
@@ -341,6 +361,7 @@ __global__ void __launch_bounds__(kShrinkThreads) shrink_block_kernel(const __nv
         const int t = t0 + e / r;
         if (t < M) S[(static_cast<size_t>(part) * M + t) * r + (e % r)] = 0.0f;
       }
+    if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
     return;
   }
   if (threadIdx.x < kBlockTokens) {
@@ -360,58 +381,86 @@ __global__ void __launch_bounds__(kShrinkThreads) shrink_block_kernel(const __nv
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int k0 = part * kslice, k1 = min(K, k0 + kslice);
-  const int nsteps = (k1 - k0) / 16;
-  const int s0 = (nsteps * warp) / 4, s1 = (nsteps * (warp + 1)) / 4;
-  float c[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c[nt][i] = 0.0f;
+  // K in chunks of 32: lane (g, tq) loads 16 bytes, k = 8 tq .. 8 tq + 7 of
+  // the chunk, of its two x rows and of each of its two rank rows; the first
+  // half feeds one m16n8k16 MMA and the second half another (the same k order
+  // on both operands, so each MMA sums 16 distinct k and the two cover the
+  // chunk). 16 ranks per pass over the slice.
+  const int nch = (k1 - k0) / 32;
+  const int c0 = (nch * warp) / 4, c1 = (nch * (warp + 1)) / 4;
   const int lj = lsh[lane & 15];
-  uint32_t rem = __ballot_sync(0xffffffffu, lj >= 0) & 0xffffu;
-  while (rem != 0u) {
-    const int l = lsh[__ffs(rem) - 1];
-    const uint32_t rows = __ballot_sync(0xffffffffu, lj == l) & 0xffffu;
-    rem &= ~rows;
-    const bool ona = (rows >> g) & 1u, onb = (rows >> (g + 8)) & 1u;
-    // rows of tokens outside the block's valid range are never "on"
-    const __nv_bfloat16* xa = X + static_cast<size_t>(ona ? t0 + g : 0) * ldx + 2 * tq;
-    const __nv_bfloat16* xb = X + static_cast<size_t>(onb ? t0 + g + 8 : 0) * ldx + 2 * tq;
-    const __nv_bfloat16* al = A + (static_cast<size_t>(l) * r + g) * K + 2 * tq;
-#pragma unroll 2
-    for (int st = s0; st < s1; ++st) {
-      const int k = k0 + st * 16;
-      uint32_t a[4];
-      a[0] = ona ? ldg_b32(xa + k) : 0u;
-      a[1] = onb ? ldg_b32(xb + k) : 0u;
-      a[2] = ona ? ldg_b32(xa + k + 8) : 0u;
-      a[3] = onb ? ldg_b32(xb + k + 8) : 0u;
+  const uint32_t act = __ballot_sync(0xffffffffu, lj >= 0) & 0xffffu;
+  float* redw = red_dyn + warp * kBlockTokens * r;
+  constexpr int U = 2;     // chunks in flight per lane
+  for (int rg = 0; rg < r / 16; ++rg) {
+    float c[2][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const __nv_bfloat16* ar = al + static_cast<size_t>(nt * 8) * K + k;
-        mma_bf16_m16n8k16(c[nt], a, ldg_b32(ar), ldg_b32(ar + 8));
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[nt][i] = 0.0f;
+    uint32_t rem = act;
+    while (rem != 0u) {
+      const int l = lsh[__ffs(rem) - 1];
+      const uint32_t rows = __ballot_sync(0xffffffffu, lj == l) & 0xffffu;
+      rem &= ~rows;
+      const bool ona = (rows >> g) & 1u, onb = (rows >> (g + 8)) & 1u;
+      // rows of tokens outside the block's valid range are never "on"
+      const uint4* xa =
+          reinterpret_cast<const uint4*>(X + static_cast<size_t>(ona ? t0 + g : 0) * ldx + k0 + 8 * tq);
+      const uint4* xb =
+          reinterpret_cast<const uint4*>(X + static_cast<size_t>(onb ? t0 + g + 8 : 0) * ldx + k0 + 8 * tq);
+      const uint4* a0 =
+          reinterpret_cast<const uint4*>(A + (static_cast<size_t>(l) * r + rg * 16 + g) * K + k0 + 8 * tq);
+      const uint4* a1 = a0 + K;    // 8 rank rows further
+      auto chunk = [&](const uint4& va, const uint4& vb, const uint4& w0, const uint4& w1) {
+        const uint32_t aA[4] = {va.x, vb.x, va.y, vb.y};
+        const uint32_t aB[4] = {va.z, vb.z, va.w, vb.w};
+        mma_bf16_m16n8k16(c[0], aA, w0.x, w0.y);
+        mma_bf16_m16n8k16(c[0], aB, w0.z, w0.w);
+        mma_bf16_m16n8k16(c[1], aA, w1.x, w1.y);
+        mma_bf16_m16n8k16(c[1], aB, w1.z, w1.w);
+      };
+      int ch = c0;
+      for (; ch + U <= c1; ch += U) {
+        uint4 va[U], vb[U], w0[U], w1[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          va[u] = ona ? __ldg(xa + (ch + u) * 4) : make_uint4(0u, 0u, 0u, 0u);
+          vb[u] = onb ? __ldg(xb + (ch + u) * 4) : make_uint4(0u, 0u, 0u, 0u);
+          w0[u] = __ldg(a0 + (ch + u) * 4);
+          w1[u] = __ldg(a1 + (ch + u) * 4);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) chunk(va[u], vb[u], w0[u], w1[u]);
+      }
+      for (; ch < c1; ++ch) {
+        const uint4 va = ona ? __ldg(xa + ch * 4) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 vb = onb ? __ldg(xb + ch * 4) : make_uint4(0u, 0u, 0u, 0u);
+        chunk(va, vb, __ldg(a0 + ch * 4), __ldg(a1 + ch * 4));
       }
     }
-  }
-  // tile [token 0..15][rank 0..r): this warp's partial, then the warps' sum
-  // in warp order
+    // this warp's partial tile [token][rank rg*16 ..]
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    red[warp][g * (8 * NT) + nt * 8 + 2 * tq] = c[nt][0];
-    red[warp][g * (8 * NT) + nt * 8 + 2 * tq + 1] = c[nt][1];
-    red[warp][(g + 8) * (8 * NT) + nt * 8 + 2 * tq] = c[nt][2];
-    red[warp][(g + 8) * (8 * NT) + nt * 8 + 2 * tq + 1] = c[nt][3];
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < kBlockTokens * 8 * NT; e += kShrinkThreads) {
-    const int tl = e / (8 * NT);
-    const int t = t0 + tl;
-    if (t < M) {
-      const float v = ((red[0][e] + red[1][e]) + red[2][e]) + red[3][e];
-      S[(static_cast<size_t>(part) * M + t) * r + (e - tl * 8 * NT)] = v;
+    for (int nt = 0; nt < 2; ++nt) {
+      const int j = rg * 16 + nt * 8 + 2 * tq;
+      redw[g * r + j] = c[nt][0];
+      redw[g * r + j + 1] = c[nt][1];
+      redw[(g + 8) * r + j] = c[nt][2];
+      redw[(g + 8) * r + j + 1] = c[nt][3];
     }
   }
-  if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
+  __syncthreads();
+  // the warps' partial tiles added in warp order
+  const int tile = kBlockTokens * r;
+  for (int e = threadIdx.x; e < tile; e += kShrinkThreads) {
+    const int tl = e / r;
+    const int t = t0 + tl;
+    if (t < M) {
+      const float v = ((red_dyn[e] + red_dyn[tile + e]) + red_dyn[2 * tile + e]) + red_dyn[3 * tile + e];
+      S[(static_cast<size_t>(part) * M + t) * r + (e - tl * r)] = v;
+    }
+  }
+  if (threadIdx.x == 0) SHRINK_TRACE_MAX(4);
 }
 
 constexpr int kShrinkSliceTarget = 1024;   // elements of K per slice when splitting
@@ -509,21 +558,11 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const int early = EPILORA_SHRINK_EARLY_ALL || ctas <= num_sms() ? 1 : 0;
-    const __nv_bfloat16* Xb = static_cast<const __nv_bfloat16*>(X);
-    const __nv_bfloat16* Ab = static_cast<const __nv_bfloat16*>(A);
-    const int ts = trace_slot_next();
-    cudaError_t e = cudaSuccess;
-    switch (r) {
-      case 0:
-      case 16: e = cudaLaunchKernelEx(&cfg, shrink_block_kernel<2>, Xb, K, ldx, Ab, L, r, idx, mask, S, status_dev, qs,
-                                      M, s_parts, kslice, ts, early); break;
-      case 32: e = cudaLaunchKernelEx(&cfg, shrink_block_kernel<4>, Xb, K, ldx, Ab, L, r, idx, mask, S, status_dev, qs,
-                                      M, s_parts, kslice, ts, early); break;
-      case 64: e = cudaLaunchKernelEx(&cfg, shrink_block_kernel<8>, Xb, K, ldx, Ab, L, r, idx, mask, S, status_dev, qs,
-                                      M, s_parts, kslice, ts, early); break;
-      default: e = cudaLaunchKernelEx(&cfg, shrink_block_kernel<16>, Xb, K, ldx, Ab, L, r, idx, mask, S, status_dev,
-                                      qs, M, s_parts, kslice, ts, early); break;
-    }
+    // per-warp partial tiles of a token block (and the quantizers' scratch)
+    cfg.dynamicSmemBytes = static_cast<size_t>(4) * kBlockTokens * (r > 4 ? r : 4) * sizeof(float);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, shrink_block_kernel, static_cast<const __nv_bfloat16*>(X), K, ldx,
+                                             static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S, status_dev, qs,
+                                             M, s_parts, kslice, trace_slot_next(), early);
     return e == cudaSuccess ? EPILORA_OK : EPILORA_ERR_CUDA;
   }
   // launched as a programmatic dependent of whatever precedes it on the
@@ -560,10 +599,10 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
 extern "C" EPILORA_API int epilora_debug_shrink_trace(void* host_out, int clear) {
   if (cudaMemcpyFromSymbol(host_out, epi::g_shrink_trace, sizeof(epi::g_shrink_trace)) != cudaSuccess) return -3;
   if (clear) {
-    static unsigned long long init[8][4];
+    static unsigned long long init[8][8];
     for (auto& row : init) {
-      row[0] = row[1] = ~0ull;
-      row[2] = row[3] = 0ull;
+      row[0] = row[1] = row[5] = ~0ull;   // earliest: entry, after the wait, block CTA start
+      row[2] = row[3] = row[4] = row[6] = row[7] = 0ull;   // latest: quantizer, rank, block CTA ends
     }
     if (cudaMemcpyToSymbol(epi::g_shrink_trace, init, sizeof(init)) != cudaSuccess) return -3;
     epi::g_shrink_trace_launches = 0;
