@@ -563,10 +563,11 @@ def run_profile(args):
 
 def run_profile_wide(args):
     """A wide-tile fused layer call alone, for ncu: the Llama-3.1-70B gate_up
-    projection's 1/8 column slice (K 8192 -> N 7168) over the prefill-chunk
-    batch (64 mask-0 decode tokens + 2048 prefill tokens on one adapter, 512
-    resident rank-16 adapters, Zipf(1.1) indices, FP8), five layer_forward
-    calls (shrink grid + GEMM each)."""
+    projection's quarter column slice (K 8192 -> N 14336: 1008 tiles of
+    256x128, the persistent kernel) over the prefill-chunk batch (64 mask-0
+    decode tokens + 2048 prefill tokens on one adapter, 512 resident rank-16
+    adapters, Zipf(1.1) indices, FP8), five layer_forward calls (shrink grid
+    + GEMM each)."""
     import torch
 
     import precision_gemm_token_gb300 as E
@@ -575,7 +576,7 @@ def run_profile_wide(args):
 
     E.build()
     E.load()
-    M, K, N = 2112, 8192, 57344 // 8
+    M, K, N = 2112, 8192, 57344 // 4
     p = make_projection(M, K, N, 512, 16, seed=5, idx_mode="zipf", mask_mode="prefill_chunk", n_decode=64,
                         device="cuda")
     w = T.quantize_weight(p.W, 0)
@@ -583,7 +584,7 @@ def run_profile_wide(args):
     for _ in range(5):
         T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, workspace=ws)
     torch.cuda.synchronize()
-    print(json.dumps({"profile": "70b_gate_up_slice_prefill2112_fp8", "kernel": f"gate_up {K}->{N} M={M}",
+    print(json.dumps({"profile": "70b_gate_up_quarter_prefill2112_fp8", "kernel": f"gate_up {K}->{N} M={M}",
                       "ok": True}))
 
 
