@@ -295,10 +295,10 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
 // of once per token: one pass per adapter, the x rows of the other tokens
 // zeroed; the four warps take consecutive quarters of the slice and their
 // partial tiles are added in warp order. Any other block is taken token by
-// token by rank CTAs as in shrink_kernel (4 ranks over the whole K each,
-// written to part 0; its block CTAs zero the other parts).
+// token by rank CTAs as in shrink_kernel (16 ranks over the whole K each, in
+// groups of 4, written to part 0; its block CTAs zero the other parts).
 // Grid: nblk * parts block CTAs (block, part) first, then per token its
-// quantizer CTA and r / 4 rank CTAs.
+// quantizer CTA and r / 16 rank CTAs.
 constexpr int kBlockTokens = 16;
 constexpr int kBlockAdapters = 2;
 
@@ -333,9 +333,9 @@ __global__ void __launch_bounds__(kShrinkThreads, 6) shrink_block_kernel(const _
   const int nblk = r > 0 ? (M + kBlockTokens - 1) / kBlockTokens : 0;
   const int q = static_cast<int>(blockIdx.x);
   if (q >= nblk * parts) {
-    // per token: its quantizer CTA, then its rank CTAs (a token of a block
-    // with many adapters)
-    const int groups = r / kRanksPerCta;
+    // per token: its quantizer CTA, then its rank CTAs of 16 ranks each (a
+    // token of a block with many adapters; four rank groups in turn)
+    const int groups = r / 16;
     const int u = q - nblk * parts;
     const int t = u / (1 + groups);
     const int role = u - t * (1 + groups);
@@ -345,8 +345,11 @@ __global__ void __launch_bounds__(kShrinkThreads, 6) shrink_block_kernel(const _
       return;
     }
     if (block_adapters(idx, mask, L, M, (t / kBlockTokens) * kBlockTokens) <= kBlockAdapters) return;
-    rank_role(X, K, ldx, A, L, r, idx, mask, S, status, M, static_cast<size_t>(t), (role - 1) * kRanksPerCta, 0, K,
-              role == 1, red_dyn);
+    for (int gq = 0; gq < 16 / kRanksPerCta; ++gq) {
+      if (gq > 0) __syncthreads();     // the previous group's partial sums are read out
+      rank_role(X, K, ldx, A, L, r, idx, mask, S, status, M, static_cast<size_t>(t),
+                (role - 1) * 16 + gq * kRanksPerCta, 0, K, role == 1 && gq == 0, red_dyn);
+    }
     if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
     return;
   }
@@ -546,7 +549,7 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
     // wide batch: M quantizer CTAs, then token-block CTAs (block, K slice)
     const int nblk = r > 0 ? (M + kBlockTokens - 1) / kBlockTokens : 0;
     const long ctas = static_cast<long>(M) + static_cast<long>(nblk) * s_parts +
-                      (r > 0 ? static_cast<long>(M) * (r / kRanksPerCta) : 0L);
+                      (r > 0 ? static_cast<long>(M) * (r / 16) : 0L);
     if (ctas > (1L << 30)) return EPILORA_ERR_INVALID_ARG;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
