@@ -147,6 +147,7 @@ __device__ __forceinline__ void prefetch_inputs(const __nv_bfloat16* X, int K, i
 
 // Quantizer CTA of a fused grid: K slice gy of token t (of `parts`), written
 // to row q (t, or its place in the adapter-sorted order when qs.perm is set).
+template <int kRegChunks>   // 16-byte chunks of the row each thread holds in registers
 __device__ __forceinline__ void quant_role(const __nv_bfloat16* __restrict__ X, int K, int ldx,
                                            const int32_t* __restrict__ idx, const uint8_t* __restrict__ mask, int L,
                                            int M, size_t t, int gy, int parts, int kslice, const QuantSide& qs,
@@ -161,7 +162,7 @@ __device__ __forceinline__ void quant_role(const __nv_bfloat16* __restrict__ X, 
   const int k1 = min(K, k0 + kslice);
   if (qs.fmt == EPILORA_FMT_FP8_E4M3) {
     if (parts == 1) {
-      quant_row_fp8<kShrinkQuantChunks>(xrow, K, qs.Xq + q * static_cast<size_t>(K), qs.x_scale + q, red);
+      quant_row_fp8<kRegChunks>(xrow, K, qs.Xq + q * static_cast<size_t>(K), qs.x_scale + q, red);
     } else {
       // every slice CTA takes the whole row's amax (the same exact max)
       const float amax = row_amax_bf16(xrow, K, red);
@@ -262,8 +263,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   int gy = static_cast<int>(blockIdx.y);
   if (qs.fmt >= 0) {
     if (gy < parts) {
-      quant_role(X, K, ldx, idx, mask, L, static_cast<int>(gridDim.x), static_cast<int>(t), gy, parts, kslice, qs,
-                 status, &red[0][0]);
+      quant_role<kShrinkQuantChunks>(X, K, ldx, idx, mask, L, static_cast<int>(gridDim.x), static_cast<int>(t), gy,
+                                     parts, kslice, qs, status, &red[0][0]);
       __syncthreads();
       if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
       return;
@@ -340,7 +341,9 @@ __global__ void __launch_bounds__(kShrinkThreads, 6) shrink_block_kernel(const _
     const int t = u / (1 + groups);
     const int role = u - t * (1 + groups);
     if (role == 0) {
-      if (qs.fmt >= 0) quant_role(X, K, ldx, idx, mask, L, M, static_cast<size_t>(t), 0, 1, K, qs, status, red_dyn);
+      // rows of up to 8192 elements stay in registers between the amax and the codes
+      if (qs.fmt >= 0)
+        quant_role<8>(X, K, ldx, idx, mask, L, M, static_cast<size_t>(t), 0, 1, K, qs, status, red_dyn);
       if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
       return;
     }
