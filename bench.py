@@ -347,7 +347,16 @@ def run_ours(args, rank, world, local):
             flops = sum(2.0 * Ml * N * K for _, K, N in plist)
             peak_l = bf16 * (2.0 if fl == 0 else 6.0)
             tf = flops / (ms_l / 1000) / 1e12
+            # the same layer against HBM: distinct adapters active per projection
+            bytes_l = 0
+            for q, (_, K, N) in zip(projs_l, plist):
+                pq = q["p"]
+                act = [int(i) for i, m in zip(pq.idx.tolist(), pq.mask.tolist()) if i >= 0 and m != 0]
+                bytes_l += algorithmic_bytes(Ml, K, N, fl, spec[5], len(set(act)))
+            gbs_l = bytes_l / (ms_l / 1000) / 1e9
             large.append({"workload": desc_l, "M": Ml, "layer_us": round(ms_l * 1000, 1), "tflops": round(tf, 1),
+                          "algorithmic_bytes": int(bytes_l), "hbm_gbs": round(gbs_l, 1),
+                          "hbm_frac_of_measured": round(gbs_l / peaks.get("hbm_gbs", 6800.0), 4),
                           "peak_tflops": round(peak_l, 1), "frac": round(tf / peak_l, 4),
                           "peak_source": "measured bf16 burst x " + ("2 (FP8)" if fl == 0 else "6 (NVFP4)")})
             del projs_l
