@@ -176,27 +176,33 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
 
 /*
  * Bytes of device workspace epilora_layer_forward needs for (fmt, M, K, r):
- * the quantized activations, their scales and S (r = 0: no adapters; for a
- * few tokens S is held as up to ceil(K / 1024) partial sums over K slices,
- * capped at 8), each region 256-byte aligned. Returns 0 for M == 0 or
- * invalid arguments.
+ * the quantized activations, their scales, S (r = 0: no adapters; S is held
+ * as up to ceil(K / 1024) partial sums over K slices, capped at 8) and, for
+ * more than 32 tokens with adapters, a row-to-token map, each region
+ * 256-byte aligned. Returns 0 for M == 0 or invalid arguments.
  */
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
 
 /*
  * Fused one-call layer (the decode path of the EpiLoRA page, §Design ›
  * Multi-adapter kernels › The decode path): enqueues two kernels,
- *   1. the shrink grid of epilora_lora_shrink (for a few tokens split over
- *      K slices) plus quantizer CTAs (the arithmetic of epilora_quant_act),
- *      launched as a programmatic dependent of the previous kernel on the
- *      stream: it lets the GEMM launch at once, then waits for that kernel's
- *      completion before reading anything, and
+ *   1. the shrink grid (the arithmetic of epilora_lora_shrink, split over K
+ *      slices into partial sums; for more than 32 tokens, blocks of 16
+ *      consecutive tokens carrying at most two adapters on the tensor
+ *      cores) plus quantizer CTAs (the arithmetic of epilora_quant_act; for
+ *      more than 32 tokens with adapters the rows of Xq are written in
+ *      adapter-sorted order), launched as a programmatic dependent of the
+ *      previous kernel on the stream: it lets the GEMM launch when its CTAs
+ *      start (decode batches, or a grid that fits the GPU) or as they
+ *      finish, and waits for that kernel's completion before reading
+ *      anything, and
  *   2. the GEMM of epilora_gemm_lora_epilogue as its programmatic dependent:
  *      it starts streaming Wq (and w_block_scale) as soon as it is resident,
  *      and reads everything else only after the shrink grid has completed;
  * using `workspace` (>= epilora_workspace_bytes, 256-byte aligned, no
- * initial value needed) for Xq, scales and S. Calls that share a workspace
- * must be ordered on one stream.
+ * initial value needed) for Xq, scales, S and the row map. Y is the same
+ * whatever the row order. Calls that share a workspace must be ordered on
+ * one stream.
  * Because the GEMM may start while the kernel that precedes this call on the
  * stream is still running, that kernel must not write Wq or w_block_scale
  * (every other input, X included, may be its output).
