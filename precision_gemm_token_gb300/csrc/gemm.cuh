@@ -75,14 +75,6 @@
 #ifndef EPILORA_GEMM_B_EARLY
 #define EPILORA_GEMM_B_EARLY 1          // one-group decode tiles load their B slice into a buffer of its own
 #endif
-#ifndef EPILORA_GEMM_TC_EXPAND
-// Wide tiles: the adapter term of one-adapter column runs from bf16 MMAs
-// added into the FP8/NVFP4 accumulator. Off: adding them into an
-// accumulator that already holds the base sum cost the base about 2^-9 of
-// its magnitude (measured), far above fp32 rounding; a separate accumulator
-// needs TMEM that two CTAs per SM do not leave.
-#define EPILORA_GEMM_TC_EXPAND 0
-#endif
 #ifndef EPILORA_GEMM_B_L2
 #define EPILORA_GEMM_B_L2 0             // prefetch streamed B slices into L2 after set-up
 #endif
@@ -139,8 +131,6 @@ struct GemmParams {
   int b_early;        // 1: a decode tile with one adapter group loads its B slice at once into its own buffer
   int trace_slot;     // tuning builds only: which trace buffer this launch fills
   int l2_ahead;       // fused call: weight stages past the ring to prefetch into L2 while waiting
-  int tc_expand;      // wide tiles: one-adapter column chunks get their adapter term from tensor-core MMAs
-  int tc_slots;       // B slices that fit in the ring beside the staged S (tensor-core expand)
   int t_tiles, n_tiles;  // persistent wide kernel: token tiles, weight tiles
   int y_stage;        // wide tiles: ring byte offset of the per-warp output staging (-1: 2-byte stores)
 };
@@ -313,20 +303,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   uint64_t* acc_bar = empty_bar + stages;
   uint64_t* meta_bar = acc_bar + 1;           // token metadata and adapter groups are in shared memory
   uint64_t* b_bar = meta_bar + 1;             // the early B slice has landed
-  uint64_t* expand_bar = b_bar + 1;           // tensor-core expand: operands staged in the ring
-  uint64_t* acc2_bar = expand_bar + 1;        // tensor-core expand: MMAs complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc2_bar + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* ngroups_s = reinterpret_cast<int*>(tmem_slot + 2);
   float* meta_sx = reinterpret_cast<float*>(tmem_slot + 4);
   int* meta_idx = reinterpret_cast<int*>(meta_sx + BT);       // adapter slot, -1 = none
   int* meta_tok = meta_idx + BT;                               // token of each tile column (row of Y and S)
-  // tensor-core expand plan: [0] runs, then (first column, columns, B slot)
-  // per run (at most 16), then the adapter of each B slot (at most 4), then
-  // a bitmask of the expanded columns
-  int* xplan = meta_tok + BT;
-  int* xslot_l = xplan + 1 + 3 * 16;
-  uint32_t* xmask = reinterpret_cast<uint32_t*>(xslot_l + 4);
   float* s_big = reinterpret_cast<float*>(smem);               // non-decode: S rows of the tile, after the main loop
   const int s_ld = p.r + 4;                                    // its row stride in floats (bank-conflict padding)
   // decode region (BT <= kDecodeBT)
@@ -399,8 +381,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     mbar_init(acc_bar, 1);
     mbar_init(meta_bar, 1);
     mbar_init(b_bar, 1);
-    mbar_init(expand_bar, 1);
-    mbar_init(acc2_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     // the ring starts empty: stream weights into it before anything else
@@ -542,9 +522,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     n_bslots = sb && !b_early_on ? (ngroups + gps - 1) / gps : 0;
     n_loads = nkb + n_bslots;
   };
-
-  // wide tiles may take their adapter term from tensor-core MMAs (uniform)
-  const bool tc_on = !C::kDecode && ks == 1 && p.tc_expand && p.S != nullptr;
 
   // epilogue state carried from the main-loop phase into the epilogue phase
   int cached_key = -1;
@@ -741,38 +718,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     }
     if (lane == 0) tc_commit(acc_bar);   // accumulator complete (or drained after an abort)
     __syncwarp();
-    if (tc_on) {
-      // Tensor-core expand: once the epilogue warps have staged S' (S / x
-      // scale) and B' (B / weight scale) in bf16 in the ring, add S'.B'^T of
-      // every one-adapter run of columns into the same accumulator; the
-      // epilogue then finishes those columns with the scales alone.
-      const bool okx = __all_sync(0xffffffffu, mbar_wait_bounded(expand_bar, 0, kWaitLimitNs));
-      if (lane == 0) {
-        if (okx && !*abort_flag) {
-          tc_fence_after();
-          const int atoms = p.r > 64 ? 2 : 1;
-          const uint32_t sp = smem_u32(smem);
-          const uint32_t bp = sp + static_cast<uint32_t>(atoms * BT * 128);
-          const int nrun = xplan[0];
-          for (int q = 0; q < nrun; ++q) {
-            const int col0 = xplan[1 + 3 * q], ncols = xplan[2 + 3 * q], slot = xplan[3 + 3 * q];
-            const uint32_t idesc = idesc_bf16(kTileN, static_cast<uint32_t>(ncols));
-            for (int a = 0; a < atoms; ++a) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t adesc = make_smem_desc(
-                    bp + static_cast<uint32_t>((slot * atoms + a) * 16384 + kk * 32), 16, 1024, kSwizzle128B);
-                const uint64_t bdesc = make_smem_desc(
-                    sp + static_cast<uint32_t>((a * BT + col0) * 128 + kk * 32), 16, 1024, kSwizzle128B);
-                mma_bf16(tmem_base + static_cast<uint32_t>(col0), adesc, bdesc, idesc, 1u);
-              }
-            }
-          }
-        }
-        tc_commit(acc2_bar);
-      }
-      __syncwarp();
-    }
     if (ks > 1) {
       cluster_wait();      // first phase (armed after setup)
       cluster_arrive();    // second phase: nothing of this warp is still to land in a peer
@@ -873,105 +818,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       }
     }
     const bool all_ok = !epi_bar_any(!ok);    // uniform over the four warps (a barrier follows)
-    if (tc_on) {
-      // every stage has been consumed: plan the one-adapter column runs,
-      // stage their S' rows and the B' slices in the ring (bf16, 128-byte
-      // rows in the 128-byte swizzle the MMA reads), hand over to the MMA
-      // warp, and wait for its MMAs
-      const int atoms = p.r > 64 ? 2 : 1;
-      if (et == 0) {
-        int nrun = 0, nslot = 0;
-        for (int w = 0; w < 8; ++w) xmask[w] = 0u;
-        auto pure = [&](int c) {   // adapter of a fully valid one-adapter 16-column chunk, else -1
-          if (c * 16 + 15 >= tv) return -1;
-          const int l = meta_idx[c * 16];
-          if (l < 0) return -1;
-          for (int j = 1; j < 16; ++j)
-            if (meta_idx[c * 16 + j] != l) return -1;
-          return l;
-        };
-        if (all_ok) {
-          int c = 0;
-          while (c < BT / 16 && nrun < 16) {
-            const int l = pure(c);
-            if (l < 0) {
-              ++c;
-              continue;
-            }
-            int c1 = c + 1;
-            while (c1 < BT / 16 && pure(c1) == l) ++c1;
-            int slot = -1;
-            for (int q = 0; q < nslot; ++q)
-              if (xslot_l[q] == l) slot = q;
-            if (slot < 0 && nslot < p.tc_slots) {
-              slot = nslot++;
-              xslot_l[slot] = l;
-            }
-            if (slot >= 0) {
-              xplan[1 + 3 * nrun] = c * 16;
-              xplan[2 + 3 * nrun] = (c1 - c) * 16;
-              xplan[3 + 3 * nrun] = slot;
-              ++nrun;
-              for (int col = c * 16; col < c1 * 16; ++col) xmask[col >> 5] |= 1u << (col & 31);
-            }
-            c = c1;
-          }
-        }
-        xplan[0] = nrun;
-        ngroups_s[1] = nslot;
-      }
-      asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
-      const int nslot = ngroups_s[1];
-      uint8_t* sp = smem;
-      uint8_t* bp = smem + atoms * BT * 128;
-      {
-        // B' rows: this thread's weight row m of each slot's adapter, / w scale
-        const int m = (warp & 3) * 32 + lane;
-        const float inv = C::kFP4 ? 1.0f : (sw_pre != 0.0f ? 1.0f / sw_pre : 0.0f);
-        for (int q = 0; q < nslot; ++q) {
-          const bool in = n0 + m < p.N;
-          const uint4* src = reinterpret_cast<const uint4*>(p.B + (static_cast<size_t>(xslot_l[q]) * p.N + n0 + m) * p.r);
-          for (int c = 0; c < 8 * atoms; ++c) {
-            uint4 o = make_uint4(0u, 0u, 0u, 0u);
-            if (in && c < p.r / 8) {
-              const uint4 v = __ldg(src + c);
-              o.x = pack_bf16x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv);
-              o.y = pack_bf16x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv);
-              o.z = pack_bf16x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv);
-              o.w = pack_bf16x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv);
-            }
-            const int a = c >> 3, cc = c & 7;
-            *reinterpret_cast<uint4*>(bp + (q * atoms + a) * 16384 + m * 128 + ((cc ^ (m & 7)) << 4)) = o;
-          }
-        }
-        // S' rows of the expanded columns: S / x scale (FP8) or S * g_x * g_w (NVFP4)
-        for (int k = et; k < BT * 8 * atoms; k += 128) {
-          const int col = k / (8 * atoms), c = k - col * 8 * atoms;
-          if (!(xmask[col >> 5] & (1u << (col & 31)))) continue;
-          const float sc = C::kFP4 ? 1.0f / alpha_pre : 1.0f / meta_sx[col];
-          uint4 o = make_uint4(0u, 0u, 0u, 0u);
-          if (c < p.r / 8) {
-            const float4* srow = reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[col]) * p.r) + 2 * c;
-            const float4 s0 = __ldcg(srow), s1 = __ldcg(srow + 1);
-            o.x = pack_bf16x2(s0.x * sc, s0.y * sc);
-            o.y = pack_bf16x2(s0.z * sc, s0.w * sc);
-            o.z = pack_bf16x2(s1.x * sc, s1.y * sc);
-            o.w = pack_bf16x2(s1.z * sc, s1.w * sc);
-          }
-          const int a = c >> 3, cc = c & 7;
-          *reinterpret_cast<uint4*>(sp + (a * BT + col) * 128 + ((cc ^ (col & 7)) << 4)) = o;
-        }
-      }
-      fence_proxy_async_smem();     // generic-proxy writes, read by the MMA (async proxy)
-      asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
-      if (et == 0) mbar_arrive(expand_bar);
-      const bool ok2 = mbar_wait_bounded(acc2_bar, 0, kWaitLimitNs);
-      if (!ok2) {
-        *abort_flag = 1;
-        record_status(p.status, EPILORA_ERR_TIMEOUT);
-      }
-      tc_fence_after();
-    } else if (!C::kDecode && p.stage_s && all_ok) {
+    if (!C::kDecode && p.stage_s && all_ok) {
       // every stage has been consumed: the ring now holds the S rows of this
       // tile's tokens (one read of each from L2 instead of one per element)
       const int n4 = p.r / 4;
@@ -1277,7 +1124,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
           const int jl = c * 16 + (lane & 15);
           const int lj = jl < tv ? meta_idx[jl] : -1;
           const uint32_t actm = __ballot_sync(0xffffffffu, lj >= 0) & 0xffffu;
-          if (kMma && !tc_on && p.stage_s && p.y_stage >= 0) {
+          if (kMma && p.stage_s && p.y_stage >= 0) {
             uint32_t va[2][8];
             tmem_ld_16x256b_x2(lane_base + c * 16, va[0]);
             tmem_ld_16x256b_x2(lane_base + (16u << 16) + c * 16, va[1]);
@@ -1348,8 +1195,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
               if (tl < tv) {
                 float y = base_value(m, tl, __uint_as_float(v[j]), sw);
                 const int l = meta_idx[tl];
-                const bool expanded = tc_on && (xmask[tl >> 5] & (1u << (tl & 31)));
-                if (l >= 0 && !expanded) {
+                if (l >= 0) {
                   if (l != cur_l) {
                     load_brow(l, m);
                     cur_l = l;
@@ -1575,23 +1421,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   // non-decode tiles stage S of their tokens in the ring once the main loop
   // is over (one fp32 row of r per token column); deepen the ring if needed
   p.stage_s = 0;
-  p.tc_expand = 0;
-  p.tc_slots = 0;
-  if (!C::kDecode && a.S != nullptr && ks == 1 && EPILORA_GEMM_TC_EXPAND) {
-    // tensor-core expand: S' of every column plus at least one B' slice in
-    // the ring once the main loop is over (rows of 128 bytes, two atoms for
-    // rank 128)
-    const int atoms = a.r > 64 ? 2 : 1;
-    const int ring = stages * C::kStageBytes;
-    const int sp = atoms * BT * 128;
-    const int slot = atoms * kTileN * 128;
-    const int nslots = (ring - sp) / slot;
-    if (nslots >= 1) {
-      p.tc_expand = 1;
-      p.tc_slots = nslots > 4 ? 4 : nslots;
-    }
-  }
-  if (!C::kDecode && a.S != nullptr && !p.tc_expand) {
+  if (!C::kDecode && a.S != nullptr) {
     const int need = BT * (a.r + 4) * 4 + 5 * 1024;     // padded S rows + the output staging
     int st_need = (need + C::kStageBytes - 1) / C::kStageBytes;
     if (st_need < stages) st_need = stages;
@@ -1606,7 +1436,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   // wide tiles without split K: output rows leave through a 5 KB staging
   // block placed after the staged S (16-byte stores need aligned rows)
   p.y_stage = -1;
-  if (!C::kDecode && ks == 1 && !p.tc_expand && (reinterpret_cast<uintptr_t>(a.Y) & 15) == 0 && a.ldy % 8 == 0) {
+  if (!C::kDecode && ks == 1 && (reinterpret_cast<uintptr_t>(a.Y) & 15) == 0 && a.ldy % 8 == 0) {
     const int off = p.stage_s ? (BT * (a.r + 4) * 4 + 127) / 128 * 128 : 0;
     if (off + 5 * 1024 <= stages * C::kStageBytes) p.y_stage = off;
   }

@@ -174,17 +174,6 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
-// D[tmem] (+)= A[smem] . B[smem]^T with bf16 operands (kind::f16), both K-major.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Block-scaled NVFP4 MMA: E2M1 operands with one UE4M3 scale per 16 elements
 // (four per row per K = 64 step), scales read from TMEM.
 __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -279,15 +268,6 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4_e4m3(uint32_t M, uint32_t N)
          | (0u << 16)            // B K-major
          | ((N >> 3) << 17)      // N / 8
          | ((M >> 4) << 24);     // M / 16
-}
-
-// Instruction descriptor, kind::f16, BF16 x BF16 -> F32, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
-  return (1u << 4)               // D format: F32
-         | (1u << 7)             // A format: BF16
-         | (1u << 10)            // B format: BF16
-         | ((N >> 3) << 17)
-         | ((M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::mxf4nvf4 (block scaled), E2M1 x E2M1, UE4M3
