@@ -127,6 +127,21 @@ def test_wide_grids_larger_than_the_gpu(fmt, M, K, N, L, r, idx_mode, mask_mode)
     assert_y_close(y, ref, bound, what=(fmt, M, N, r))
 
 
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+@pytest.mark.parametrize("M,K,N,L,r,idx_mode,mask_mode", [
+    (48, 4096, 256, 4, 16, "zipf", "prefill_chunk"),      # token blocks over 2 K slices
+    (80, 6144, 128, 6, 64, "zipf", "prefill_chunk"),      # rank 64, 3 K slices, ragged last block
+    (64, 4096, 256, 8, 32, "uniform", "all"),             # blocks with many adapters: per-token CTAs + zeroed parts
+])
+def test_wide_shrink_split_over_k(fmt, M, K, N, L, r, idx_mode, mask_mode):
+    """More than 32 tokens with K long enough for the shrink to split it:
+    token-block CTAs on the tensor cores write partial sums per K slice (and
+    zero them for blocks taken token by token); the GEMM adds them in order."""
+    y, ref, bound, _ = run_case(fmt, M, K, N, L, r, seed=M + r, idx_mode=idx_mode, mask_mode=mask_mode,
+                                n_decode=8 if mask_mode == "prefill_chunk" else 0)
+    assert_y_close(y, ref, bound, what=(fmt, M, K, r))
+
+
 def test_fp8_integer_codes_exact():
     """Rows whose amax is 448 quantize with scale 1; with small-integer values
     the codes are those integers, the fp32 accumulation is exact and Y must be
