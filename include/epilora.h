@@ -221,6 +221,31 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K,
                           int* status_dev, void* stream);
 
 /*
+ * Multi-slice projection (the EpiLoRA page, §Design › Multi-adapter kernels:
+ * fused projections such as qkv or gate_up carry one adapter per slice):
+ * epilora_layer_forward where output columns [slice_end[s-1], slice_end[s])
+ * (slice_end[-1] = 0) take slice s's own rank-r adapter pair. A is bf16
+ * [L, n_slices * r, K] (slice s's A rows at [s*r, (s+1)*r)), B stays
+ * [L, N, r] (row n belongs to its column's slice). n_slices in 1..4;
+ * slice_end (host memory, read during the call) ascending, every end but the
+ * last a multiple of 128, the last == N. The workspace must hold
+ * epilora_workspace_bytes(fmt, M, K, n_slices * r) bytes. idx / mask select
+ * one adapter slot per token for all slices. Other arguments and errors as
+ * epilora_layer_forward (A and B are required).
+ */
+EPILORA_API int epilora_layer_forward_slices(int fmt, int M, int N, int K,
+                          const void* X, int ldx,
+                          const void* Wq, const float* w_scale,
+                          const uint8_t* w_block_scale, const float* w_global_scale,
+                          const float* x_global_scale,
+                          const void* A, const void* B, int L, int r,
+                          int n_slices, const int* slice_end,
+                          const int32_t* idx, const uint8_t* mask,
+                          void* Y, int ldy,
+                          void* workspace, size_t workspace_bytes,
+                          int* status_dev, void* stream);
+
+/*
  * epilora_layer_forward without a caller workspace. The EpiLoRA page has no
  * counterpart of this entry point: it serves callers that cannot hand the
  * library device memory, such as a plain C host with no device allocator of

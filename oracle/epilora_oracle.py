@@ -193,16 +193,35 @@ def base_gemm_nvfp4(xq: np.ndarray, sbx: np.ndarray, gx, wq: np.ndarray, sbw: np
     return acc / (np.float64(F32(gx)) * np.float64(F32(gw)))
 
 
+def expand_slices(S: np.ndarray, B: np.ndarray, idx: np.ndarray, mask: np.ndarray | None,
+                  slice_end) -> np.ndarray:
+    """Multi-slice projection (EpiLoRA, §Design › Multi-adapter kernels: a
+    fused projection carries one adapter per slice): output columns
+    [slice_end[s-1], slice_end[s]) take S[:, s*r:(s+1)*r] . B[idx_t][n]^T."""
+    B = np.asarray(B, dtype=np.float64)
+    r = B.shape[2]
+    delta = np.zeros((S.shape[0], B.shape[1]), dtype=np.float64)
+    start = 0
+    for s, end in enumerate(slice_end):
+        delta[:, start:end] = expand(S[:, s * r:(s + 1) * r], B[:, start:end, :], idx, mask)
+        start = end
+    return delta
+
+
 def layer_fp8(x: np.ndarray, wq: np.ndarray, sw: np.ndarray, A: np.ndarray, B: np.ndarray,
-              idx: np.ndarray, mask: np.ndarray | None, cols: np.ndarray | None = None):
+              idx: np.ndarray, mask: np.ndarray | None, cols: np.ndarray | None = None, slice_end=None):
     """Reference Y (float64) of the FP8 layer plus its parts.
 
     Returns dict(Y, base, delta, S, xq, sx). With `cols`, Y/base/delta hold only
-    those output columns.
+    those output columns. With `slice_end` (no `cols`), A is [L, n * r, K] and
+    the columns of slice s use its rank-r block (expand_slices).
     """
     xq, sx = quant_fp8_rows(x)
     base = base_gemm_fp8(xq, sx, wq, sw, cols)
     S = shrink(x, A, idx, mask)
+    if slice_end is not None:
+        delta = expand_slices(S, B, idx, mask, slice_end)
+        return dict(Y=base + delta, base=base, delta=delta, S=S, xq=xq, sx=sx)
     Bc = B if cols is None else np.asarray(B)[:, cols, :]
     delta = expand(S, Bc, idx, mask)
     return dict(Y=base + delta, base=base, delta=delta, S=S, xq=xq, sx=sx)
@@ -210,10 +229,13 @@ def layer_fp8(x: np.ndarray, wq: np.ndarray, sw: np.ndarray, A: np.ndarray, B: n
 
 def layer_nvfp4(x: np.ndarray, gx, wq: np.ndarray, sbw: np.ndarray, gw, A: np.ndarray,
                 B: np.ndarray, idx: np.ndarray, mask: np.ndarray | None,
-                cols: np.ndarray | None = None):
+                cols: np.ndarray | None = None, slice_end=None):
     xq, sbx = quant_nvfp4_rows(x, gx)
     base = base_gemm_nvfp4(xq, sbx, gx, wq, sbw, gw, cols)
     S = shrink(x, A, idx, mask)
+    if slice_end is not None:
+        delta = expand_slices(S, B, idx, mask, slice_end)
+        return dict(Y=base + delta, base=base, delta=delta, S=S, xq=xq, sbx=sbx)
     Bc = B if cols is None else np.asarray(B)[:, cols, :]
     delta = expand(S, Bc, idx, mask)
     return dict(Y=base + delta, base=base, delta=delta, S=S, xq=xq, sbx=sbx)

@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     epilora_gemm_lora_epilogue,
     epilora_layer_forward,
     epilora_layer_forward_noalloc,
+    epilora_layer_forward_slices,
     epilora_lora_shrink,
     epilora_nvfp4_global_scale,
     epilora_quant_act,

@@ -40,6 +40,9 @@ SIGNATURES = {
                                        _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _sz, _vp, _vp]),
     "epilora_layer_forward_noalloc": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp,
                                                _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp]),
+    "epilora_layer_forward_slices": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp, _vp,
+                                              _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp,
+                                              _sz, _vp, _vp]),
 }
 
 _lib = None
@@ -140,6 +143,18 @@ def epilora_layer_forward(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_gl
                                         _p(w_global_scale), _p(x_global_scale), _p(A), _p(B), L, r, _p(idx),
                                         _p(mask), _p(Y), ldy, _p(workspace), workspace_bytes, _p(status_dev),
                                         _stream(stream))
+
+
+def epilora_layer_forward_slices(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale, x_global_scale,
+                                 A, B, L, r, n_slices, slice_end, idx, mask, Y, ldy, workspace, workspace_bytes,
+                                 status_dev=None, stream=None) -> int:
+    """slice_end: a sequence of n_slices column ends (host ints)."""
+    ends = (ctypes.c_int * max(1, n_slices))(*[int(e) for e in slice_end])
+    return load().epilora_layer_forward_slices(fmt, M, N, K, _p(X), ldx, _p(Wq), _p(w_scale), _p(w_block_scale),
+                                               _p(w_global_scale), _p(x_global_scale), _p(A), _p(B), L, r,
+                                               n_slices, ctypes.cast(ends, ctypes.c_void_p), _p(idx), _p(mask),
+                                               _p(Y), ldy, _p(workspace), workspace_bytes, _p(status_dev),
+                                               _stream(stream))
 
 
 def epilora_layer_forward_noalloc(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale,

@@ -241,19 +241,23 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   return bytes;
 }
 
-EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* X, int ldx, const void* Wq,
-                                      const float* w_scale, const uint8_t* w_block_scale,
-                                      const float* w_global_scale, const float* x_global_scale, const void* A,
-                                      const void* B, int L, int r, const int32_t* idx, const uint8_t* mask,
-                                      void* Y, int ldy, void* workspace, size_t workspace_bytes, int* status_dev,
-                                      void* stream) {
+}  // extern "C"
+
+static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int ldx, const void* Wq,
+                              const float* w_scale, const uint8_t* w_block_scale, const float* w_global_scale,
+                              const float* x_global_scale, const void* A, const void* B, int L, int r,
+                              const int32_t* idx, const uint8_t* mask, void* Y, int ldy, void* workspace,
+                              size_t workspace_bytes, int* status_dev, void* stream, int n_slices,
+                              const int* slice_end) {
   const bool adapters = A != nullptr && B != nullptr;
+  // S rows: n_slices rank-r blocks (the shrink runs with rank r * n_slices)
+  const int rs = r * n_slices;
   if (!fmt_ok(fmt) || M < 0 || !k_ok(K) || ldx < K || ldx % 8 != 0) return EPILORA_ERR_INVALID_ARG;
   if (adapters && (L < 1 || !rank_ok(r) || idx == nullptr)) return EPILORA_ERR_INVALID_ARG;
   if (fmt == EPILORA_FMT_NVFP4 && (x_global_scale == nullptr || K % 256 != 0))
     return x_global_scale == nullptr ? EPILORA_ERR_INVALID_ARG : EPILORA_ERR_UNSUPPORTED;
   if (M == 0) return EPILORA_OK;
-  const int rr = adapters ? r : 0;
+  const int rr = adapters ? rs : 0;
   const size_t need = epilora_workspace_bytes(fmt, M, K, rr);
   if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return EPILORA_ERR_WORKSPACE;
@@ -276,7 +280,7 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
   int32_t* perm = nullptr;
   if (adapters) {
     S = reinterpret_cast<float*>(ws + off);
-    off += round256(m * static_cast<size_t>(r) * 4 * static_cast<size_t>(shrink_parts_max(K)));
+    off += round256(m * static_cast<size_t>(rs) * 4 * static_cast<size_t>(shrink_parts_max(K)));
     if (M > 32) perm = reinterpret_cast<int32_t*>(ws + off);
   }
 
@@ -291,8 +295,8 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
   // streams W immediately and reads everything the shrink grid writes (and
   // the token metadata) only after that grid has completed.
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int parts = adapters ? shrink_parts(M, K, r) : shrink_parts(M, K, 0);
-  rc = launch_shrink_quant(X, M, K, ldx, A, adapters ? L : 1, adapters ? r : 0, idx, mask, S, parts, fmt, Xq,
+  const int parts = adapters ? shrink_parts(M, K, rs) : shrink_parts(M, K, 0);
+  rc = launch_shrink_quant(X, M, K, ldx, A, adapters ? L : 1, adapters ? rs : 0, idx, mask, S, parts, fmt, Xq,
                            x_scale, x_block_scale, x_global_scale, perm, status_dev, st);
   if (rc != EPILORA_OK) return rc;
   GemmArgs a{};
@@ -322,7 +326,44 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* 
   a.fused = 1;
   a.s_parts = parts;
   a.perm = perm;
+  a.s_row = adapters ? rs : 0;
+  a.n_slices = n_slices;
+  for (int q = 0; q < n_slices && q < 4; ++q) a.slice_end[q] = slice_end != nullptr ? slice_end[q] : N;
   return fmt == EPILORA_FMT_FP8_E4M3 ? launch_gemm_fp8(a) : launch_gemm_nvfp4(a);
+}
+
+extern "C" {
+
+EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K, const void* X, int ldx, const void* Wq,
+                                      const float* w_scale, const uint8_t* w_block_scale,
+                                      const float* w_global_scale, const float* x_global_scale, const void* A,
+                                      const void* B, int L, int r, const int32_t* idx, const uint8_t* mask,
+                                      void* Y, int ldy, void* workspace, size_t workspace_bytes, int* status_dev,
+                                      void* stream) {
+  return layer_forward_impl(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale, x_global_scale, A, B,
+                            L, r, idx, mask, Y, ldy, workspace, workspace_bytes, status_dev, stream, 1, nullptr);
+}
+
+EPILORA_API int epilora_layer_forward_slices(int fmt, int M, int N, int K, const void* X, int ldx, const void* Wq,
+                                             const float* w_scale, const uint8_t* w_block_scale,
+                                             const float* w_global_scale, const float* x_global_scale,
+                                             const void* A, const void* B, int L, int r, int n_slices,
+                                             const int* slice_end, const int32_t* idx, const uint8_t* mask,
+                                             void* Y, int ldy, void* workspace, size_t workspace_bytes,
+                                             int* status_dev, void* stream) {
+  if (A == nullptr || B == nullptr || n_slices < 1 || n_slices > 4 || slice_end == nullptr)
+    return EPILORA_ERR_INVALID_ARG;
+  int prev = 0;
+  for (int q = 0; q < n_slices; ++q) {
+    const int e = slice_end[q];
+    if (e <= prev || e > N) return EPILORA_ERR_INVALID_ARG;
+    if (q + 1 < n_slices && e % 128 != 0) return EPILORA_ERR_INVALID_ARG;   // a weight tile lies in one slice
+    prev = e;
+  }
+  if (prev != N) return EPILORA_ERR_INVALID_ARG;
+  return layer_forward_impl(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale, x_global_scale, A, B,
+                            L, r, idx, mask, Y, ldy, workspace, workspace_bytes, status_dev, stream, n_slices,
+                            slice_end);
 }
 
 }  // extern "C"

@@ -58,6 +58,13 @@ struct GemmArgs {
   // fused call, more than one decode tile of tokens: rows of Xq / x_scale /
   // x_block_scale are in adapter-sorted order, perm[row] = token
   const int32_t* perm = nullptr;
+  // multi-slice projection: S rows hold n_slices consecutive rank-r blocks
+  // (s_row = n_slices * r floats); output columns [slice_end[s-1],
+  // slice_end[s]) take block s. slice_end ascending, multiples of 128 but the
+  // last (= N). s_row 0: r.
+  int s_row = 0;
+  int n_slices = 1;
+  int slice_end[4] = {0, 0, 0, 0};
 };
 
 int launch_quant(int fmt, const void* X, int M, int K, int ldx, void* Xq, float* x_scale,

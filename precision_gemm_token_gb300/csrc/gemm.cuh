@@ -132,6 +132,11 @@ struct GemmParams {
   int trace_slot;     // tuning builds only: which trace buffer this launch fills
   int l2_ahead;       // fused call: weight stages past the ring to prefetch into L2 while waiting
   int t_tiles, n_tiles;  // persistent wide kernel: token tiles, weight tiles
+  // S in memory: rows of s_row floats; a weight tile starting at column n0
+  // reads the rank-r block of its slice (the number of slice ends <= n0)
+  int s_row;
+  int n_slices;
+  int slice_end[4];
   int y_stage;        // wide tiles: ring byte offset of the per-warp output staging (-1: 2-byte stores)
 };
 
@@ -181,6 +186,15 @@ __host__ __device__ constexpr int gemm_red_bytes(int ks) {
 // group of each ordered token [BT].
 __host__ __device__ constexpr int gemm_decode_bytes(int BT, int r, int ks) {
   return BT > kDecodeBT ? 0 : (BT * r * 4 + BT * gemm_red_rows(ks) * 4 + (4 * BT + 4) * 4 + 15) / 16 * 16;
+}
+
+// Rank-r block of S that output column n0's slice reads (floats from the
+// start of an S row).
+__device__ __forceinline__ int s_slice_offset(const GemmParams& p, int n0) {
+  int off = 0;
+  for (int q = 0; q + 1 < p.n_slices && q < 4; ++q)
+    if (n0 >= p.slice_end[q]) off += p.r;
+  return off;
 }
 
 // Optional per-CTA phase timestamps (built only with -DEPILORA_GEMM_TRACE, for
@@ -332,6 +346,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   const int kb_end = (p.num_kb * (rank + 1)) / ks;
   const int nkb = kb_end - kb_begin;
   const int tv = min(BT, p.M - t0);           // valid token columns of this tile
+  const float* S_t = p.S != nullptr ? p.S + s_slice_offset(p, n0) : nullptr;   // this tile's slice of S rows
   const int row_lo = ks > 1 ? RR * rank : 0;
   const int row_hi = ks > 1 ? min(kTileN, RR * (rank + 1)) : kTileN;
   const int R = row_hi - row_lo;
@@ -762,13 +777,16 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     if (C::kDecode && p.S != nullptr) {
       // S rows of this tile's tokens into shared memory (partials of a split
       // shrink added in part order)
-      const size_t part = static_cast<size_t>(p.M) * p.r / 4;
-      const float4* src = reinterpret_cast<const float4*>(p.S + static_cast<size_t>(t0) * p.r);
+      const size_t part = static_cast<size_t>(p.M) * p.s_row / 4;
+      const int n4 = p.r / 4;
       float4* dst = reinterpret_cast<float4*>(s_stage);
-      for (int i = et; i < tv * p.r / 4; i += 128) {
-        float4 v = __ldcg(src + i);
+      for (int i = et; i < tv * n4; i += 128) {
+        const int tl = i / n4;
+        const float4* src =
+            reinterpret_cast<const float4*>(S_t + static_cast<size_t>(t0 + tl) * p.s_row) + (i - tl * n4);
+        float4 v = __ldcg(src);
         for (int q = 1; q < p.s_parts; ++q) {
-          const float4 w = __ldcg(src + q * part + i);
+          const float4 w = __ldcg(src + q * part);
           v.x += w.x;
           v.y += w.y;
           v.z += w.z;
@@ -822,10 +840,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       // every stage has been consumed: the ring now holds the S rows of this
       // tile's tokens (one read of each from L2 instead of one per element)
       const int n4 = p.r / 4;
-      const size_t part = static_cast<size_t>(p.M) * p.r / 4;     // partial sums of a split shrink, in part order
+      const size_t part = static_cast<size_t>(p.M) * p.s_row / 4;   // partial sums of a split shrink, in part order
       for (int k = et; k < tv * n4; k += 128) {
         const int tl = k / n4;
-        const float4* src = reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r) + (k - tl * n4);
+        const float4* src =
+            reinterpret_cast<const float4*>(S_t + static_cast<size_t>(meta_tok[tl]) * p.s_row) + (k - tl * n4);
         float4 v = __ldcg(src);
         for (int q = 1; q < p.s_parts; ++q) {
           const float4 w = __ldcg(src + q * part);
@@ -867,7 +886,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       const float4* srow =
           C::kDecode ? reinterpret_cast<const float4*>(s_stage + tl * p.r)
           : p.stage_s ? reinterpret_cast<const float4*>(s_big + tl * s_ld)
-                      : reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r);
+                      : reinterpret_cast<const float4*>(S_t + static_cast<size_t>(meta_tok[tl]) * p.s_row);
       y += dot_srow_brow(srow, brow, p.r, s_smem);
     }
     if (et == 0 && tl == 0) EPI_TRACE_AFTER(10, y);
@@ -1202,7 +1221,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
                   }
                   const float4* srow = p.stage_s ? reinterpret_cast<const float4*>(s_big + tl * s_ld)
                                                  : reinterpret_cast<const float4*>(
-                                                       p.S + static_cast<size_t>(meta_tok[tl]) * p.r);
+                                                       S_t + static_cast<size_t>(meta_tok[tl]) * p.s_row);
                   y += p.stage_s ? dot_srow_brow_n<R4, true>(srow, brow) : dot_srow_brow_n<R4, false>(srow, brow);
                 }
                 yv[j] = y;
@@ -1349,6 +1368,9 @@ int launch_gemm_tiled(const GemmArgs& a) {
   p.K = a.K;
   p.L = a.L;
   p.r = a.r;
+  p.s_row = a.s_row > 0 ? a.s_row : a.r;
+  p.n_slices = a.n_slices < 1 ? 1 : a.n_slices;
+  for (int q = 0; q < 4; ++q) p.slice_end[q] = a.slice_end[q];
   p.ldy = a.ldy;
   p.num_kb = (kbytes + KA * kAtomBytes - 1) / (KA * kAtomBytes);
   p.rotate = EPILORA_GEMM_ROTATE;

@@ -343,11 +343,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_wide_kernel(const __grid
       asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
       if (KS > 0) {
         const int n4 = p.r / 4;
-        const size_t part = static_cast<size_t>(p.M) * p.r / 4;   // partial sums of a split shrink, in part order
+        const size_t part = static_cast<size_t>(p.M) * p.s_row / 4;   // partial sums of a split shrink, in part order
+        const float* S_t = p.S + s_slice_offset(p, n0);               // this tile's slice of S rows
         for (int k = et; k < tv * n4; k += 128) {
           const int tl = k / n4;
           const float4* src =
-              reinterpret_cast<const float4*>(p.S + static_cast<size_t>(meta_tok[tl]) * p.r) + (k - tl * n4);
+              reinterpret_cast<const float4*>(S_t + static_cast<size_t>(meta_tok[tl]) * p.s_row) + (k - tl * n4);
           float4 v = __ldcg(src);
           for (int q = 1; q < p.s_parts; ++q) {
             const float4 w = __ldcg(src + q * part);
@@ -473,6 +474,9 @@ int launch_gemm_wide(const GemmArgs& a) {
   p.K = a.K;
   p.L = a.L;
   p.r = lora ? a.r : 0;
+  p.s_row = a.s_row > 0 ? a.s_row : p.r;
+  p.n_slices = a.n_slices < 1 ? 1 : a.n_slices;
+  for (int q = 0; q < 4; ++q) p.slice_end[q] = a.slice_end[q];
   p.ldy = a.ldy;
   p.num_kb = (a.K + kAtomBytes - 1) / kAtomBytes;
   p.ks = 1;

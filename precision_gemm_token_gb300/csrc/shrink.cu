@@ -566,6 +566,18 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
     const int early = EPILORA_SHRINK_EARLY_ALL || ctas <= num_sms() ? 1 : 0;
     // per-warp partial tiles of a token block (and the quantizers' scratch)
     cfg.dynamicSmemBytes = static_cast<size_t>(4) * kBlockTokens * (r > 4 ? r : 4) * sizeof(float);
+    if (cfg.dynamicSmemBytes > 227 * 1024) return EPILORA_ERR_UNSUPPORTED;
+    if (cfg.dynamicSmemBytes > 48 * 1024) {
+      static int attr_done[64] = {0};
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return EPILORA_ERR_CUDA;
+      if (attr_done[dev] < static_cast<int>(cfg.dynamicSmemBytes)) {
+        if (cudaFuncSetAttribute(shrink_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(cfg.dynamicSmemBytes)) != cudaSuccess)
+          return EPILORA_ERR_CUDA;
+        attr_done[dev] = static_cast<int>(cfg.dynamicSmemBytes);
+      }
+    }
     const cudaError_t e = cudaLaunchKernelEx(&cfg, shrink_block_kernel, static_cast<const __nv_bfloat16*>(X), K, ldx,
                                              static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S, status_dev, qs,
                                              M, s_parts, kslice, trace_slot_next(), early);

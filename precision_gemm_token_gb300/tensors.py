@@ -97,6 +97,25 @@ class LayerWorkspace:
         return self.buf
 
 
+def layer_forward_slices(X, w: QuantWeight, A, B, idx, slice_end, mask=None, x_global_scale=None,
+                         workspace: Optional[LayerWorkspace] = None, status=None, stream=None, Y=None):
+    """Multi-slice projection: A [L, n_slices * r, K], B [L, N, r]; output
+    columns [slice_end[s-1], slice_end[s]) use slice s's adapter pair."""
+    M, K = X.shape
+    N = w.N
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    n = len(slice_end)
+    L, r = A.shape[0], B.shape[2]
+    ws = workspace or LayerWorkspace(X.device)
+    buf = ws.get(w.fmt, M, K, n * r)
+    rc = E.epilora_layer_forward_slices(w.fmt, M, N, K, X, X.stride(0), w.codes, w.scale, w.block_scale,
+                                        w.global_scale, x_global_scale, A, B, L, r, n, slice_end, idx, mask, Y,
+                                        Y.stride(0), buf, buf.numel(), status, stream)
+    E.check(rc, "layer_forward_slices")
+    return Y
+
+
 def layer_forward(X, w: QuantWeight, A=None, B=None, idx=None, mask=None, x_global_scale=None,
                   workspace: Optional[LayerWorkspace] = None, status=None, stream=None, Y=None):
     M, K = X.shape

@@ -142,6 +142,58 @@ def test_wide_shrink_split_over_k(fmt, M, K, N, L, r, idx_mode, mask_mode):
     assert_y_close(y, ref, bound, what=(fmt, M, K, r))
 
 
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+@pytest.mark.parametrize("M,K,N,r,ends", [
+    (4, 512, 640, 16, [384, 512, 640]),          # decode tile, split-K cluster, three slices
+    (24, 1024, 384, 64, [256, 384]),             # 32-token decode tile, two slices, rank 64
+    (300, 512, 640, 32, [384, 512, 640]),        # wide tiles (two CTAs per SM), three slices
+    (520, 256, 26112, 16, [18432, 22272, 26112]),   # more tiles than 4 per SM: persistent kernel (FP8)
+])
+def test_multi_slice_projection(fmt, M, K, N, r, ends):
+    """Fused projections with one adapter pair per slice (qkv, gate_up): the
+    columns of slice s use its rank-r block of A and of S."""
+    L = 6
+    rng = np.random.default_rng(M + N)
+    X = torch.tensor(rng.standard_normal((M, K)), dtype=torch.bfloat16)
+    W = torch.tensor(0.02 * rng.standard_normal((N, K)), dtype=torch.bfloat16)
+    A = torch.tensor(rng.standard_normal((L, len(ends) * r, K)) / np.sqrt(K), dtype=torch.bfloat16)
+    B = torch.tensor(0.01 * rng.standard_normal((L, N, r)), dtype=torch.bfloat16)
+    idx = torch.tensor(rng.integers(-1, L, size=M), dtype=torch.int32)
+    mask = torch.tensor(rng.integers(0, 2, size=M), dtype=torch.uint8)
+    x, Wn, An, Bn = (t.float().numpy() for t in (X, W, A, B))
+    w = T.quantize_weight(W.cuda(), fmt)
+    st = status_buf()
+    if fmt == FP8:
+        wq, sw = O.quant_fp8_rows(Wn)
+        ref = O.layer_fp8(x, wq, sw, An, Bn, idx.numpy(), mask.numpy(), slice_end=ends)
+        xv = F.e4m3_decode(ref["xq"]) * ref["sx"][:, None].astype(np.float64)
+        wv = F.e4m3_decode(wq) * sw[:, None].astype(np.float64)
+        gx = None
+    else:
+        gw = O.nvfp4_global_scale(Wn)
+        wq, sbw = O.quant_nvfp4_rows(Wn, gw)
+        gxv = O.nvfp4_global_scale(x)
+        gx = torch.tensor([gxv], dtype=torch.float32, device="cuda")
+        ref = O.layer_nvfp4(x, gxv, wq, sbw, gw, An, Bn, idx.numpy(), mask.numpy(), slice_end=ends)
+        xv = O.dequant_nvfp4_rows(ref["xq"], ref["sbx"], gxv)
+        wv = O.dequant_nvfp4_rows(wq, sbw, gw)
+    Y = T.layer_forward_slices(X.cuda(), w, A.cuda(), B.cuda(), idx.cuda(), ends, mask=mask.cuda(),
+                               x_global_scale=gx, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # bound: bf16 rounding + fp32 accumulation of every product term
+    mag = np.abs(xv) @ np.abs(wv).T
+    S = np.abs(ref["S"])
+    act = O.active_tokens(idx.numpy(), mask.numpy(), L)
+    start = 0
+    for s_i, end in enumerate(ends):
+        for t in np.nonzero(act)[0]:
+            mag[t, start:end] += np.abs(Bn[int(idx[t]), start:end]) @ S[t, s_i * r:(s_i + 1) * r]
+        start = end
+    bound = 2.0 ** -8 * np.abs(ref["Y"]) + 1e-5 * mag + 1e-30
+    assert_y_close(np32(Y), ref, bound, what=(fmt, M, N, ends))
+
+
 def test_fp8_integer_codes_exact():
     """Rows whose amax is 448 quantize with scale 1; with small-integer values
     the codes are those integers, the fp32 accumulation is exact and Y must be

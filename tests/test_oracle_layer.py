@@ -186,6 +186,34 @@ def test_delta_equals_merged_update_W_plus_BA():
         assert np.allclose(ref["delta"][t], d, rtol=1e-12, atol=1e-15)
 
 
+def test_slices_equal_per_slice_merged_updates():
+    """Multi-slice projection: the columns of slice s take x . (B_l[cols_s]
+    A_l[slice s rows])^T with the explicit merged product of that slice, and
+    a single slice is the ordinary layer."""
+    rng = np.random.default_rng(7)
+    M, K, N, L, r = 5, 64, 48, 3, 4
+    ends = [16, 40, 48]
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    W = (0.02 * rng.standard_normal((N, K))).astype(np.float32)
+    A = rng.standard_normal((L, len(ends) * r, K)) / np.sqrt(K)
+    B = 0.01 * rng.standard_normal((L, N, r))
+    idx = np.array([0, 2, -1, 1, 2])
+    mask = np.array([1, 1, 1, 0, 1], dtype=np.uint8)
+    wq, sw = O.quant_fp8_rows(W)
+    ref = O.layer_fp8(x, wq, sw, A, B, idx, mask, slice_end=ends)
+    start = 0
+    for s_i, end in enumerate(ends):
+        for t in range(M):
+            if idx[t] < 0 or mask[t] == 0:
+                assert (ref["delta"][t, start:end] == 0).all()
+                continue
+            BA = B[idx[t], start:end] @ A[idx[t], s_i * r:(s_i + 1) * r]
+            assert np.allclose(ref["delta"][t, start:end], BA @ x[t].astype(np.float64), rtol=1e-12, atol=1e-15)
+        start = end
+    one = O.layer_fp8(x, wq, sw, A[:, :r], B, idx, mask, slice_end=[N])
+    assert (one["Y"] == O.layer_fp8(x, wq, sw, A[:, :r], B, idx, mask)["Y"]).all()
+
+
 def test_zero_B_mask_and_negative_index_give_base():
     p, x, wq, sw = _small_layer(seed=1)
     A, B = p.A.float().numpy(), p.B.float().numpy()
