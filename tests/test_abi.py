@@ -145,3 +145,30 @@ def test_layer_forward_workspace_checks(lib):
     assert E.epilora_layer_forward(*args(None, need)) == WS
     assert E.epilora_layer_forward(*args(FAKE, need - 1)) == WS
     assert E.epilora_layer_forward(*args(FAKE + 16, need)) == WS      # 256-byte alignment
+
+
+@pytest.mark.skipif(not _no_gpu(), reason="fake-pointer validation runs only where nothing can launch")
+@pytest.mark.parametrize("n,ends,A,want", [
+    (0, [1024], FAKE, INVALID),                     # no slice
+    (5, [128, 256, 384, 512, 1024], FAKE, INVALID),  # more than 4 slices
+    (2, [512, 512], FAKE, INVALID),                 # not ascending
+    (2, [500, 1024], FAKE, INVALID),                # inner end not a multiple of 128
+    (2, [512, 896], FAKE, INVALID),                 # last end != N
+    (2, [512, 1024], None, INVALID),                # A required
+])
+def test_layer_forward_slices_validation(lib, n, ends, A, want):
+    need = E.epilora_workspace_bytes(0, 4, 512, 16 * max(n, 1))
+    rc = E.epilora_layer_forward_slices(0, 4, 1024, 512, FAKE, 512, FAKE, FAKE, None, None, None, A, FAKE, 4, 16, n,
+                                        ends, FAKE, None, FAKE, 1024, FAKE, need, None, 0)
+    assert rc == want
+
+
+@pytest.mark.skipif(not _no_gpu(), reason="fake-pointer validation runs only where nothing can launch")
+def test_layer_forward_slices_workspace_sized_for_all_slices(lib):
+    """The workspace of a sliced call holds S rows of n_slices * r floats."""
+    small = E.epilora_workspace_bytes(0, 4, 512, 16)
+    big = E.epilora_workspace_bytes(0, 4, 512, 48)
+    assert big > small
+    args = lambda nbytes: (0, 4, 1024, 512, FAKE, 512, FAKE, FAKE, None, None, None, FAKE, FAKE, 4, 16, 3,  # noqa
+                           [384, 768, 1024], FAKE, None, FAKE, 1024, FAKE, nbytes, None, 0)
+    assert E.epilora_layer_forward_slices(*args(small)) == WS
