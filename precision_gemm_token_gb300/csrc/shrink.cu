@@ -9,14 +9,17 @@
 // a few extra thread blocks of it quantize the activations). PreFT,
 // "Prefill-only finetuning", Core claim: tokens with mask 0 skip the adapter.
 //
-// One shrink CTA (128 threads) computes kRanksPerCta rank rows for one token.
-// Its threads split the K dimension into 16-byte chunks (8 bf16): each chunk
-// of x is loaded once and multiplied with the same chunk of the CTA's A rows
-// (coalesced 128-bit loads). Partial sums are reduced with a fixed
-// xor-butterfly inside each warp and then over the warps in index order, so S
-// is bitwise reproducible and independent of the token's position in the
-// batch. The CTAs are small (128 threads, at most 64 registers each) so that
-// two GEMM CTAs still fit beside one on an SM: the GEMM runs concurrently.
+// Decode batches (shrink_kernel): one rank CTA (128 threads) computes
+// kRanksPerCta rank rows for one token. Its threads split the K dimension
+// into 16-byte chunks (8 bf16): each chunk of x is loaded once and multiplied
+// with the same chunk of the CTA's A rows (coalesced 128-bit loads). Partial
+// sums are reduced with a fixed xor-butterfly inside each warp and then over
+// the warps in index order, so S is bitwise reproducible and independent of
+// the token's position in the batch. The CTAs are small (128 threads, at
+// most 64 registers each) so that the GEMM's CTAs still fit beside them.
+// Batches of more than 32 tokens (shrink_block_kernel): blocks of 16
+// consecutive tokens that carry at most two adapters go to tensor-core CTAs
+// (see there); the others to rank CTAs as above, in the same grid.
 #include "quant_row.cuh"
 
 namespace epi {
