@@ -296,6 +296,74 @@ def run_ours(args, rank, world, local):
                 raise RuntimeError(f"device status {int(q['st'].item())} in {q['name']}")
         return float(np.mean(per)), float(np.median(per)), t_wall, clocks
 
+    def time_calls(fn, steps, warmup):
+        """Median and mean (ms) of `fn` (one projection's enqueue) captured as
+        a CUDA graph, each replay behind an L2 flush outside the events."""
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn(s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn(s)
+        for _ in range(warmup):
+            flush.fill_(1)
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush.fill_(1)
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        per = sorted(a.elapsed_time(b) for a, b in evs)
+        return per[len(per) // 2], float(np.mean(per))
+
+    def exposure_controls(projs, steps, warmup):
+        """Per projection (EpiLoRA, Evaluation › Kernels, Tables 10-12 and 17):
+        T(fused call), T(no adapter: the same call with A = B = NULL),
+        T(GEMM, h given: the standalone GEMM with its adapter epilogue reading
+        a precomputed S and quantized X), T(serial: quantizer, shrink and GEMM
+        as three ordinary launches), and exposed = T(fused) - T(h given), the
+        adapter cost added = T(fused) - T(no adapter). Medians in us."""
+        out, tot = {}, {}
+        for q in projs:
+            p, w, gx, Y = q["p"], q["w"], q["gx"], q["Y"]
+            Mq, Kq = p.X.shape
+            Xq, xs = T.quant_act(p.X, w.fmt, global_scale=gx)
+            S = T.lora_shrink(p.X, p.A, p.idx, p.mask)
+            ws0 = T.LayerWorkspace(dev)
+            torch.cuda.synchronize()
+            fns = {
+                "fused": lambda st, p=p, w=w, gx=gx, Y=Y, ws=q["ws"]: T.layer_forward(
+                    p.X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx, workspace=ws, stream=st, Y=Y),
+                "no_adapter": lambda st, p=p, w=w, gx=gx, Y=Y, ws=ws0: T.layer_forward(
+                    p.X, w, x_global_scale=gx, workspace=ws, stream=st, Y=Y),
+                "h_given": lambda st, p=p, w=w, gx=gx, Y=Y, Xq=Xq, xs=xs, S=S, Mq=Mq, Kq=Kq: T.gemm_lora_epilogue(
+                    Xq, xs, w, Mq, Kq, S=S, B=p.B, idx=p.idx, mask=p.mask, x_global_scale=gx, stream=st, Y=Y),
+            }
+
+            def serial(st, p=p, w=w, gx=gx, Y=Y, Mq=Mq, Kq=Kq, Xq=Xq, xs=xs, S=S):
+                T.quant_act_into(p.X, w.fmt, Xq, xs, global_scale=gx, stream=st)
+                T.lora_shrink_into(p.X, p.A, p.idx, p.mask, S, stream=st)
+                T.gemm_lora_epilogue(Xq, xs, w, Mq, Kq, S=S, B=p.B, idx=p.idx, mask=p.mask, x_global_scale=gx,
+                                     stream=st, Y=Y)
+            fns["serial"] = serial
+            row = {}
+            for k, fn in fns.items():
+                med, _ = time_calls(fn, steps, warmup)
+                row[k] = round(med * 1000, 2)
+            row["exposed_vs_h_given"] = round(row["fused"] - row["h_given"], 2)
+            row["adapter_cost_vs_no_adapter"] = round(row["fused"] - row["no_adapter"], 2)
+            out[q["name"]] = row
+            for k, v in row.items():
+                tot[k] = round(tot.get(k, 0.0) + v, 2)
+        out["sum"] = tot
+        return out
+
     workload = args.workload
     M, fmt, L, r, idx_mode, desc = WORKLOADS[workload]
     projs = make_layer(workload, seed=100)
@@ -303,6 +371,10 @@ def run_ours(args, rank, world, local):
     ms_mean, ms_med, t_wall, clocks = time_graph(projs, args.steps, args.warmup, sampler)
     ms_max = max_over_ranks(ms_mean, world, dev)
     value_us = ms_max * 1000.0
+
+    controls = None
+    if not args.skip_controls:
+        controls = exposure_controls(projs, max(args.steps // 2, 10), args.warmup)
 
     # 32-tenant tokens/s (same format)
     t32 = None
@@ -354,11 +426,19 @@ def run_ours(args, rank, world, local):
                 act = [int(i) for i, m in zip(pq.idx.tolist(), pq.mask.tolist()) if i >= 0 and m != 0]
                 bytes_l += algorithmic_bytes(Ml, K, N, fl, spec[5], len(set(act)))
             gbs_l = bytes_l / (ms_l / 1000) / 1e9
+            # the layer's roofline: the slower of its HBM time (algorithmic
+            # bytes at the measured copy bandwidth) and its tensor time
+            t_hbm = bytes_l / (peaks.get("hbm_gbs", 6800.0) * 1e9)
+            t_tc = flops / (peak_l * 1e12)
             large.append({"workload": desc_l, "M": Ml, "layer_us": round(ms_l * 1000, 1), "tflops": round(tf, 1),
                           "algorithmic_bytes": int(bytes_l), "hbm_gbs": round(gbs_l, 1),
                           "hbm_frac_of_measured": round(gbs_l / peaks.get("hbm_gbs", 6800.0), 4),
-                          "peak_tflops": round(peak_l, 1), "frac": round(tf / peak_l, 4),
-                          "peak_source": "measured bf16 burst x " + ("2 (FP8)" if fl == 0 else "6 (NVFP4)")})
+                          "peak_tflops": round(peak_l, 1), "tensor_frac": round(tf / peak_l, 4),
+                          "bound": "hbm" if t_hbm > t_tc else "tensor",
+                          "roofline_us": round(max(t_hbm, t_tc) * 1e6, 1),
+                          "frac": round(max(t_hbm, t_tc) / (ms_l / 1000), 4),
+                          "peak_source": "measured bf16 burst x " + ("2 (FP8)" if fl == 0 else "6 (NVFP4)")
+                                         + "; measured copy bandwidth"})
             del projs_l
             torch.cuda.empty_cache()
 
@@ -442,6 +522,7 @@ def run_ours(args, rank, world, local):
         "layer_hbm_gbs": round(layer_bytes / (ms_max / 1000) / 1e9, 1),
         "layer_hbm_frac_of_measured": round(layer_bytes / (ms_max / 1000) / 1e9 / peak, 4),
         "roofline": roofline,
+        "exposure": controls,
         "tenants32": t32,
         "nvfp4_m1": nv,
         "large_m": large,
@@ -607,6 +688,7 @@ def main():
     ap.add_argument("--skip-tenants", action="store_true")
     ap.add_argument("--skip-large", action="store_true", help="skip the wide-tile (tensor-bound) layers")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-controls", action="store_true", help="skip the per-projection exposure controls")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true", help="run the dominant kernel alone (for ncu)")

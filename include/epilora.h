@@ -158,11 +158,13 @@ EPILORA_API int epilora_lora_shrink(const void* X, int M, int K, int ldx,
  *            shrink), else 0; with S == NULL there is no adapter term.
  * pdl_dependent = 1 launches the kernel with programmatic stream
  * serialization: it may start while the previous kernel on the stream (the
- * shrink) is still running, streams W, and executes the grid-dependency wait
- * just before reading S. pdl_dependent = 0 is an ordinary launch.
- * Xq/x_scale/x_block_scale must already be complete when the previous kernel
- * on the stream started (e.g. written by epilora_quant_act before the
- * shrink).
+ * shrink) is still running, streams W and Xq at once, and executes the
+ * grid-dependency wait before it reads x_scale, idx, mask or S.
+ * pdl_dependent = 0 is an ordinary launch.
+ * With pdl_dependent = 1, Xq and x_block_scale must already be complete when
+ * the previous kernel on the stream started (e.g. written by
+ * epilora_quant_act before the shrink); x_scale, S, idx and mask may be
+ * written by that kernel.
  */
 EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
                                const void* Xq, const float* x_scale,
@@ -261,8 +263,10 @@ EPILORA_API int epilora_layer_forward_slices(int fmt, int M, int N, int K,
  *
  * Returns EPILORA_ERR_WORKSPACE, having enqueued nothing, when
  * epilora_workspace_bytes(fmt, M, K, A && B ? r : 0) exceeds
- * EPILORA_NOALLOC_SCRATCH_BYTES (8 MiB: e.g. FP8 with M * K up to about 7.9
- * million elements at r = 64); EPILORA_ERR_CUDA if the address lookup fails.
+ * EPILORA_NOALLOC_SCRATCH_BYTES (8 MiB); the test is exactly that size query,
+ * whose S term grows with the number of K slices of the shrink (e.g. FP8,
+ * r = 64: M up to 1635 at K = 4096); EPILORA_ERR_CUDA if the address lookup
+ * fails.
  * Otherwise it enqueues what epilora_layer_forward enqueues (the scratch
  * needs no starting value: every byte is written before it is read).
  *

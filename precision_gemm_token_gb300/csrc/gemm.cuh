@@ -113,6 +113,10 @@ struct GemmParams {
   // first and executes griddepcontrol.wait before the first activation load,
   // the epilogue warps before reading any token metadata.
   int fused;
+  // 1: launched as a programmatic dependent outside the fused call: Xq (and
+  // its block scales) may be loaded at once, but x_scale, idx, mask and S only
+  // after griddepcontrol.wait (the previous kernel may write them)
+  int pdl;
   const int32_t* perm;  // rows of Xq / x_scale are in this token order (perm[row] = token), or identity if null
   int stage_s;          // non-decode tiles: S of the tile's tokens is staged in the ring after the main loop
   // S is the sum of s_parts partial arrays [s_parts][M][r] (split K of the
@@ -512,7 +516,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     }
     asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");   // groups visible to all four warps
   };
-  if (warp >= 2 && !p.fused) build_meta();
+  if (warp >= 2 && !p.fused && !p.pdl) build_meta();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -739,8 +743,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     }
   } else {
     // ===== epilogue warps, main-loop phase =====
-    if (p.fused) {
-      // the shrink grid (quantized activations, scales, S) has completed
+    if (p.fused || p.pdl) {
+      // the primary grid (in the fused call the shrink grid: quantized
+      // activations, scales, S) has completed; token metadata is read after
       pdl_wait_primary();
       build_meta();
     }
@@ -1358,6 +1363,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   p.Y = static_cast<__nv_bfloat16*>(a.Y);
   p.status = a.status_dev;
   p.fused = a.fused;
+  p.pdl = !a.fused && a.pdl_dependent ? 1 : 0;
   p.perm = a.perm;
 #ifdef EPILORA_GEMM_TRACE
   p.trace_slot = gemm_trace_launches()++ % kTraceSlots;

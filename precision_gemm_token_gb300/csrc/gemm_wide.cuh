@@ -311,7 +311,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_wide_kernel(const __grid
     __syncwarp();
   } else {
     // ===== epilogue warps =====
-    if (p.fused) pdl_wait_primary();   // the shrink grid (quantized activations, scales, S, perm)
+    // the primary grid: in the fused call the shrink grid (quantized
+    // activations, scales, S, perm); in a standalone dependent launch the
+    // kernel that writes S, idx or mask
+    if (p.fused || p.pdl) pdl_wait_primary();
     __nv_bfloat16* ys = ystage + (warp & 3) * 16 * 40;
     int j = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++j) {
@@ -464,6 +467,7 @@ int launch_gemm_wide(const GemmArgs& a) {
   p.Y = static_cast<__nv_bfloat16*>(a.Y);
   p.status = a.status_dev;
   p.fused = a.fused;
+  p.pdl = !a.fused && a.pdl_dependent ? 1 : 0;
   p.perm = a.perm;
 #ifdef EPILORA_GEMM_TRACE
   p.trace_slot = gemm_trace_launches()++ % kTraceSlots;

@@ -47,6 +47,17 @@ def quant_act(X: torch.Tensor, fmt: int, global_scale: Optional[torch.Tensor] = 
     return q, sb
 
 
+def quant_act_into(X: torch.Tensor, fmt: int, Xq, scale, global_scale=None, status=None, stream=None):
+    """quant_act into caller-owned outputs (codes, and the FP8 scales or the
+    NVFP4 block scales)."""
+    M, K = X.shape
+    if fmt == E.FMT_FP8:
+        rc = E.epilora_quant_act(fmt, X, M, K, X.stride(0), Xq, scale, None, None, status, stream)
+    else:
+        rc = E.epilora_quant_act(fmt, X, M, K, X.stride(0), Xq, None, scale, global_scale, status, stream)
+    E.check(rc, "quant_act")
+
+
 def quantize_weight(W: torch.Tensor, fmt: int, stream=None) -> QuantWeight:
     """Load-time quantization of a bf16 weight [N, K] with the same kernels:
     FP8 per-output-channel scales, or NVFP4 with g_w from W's amax."""
@@ -64,6 +75,13 @@ def lora_shrink(X, A, idx, mask=None, status=None, stream=None) -> torch.Tensor:
     S = torch.empty((M, r), dtype=torch.float32, device=X.device)
     E.check(E.epilora_lora_shrink(X, M, K, X.stride(0), A, L, r, idx, mask, S, status, stream), "lora_shrink")
     return S
+
+
+def lora_shrink_into(X, A, idx, mask, S, status=None, stream=None):
+    """lora_shrink into a caller-owned S [M, r] fp32."""
+    M, K = X.shape
+    L, r, _ = A.shape
+    E.check(E.epilora_lora_shrink(X, M, K, X.stride(0), A, L, r, idx, mask, S, status, stream), "lora_shrink")
 
 
 def gemm_lora_epilogue(Xq, x_scale, w: QuantWeight, M, K, S=None, B=None, idx=None, mask=None,

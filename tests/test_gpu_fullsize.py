@@ -5,9 +5,10 @@ Every output Y[t, n] depends only on token t's activations, weight row n and
 token t's adapter, so the oracle recomputes a sample of tokens (all of them
 up to 64) and of weight rows exactly as it would the whole layer. Checked:
 the weight codes / scales of the sampled rows and the activation codes /
-scales that the fused call left in its workspace and S (bit-exact codes,
-fp32-rounding S from the standalone shrink), and Y on the sampled grid
-within the layer tolerance.
+scales that the fused call left in its workspace (bit-exact), the partial
+sums of S it left there and S from the standalone shrink (both within fp32
+rounding of the oracle's S), and Y on the sampled grid within the layer
+tolerance.
 
 Cases: the 8B decode layer at M = 1 (one rank-64 adapter) and at M = 32 (32
 tenants), FP8; the 8B layer with an NVFP4 base and 128 resident adapters
@@ -59,6 +60,8 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
     w = T.quantize_weight(p.W, fmt)
     gx_t = T.nvfp4_global_scale(p.X) if fmt == NVFP4 else None
     ws = T.LayerWorkspace(p.X.device)
+    # zero-filled: partial-sum slots the shrink leaves unused then read as 0
+    ws.get(fmt, M, K, r).zero_()
     st = status_buf()
     Y = T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx_t, workspace=ws, status=st)
     torch.cuda.synchronize()
@@ -122,12 +125,21 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
         sb_gpu = buf[o2:o2 + M * K // 16].view(M, K // 16)[qrows_t]
         assert same_codes_e2m1_packed(npu8(xq_gpu), ref["xq"]).all()
         assert (npu8(sb_gpu) == ref["sbx"]).all()
-    # S of the same tokens from the standalone shrink (the fused call keeps it
-    # as partial sums over K slices in its workspace)
-    S_gpu = np32(T.lora_shrink(p.X, p.A, p.idx, p.mask)[rows_t]).astype(np.float64)
+    # S of the same tokens as the fused call left it in its workspace: partial
+    # sums over K slices [part][token][r], added here in part order as the
+    # GEMM adds them; and from the standalone shrink
     S_ref = ref["S"]
-    s_err = np.abs(S_gpu - S_ref).max() if S_ref.size else 0.0
-    assert s_err <= 1e-5 * max(1.0, float(np.abs(S_ref).max())) + 1e-6, s_err
+    n_parts = min(8, -(-K // 1024))
+    off_s = _r256(xq_bytes) + _r256(sc_bytes)
+    parts = buf[off_s:off_s + n_parts * M * r * 4].view(torch.float32).view(n_parts, M, r)[:, rows_t, :]
+    S_fused = parts[0].clone()
+    for q in range(1, n_parts):
+        S_fused += parts[q]
+    S_tol = 1e-5 * max(1.0, float(np.abs(S_ref).max()) if S_ref.size else 1.0) + 1e-6
+    for S_gpu in (np32(S_fused).astype(np.float64),
+                  np32(T.lora_shrink(p.X, p.A, p.idx, p.mask)[rows_t]).astype(np.float64)):
+        s_err = np.abs(S_gpu - S_ref).max() if S_ref.size else 0.0
+        assert s_err <= S_tol, s_err
     y = np32(Y[rows_t][:, cols_t])
     ok, info = O.y_within_tolerance(y, ref["Y"])
     assert ok, info

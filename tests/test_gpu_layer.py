@@ -271,6 +271,38 @@ def test_gemm_with_h_given_matches_fused():
     assert torch.equal(Yf, Yg)
 
 
+@pytest.mark.parametrize("fmt,M,K,N,r", [
+    (FP8, 8, 2048, 512, 32),        # decode tile
+    (FP8, 520, 256, 26112, 16),     # more than 4 wide tiles per SM: the persistent kernel
+    (NVFP4, 8, 2048, 512, 32),
+])
+def test_standalone_shrink_then_dependent_gemm(fmt, M, K, N, r):
+    """epilora_lora_shrink, then on the same stream epilora_gemm_lora_epilogue
+    launched as its programmatic dependent: the GEMM may start while the
+    shrink still runs, but reads S, idx and mask only after it; Y equals an
+    ordinary launch's bit for bit (S starts out as NaN each time)."""
+    import precision_gemm_token_gb300 as E
+    p = make_projection(M, K, N, 6, r, seed=M + N)
+    X, W = p.X.cuda(), p.W.cuda()
+    A, B, idx, mask = p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda()
+    w = T.quantize_weight(W, fmt)
+    gx = T.nvfp4_global_scale(X) if fmt == NVFP4 else None
+    Xq, xs = T.quant_act(X, fmt, global_scale=gx)
+    st = status_buf()
+    outs = []
+    for pdl in (False, True):
+        S = torch.full((M, r), float("nan"), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        rc = E.epilora_lora_shrink(X, M, K, X.stride(0), A, A.shape[0], r, idx, mask, S, st, None)
+        assert rc == E.EPILORA_OK
+        outs.append(T.gemm_lora_epilogue(Xq, xs, w, M, K, S=S, B=B, idx=idx, mask=mask, x_global_scale=gx,
+                                         pdl_dependent=pdl, status=st))
+        torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert not torch.isnan(outs[0].float()).any()
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_out_of_range_index_in_gemm():
     p = make_projection(6, 512, 256, 3, 16, seed=12)
     idx = p.idx.clone()

@@ -86,6 +86,38 @@ def test_nvfp4_quant_zero_block_and_amax_hits_6():
             assert (codes[t, b * 16 + j] & 7) == 7                  # |code| = 6
 
 
+def test_nvfp4_global_scale_closed_forms():
+    """The encode multiplier g = 448 * 6 / amax (reading O3) through what it
+    implies rather than its formula: a tensor whose amax is 2688 = 448 * 6
+    needs no scaling (g = 1), one whose amax is 6 gets g = 448 exactly, and in
+    every case the block holding the tensor's amax gets the largest E4M3 block
+    scale (code 0x7E = 448), its amax element the E2M1 code +-6, and that
+    element dequantizes back to the amax. A dropped factor 6, a missing 448
+    or a decode-direction g (amax / 2688) breaks one of these."""
+    rng = np.random.default_rng(21)
+    base = rng.standard_normal((4, 64)).astype(F32)
+    for amax, g_want in ((F32(2688.0), F32(1.0)), (F32(6.0), F32(448.0)), (F32(0.75), F32(3584.0))):
+        x = (base / np.abs(base).max() * amax).astype(F32)
+        t, k = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+        x[t, k] = amax if x[t, k] > 0 else -amax
+        g = O.nvfp4_global_scale(x)
+        assert g == g_want, (amax, g)
+        packed, sb = O.quant_nvfp4_rows(x, g)
+        codes = F.unpack_e2m1(packed)
+        assert sb[t, k // 16] == 0x7E                          # block scale 448: E4M3's largest finite
+        assert F.e4m3_decode(sb[t, k // 16]) == 448.0
+        assert (codes[t, k] & 7) == 7                          # |E2M1 code| = 6
+        xh = O.dequant_nvfp4_rows(packed, sb, g)
+        assert xh[t, k] == np.float64(x[t, k])                 # 6 * 448 / g = amax exactly here
+    # any tensor: the amax block's scale is 448, the others no larger
+    x = (rng.standard_normal((8, 256)) * 0.37).astype(F32)
+    g = O.nvfp4_global_scale(x)
+    _, sb = O.quant_nvfp4_rows(x, g)
+    t, k = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert sb[t, k // 16] == 0x7E
+    assert (F.e4m3_decode(sb) <= 448.0).all()
+
+
 def test_nvfp4_dequant_error_bound():
     """Each element is within half an E2M1 step of the block-scaled grid, the
     block scale within half an E4M3 step: |x - xhat| <= |x|/4*(1+1/16) + slack."""
