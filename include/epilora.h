@@ -178,16 +178,41 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
 
 /*
  * Bytes of device workspace epilora_layer_forward needs for (fmt, M, K, r):
- * the quantized activations, their scales, S (r = 0: no adapters; S is held
- * as up to ceil(K / 1024) partial sums over K slices, capped at 8) and, for
- * more than 32 tokens with adapters, a row-to-token map, each region
- * 256-byte aligned. Returns 0 for M == 0 or invalid arguments.
+ * EPILORA_WORKSPACE_SYNC_BYTES of grid-wide counters first, then the
+ * quantized activations, their scales, S (r = 0: no adapters; S is held as
+ * up to ceil(K / 1024) partial sums over K slices, capped at 8), for more
+ * than 32 tokens with adapters a row-to-token map, and for the single-kernel
+ * decode path (see epilora_layer_forward_kernels) partial rows of weight
+ * tiles split between thread blocks; each region 256-byte aligned. Returns 0
+ * for M == 0 or invalid arguments.
  */
+#define EPILORA_WORKSPACE_SYNC_BYTES 1280
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
 
 /*
+ * Number of kernels epilora_layer_forward (and _slices, _noalloc) enqueues
+ * for (fmt, M, K): 1 when the single-kernel decode path takes the call (a few
+ * tokens: M <= 8 and the quantized rows of all tokens within 16 KB, i.e.
+ * M * K <= 16384 for FP8, M * K <= 32768 for NVFP4), else 2 (the shrink grid
+ * with its quantizer blocks, then the GEMM as its programmatic dependent).
+ * Returns 0 for invalid arguments.
+ */
+EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K);
+
+/*
  * Fused one-call layer (the decode path of the EpiLoRA page, §Design ›
- * Multi-adapter kernels › The decode path): enqueues two kernels,
+ * Multi-adapter kernels › The decode path).
+ *
+ * A few tokens (epilora_layer_forward_kernels == 1) run as ONE persistent
+ * kernel, a programmatic dependent of the previous kernel on the stream: it
+ * streams Wq (and w_block_scale) at once, waits for that kernel, then every
+ * thread block quantizes the activations of all tokens for itself (the
+ * arithmetic of epilora_quant_act), takes shrink work items (token, 4 ranks,
+ * K slice: the arithmetic of epilora_lora_shrink split into partial sums)
+ * from a counter in the workspace, and finishes its share of the output; the
+ * weight stream is split evenly over the SMs, a weight tile split between
+ * thread blocks being summed in a fixed order. Otherwise it enqueues two
+ * kernels,
  *   1. the shrink grid (the arithmetic of epilora_lora_shrink, split over K
  *      slices into partial sums; for more than 32 tokens, blocks of 16
  *      consecutive tokens carrying at most two adapters on the tensor
@@ -201,10 +226,13 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
  *   2. the GEMM of epilora_gemm_lora_epilogue as its programmatic dependent:
  *      it starts streaming Wq (and w_block_scale) as soon as it is resident,
  *      and reads everything else only after the shrink grid has completed;
- * using `workspace` (>= epilora_workspace_bytes, 256-byte aligned, no
- * initial value needed) for Xq, scales, S and the row map. Y is the same
- * whatever the row order. Calls that share a workspace must be ordered on
- * one stream.
+ * using `workspace` (>= epilora_workspace_bytes, 256-byte aligned) for the
+ * counters, Xq, scales, S, the row map and partial rows. The first
+ * EPILORA_WORKSPACE_SYNC_BYTES of the workspace must be zero before the
+ * first call that uses it (zero-fill a workspace once after allocating it);
+ * every call leaves them zero again, and nothing else in the workspace needs
+ * an initial value. Y is the same whatever the row order. Calls that share a
+ * workspace must be ordered on one stream.
  * Because the GEMM may start while the kernel that precedes this call on the
  * stream is still running, that kernel must not write Wq or w_block_scale
  * (every other input, X included, may be its output).
@@ -268,7 +296,8 @@ EPILORA_API int epilora_layer_forward_slices(int fmt, int M, int N, int K,
  * r = 64: M up to 1635 at K = 4096); EPILORA_ERR_CUDA if the address lookup
  * fails.
  * Otherwise it enqueues what epilora_layer_forward enqueues (the scratch
- * needs no starting value: every byte is written before it is read).
+ * starts zeroed when the library is loaded, and every call leaves its
+ * counters zero again, as epilora_layer_forward requires).
  *
  * All calls on one device share the one scratch array: calls that overlap in
  * time (on different streams, or from host threads that do not order their

@@ -222,11 +222,18 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K, const v
   return fmt == EPILORA_FMT_FP8_E4M3 ? launch_gemm_fp8(a) : launch_gemm_nvfp4(a);
 }
 
+EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K) {
+  if (!fmt_ok(fmt) || M < 0 || !k_ok(K)) return 0;
+  if (M == 0) return 0;
+  return decode_path_eligible(fmt, M, K) ? 1 : 2;
+}
+
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   if (!fmt_ok(fmt) || M < 0 || K < 0 || r < 0) return 0;
   const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
   if (M == 0) return 0;
-  size_t bytes = 0;
+  // counters of the single-kernel decode path, at a fixed place
+  size_t bytes = round256(decode_sync_bytes());
   if (fmt == EPILORA_FMT_FP8_E4M3) {
     bytes += round256(m * k);          // Xq
     bytes += round256(m * 4);          // x_scale
@@ -238,6 +245,8 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   bytes += round256(m * static_cast<size_t>(r) * 4 * static_cast<size_t>(r > 0 ? shrink_parts_max(K) : 1));
   // more than one decode tile of tokens with adapters: the adapter-sorted row order
   if (r > 0 && M > 32) bytes += round256(m * 4);
+  // single-kernel decode path: partial rows of weight tiles split over CTAs
+  if (decode_path_eligible(fmt, M, K)) bytes += round256(decode_partial_bytes(M));
   return bytes;
 }
 
@@ -263,7 +272,8 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
     return EPILORA_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
-  size_t off = 0;
+  void* sync = ws;
+  size_t off = round256(decode_sync_bytes());
   void* Xq = ws + off;
   float* x_scale = nullptr;
   uint8_t* x_block_scale = nullptr;
@@ -281,8 +291,12 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
   if (adapters) {
     S = reinterpret_cast<float*>(ws + off);
     off += round256(m * static_cast<size_t>(rs) * 4 * static_cast<size_t>(shrink_parts_max(K)));
-    if (M > 32) perm = reinterpret_cast<int32_t*>(ws + off);
+    if (M > 32) {
+      perm = reinterpret_cast<int32_t*>(ws + off);
+      off += round256(m * 4);
+    }
   }
+  float* accp = reinterpret_cast<float*>(ws + off);   // decode path only
 
   int rc = gemm_validate(fmt, M, N, K, Xq, x_scale, x_block_scale, x_global_scale, Wq, w_scale, w_block_scale,
                          w_global_scale, S, B, L, r, idx, Y, ldy);
@@ -290,11 +304,51 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
   if (adapters && !shrink_args_ok(X, M, K, ldx, A, L, r, idx, mask, S)) return EPILORA_ERR_INVALID_ARG;
   if (!quant_args_ok(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale)) return EPILORA_ERR_INVALID_ARG;
 
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (decode_path_eligible(fmt, M, K)) {
+    // a few tokens: quantizer, shrink and GEMM in one persistent launch
+    DecodeArgs d{};
+    d.fmt = fmt;
+    d.M = M;
+    d.N = N;
+    d.K = K;
+    d.ldx = ldx;
+    d.ldy = ldy;
+    d.L = adapters ? L : 1;
+    d.r = adapters ? r : 16;
+    d.s_row = adapters ? rs : 0;
+    d.n_slices = n_slices;
+    for (int q = 0; q < n_slices && q < 4; ++q) d.slice_end[q] = slice_end != nullptr ? slice_end[q] : N;
+    int parts = shrink_parts_max(K);
+    while (parts > 1 && shrink_kslice(K, parts) * (parts - 1) >= K) --parts;
+    d.parts = parts;
+    d.kslice = shrink_kslice(K, parts);
+    d.X = X;
+    d.Wq = Wq;
+    d.w_scale = w_scale;
+    d.w_block_scale = w_block_scale;
+    d.w_global_scale = w_global_scale;
+    d.x_global_scale = x_global_scale;
+    d.A = adapters ? A : nullptr;
+    d.B = adapters ? B : nullptr;
+    d.idx = idx;
+    d.mask = mask;
+    d.Y = Y;
+    d.status_dev = status_dev;
+    d.stream = st;
+    d.sync = sync;
+    d.S = S;
+    d.accp = accp;
+    d.Xq = Xq;
+    d.x_scale = x_scale;
+    d.x_block_scale = x_block_scale;
+    return launch_fused_decode(d);
+  }
+
   // The shrink grid (with the quantizer CTAs) is a programmatic dependent of
   // the previous kernel on the stream and releases the GEMM at once; the GEMM
   // streams W immediately and reads everything the shrink grid writes (and
   // the token metadata) only after that grid has completed.
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int parts = adapters ? shrink_parts(M, K, rs) : shrink_parts(M, K, 0);
   rc = launch_shrink_quant(X, M, K, ldx, A, adapters ? L : 1, adapters ? rs : 0, idx, mask, S, parts, fmt, Xq,
                            x_scale, x_block_scale, x_global_scale, perm, status_dev, st);

@@ -88,6 +88,43 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
 // and the largest it can use for K (sizes the workspace).
 int shrink_parts(int M, int K, int r);
 int shrink_parts_max(int K);
+// Single-kernel decode path (decode.cu): the whole fused layer call for a few
+// tokens in one persistent launch.
+struct DecodeArgs {
+  int fmt;
+  int M, N, K, ldx, ldy, L, r;
+  int s_row;            // floats per S row (n_slices * r)
+  int n_slices;
+  int slice_end[4];
+  int parts, kslice;    // K slices of the shrink items
+  const void* X;
+  const void* Wq;
+  const float* w_scale;
+  const uint8_t* w_block_scale;
+  const float* w_global_scale;
+  const float* x_global_scale;
+  const void* A;        // NULL with B: no adapters
+  const void* B;
+  const int32_t* idx;
+  const uint8_t* mask;
+  void* Y;
+  int* status_dev;
+  cudaStream_t stream;
+  // workspace regions
+  void* sync;           // decode_sync_bytes(), zero before the call, zero after it
+  float* S;             // [parts][M][s_row]
+  float* accp;          // decode_partial_bytes(M)
+  void* Xq;             // the quantized activations as used (written by one CTA)
+  float* x_scale;
+  uint8_t* x_block_scale;
+};
+bool decode_path_eligible(int fmt, int M, int K);
+size_t decode_sync_bytes();
+size_t decode_partial_bytes(int M);
+int launch_fused_decode(const DecodeArgs& a);
+// K slice length of a shrink split into `parts` slices (multiple of 256)
+int shrink_kslice(int K, int parts);
+
 int launch_gemm_fp8(const GemmArgs& a);
 int launch_gemm_nvfp4(const GemmArgs& a);
 

@@ -1,0 +1,909 @@
+// Single-kernel decode path: the whole multi-tenant LoRA layer of a few decode
+// tokens in ONE launch per projection.
+//
+// EpiLoRA, "Fusing Many LoRA Adapters into Low-Precision GEMMs for Serving and
+// RL":
+//  * §Design › Multi-adapter kernels › K1 and K2 — activations quantized once
+//    per token, h = x A^T from the bf16 activations, the GEMM epilogue applies
+//    the weight and activation scales and adds h B^T before Y is written once;
+//  * › The decode path — the GEMM streams its weights while the
+//    down-projection runs and needs h only before its epilogue; the page does
+//    this with two launches chained by programmatic dependent launch and
+//    counts the second launch and its hand-off in "exposed + launch"
+//    (§Evaluation › Kernels, Table 13); here both are one kernel.
+//
+// GB300 design: one persistent CTA per SM (about 113 KB of shared memory, so
+// the next projection's CTA fits beside it and streams its weights while this
+// one finishes). The weight matrix is cut into units (128 rows x 128 bytes of
+// K, 16 KB of codes) in tile-major order and every CTA takes an equal
+// contiguous run of units (stream-K), so no SM streams more than its share.
+// Roles (192 threads):
+//   warp 0      TMA producer: the CTA's weight units (and NVFP4 weight scale
+//               boxes) through a ring, started before the dependency wait
+//               (weights are never written by the preceding kernel), plus an
+//               L2 prefetch of the units behind the ring;
+//   warp 1      MMA issuer: copies the unit's quantized activation rows from
+//               shared memory into the stage, then tcgen05.mma (kind::f8f6f4,
+//               or kind::mxf4nvf4 with scales copied into TMEM) into one of
+//               two TMEM accumulators (one per segment of the run that falls
+//               in one weight tile);
+//   warps 2..5  helpers: wait for the preceding kernel (griddepcontrol.wait),
+//               quantize the activations of all tokens into shared memory
+//               (every CTA does it for itself: at most 16 KB of codes), then
+//               take shrink work items from a grid-wide counter (token x 4
+//               ranks x K slice, the arithmetic of the standalone shrink),
+//               publish each partial sum of S and count it done; then the
+//               epilogue of each segment.
+// A weight tile split over several CTAs is finished by the CTA that holds its
+// first K unit (it reaches that tile last): the other CTAs store their fp32
+// partial rows and raise a flag; the finisher adds them in CTA order
+// (deterministic), then the scales, then the adapter term once every shrink
+// item is counted, and writes Y. Every wait is bounded (an error status, then
+// an orderly exit), and waits only on work already claimed by running CTAs.
+// The grid-wide counters live in the first bytes of the workspace; the last
+// CTA to exit returns them to zero.
+#include "quant_row.cuh"
+
+namespace epi {
+
+namespace {
+
+constexpr int kDecThreads = 192;
+constexpr int kDecMaxTokens = 8;
+constexpr int kDecMaxCtas = 256;
+constexpr int kDecXcBytes = 16384;         // compact quantized activations per CTA
+constexpr int kDecRanksPerItem = 4;
+constexpr int kDecHelperBar = 1;           // named barrier of the 4 helper warps
+constexpr int kDecUnitW = 128 * 128;       // weight codes per unit (bytes)
+constexpr int kDecXSlot = 16 * 128;        // activation rows of a stage (16-row MMA operand)
+constexpr int kDecSmemBudget = 113 * 1024;
+constexpr int kDecMaxStages = 8;
+constexpr int kMaxRankBrow = 64;           // 32-bit words of a rank-128 bf16 B row
+
+// sync block at the start of the workspace: [0] claim, [1] done, [2] exit;
+// flags of the partial-row slots from word 64 on
+constexpr int kDecSyncWords = 64;
+
+struct DecParams {
+  CUtensorMap tmW;     // uint8 [N, Kb], box 128 rows x 128 B, 128-B swizzle
+  CUtensorMap tmSW;    // NVFP4: uint8 [N, K/16], box 128 rows x 16 B
+  const __nv_bfloat16* X;
+  const __nv_bfloat16* A;
+  const __nv_bfloat16* B;
+  const int32_t* idx;
+  const uint8_t* mask;
+  const float* w_scale;
+  const float* w_gs;
+  const float* x_gs;
+  __nv_bfloat16* Y;
+  int* status;
+  unsigned* sync;      // [claim, done, exit, ..., flags from kDecSyncWords]
+  float* S;            // [parts][M][s_row] partial sums of the shrink
+  float* accp;         // [G][M][128] fp32 partial rows of split weight tiles
+  uint8_t* xq_out;     // CTA 0 also stores the quantized activations here
+  float* xs_out;       // FP8 scales
+  uint8_t* xsb_out;    // NVFP4 block scales
+  long long U;         // units in total
+  int G, nkb, n_tiles, stages, l2_ahead;
+  int M, N, K, ldx, ldy, L, r, s_row, n_slices;
+  int slice_end[4];
+  int adapters, parts, kslice, n_items;
+  int kb_pad;          // bytes of one compact activation row (nkb * 128)
+};
+
+template <int FMT>
+struct DecCfg {
+  static constexpr bool kFP4 = FMT == EPILORA_FMT_NVFP4;
+  static constexpr int kSfA = kFP4 ? 4 * 512 : 0;          // weight scale atoms of a stage (4 MMA k-steps)
+  static constexpr int kSfB = kFP4 ? 4 * 512 : 0;          // token scale atoms
+  static constexpr int kSfWRaw = kFP4 ? 128 * 16 : 0;      // TMA box of weight scales
+  static constexpr int kStage = kDecUnitW + kDecXSlot + kSfA + kSfB + kSfWRaw;
+  static constexpr int kStageTx = kDecUnitW + kSfWRaw;     // bytes TMA delivers per stage
+  static constexpr int kSfColsA = 16;                      // 4 k-steps x 4 columns
+  static constexpr int kSfColsB = 16;
+  static constexpr int kSfSlot = kSfColsA + kSfColsB;
+  static constexpr int kTmemCols = kFP4 ? 128 : 32;        // 2 accumulators of 16 (+ 2 scale slots)
+  static constexpr uint32_t kIdesc = kFP4 ? idesc_mxf4nvf4(128, 16) : idesc_f8f6f4_e4m3(128, 16);
+  static_assert(kStage % 1024 == 0, "stage alignment");
+};
+
+__device__ __forceinline__ void helper_sync() {
+  asm volatile("bar.sync %0, 128;" ::"r"(kDecHelperBar) : "memory");
+}
+
+// OR of a flag over the 4 helper warps (also a barrier among them)
+__device__ __forceinline__ bool helper_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(kDecHelperBar)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded spin of one thread until *p >= target (1 s limit); false on timeout.
+__device__ __forceinline__ bool spin_until_at_least(const unsigned* p, unsigned target) {
+  if (ld_acquire_u32(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (ld_acquire_u32(p) >= target) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    __nanosleep(64);
+  }
+}
+
+__device__ __forceinline__ float dec_dot8(const uint4& xv, const uint4& av, float acc) {
+  acc = fmaf(bf16_lo(xv.x), bf16_lo(av.x), acc);
+  acc = fmaf(bf16_hi(xv.x), bf16_hi(av.x), acc);
+  acc = fmaf(bf16_lo(xv.y), bf16_lo(av.y), acc);
+  acc = fmaf(bf16_hi(xv.y), bf16_hi(av.y), acc);
+  acc = fmaf(bf16_lo(xv.z), bf16_lo(av.z), acc);
+  acc = fmaf(bf16_hi(xv.z), bf16_hi(av.z), acc);
+  acc = fmaf(bf16_lo(xv.w), bf16_lo(av.w), acc);
+  acc = fmaf(bf16_hi(xv.w), bf16_hi(av.w), acc);
+  return acc;
+}
+
+// S[v] . B[l, n] with the B row in registers (R4 float4 chunks of S from
+// shared memory; two accumulators)
+template <int R4>
+__device__ __forceinline__ float dec_dot_row(const float4* srow, const uint32_t* brow) {
+  float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+  for (int c = 0; c < R4; ++c) {
+    const float4 s4 = srow[c];
+    float& d = (c & 1) ? d1 : d0;
+    d = fmaf(s4.x, bf16_lo(brow[2 * c]), d);
+    d = fmaf(s4.y, bf16_hi(brow[2 * c]), d);
+    d = fmaf(s4.z, bf16_lo(brow[2 * c + 1]), d);
+    d = fmaf(s4.w, bf16_hi(brow[2 * c + 1]), d);
+  }
+  return d0 + d1;
+}
+
+// Run of units of CTA c: [U c / G, U (c + 1) / G), walked as segments that
+// each lie in one weight tile.
+struct SegWalk {
+  long long u, u1;
+  int nkb;
+  __device__ SegWalk(const DecParams& p, int c)
+      : u((p.U * c) / p.G), u1((p.U * (c + 1)) / p.G), nkb(p.nkb) {}
+  __device__ bool next(int& T, int& kb0, int& kb1) {
+    if (u >= u1) return false;
+    T = static_cast<int>(u / nkb);
+    kb0 = static_cast<int>(u - static_cast<long long>(T) * nkb);
+    const long long left = u1 - u;
+    kb1 = left < nkb - kb0 ? kb0 + static_cast<int>(left) : nkb;
+    u += kb1 - kb0;
+    return true;
+  }
+};
+
+// CTA whose run holds unit u
+__device__ __forceinline__ int cta_of_unit(const DecParams& p, long long u) {
+  return static_cast<int>(((u + 1) * p.G + p.U - 1) / p.U) - 1;
+}
+
+__device__ __forceinline__ int dec_slice_offset(const DecParams& p, int n0) {
+  int off = 0;
+  for (int q = 0; q + 1 < p.n_slices && q < 4; ++q)
+    if (n0 >= p.slice_end[q]) off += p.r;
+  return off;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __grid_constant__ DecParams p) {
+  using C = DecCfg<FMT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stages = p.stages;
+  const int M = p.M;
+  uint8_t* xc = smem + static_cast<size_t>(stages) * C::kStage;       // [M][kb_pad] swizzled codes
+  uint8_t* xsf = xc + M * p.kb_pad;                                   // NVFP4: [M][nkb * 16] block scales
+  float* s_stage = reinterpret_cast<float*>(xsf + (C::kFP4 ? (M * p.nkb * 16 + 127) / 128 * 128 : 0));
+  uint8_t* misc = reinterpret_cast<uint8_t*>(s_stage) + (M * p.s_row * 4 + 127) / 128 * 128;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(misc);
+  uint64_t* empty_bar = full_bar + kDecMaxStages;
+  uint64_t* accf_bar = empty_bar + kDecMaxStages;    // [2] accumulator complete
+  uint64_t* acce_bar = accf_bar + 2;                 // [2] accumulator read out
+  uint64_t* xrdy_bar = acce_bar + 2;                 // compact activations written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xrdy_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* bcast = reinterpret_cast<int*>(tmem_slot + 2);                 // helper broadcast word
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);               // [4 warps][8]
+  int* meta_idx = reinterpret_cast<int*>(red + 32);                   // [kDecMaxTokens] adapter or -1
+  float* meta_sx = reinterpret_cast<float*>(meta_idx + kDecMaxTokens);   // FP8 activation scales
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf_bar[b], 1);
+      mbar_init(&acce_bar[b], 1);
+    }
+    mbar_init(xrdy_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&p.tmW);
+    if (C::kFP4) tma_prefetch_desc(&p.tmSW);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ===== TMA producer: the run's weight units, in order =====
+    if (lane == 0) {
+      uint32_t issued_mask = 0, parity_mask = 0;
+      long long it = 0;
+      const long long u_begin = (p.U * c) / p.G, u_end = (p.U * (c + 1)) / p.G;
+      for (long long u = u_begin; u < u_end; ++u, ++it) {
+        const int s = static_cast<int>(it % stages);
+        const uint32_t ph = static_cast<uint32_t>(it / stages) & 1u;
+        if (*abort_flag || !mbar_wait_bounded(&empty_bar[s], ph ^ 1u, kWaitLimitNs)) {
+          *abort_flag = 1;
+          record_status(p.status, EPILORA_ERR_TIMEOUT);
+          break;
+        }
+        const int T = static_cast<int>(u / p.nkb);
+        const int kb = static_cast<int>(u - static_cast<long long>(T) * p.nkb);
+        uint8_t* st = smem + static_cast<size_t>(s) * C::kStage;
+        mbar_arrive_expect_tx(&full_bar[s], C::kStageTx);
+        tma_load_2d(st, &p.tmW, &full_bar[s], kb * 128, T * 128);
+        if (C::kFP4) tma_load_2d(st + kDecUnitW + kDecXSlot + C::kSfA + C::kSfB, &p.tmSW, &full_bar[s], kb * 16,
+                                 T * 128);
+        issued_mask |= 1u << s;
+        parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
+        if (it == stages - 1 || u + 1 == u_end) {
+          // the ring is primed: the units behind it go to L2 now
+          const long long a_end = min(u_end, u + 1 + p.l2_ahead);
+          for (long long v = u + 1; v < a_end; ++v) {
+            const int T2 = static_cast<int>(v / p.nkb);
+            const int kb2 = static_cast<int>(v - static_cast<long long>(T2) * p.nkb);
+            tma_prefetch_l2_2d(&p.tmW, kb2 * 128, T2 * 128);
+            if (C::kFP4) tma_prefetch_l2_2d(&p.tmSW, kb2 * 16, T2 * 128);
+          }
+        }
+      }
+      // every weight byte of this CTA is requested: the next kernel on the
+      // stream may start its CTAs (they wait for this grid before reading
+      // anything it writes)
+      pdl_allow_dependents();
+      if (*abort_flag) {
+        for (int s = 0; s < stages; ++s)
+          if (issued_mask & (1u << s)) (void)mbar_wait_bounded(&full_bar[s], (parity_mask >> s) & 1u, kWaitLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ===== MMA issuer =====
+    const bool xok = __all_sync(0xffffffffu, mbar_wait_bounded(xrdy_bar, 0, kWaitLimitNs));
+    if (!xok && lane == 0) {
+      *abort_flag = 1;
+      record_status(p.status, EPILORA_ERR_TIMEOUT);
+    }
+    SegWalk walk(p, c);
+    int T, kb0, kb1, j = 0;
+    long long it = 0;
+    bool stop = !xok;
+    while (!stop && walk.next(T, kb0, kb1)) {
+      const int b = j & 1;
+      // the helpers have read this accumulator's previous segment
+      const bool oke = __all_sync(0xffffffffu, mbar_wait_bounded(&acce_bar[b], ((j >> 1) & 1) ^ 1u, kWaitLimitNs));
+      if (!oke || *abort_flag) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          record_status(p.status, EPILORA_ERR_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * 16);
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int s = static_cast<int>(it % stages);
+        const uint32_t ph = static_cast<uint32_t>(it / stages) & 1u;
+        const int ab = __shfl_sync(0xffffffffu, *abort_flag, 0);
+        const bool ok = !ab && __all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[s], ph, kWaitLimitNs));
+        if (!ok) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            record_status(p.status, EPILORA_ERR_TIMEOUT);
+          }
+          stop = true;
+          break;
+        }
+        uint8_t* st = smem + static_cast<size_t>(s) * C::kStage;
+        uint8_t* xs = st + kDecUnitW;
+        // activation rows of this unit (row t of the 8-row group at t * 128;
+        // the compact rows already carry the swizzle of row t)
+        for (int q = lane; q < M * 8; q += 32) {
+          const int t = q >> 3, ch = q & 7;
+          *reinterpret_cast<uint4*>(xs + t * 128 + ch * 16) =
+              *reinterpret_cast<const uint4*>(xc + t * p.kb_pad + kb * 128 + ch * 16);
+        }
+        if (C::kFP4) {
+          // weight scales: canonical [128 rows][16 B] box -> one 512-B atom
+          // per K = 64 step (line r0 = 4 bytes of rows r0, r0+32, r0+64, r0+96);
+          // token scales from the compact copy the same way (rows < M)
+          uint8_t* sfa = xs + kDecXSlot;
+          uint8_t* sfb = sfa + C::kSfA;
+          const uint8_t* raw_w = sfb + C::kSfB;
+          uint4 v[4];
+#pragma unroll
+          for (int r1 = 0; r1 < 4; ++r1) v[r1] = *reinterpret_cast<const uint4*>(raw_w + (lane + 32 * r1) * 16);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            uint4 o;
+            o.x = (&v[0].x)[kk];
+            o.y = (&v[1].x)[kk];
+            o.z = (&v[2].x)[kk];
+            o.w = (&v[3].x)[kk];
+            *reinterpret_cast<uint4*>(sfa + kk * 512 + lane * 16) = o;
+          }
+          uint4 tv4 = make_uint4(0u, 0u, 0u, 0u);
+          if (lane < M) tv4 = *reinterpret_cast<const uint4*>(xsf + (lane * p.nkb + kb) * 16);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            *reinterpret_cast<uint4*>(sfb + kk * 512 + lane * 16) = make_uint4((&tv4.x)[kk], 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t w_addr = smem_u32(st);
+          const uint32_t x_addr = smem_u32(xs);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = make_smem_desc(w_addr + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bdesc = make_smem_desc(x_addr + kk * 32, 16, 1024, kSwizzle128B);
+            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+            if (C::kFP4) {
+              const uint32_t slot = 32u + static_cast<uint32_t>(it & 1) * C::kSfSlot;
+              const uint32_t sfa_col = slot + kk * 4;
+              const uint32_t sfb_col = slot + C::kSfColsA + kk * 4;
+              tc_cp_32x128b_warpx4(tmem_base + sfa_col,
+                                   make_smem_desc(smem_u32(xs + kDecXSlot) + kk * 512, 16, 128, kSwizzleNone));
+              tc_cp_32x128b_warpx4(tmem_base + sfb_col, make_smem_desc(smem_u32(xs + kDecXSlot + C::kSfA) + kk * 512,
+                                                                       16, 128, kSwizzleNone));
+              mma_mxf4nvf4(d_tmem, adesc, bdesc, C::kIdesc, tmem_base + sfa_col, tmem_base + sfb_col, accum);
+            } else {
+              mma_f8f6f4(d_tmem, adesc, bdesc, C::kIdesc, accum);
+            }
+          }
+          tc_commit(&empty_bar[s]);   // frees the stage once these MMAs have read it
+        }
+        __syncwarp();
+      }
+      if (lane == 0) tc_commit(&accf_bar[b]);   // this segment's accumulator (or a drain after an abort)
+      __syncwarp();
+      ++j;
+    }
+    if (lane == 0 && j > 0) {
+      // nothing of this warp in flight at exit
+      const int bl = (j - 1) & 1;
+      (void)mbar_wait_bounded(&accf_bar[bl], ((j - 1) >> 1) & 1u, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ===== helpers =====
+    const int et = threadIdx.x - 64;
+    const int hw = warp - 2;                      // helper warp 0..3
+    // hints before the wait: the activation rows and this CTA's share of the
+    // adapters' A rows into L2 (the index read here may still change)
+    if (et == 0) {
+      for (int t = 0; t < M; ++t)
+        prefetch_l2_bulk(p.X + static_cast<size_t>(t) * p.ldx, static_cast<uint32_t>(p.K * 2));
+      if (p.adapters) {
+        const size_t abytes = static_cast<size_t>(p.s_row) * p.K * 2;
+        const size_t share = ((abytes + p.G - 1) / p.G + 255) / 256 * 256;
+        const size_t lo = share * c;
+        for (int t = 0; t < M && lo < abytes; ++t) {
+          int l;
+          asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(l) : "l"(p.idx + t));
+          if (l < 0 || l >= p.L) continue;
+          const size_t n = min(share, abytes - lo);
+          prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.A) + static_cast<size_t>(l) * abytes + lo,
+                           static_cast<uint32_t>(n));
+        }
+      }
+    }
+    // the preceding kernel on the stream has completed: X, idx, mask and the
+    // workspace are valid from here on
+    pdl_wait_primary();
+    if (et < M) {
+      int l = -1;
+      if (p.adapters) {
+        const int li = p.idx[et];
+        if (li >= p.L) record_status(p.status, EPILORA_ERR_INVALID_ARG);
+        l = (li >= 0 && li < p.L && (p.mask == nullptr || p.mask[et] != 0)) ? li : -1;
+      }
+      meta_idx[et] = l;
+    }
+    float alpha = 1.0f;
+    // ---- activation quantization into the compact copy ----
+    const int nch = p.K / 8;                      // 16-byte bf16 chunks per row
+    if (!C::kFP4) {
+      // all M rows at once: chunk q = et + 128 j of the M x nch chunks is held
+      // in registers between the amax and the codes (M * K <= 16384)
+      constexpr int kHold = 16;
+      uint4 v[kHold];
+      float am[kDecMaxTokens];
+#pragma unroll
+      for (int t = 0; t < kDecMaxTokens; ++t) am[t] = 0.0f;
+      const int total = M * nch;
+#pragma unroll
+      for (int jj = 0; jj < kHold; ++jj) {
+        const int q = et + 128 * jj;
+        if (q < total) {
+          const int t = q / nch;
+          v[jj] = __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch));
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < kHold; ++jj) {
+        const int q = et + 128 * jj;
+        if (q < total) {
+          const int t = q / nch;
+          float x[8];
+          unpack8(v[jj], x);
+          float m = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+#pragma unroll
+          for (int tt = 0; tt < kDecMaxTokens; ++tt)
+            if (tt == t) am[tt] = fmaxf(am[tt], m);
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < kDecMaxTokens; ++tt) {
+        float m = am[tt];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) red[hw * kDecMaxTokens + tt] = m;
+      }
+      helper_sync();
+      if (et < M) {
+        const float m = fmaxf(fmaxf(red[et], red[kDecMaxTokens + et]),
+                              fmaxf(red[2 * kDecMaxTokens + et], red[3 * kDecMaxTokens + et]));
+        const float sc = __fdiv_rn(fmaxf(m, kAmaxFloor), kE4M3Max);
+        meta_sx[et] = sc;
+        if (c == 0) p.xs_out[et] = sc;
+      }
+      helper_sync();
+#pragma unroll
+      for (int jj = 0; jj < kHold; ++jj) {
+        const int q = et + 128 * jj;
+        if (q < total) {
+          const int t = q / nch;
+          const int k0 = (q - t * nch) * 8;
+          const uint2 code = quant8_e4m3(v[jj], meta_sx[t]);
+          const int a = k0 >> 7, ch = (k0 & 127) >> 4, half = (k0 & 15) >> 3;
+          *reinterpret_cast<uint2*>(xc + t * p.kb_pad + a * 128 + ((ch ^ (t & 7)) << 4) + half * 8) = code;
+          if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+        }
+      }
+      // zero codes past K in the last unit (finite values against the
+      // weight box's zero fill)
+      for (int q = et; q < M * (p.kb_pad - p.K) / 8; q += 128) {
+        const int per = (p.kb_pad - p.K) / 8;
+        const int t = q / per;
+        const int k0 = p.K + (q - t * per) * 8;
+        const int a = k0 >> 7, ch = (k0 & 127) >> 4, half = (k0 & 15) >> 3;
+        *reinterpret_cast<uint2*>(xc + t * p.kb_pad + a * 128 + ((ch ^ (t & 7)) << 4) + half * 8) = make_uint2(0, 0);
+      }
+    } else {
+      // NVFP4: per 16-element block, its scale and codes (block-local)
+      const float g = *p.x_gs;
+      const bool g_ok = (g > 0.0f) && isfinite(g);
+      if (!g_ok && et == 0) record_status(p.status, EPILORA_ERR_INVALID_ARG);
+      alpha = 1.0f / (g * *p.w_gs);
+      const int nb = p.K / kNvfp4Block;
+      const int total = M * nb;
+#pragma unroll 4
+      for (int q = et; q < total; q += 128) {
+        const int t = q / nb;
+        const int b = q - t * nb;
+        const uint4* row = reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx);
+        float x[16];
+        {
+          float a0[8], a1[8];
+          unpack8(__ldcg(row + 2 * b), a0);
+          unpack8(__ldcg(row + 2 * b + 1), a1);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            x[i] = a0[i];
+            x[8 + i] = a1[i];
+          }
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        uint32_t sb = 0, lo = 0, hi = 0;
+        if (g_ok) {
+          const float t2 = __fmul_rn(__fdiv_rn(amax, kE2M1Max), g);
+          sb = cvt_e4m3x2(t2, 0.0f) & 0xFFu;
+          const float sbf = e4m3_to_f32(sb);
+          if (sbf > 0.0f) {
+            const float inv = __fdiv_rn(g, sbf);
+            uint32_t by[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) by[i] = cvt_e2m1x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
+            lo = by[0] | (by[1] << 8) | (by[2] << 16) | (by[3] << 24);
+            hi = by[4] | (by[5] << 8) | (by[6] << 16) | (by[7] << 24);
+          }
+        }
+        // byte k/2 of the packed row: atom b / 16, 16-byte chunk (b % 16) / 2, half b % 2
+        const int a = b >> 4, ch = (b & 15) >> 1, half = b & 1;
+        *reinterpret_cast<uint2*>(xc + t * p.kb_pad + a * 128 + ((ch ^ (t & 7)) << 4) + half * 8) = make_uint2(lo, hi);
+        xsf[t * p.nkb * 16 + b] = static_cast<uint8_t>(sb);
+        if (c == 0) {
+          *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * (p.K / 2) + b * 8) = make_uint2(lo, hi);
+          p.xsb_out[static_cast<size_t>(t) * nb + b] = static_cast<uint8_t>(sb);
+        }
+      }
+    }
+    helper_sync();
+    if (et == 0) mbar_arrive(xrdy_bar);           // the MMA warp may start
+    // ---- this CTA's finisher tiles: B slices of their adapters into L2 ----
+    if (p.adapters && et == 0) {
+      SegWalk w2(p, c);
+      int T, kb0, kb1;
+      while (w2.next(T, kb0, kb1)) {
+        if (kb0 != 0) continue;
+        const int rows = min(128, p.N - T * 128);
+        int prev = -1;
+        for (int t = 0; t < M; ++t) {
+          const int l = meta_idx[t];
+          if (l < 0 || l == prev) continue;
+          prefetch_l2_bulk(p.B + (static_cast<size_t>(l) * p.N + T * 128) * p.r,
+                           static_cast<uint32_t>(rows * p.r * 2));
+          prev = l;
+        }
+      }
+    }
+    // ---- shrink items: (token, 4 ranks, K slice), claimed grid-wide ----
+    const int groups = p.s_row / kDecRanksPerItem;
+    if (p.adapters) {
+      while (true) {
+        if (et == 0) *bcast = static_cast<int>(atomicAdd(&p.sync[0], 1u));
+        helper_sync();
+        const int item = *bcast;
+        helper_sync();
+        if (item >= p.n_items) break;
+        const int t = item / (groups * p.parts);
+        const int rem = item - t * groups * p.parts;
+        const int part = rem / groups;
+        const int j0 = (rem - part * groups) * kDecRanksPerItem;
+        const int l = meta_idx[t];
+        if (l >= 0) {
+          const int c0 = part * p.kslice / 8;
+          const int c1 = min(p.K, (part + 1) * p.kslice) / 8;
+          const uint4* xr = reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx);
+          const uint4* ar =
+              reinterpret_cast<const uint4*>(p.A + (static_cast<size_t>(l) * p.s_row + j0) * static_cast<size_t>(p.K));
+          float acc[kDecRanksPerItem];
+#pragma unroll
+          for (int jr = 0; jr < kDecRanksPerItem; ++jr) acc[jr] = 0.0f;
+#pragma unroll 2
+          for (int ch = c0 + et; ch < c1; ch += 128) {
+            const uint4 xv = __ldcg(xr + ch);
+            uint4 av[kDecRanksPerItem];
+#pragma unroll
+            for (int jr = 0; jr < kDecRanksPerItem; ++jr) av[jr] = __ldg(ar + static_cast<size_t>(jr) * nch + ch);
+#pragma unroll
+            for (int jr = 0; jr < kDecRanksPerItem; ++jr) acc[jr] = dec_dot8(xv, av[jr], acc[jr]);
+          }
+#pragma unroll
+          for (int jr = 0; jr < kDecRanksPerItem; ++jr) {
+            float s = acc[jr];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) red[hw * kDecRanksPerItem + jr] = s;
+          }
+          helper_sync();
+          if (et == 0) {
+            float4 o;
+            float* ov = &o.x;
+#pragma unroll
+            for (int jr = 0; jr < kDecRanksPerItem; ++jr) {
+              float sum = 0.0f;
+              for (int w = 0; w < 4; ++w) sum += red[w * kDecRanksPerItem + jr];
+              ov[jr] = sum;
+            }
+            *reinterpret_cast<float4*>(p.S + (static_cast<size_t>(part) * M + t) * p.s_row + j0) = o;
+          }
+        }
+        if (et == 0) {
+          __threadfence();
+          atomicAdd(&p.sync[1], 1u);
+        }
+      }
+    }
+    // ---- epilogue of each segment ----
+    const int q4 = warp & 3;                      // TMEM lane quadrant of this warp
+    const int m = q4 * 32 + lane;                 // weight row within the tile
+    bool s_ready = false;
+    uint32_t brow[kMaxRankBrow];
+    long long brow_key = -1;
+    SegWalk walk(p, c);
+    int T, kb0, kb1, j = 0;
+    while (walk.next(T, kb0, kb1)) {
+      const int b = j & 1;
+      const int n = T * 128 + m;
+      const bool finisher = kb0 == 0;
+      float sw = 0.0f;
+      if (finisher && !C::kFP4 && n < p.N) sw = ldg_nc_f32_now(p.w_scale + n);
+      const bool ok = mbar_wait_bounded(&accf_bar[b], (j >> 1) & 1u, kWaitLimitNs);
+      if (helper_any(!ok || *abort_flag)) {
+        if (et == 0) {
+          *abort_flag = 1;
+          record_status(p.status, EPILORA_ERR_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(b * 16), v);
+      tmem_ld_wait();
+      tc_fence_before();
+      helper_sync();
+      if (et == 0) mbar_arrive(&acce_bar[b]);     // the accumulator may take the next segment
+      float acc[kDecMaxTokens];
+#pragma unroll
+      for (int t = 0; t < kDecMaxTokens; ++t) acc[t] = __uint_as_float(v[t]);
+      if (!finisher) {
+        // publish this CTA's partial rows of tile T: slot c, [token][row]
+        float* dst = p.accp + static_cast<size_t>(c) * M * 128;
+#pragma unroll
+        for (int t = 0; t < kDecMaxTokens; ++t)
+          if (t < M) dst[t * 128 + m] = acc[t];
+        __threadfence();
+        helper_sync();
+        if (et == 0) st_release_u32(&p.sync[kDecSyncWords + c], 1u);
+        ++j;
+        continue;
+      }
+      // finisher: add the partial rows of the CTAs holding the rest of tile T,
+      // in CTA order
+      if (kb1 < p.nkb) {
+        const int c_last = cta_of_unit(p, static_cast<long long>(T) * p.nkb + p.nkb - 1);
+        bool late = false;
+        for (int c2 = c + 1; c2 <= c_last; ++c2) {
+          if (et == 0) *bcast = spin_until_at_least(&p.sync[kDecSyncWords + c2], 1u) ? 1 : 0;
+          helper_sync();
+          if (*bcast == 0) {
+            late = true;
+            break;
+          }
+          const float* src = p.accp + static_cast<size_t>(c2) * M * 128;
+#pragma unroll
+          for (int t = 0; t < kDecMaxTokens; ++t)
+            if (t < M) acc[t] += __ldcg(src + t * 128 + m);
+          helper_sync();
+        }
+        if (late) {
+          if (et == 0) {
+            *abort_flag = 1;
+            record_status(p.status, EPILORA_ERR_TIMEOUT);
+          }
+          break;
+        }
+      }
+      // S: every shrink item counted, partial sums added in part order
+      if (p.adapters && !s_ready) {
+        if (et == 0) *bcast = spin_until_at_least(&p.sync[1], static_cast<unsigned>(p.n_items)) ? 1 : 0;
+        helper_sync();
+        if (*bcast == 0) {
+          if (et == 0) {
+            *abort_flag = 1;
+            record_status(p.status, EPILORA_ERR_TIMEOUT);
+          }
+          break;
+        }
+        const size_t part_stride = static_cast<size_t>(M) * p.s_row;
+        for (int e = et; e < M * p.s_row; e += 128) {
+          const int t = e / p.s_row;
+          float sum = 0.0f;
+          if (meta_idx[t] >= 0) {
+            sum = __ldcg(p.S + e);
+            for (int q = 1; q < p.parts; ++q) sum += __ldcg(p.S + q * part_stride + e);
+          }
+          s_stage[e] = sum;
+        }
+        helper_sync();
+        s_ready = true;
+      }
+      if (n < p.N) {
+        const int soff = p.adapters ? dec_slice_offset(p, T * 128) : 0;
+#pragma unroll
+        for (int t = 0; t < kDecMaxTokens; ++t) {
+          if (t >= M) break;
+          float y = C::kFP4 ? acc[t] * alpha : (acc[t] * meta_sx[t]) * sw;
+          const int l = meta_idx[t];
+          if (l >= 0) {
+            const long long key = static_cast<long long>(l) * p.n_tiles + T;
+            if (key != brow_key) {
+              const uint4* bsrc = reinterpret_cast<const uint4*>(p.B + (static_cast<size_t>(l) * p.N + n) * p.r);
+#pragma unroll
+              for (int cc = 0; cc < kMaxRankBrow / 4; ++cc)
+                if (cc < p.r / 8) {
+                  const uint4 bv = __ldg(bsrc + cc);
+                  brow[4 * cc] = bv.x;
+                  brow[4 * cc + 1] = bv.y;
+                  brow[4 * cc + 2] = bv.z;
+                  brow[4 * cc + 3] = bv.w;
+                }
+              brow_key = key;
+            }
+            const float4* srow = reinterpret_cast<const float4*>(s_stage + t * p.s_row + soff);
+            switch (p.r) {
+              case 16: y += dec_dot_row<4>(srow, brow); break;
+              case 32: y += dec_dot_row<8>(srow, brow); break;
+              case 64: y += dec_dot_row<16>(srow, brow); break;
+              default: y += dec_dot_row<32>(srow, brow); break;
+            }
+          }
+          p.Y[static_cast<size_t>(t) * p.ldy + n] = __float2bfloat16_rn(y);
+        }
+      }
+      ++j;
+    }
+  }
+
+  // ---------------------------------------------------------------- exit
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 64) {
+    // (a helper thread: it has passed the dependency wait)
+    // the last CTA out returns the grid-wide counters and flags to zero
+    __threadfence();
+    const unsigned old = atomicAdd(&p.sync[2], 1u);
+    if (old == static_cast<unsigned>(p.G - 1)) {
+      __threadfence();
+      p.sync[0] = 0u;
+      p.sync[1] = 0u;
+      for (int q = 0; q < p.G; ++q) p.sync[kDecSyncWords + q] = 0u;
+      __threadfence();
+      p.sync[2] = 0u;
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace
+
+// Whether the single-kernel decode path takes (fmt, M, K): a few tokens whose
+// quantized rows fit the per-CTA compact copy (and, for FP8, the quantizer's
+// registers).
+bool decode_path_eligible(int fmt, int M, int K) {
+  if (M < 1 || M > kDecMaxTokens || K < 32 || K % 32 != 0) return false;
+  if (fmt == EPILORA_FMT_FP8_E4M3) {
+    const long kb_pad = (static_cast<long>(K) + 127) / 128 * 128;
+    return M * kb_pad <= kDecXcBytes && static_cast<long>(M) * (K / 8) <= 16L * 128;
+  }
+  if (fmt == EPILORA_FMT_NVFP4) return K % 256 == 0 && static_cast<long>(M) * (K / 2) <= kDecXcBytes;
+  return false;
+}
+
+size_t decode_sync_bytes() { return static_cast<size_t>(kDecSyncWords + kDecMaxCtas) * 4; }
+static_assert((kDecSyncWords + kDecMaxCtas) * 4 == EPILORA_WORKSPACE_SYNC_BYTES, "sync block size");
+
+size_t decode_partial_bytes(int M) { return static_cast<size_t>(kDecMaxCtas) * M * 128 * 4; }
+
+int launch_fused_decode(const DecodeArgs& a) {
+  const bool fp4 = a.fmt == EPILORA_FMT_NVFP4;
+  const int kbytes = fp4 ? a.K / 2 : a.K;
+  DecParams p{};
+  p.X = static_cast<const __nv_bfloat16*>(a.X);
+  p.A = static_cast<const __nv_bfloat16*>(a.A);
+  p.B = static_cast<const __nv_bfloat16*>(a.B);
+  p.idx = a.idx;
+  p.mask = a.mask;
+  p.w_scale = a.w_scale;
+  p.w_gs = a.w_global_scale;
+  p.x_gs = a.x_global_scale;
+  p.Y = static_cast<__nv_bfloat16*>(a.Y);
+  p.status = a.status_dev;
+  p.sync = static_cast<unsigned*>(a.sync);
+  p.S = a.S;
+  p.accp = a.accp;
+  p.xq_out = static_cast<uint8_t*>(a.Xq);
+  p.xs_out = a.x_scale;
+  p.xsb_out = a.x_block_scale;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.ldx = a.ldx;
+  p.ldy = a.ldy;
+  p.L = a.L;
+  p.r = a.r;
+  p.s_row = a.s_row;
+  p.n_slices = a.n_slices;
+  for (int q = 0; q < 4; ++q) p.slice_end[q] = a.slice_end[q];
+  p.adapters = a.A != nullptr && a.B != nullptr ? 1 : 0;
+  p.parts = a.parts;
+  p.kslice = a.kslice;
+  p.n_items = p.adapters ? a.M * (a.s_row / kDecRanksPerItem) * a.parts : 0;
+  p.nkb = (kbytes + 127) / 128;
+  p.kb_pad = p.nkb * 128;
+  p.n_tiles = (a.N + 127) / 128;
+  p.U = static_cast<long long>(p.n_tiles) * p.nkb;
+  int G = num_sms();
+  if (G > kDecMaxCtas) G = kDecMaxCtas;
+  if (p.U < G) G = static_cast<int>(p.U);
+  p.G = G;
+
+  int rc = make_tma_2d_u8(&p.tmW, a.Wq, a.N, kbytes, kbytes, 128, 128, true);
+  if (rc != EPILORA_OK) return rc;
+  if (fp4) {
+    rc = make_tma_2d_u8(&p.tmSW, a.w_block_scale, a.N, a.K / 16, a.K / 16, 128, 16, false);
+    if (rc != EPILORA_OK) return rc;
+  }
+  const int stage = fp4 ? DecCfg<EPILORA_FMT_NVFP4>::kStage : DecCfg<EPILORA_FMT_FP8_E4M3>::kStage;
+  const int xsf_bytes = fp4 ? (a.M * p.nkb * 16 + 127) / 128 * 128 : 0;
+  const int fixed = 1024 + a.M * p.kb_pad + xsf_bytes + (a.M * a.s_row * 4 + 127) / 128 * 128 + 1024;
+  int stages = (kDecSmemBudget - fixed) / stage;
+  if (stages > kDecMaxStages) stages = kDecMaxStages;
+  if (stages < 2) return EPILORA_ERR_UNSUPPORTED;
+  p.stages = stages;
+  // L2 prefetch behind the ring: about 40 MB over the grid
+  {
+    const long per = (40L << 20) / (static_cast<long>(G) * (kDecUnitW + (fp4 ? 2048 : 0)));
+    p.l2_ahead = static_cast<int>(per);
+  }
+  const int smem = fixed + stages * stage;
+  if (smem > 227 * 1024) return EPILORA_ERR_UNSUPPORTED;
+
+  const void* kern = fp4 ? reinterpret_cast<const void*>(fused_decode_kernel<EPILORA_FMT_NVFP4>)
+                         : reinterpret_cast<const void*>(fused_decode_kernel<EPILORA_FMT_FP8_E4M3>);
+  static int attr_done[2][64] = {{0}};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return EPILORA_ERR_CUDA;
+  if (attr_done[fp4][dev] < smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return EPILORA_ERR_CUDA;
+    attr_done[fp4][dev] = smem;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(G, 1, 1);
+  cfg.blockDim = dim3(kDecThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&p};
+  if (cudaLaunchKernelExC(&cfg, kern, args) != cudaSuccess) return EPILORA_ERR_CUDA;
+  return EPILORA_OK;
+}
+
+}  // namespace epi

@@ -492,6 +492,8 @@ int trace_slot_next() {
 
 }  // namespace
 
+int shrink_kslice(int K, int parts) { return kslice_for(K, parts); }
+
 int shrink_parts_max(int K) {
   const int p = (K + kShrinkSliceTarget - 1) / kShrinkSliceTarget;
   return p < 1 ? 1 : p > kShrinkMaxParts ? kShrinkMaxParts : p;

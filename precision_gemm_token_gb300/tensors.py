@@ -102,16 +102,18 @@ def gemm_lora_epilogue(Xq, x_scale, w: QuantWeight, M, K, S=None, B=None, idx=No
 
 
 class LayerWorkspace:
-    """Caller-owned workspace for epilora_layer_forward (grown on demand)."""
+    """Caller-owned workspace for epilora_layer_forward (grown on demand).
+    Zero-filled when (re)allocated: the library wants the counters at its
+    start zero before the first call and leaves them zero after each."""
 
     def __init__(self, device):
         self.device = torch.device(device)
-        self.buf = torch.empty(0, dtype=torch.uint8, device=self.device)
+        self.buf = torch.zeros(0, dtype=torch.uint8, device=self.device)
 
     def get(self, fmt, M, K, r) -> torch.Tensor:
         need = E.epilora_workspace_bytes(fmt, M, K, r)
         if self.buf.numel() < need:
-            self.buf = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+            self.buf = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
         return self.buf
 
 

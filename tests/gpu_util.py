@@ -9,6 +9,7 @@ import precision_gemm_token_gb300 as E
 from oracle import epilora_oracle as O
 from oracle import fpformats as F
 from precision_gemm_token_gb300 import tensors as T
+from synth import make_projection
 
 FP8, NVFP4 = E.FMT_FP8, E.FMT_NVFP4
 
@@ -78,3 +79,43 @@ def assert_y_close(y: np.ndarray, ref: dict, bound: np.ndarray | None = None, wh
         err = np.abs(y.astype(np.float64) - ref["Y"])
         bad = err > bound
         assert not bad.any(), (what, np.argwhere(bad)[:5], float((err / bound).max()))
+
+
+def run_case(fmt, M, K, N, L, r, seed=0, idx_mode="uniform", mask_mode="all", n_decode=0, zero_w=False,
+             use_adapter=True):
+    """Run GPU and oracle on the same inputs; returns (Y_gpu np, ref dict, bound, inputs)."""
+    p = make_projection(M, K, N, L, r, seed=seed, idx_mode=idx_mode, mask_mode=mask_mode, n_decode=n_decode)
+    W = torch.zeros_like(p.W) if zero_w else p.W
+    Xg, Wg = p.X.cuda(), W.cuda()
+    w = T.quantize_weight(Wg, fmt)
+    x, Wn = p.X.float().numpy(), W.float().numpy()
+    A, B = p.A.float().numpy(), p.B.float().numpy()
+    idx, mask = p.idx.numpy(), p.mask.numpy()
+    gx = None
+    if fmt == FP8:
+        wq, sw = O.quant_fp8_rows(Wn)
+        assert same_codes_e4m3(npu8(w.codes), wq).all() and (np32(w.scale) == sw).all()
+        ref = O.layer_fp8(x, wq, sw, A, B, idx, mask) if use_adapter else O.layer_fp8(
+            x, wq, sw, A, np.zeros_like(B), idx, mask)
+        xv = F.e4m3_decode(ref["xq"]) * ref["sx"][:, None].astype(np.float64)
+        wv = F.e4m3_decode(wq) * sw[:, None].astype(np.float64)
+    else:
+        gw = O.nvfp4_global_scale(Wn)
+        wq, sbw = O.quant_nvfp4_rows(Wn, gw)
+        assert np32(w.global_scale)[0] == gw
+        assert (npu8(w.block_scale) == sbw).all() and same_codes_e2m1_packed(npu8(w.codes), wq).all()
+        gxv = O.nvfp4_global_scale(x)
+        gx = torch.tensor([gxv], dtype=torch.float32, device="cuda")
+        Bref = B if use_adapter else np.zeros_like(B)
+        ref = O.layer_nvfp4(x, gxv, wq, sbw, gw, A, Bref, idx, mask)
+        xv = O.dequant_nvfp4_rows(ref["xq"], ref["sbx"], gxv)
+        wv = O.dequant_nvfp4_rows(wq, sbw, gw)
+    st = status_buf()
+    if use_adapter:
+        Y = T.layer_forward(Xg, w, p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda(), x_global_scale=gx, status=st)
+    else:
+        Y = T.layer_forward(Xg, w, x_global_scale=gx, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    bound = tight_bound(ref, xv, wv, B if use_adapter else np.zeros_like(B), idx, mask)
+    return np32(Y), ref, bound, (p, w, gx)

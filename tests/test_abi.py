@@ -59,18 +59,34 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    # Xq, scales, then S with room for ceil(K / 1024) partial sums (at most 8)
-    assert E.epilora_workspace_bytes(0, 4, 512, 16) == r256(4 * 512) + r256(16) + r256(4 * 16 * 4)
-    assert E.epilora_workspace_bytes(1, 4, 512, 16) == r256(4 * 256) + r256(4 * 32) + r256(4 * 16 * 4)
-    assert E.epilora_workspace_bytes(0, 4, 512, 0) == r256(4 * 512) + r256(16)
-    assert E.epilora_workspace_bytes(0, 2, 14336, 64) == r256(2 * 14336) + r256(8) + r256(2 * 64 * 4 * 8)
-    assert E.epilora_workspace_bytes(0, 1, 40960, 16) == r256(40960) + r256(4) + r256(16 * 4 * 8)
-    assert E.epilora_workspace_bytes(0, 3, 4096, 32) == r256(3 * 4096) + r256(12) + r256(3 * 32 * 4 * 4)
+    sync = 1280                   # grid-wide counters of the single-kernel decode path, first
+    part = 256 * 128 * 4          # per token: partial rows of split weight tiles (single-kernel path)
+    # counters, Xq, scales, then S with room for ceil(K / 1024) partial sums (at most 8)
+    assert E.epilora_workspace_bytes(0, 4, 512, 16) == sync + r256(4 * 512) + r256(16) + r256(4 * 16 * 4) + 4 * part
+    assert E.epilora_workspace_bytes(1, 4, 512, 16) == sync + r256(4 * 256) + r256(4 * 32) + r256(4 * 16 * 4) + \
+        4 * part
+    assert E.epilora_workspace_bytes(0, 4, 512, 0) == sync + r256(4 * 512) + r256(16) + 4 * part
+    assert E.epilora_workspace_bytes(0, 2, 14336, 64) == sync + r256(2 * 14336) + r256(8) + r256(2 * 64 * 4 * 8)
+    assert E.epilora_workspace_bytes(0, 1, 40960, 16) == sync + r256(40960) + r256(4) + r256(16 * 4 * 8)
+    assert E.epilora_workspace_bytes(0, 3, 4096, 32) == sync + r256(3 * 4096) + r256(12) + r256(3 * 32 * 4 * 4) + \
+        3 * part
     # more than 32 tokens with adapters: plus the adapter-sorted row order (int32 per token)
-    assert E.epilora_workspace_bytes(0, 64, 512, 16) == r256(64 * 512) + r256(256) + r256(64 * 16 * 4) + r256(256)
-    assert E.epilora_workspace_bytes(0, 64, 512, 0) == r256(64 * 512) + r256(256)
+    assert E.epilora_workspace_bytes(0, 64, 512, 16) == sync + r256(64 * 512) + r256(256) + r256(64 * 16 * 4) + \
+        r256(256)
+    assert E.epilora_workspace_bytes(0, 64, 512, 0) == sync + r256(64 * 512) + r256(256)
     assert E.epilora_workspace_bytes(0, 0, 512, 16) == 0
     assert E.epilora_workspace_bytes(7, 4, 512, 16) == 0
+
+
+def test_layer_forward_kernels(lib):
+    """One persistent kernel for a few tokens whose quantized rows fit 16 KB
+    (FP8: M * K <= 16384, NVFP4: M * K <= 32768, M <= 8), else two."""
+    k = E.epilora_layer_forward_kernels
+    assert k(0, 1, 14336) == 1 and k(0, 1, 16384) == 1 and k(0, 1, 16416) == 2
+    assert k(0, 4, 4096) == 1 and k(0, 5, 4096) == 2 and k(0, 8, 2048) == 1 and k(0, 9, 512) == 2
+    assert k(1, 2, 14336) == 1 and k(1, 8, 4096) == 1 and k(1, 3, 14336) == 2
+    assert k(1, 1, 4128) == 2            # NVFP4 wants K % 256 == 0
+    assert k(0, 32, 4096) == 2 and k(0, 0, 4096) == 0 and k(2, 1, 4096) == 0 and k(0, 1, 100) == 0
 
 
 # ---------------------------------------------------------------------------

@@ -36,6 +36,9 @@ def _lib():
     ensure_lib()
 
 
+SYNC_BYTES = 1280      # EPILORA_WORKSPACE_SYNC_BYTES
+
+
 def _r256(v):
     return (v + 255) // 256 * 256
 
@@ -86,13 +89,14 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
     cols_t = torch.from_numpy(cols).cuda()
     rows_t = torch.from_numpy(rows).cuda()
     buf = ws.buf
-    off_xq = 0
-    # workspace: Xq, scales, S (room for min(8, ceil(K / 1024)) partial sums),
-    # and for more than 32 tokens the adapter-sorted row order: row q holds
-    # token perm[q]
+    # workspace: the counters (zero again after the call), Xq, scales, S (room
+    # for min(8, ceil(K / 1024)) partial sums), and for more than 32 tokens
+    # the adapter-sorted row order: row q holds token perm[q]
+    off_xq = SYNC_BYTES
+    assert int(buf[:SYNC_BYTES].count_nonzero().item()) == 0
     xq_bytes = M * K if fmt == FP8 else M * K // 2
     sc_bytes = 4 * M if fmt == FP8 else M * K // 16
-    off_perm = _r256(xq_bytes) + _r256(sc_bytes) + _r256(M * r * 4 * min(8, -(-K // 1024)))
+    off_perm = off_xq + _r256(xq_bytes) + _r256(sc_bytes) + _r256(M * r * 4 * min(8, -(-K // 1024)))
     if M > 32:
         perm = buf[off_perm:off_perm + 4 * M].view(torch.int32).cpu().numpy()
         assert np.array_equal(np.sort(perm), np.arange(M))
@@ -130,7 +134,7 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
     # GEMM adds them; and from the standalone shrink
     S_ref = ref["S"]
     n_parts = min(8, -(-K // 1024))
-    off_s = _r256(xq_bytes) + _r256(sc_bytes)
+    off_s = off_xq + _r256(xq_bytes) + _r256(sc_bytes)
     parts = buf[off_s:off_s + n_parts * M * r * 4].view(torch.float32).view(n_parts, M, r)[:, rows_t, :]
     S_fused = parts[0].clone()
     for q in range(1, n_parts):

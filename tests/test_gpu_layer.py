@@ -13,8 +13,7 @@ from oracle import fpformats as F
 from precision_gemm_token_gb300 import tensors as T
 from synth import make_projection
 
-from .gpu_util import (FP8, NVFP4, assert_y_close, ensure_lib, np32, npu8, same_codes_e2m1_packed,
-                       same_codes_e4m3, status_buf, tight_bound)
+from .gpu_util import FP8, NVFP4, assert_y_close, ensure_lib, np32, run_case, status_buf
 
 pytestmark = pytest.mark.gpu
 
@@ -22,46 +21,6 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     ensure_lib()
-
-
-def run_case(fmt, M, K, N, L, r, seed=0, idx_mode="uniform", mask_mode="all", n_decode=0, zero_w=False,
-             use_adapter=True):
-    """Run GPU and oracle on the same inputs; returns (Y_gpu np, ref dict, bound, inputs)."""
-    p = make_projection(M, K, N, L, r, seed=seed, idx_mode=idx_mode, mask_mode=mask_mode, n_decode=n_decode)
-    W = torch.zeros_like(p.W) if zero_w else p.W
-    Xg, Wg = p.X.cuda(), W.cuda()
-    w = T.quantize_weight(Wg, fmt)
-    x, Wn = p.X.float().numpy(), W.float().numpy()
-    A, B = p.A.float().numpy(), p.B.float().numpy()
-    idx, mask = p.idx.numpy(), p.mask.numpy()
-    gx = None
-    if fmt == FP8:
-        wq, sw = O.quant_fp8_rows(Wn)
-        assert same_codes_e4m3(npu8(w.codes), wq).all() and (np32(w.scale) == sw).all()
-        ref = O.layer_fp8(x, wq, sw, A, B, idx, mask) if use_adapter else O.layer_fp8(
-            x, wq, sw, A, np.zeros_like(B), idx, mask)
-        xv = F.e4m3_decode(ref["xq"]) * ref["sx"][:, None].astype(np.float64)
-        wv = F.e4m3_decode(wq) * sw[:, None].astype(np.float64)
-    else:
-        gw = O.nvfp4_global_scale(Wn)
-        wq, sbw = O.quant_nvfp4_rows(Wn, gw)
-        assert np32(w.global_scale)[0] == gw
-        assert (npu8(w.block_scale) == sbw).all() and same_codes_e2m1_packed(npu8(w.codes), wq).all()
-        gxv = O.nvfp4_global_scale(x)
-        gx = torch.tensor([gxv], dtype=torch.float32, device="cuda")
-        Bref = B if use_adapter else np.zeros_like(B)
-        ref = O.layer_nvfp4(x, gxv, wq, sbw, gw, A, Bref, idx, mask)
-        xv = O.dequant_nvfp4_rows(ref["xq"], ref["sbx"], gxv)
-        wv = O.dequant_nvfp4_rows(wq, sbw, gw)
-    st = status_buf()
-    if use_adapter:
-        Y = T.layer_forward(Xg, w, p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda(), x_global_scale=gx, status=st)
-    else:
-        Y = T.layer_forward(Xg, w, x_global_scale=gx, status=st)
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0
-    bound = tight_bound(ref, xv, wv, B if use_adapter else np.zeros_like(B), idx, mask)
-    return np32(Y), ref, bound, (p, w, gx)
 
 
 SHAPES = [
@@ -229,7 +188,7 @@ def test_no_adapter_cases_are_bit_exact_base(fmt):
 
 
 @pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
-@pytest.mark.parametrize("M", [29, 300])   # one decode tile; several adapter-sorted wide tiles
+@pytest.mark.parametrize("M", [7, 29, 300])   # single kernel; one decode tile; several adapter-sorted wide tiles
 def test_permutation_and_determinism(fmt, M):
     p = make_projection(M, 1024, 640, 5, 32, seed=8, mask_mode="random")
     X, W = p.X.cuda(), p.W.cuda()
@@ -258,8 +217,11 @@ def test_adapter_contribution_with_zero_base(fmt, M, K, N, L, r):
 
 def test_gemm_with_h_given_matches_fused():
     """The standalone GEMM (S already in memory, ordinary launch) equals the
-    fused decode path bit for bit."""
-    p = make_projection(8, 1024, 512, 4, 32, seed=10)
+    two-kernel fused call bit for bit (12 tokens: more than the single-kernel
+    path takes)."""
+    import precision_gemm_token_gb300 as E
+    assert E.epilora_layer_forward_kernels(FP8, 12, 1024) == 2
+    p = make_projection(12, 1024, 512, 4, 32, seed=10)
     X, W = p.X.cuda(), p.W.cuda()
     w = T.quantize_weight(W, FP8)
     A, B, idx, mask = p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda()
@@ -267,7 +229,7 @@ def test_gemm_with_h_given_matches_fused():
     Xq, sx = T.quant_act(X, FP8)
     S = T.lora_shrink(X, A, idx, mask)
     torch.cuda.synchronize()
-    Yg = T.gemm_lora_epilogue(Xq, sx, w, 8, 1024, S=S, B=B, idx=idx, mask=mask, pdl_dependent=False)
+    Yg = T.gemm_lora_epilogue(Xq, sx, w, 12, 1024, S=S, B=B, idx=idx, mask=mask, pdl_dependent=False)
     assert torch.equal(Yf, Yg)
 
 
