@@ -527,7 +527,9 @@ def run_ours(args, rank, world, local):
         "nvfp4_m1": nv,
         "large_m": large,
         "e2e": e2e,
-        "gpu_launches": args.steps * 2 * len(PROJ8B),   # per projection: the shrink grid and the GEMM
+        # per projection: one persistent kernel (single-kernel decode path) or
+        # the shrink grid and the GEMM, as the library reports for the shape
+        "gpu_launches": args.steps * sum(E.epilora_layer_forward_kernels(fmt, M, K) for _, K, _ in PROJ8B),
         "clocks": clocks,
         "median_ms_per_step": round(ms_med, 5),
     }
@@ -651,6 +653,34 @@ def run_profile(args):
     print(json.dumps({"profile": args.workload, "kernel": f"gate_up {K}->{N} M={M}", "ok": True}))
 
 
+def run_profile_fused(args):
+    """One fused layer call alone, for ncu: the workload's gate_up projection
+    (4096 -> 28672) through epilora_layer_forward five times on one
+    workspace (for a few tokens this is the single-kernel decode path)."""
+    import torch
+
+    import precision_gemm_token_gb300 as E
+    from precision_gemm_token_gb300 import tensors as T
+    from synth import make_projection
+
+    E.build()
+    E.load()
+    M, fmt, L, r, idx_mode, _ = WORKLOADS[args.workload]
+    _, K, N = PROJ8B[2]
+    p = make_projection(M, K, N, L, r, seed=102, idx_mode=idx_mode, device="cuda")
+    w = T.quantize_weight(p.W, fmt)
+    gx = T.nvfp4_global_scale(p.X) if fmt == 1 else None
+    ws = T.LayerWorkspace("cuda")
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(5):
+        T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx, workspace=ws, status=st, Y=Y)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    print(json.dumps({"profile": args.workload, "kernel": f"fused gate_up {K}->{N} M={M}",
+                      "kernels_per_call": E.epilora_layer_forward_kernels(fmt, M, K), "ok": True}))
+
+
 def run_profile_wide(args):
     """A wide-tile fused layer call alone, for ncu: the Llama-3.1-70B gate_up
     projection's quarter column slice (K 8192 -> N 14336: 1008 tiles of
@@ -693,6 +723,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true", help="run the dominant kernel alone (for ncu)")
     ap.add_argument("--profile-wide", action="store_true", help="run one wide-tile fused layer call alone (for ncu)")
+    ap.add_argument("--profile-fused", action="store_true",
+                    help="run the workload's fused gate_up layer call alone (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -701,6 +733,9 @@ def main():
         return
     if args.profile_wide:
         run_profile_wide(args)
+        return
+    if args.profile_fused:
+        run_profile_fused(args)
         return
     rank, world, local = dist_setup()
     if args.impl == "reference":

@@ -32,18 +32,17 @@ def _inputs_mtime() -> float:
     return max(os.path.getmtime(f) for f in files if os.path.isfile(f))
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str | None = None) -> str:
+def build(force: bool = False, verbose: bool = False) -> str:
     """Compile every CUDA translation unit and link libepilora.so; returns its
-    path. `extra_flags` (e.g. -D tuning macros) with `out_dir` build a variant
-    of the library elsewhere without touching the in-tree one."""
-    build_dir = out_dir or BUILD_DIR
-    lib_path = os.path.join(build_dir, "libepilora.so")
+    path."""
+    build_dir = BUILD_DIR
+    lib_path = LIB_PATH
     if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _inputs_mtime():
         return lib_path
     os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     common = ARCH_FLAGS + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
-                           "-I", os.path.join(ROOT, "include")] + list(extra_flags)
+                           "-I", os.path.join(ROOT, "include")]
 
     def compile_one(src: str) -> str:
         obj = os.path.join(build_dir, src.replace(".cu", ".o"))

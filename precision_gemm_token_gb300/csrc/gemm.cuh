@@ -51,37 +51,6 @@
 #include "common.cuh"
 #include "ptx.cuh"
 
-#ifndef EPILORA_GEMM_FUSED_MODE
-// fused call, order of the producer's first steps: 0 = weight stages and L2
-// prefetch, then wait for the shrink grid; 1 = wait first; 2 = weight stages,
-// wait, then L2 prefetch
-#define EPILORA_GEMM_FUSED_MODE 2
-#endif
-#ifndef EPILORA_GEMM_EARLY_TRIGGER
-#define EPILORA_GEMM_EARLY_TRIGGER 1  // release the next kernel on the stream after the main loop
-#endif
-#ifndef EPILORA_GEMM_SB_MIN_GROUPS
-// decode tiles with at least this many adapter groups stream their B slices
-// through the TMA ring (behind the weights) instead of loading B rows with
-// ordinary loads, which queue behind the weight stream
-#define EPILORA_GEMM_SB_MIN_GROUPS 1
-#endif
-#ifndef EPILORA_GEMM_PREWAIT_STAGES
-#define EPILORA_GEMM_PREWAIT_STAGES 16  // weight stages a fused call issues before its wait
-#endif
-#ifndef EPILORA_GEMM_X_FIRST
-#define EPILORA_GEMM_X_FIRST 1          // fused call: activation loads right after the wait, before the L2 prefetch
-#endif
-#ifndef EPILORA_GEMM_B_EARLY
-#define EPILORA_GEMM_B_EARLY 1          // one-group decode tiles load their B slice into a buffer of its own
-#endif
-#ifndef EPILORA_GEMM_B_L2
-#define EPILORA_GEMM_B_L2 0             // prefetch streamed B slices into L2 after set-up
-#endif
-#ifndef EPILORA_GEMM_L2_AHEAD_MB
-#define EPILORA_GEMM_L2_AHEAD_MB 32  // weight bytes a fused call may prefetch into L2 after its wait
-#endif
-
 namespace epi {
 
 constexpr int kGemmThreads = 192;
@@ -91,6 +60,11 @@ constexpr int kMaxRank = 128;
 constexpr int kEpiBarrier = 1;       // named barrier of the 4 epilogue warps
 constexpr int kMaxSplit = 8;         // largest cluster along K
 constexpr int kDecodeBT = 32;        // token tiles up to this width use the decode epilogue
+// fused call: weight stages issued before the wait for the shrink grid (a
+// deep queue of weight reads would delay the shrink grid's own loads), and
+// the weight bytes prefetched into L2 over the grid after it
+constexpr int kPrewaitStages = 16;
+constexpr long kL2AheadBytes = 32L << 20;
 
 struct GemmParams {
   CUtensorMap tmW;    // uint8 [N, Kbytes], box 128 x 128 B, 128-B swizzle
@@ -133,7 +107,6 @@ struct GemmParams {
   int b_group_bytes;  // ring bytes of one group's boxes (1024-byte aligned)
   int b_groups_per_slot;
   int b_early;        // 1: a decode tile with one adapter group loads its B slice at once into its own buffer
-  int trace_slot;     // tuning builds only: which trace buffer this launch fills
   int l2_ahead;       // fused call: weight stages past the ring to prefetch into L2 while waiting
   int t_tiles, n_tiles;  // persistent wide kernel: token tiles, weight tiles
   // S in memory: rows of s_row floats; a weight tile starting at column n0
@@ -200,34 +173,6 @@ __device__ __forceinline__ int s_slice_offset(const GemmParams& p, int n0) {
     if (n0 >= p.slice_end[q]) off += p.r;
   return off;
 }
-
-// Optional per-CTA phase timestamps (built only with -DEPILORA_GEMM_TRACE, for
-// tuning): entry, ring primed, first stage landed, last stage landed,
-// accumulator ready, S readable, epilogue done, SM id.
-#ifdef EPILORA_GEMM_TRACE
-constexpr int kTraceSlots = 8;       // consecutive launches, round robin
-constexpr int kTraceCtas = 2048;
-static __device__ unsigned long long g_gemm_trace[kTraceSlots][kTraceCtas][16];
-inline int& gemm_trace_launches() {
-  static int n = 0;
-  return n;
-}
-#define EPI_TRACE(slot, value)                                                                     \
-  do {                                                                                             \
-    const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);          \
-    if (cta_ < kTraceCtas) g_gemm_trace[p.trace_slot][cta_][slot] = (value);                       \
-  } while (0)
-#else
-#define EPI_TRACE(slot, value) \
-  do {                         \
-  } while (0)
-#endif
-// timestamp taken once `dep` is available (tuning builds)
-#define EPI_TRACE_AFTER(slot, dep)                      \
-  do {                                                  \
-    asm volatile("" ::"f"(static_cast<float>(dep)));    \
-    EPI_TRACE(slot, globaltimer_ns());                  \
-  } while (0)
 
 // Two floats to packed bf16x2 (lo in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -392,7 +337,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   // ---------------------------------------------------------------- setup
   const int prologue = nkb < stages ? nkb : stages;
   if (warp == 0 && lane == 0) {
-    EPI_TRACE(0, globaltimer_ns());
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
@@ -413,37 +357,22 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         if (C::kFP4) tma_prefetch_l2_2d(&p.tmSW, kb * C::kSfRow, n0);
       }
     };
-    if (p.fused && EPILORA_GEMM_FUSED_MODE == 1) {
-      pdl_wait_primary();
-      fence_proxy_async_global();
-    }
-    // before the wait only the first EPILORA_GEMM_PREWAIT_STAGES stages (a
-    // deep queue of weight reads would delay the shrink grid's own loads)
-    const int prewait = p.fused && EPILORA_GEMM_FUSED_MODE != 1 ? min(prologue, EPILORA_GEMM_PREWAIT_STAGES)
-                                                                  : prologue;
+    // fused call: only the first kPrewaitStages weight stages before the wait
+    const int prewait = p.fused ? min(prologue, kPrewaitStages) : prologue;
     for (int i = 0; i < prewait; ++i) issue_w(i, i);
     if (p.fused) {
-      if (EPILORA_GEMM_FUSED_MODE == 0) l2_ahead();
-      if (EPILORA_GEMM_FUSED_MODE != 1) {
-        // the shrink grid quantizes the activations: its completion (and
-        // that of everything before it) makes them visible
-        pdl_wait_primary();
-        fence_proxy_async_global();
+      // the shrink grid quantizes the activations: its completion (and that
+      // of everything before it) makes them visible
+      pdl_wait_primary();
+      fence_proxy_async_global();
+      // activations of the stages already requested first (the MMA waits for
+      // them), then the rest of the ring, then the L2 prefetch
+      for (int i = 0; i < prewait; ++i) issue_x(i, i);
+      for (int i = prewait; i < prologue; ++i) {
+        issue_w(i, i);
+        issue_x(i, i);
       }
-      if (EPILORA_GEMM_X_FIRST) {
-        // activations of the stages already requested first (the MMA waits
-        // for them), then the rest of the ring, then the L2 prefetch
-        for (int i = 0; i < prewait; ++i) issue_x(i, i);
-        for (int i = prewait; i < prologue; ++i) {
-          issue_w(i, i);
-          issue_x(i, i);
-        }
-        if (EPILORA_GEMM_FUSED_MODE != 0) l2_ahead();
-      } else {
-        for (int i = prewait; i < prologue; ++i) issue_w(i, i);
-        if (EPILORA_GEMM_FUSED_MODE != 0) l2_ahead();
-        for (int i = 0; i < prologue; ++i) issue_x(i, i);
-      }
+      l2_ahead();
     } else {
       for (int i = 0; i < prologue; ++i) issue_x(i, i);
     }
@@ -521,7 +450,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if (threadIdx.x == 0) EPI_TRACE(1, globaltimer_ns());
   // every CTA of the cluster has started once this phase completes (its wait
   // comes before the first store into a peer's shared memory)
   if (ks > 1) cluster_arrive_relaxed();
@@ -536,7 +464,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   bool b_early_on = false;  // the tile's only group comes through b_early_buf instead of the ring
   auto set_groups = [&]() {
     ngroups = *ngroups_s;
-    sb = C::kDecode && p.stream_b && ngroups >= EPILORA_GEMM_SB_MIN_GROUPS && p.S != nullptr;
+    sb = C::kDecode && p.stream_b && ngroups >= 1 && p.S != nullptr;
     b_early_on = sb && p.b_early && ngroups == 1;
     n_bslots = sb && !b_early_on ? (ngroups + gps - 1) / gps : 0;
     n_loads = nkb + n_bslots;
@@ -620,16 +548,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         stop = true;
       }
       if (!stop) set_groups();
-      EPI_TRACE(15, globaltimer_ns());
-      if (EPILORA_GEMM_B_L2 == 2 && sb && !stop) {
-        // the weights are all requested: the B slices go to L2 behind them,
-        // so that their ring loads below find them there
-        const int rows = min(row_hi, p.N - n0) - row_lo;
-        if (rows > 0)
-          for (int g = 0; g < ngroups; ++g)
-            prefetch_l2_bulk(p.B + (static_cast<size_t>(g_adapter[g]) * p.N + n0 + row_lo) * p.r,
-                             static_cast<uint32_t>(rows * p.r * 2));
-      }
       for (int i = (prologue > nkb ? prologue : nkb); i < n_loads && !stop; ++i) produce(i);
       if (*abort_flag) {
         // do not leave with copies in flight: wait for every issued fill
@@ -654,8 +572,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         }
         break;
       }
-      if (lane == 0 && i == 0) EPI_TRACE(2, globaltimer_ns());
-      if (lane == 0 && i == nkb - 1) EPI_TRACE(3, globaltimer_ns());
       uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
       const uint32_t w_addr = smem_u32(st);
       const uint32_t x_addr = smem_u32(st + C::kWBytes);
@@ -810,7 +726,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     }
     asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
     const bool ok = mbar_wait_bounded(acc_bar, 0, kWaitLimitNs);
-    if (et == 0) EPI_TRACE(4, globaltimer_ns());
     if (!ok) {
       *abort_flag = 1;
       record_status(p.status, EPILORA_ERR_TIMEOUT);
@@ -867,7 +782,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   // The main loop is done: the next kernel on the stream (the next layer
   // call's shrink grid) may become resident now; it waits for this grid's
   // completion before it reads anything this grid writes.
-  if (EPILORA_GEMM_EARLY_TRIGGER) pdl_allow_dependents();
+  pdl_allow_dependents();
 
   // ---------------------------------------------------------------- epilogue
   const float alpha = alpha_pre;
@@ -882,11 +797,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     const int t = t0 + tl;
     if (n >= p.N || t >= p.M) return;
     float y = base_value(mm, tl, acc, sw);
-    if (et == 0 && tl == 0) EPI_TRACE_AFTER(8, y);
     const int l = meta_idx[tl];
     if (l >= 0) {
       if (l * kTileN + mm != cached_key) load_brow(l, mm);
-      if (et == 0 && tl == 0) EPI_TRACE_AFTER(9, __uint_as_float(brow[0] | brow[31]));
       const bool s_smem = C::kDecode || p.stage_s;
       const float4* srow =
           C::kDecode ? reinterpret_cast<const float4*>(s_stage + tl * p.r)
@@ -894,9 +807,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
                       : reinterpret_cast<const float4*>(S_t + static_cast<size_t>(meta_tok[tl]) * p.s_row);
       y += dot_srow_brow(srow, brow, p.r, s_smem);
     }
-    if (et == 0 && tl == 0) EPI_TRACE_AFTER(10, y);
     p.Y[static_cast<size_t>(meta_tok[tl]) * p.ldy + n] = __float2bfloat16_rn(y);
-    if (et == 0 && tl == 0) EPI_TRACE(7, globaltimer_ns());
   };
 
   // wide tiles: 16 token columns of this warp's 32 output rows go through a
@@ -941,16 +852,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     cluster_arrive();
     cluster_wait();
   }
-#ifdef EPILORA_GEMM_TRACE
-  long long epi_clk0 = 0;
-#endif
   // the 4 epilogue warps agree on whether to produce output (the sections
   // below contain their named barrier, which all four must reach)
   if (warp >= 2 && !epi_bar_any(*abort_flag != 0)) {
-    if (et == 0) EPI_TRACE(5, globaltimer_ns());
-#ifdef EPILORA_GEMM_TRACE
-    epi_clk0 = clock64();
-#endif
     const float* red = reinterpret_cast<const float*>(red_buf);
     if (sb) {
       // ---- streamed-B epilogue (decode tile with >= 2 adapter groups) ----
@@ -1024,19 +928,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
         // every thread waits itself (TMA data visibility); the outcome is
         // made uniform over the 4 epilogue warps before anyone leaves
         const bool late = !mbar_wait_bounded(&full_bar[s], ph, kWaitLimitNs);
-        if (et == 0 && j == 0) EPI_TRACE(12, globaltimer_ns());
-        if (et == 0 && j == n_bslots - 1) EPI_TRACE(13, globaltimer_ns());
-#ifdef EPILORA_GEMM_TRACE
-        const long long ck0 = clock64();
-#endif
         if (epi_bar_any(late)) {
           *abort_flag = 1;
           record_status(p.status, EPILORA_ERR_TIMEOUT);
           break;
         }
-#ifdef EPILORA_GEMM_TRACE
-        const long long ck1 = clock64();
-#endif
         const uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
         // y[t][i] += S[t] . B_g[row i], B's row read 16 bytes at a time from
         // the swizzled box (chunk c of row i lives at chunk c ^ f(i))
@@ -1056,20 +952,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
           }
           y_tile[tl * RR + i] += d;
         }
-#ifdef EPILORA_GEMM_TRACE
-        const long long ck2 = clock64();
-#endif
         asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
-#ifdef EPILORA_GEMM_TRACE
-        if (et == 0 && j == 0) {
-          EPI_TRACE(8, static_cast<unsigned long long>(ck1 - ck0));
-          EPI_TRACE(9, static_cast<unsigned long long>(ck2 - ck1));
-          EPI_TRACE(10, static_cast<unsigned long long>(clock64() - ck2));
-        }
-#endif
         if (et == 0) mbar_arrive(&empty_bar[s]);          // slot free for the producer
       }
-      if (et == 0) EPI_TRACE(14, globaltimer_ns());
       // 3) the output tile
       for (int e = et; e < R * tv; e += 128) {
         const int ii = e % R, tl = e / R;
@@ -1253,22 +1138,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       const int m = q * 32 + lane;
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       const float sw = sw_pre;
-#ifdef EPILORA_GEMM_TRACE
-      long long ck_ld = 0, ck_fin = 0;
-#endif
 #pragma unroll 1
       for (int c = 0; c < BT / 16; ++c) {
         if (c * 16 >= tv) break;
         uint32_t v[16];
-#ifdef EPILORA_GEMM_TRACE
-        const long long ca = clock64();
-#endif
         tmem_ld_32x32b_x16(lane_base + c * 16, v);
         tmem_ld_wait();
-#ifdef EPILORA_GEMM_TRACE
-        const long long cb = clock64();
-        ck_ld += cb - ca;
-#endif
         if (C::kDecode) {
           // valid token columns to this thread's row of the output tile;
           // only they are finished below (a loop with a run-time bound, so
@@ -1285,16 +1160,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
 #pragma unroll
           for (int j = 0; j < 16; ++j) finish(m, c * 16 + j, __uint_as_float(v[j]), sw);
         }
-#ifdef EPILORA_GEMM_TRACE
-        if (!C::kDecode) ck_fin += clock64() - cb;
-#endif
       }
-#ifdef EPILORA_GEMM_TRACE
-      if (et == 0 && !C::kDecode) {
-        EPI_TRACE(12, static_cast<unsigned long long>(ck_ld));
-        EPI_TRACE(13, static_cast<unsigned long long>(ck_fin));
-      }
-#endif
       if (C::kDecode) {
 #pragma unroll 1
         for (int tl = 0; tl < tv; ++tl) finish(m, tl, y_tile[tl * RR + m], sw);
@@ -1316,15 +1182,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
   // ---------------------------------------------------------------- teardown
   if (b_early_on && et == 0 && *abort_flag) (void)mbar_wait_bounded(b_bar, 0, kWaitLimitNs);   // no copy in flight
   if (ks > 1 && warp < 2) cluster_wait();   // second phase, for the producer and MMA warps
-  if (threadIdx.x == 64) {
-    unsigned smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    EPI_TRACE(6, globaltimer_ns());
-    (void)smid;
-#ifdef EPILORA_GEMM_TRACE
-    if (!*abort_flag) EPI_TRACE(11, static_cast<unsigned long long>(clock64() - epi_clk0));
-#endif
-  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -1336,15 +1193,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
 // Host side ------------------------------------------------------------------
 int gemm_smem_bytes(int stage_bytes, int stages, int red_bytes);
 
-#ifndef EPILORA_GEMM_ROTATE
-#define EPILORA_GEMM_ROTATE 1
-#endif
-#ifndef EPILORA_GEMM_RESIDENT
-#define EPILORA_GEMM_RESIDENT 2      // CTAs per SM a large decode grid is sized for
-#endif
-#ifndef EPILORA_GEMM_STREAM_B
-#define EPILORA_GEMM_STREAM_B 1
-#endif
+// CTAs per SM a decode grid larger than the GPU is sized for
+constexpr int kResident = 2;
 
 template <int FMT, int BT, int KA>
 int launch_gemm_tiled(const GemmArgs& a) {
@@ -1365,9 +1215,6 @@ int launch_gemm_tiled(const GemmArgs& a) {
   p.fused = a.fused;
   p.pdl = !a.fused && a.pdl_dependent ? 1 : 0;
   p.perm = a.perm;
-#ifdef EPILORA_GEMM_TRACE
-  p.trace_slot = gemm_trace_launches()++ % kTraceSlots;
-#endif
   p.s_parts = a.s_parts < 1 ? 1 : a.s_parts;
   p.M = a.M;
   p.N = a.N;
@@ -1379,7 +1226,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   for (int q = 0; q < 4; ++q) p.slice_end[q] = a.slice_end[q];
   p.ldy = a.ldy;
   p.num_kb = (kbytes + KA * kAtomBytes - 1) / (KA * kAtomBytes);
-  p.rotate = EPILORA_GEMM_ROTATE;
+  p.rotate = 1;
 
   int rc = make_tma_2d_u8(&p.tmW, a.Wq, a.N, kbytes, kbytes, kTileN, kAtomBytes, true);
   if (rc != EPILORA_OK) return rc;
@@ -1393,7 +1240,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   }
 
   // Decode grids: split K over clusters of 2/4/8 CTAs while the grid stays
-  // resident (EPILORA_GEMM_RESIDENT CTAs per SM); a grid larger than the SM
+  // resident (kResident CTAs per SM); a grid larger than the SM
   // count gets the shared memory of that many CTAs per SM.
   const int sms = num_sms();
   const int n_tiles = (a.N + kTileN - 1) / kTileN;
@@ -1403,7 +1250,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   if (BT <= 64) {
     const int max_by_k = p.num_kb / 2 > 0 ? p.num_kb / 2 : 1;
     for (int cand = 2; cand <= kMaxSplit; cand *= 2)
-      if (tiles * cand <= static_cast<long>(sms) * EPILORA_GEMM_RESIDENT && cand <= max_by_k) ks = cand;
+      if (tiles * cand <= static_cast<long>(sms) * kResident && cand <= max_by_k) ks = cand;
   }
   p.ks = ks;
   const int RR = gemm_red_rows(ks);
@@ -1417,7 +1264,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   p.b_group_bytes = (RR * brow_bytes + 1023) / 1024 * 1024;
   p.b_groups_per_slot = C::kStageBytes / p.b_group_bytes;
   if (p.b_groups_per_slot > BT) p.b_groups_per_slot = BT;
-  if (C::kDecode && a.S != nullptr && EPILORA_GEMM_STREAM_B && p.b_groups_per_slot >= 1) {
+  if (C::kDecode && a.S != nullptr && p.b_groups_per_slot >= 1) {
     const uint64_t rows = static_cast<uint64_t>(a.L) * static_cast<uint64_t>(a.N);
     rc = make_tma_2d_swz(&p.tmB, a.B, rows, brow_bytes, brow_bytes, RR, p.b_box_bytes, p.b_box_bytes);
     if (rc != EPILORA_OK) return rc;
@@ -1425,10 +1272,10 @@ int launch_gemm_tiled(const GemmArgs& a) {
   }
 
   const long ctas = tiles * ks;
-  // a grid larger than the GPU keeps EPILORA_GEMM_RESIDENT CTAs per SM: one
+  // a grid larger than the GPU keeps kResident CTAs per SM: one
   // CTA's epilogue then runs while the other's main loop keeps the weight
   // stream (decode) or the tensor pipe (wide tiles) busy
-  const int budget = ctas > sms ? (227 * 1024) / EPILORA_GEMM_RESIDENT - 2048 : 200 * 1024;
+  const int budget = ctas > sms ? (227 * 1024) / kResident - 2048 : 200 * 1024;
   const int red = gemm_red_bytes<BT>(ks);
   const int dec = gemm_decode_bytes(BT, a.r, ks);
   int stages = (budget - 1024 - red - kGemmMiscBytes - dec) / C::kStageBytes;
@@ -1441,7 +1288,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   // beside the ring without giving up a stage
   int early_bytes = 0;
   p.b_early = 0;
-  if (p.stream_b && EPILORA_GEMM_B_EARLY) {
+  if (p.stream_b) {
     early_bytes = p.b_group_bytes + 1024;      // + alignment of the swizzled box
     if (gemm_smem_bytes(C::kStageBytes, stages, red) + dec + early_bytes <= budget) p.b_early = 1;
     else early_bytes = 0;
@@ -1469,9 +1316,9 @@ int launch_gemm_tiled(const GemmArgs& a) {
     if (off + 5 * 1024 <= stages * C::kStageBytes) p.y_stage = off;
   }
   // fused call: prefetch into L2 (while the shrink grid runs) up to about
-  // EPILORA_GEMM_L2_AHEAD_MB of weight stages beyond the ring, over the grid
+  // kL2AheadBytes of weight stages beyond the ring, over the grid
   {
-    const long budget_bytes = static_cast<long>(EPILORA_GEMM_L2_AHEAD_MB) << 20;
+    const long budget_bytes = kL2AheadBytes;
     const long per_stage_grid = ctas * static_cast<long>(C::kWBytes + C::kSfWRaw);
     long ahead = per_stage_grid > 0 ? budget_bytes / per_stage_grid : 0;
     const long left = per_cta - stages;
@@ -1517,22 +1364,6 @@ int launch_gemm_tiled(const GemmArgs& a) {
   return EPILORA_OK;
 }
 
-#ifndef EPILORA_GEMM_KA
-#define EPILORA_GEMM_KA 2
-#endif
-#ifndef EPILORA_GEMM_KA32
-#define EPILORA_GEMM_KA32 1           // atoms per stage of 32-token decode tiles
-#endif
-#ifndef EPILORA_NV_BT256
-#define EPILORA_NV_BT256 0            // 1: NVFP4 wide batches in 256-token tiles too
-#endif
-#ifndef EPILORA_GEMM_MAX_BT
-#define EPILORA_GEMM_MAX_BT 256       // widest token tile
-#endif
-#ifndef EPILORA_GEMM_KA_WIDE
-#define EPILORA_GEMM_KA_WIDE 1
-#endif
-
 }  // namespace epi
 
 #include "gemm_wide.cuh"
@@ -1541,27 +1372,24 @@ namespace epi {
 
 template <int FMT>
 int launch_gemm_by_m(const GemmArgs& a) {
-  constexpr int KA = EPILORA_GEMM_KA;
-  // wide token tiles: EPILORA_GEMM_KA_WIDE atoms per stage (a 256-token FP8
-  // stage is then 48 KB and the ring four deep)
-  constexpr int KAW = EPILORA_GEMM_KA_WIDE;
-  // NVFP4 decode stages carry scale boxes too: one atom per stage keeps
-  // three or more stages in flight at two CTAs per SM
-  constexpr int KAD = FMT == EPILORA_FMT_NVFP4 ? 1 : KA;
-  // 32-token decode tiles also keep output-tile and S buffers: one atom per
-  // stage leaves room for three or more stages
+  // decode tiles of 16 tokens: two 128-byte K atoms per stage (NVFP4 stages
+  // also carry scale boxes: one atom keeps three or more stages in flight at
+  // two CTAs per SM); 32-token decode tiles also keep output-tile and S
+  // buffers: one atom per stage leaves room for three or more stages
+  constexpr int KAD = FMT == EPILORA_FMT_NVFP4 ? 1 : 2;
   if (a.M <= 16) return launch_gemm_tiled<FMT, 16, KAD>(a);
-  if (a.M <= 32) return launch_gemm_tiled<FMT, 32, EPILORA_GEMM_KA32>(a);
-  if (a.M <= 64) return launch_gemm_tiled<FMT, 64, KA>(a);
-  // (NVFP4 stages of 256 tokens carry scale boxes too: at two CTAs per SM
-  // the ring would be one stage deep, so NVFP4 stays at 128-token tiles)
-  if (a.M <= 128 || EPILORA_GEMM_MAX_BT <= 128 || (FMT == EPILORA_FMT_NVFP4 && !EPILORA_NV_BT256))
-    return launch_gemm_tiled<FMT, 128, KAW>(a);
+  if (a.M <= 32) return launch_gemm_tiled<FMT, 32, 1>(a);
+  if (a.M <= 64) return launch_gemm_tiled<FMT, 64, 2>(a);
+  // wide token tiles: one atom per stage (a 256-token FP8 stage is then 48 KB
+  // and the ring four deep); NVFP4 stages of 256 tokens carry scale boxes too
+  // and at two CTAs per SM the ring would be one stage deep, so NVFP4 stays
+  // at 128-token tiles
+  if (a.M <= 128 || FMT == EPILORA_FMT_NVFP4) return launch_gemm_tiled<FMT, 128, 1>(a);
   if constexpr (FMT == EPILORA_FMT_FP8_E4M3) {
     const int rc = launch_gemm_wide<FMT>(a);     // persistent, two accumulators
     if (rc != EPILORA_ERR_UNSUPPORTED) return rc;
   }
-  return launch_gemm_tiled<FMT, 256, KAW>(a);
+  return launch_gemm_tiled<FMT, 256, 1>(a);
 }
 
 }  // namespace epi

@@ -172,7 +172,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_wide_kernel(const __grid
   const int nkb = p.num_kb;
 
   if (warp == 0 && lane == 0) {
-    EPI_TRACE(0, globaltimer_ns());
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
@@ -371,7 +370,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_wide_kernel(const __grid
       }
       if (epi_bar_any(*abort_flag != 0)) break;
       tc_fence_after();
-      if (et == 0) EPI_TRACE(4, globaltimer_ns());
       wide_epilogue_tile<KS>(p, tmem_base + static_cast<uint32_t>(b * kWideBT), meta_sx, meta_idx, meta_tok, s_big,
                              s_ld, ys, n0, tv, warp, lane);
       // accumulator b may take the next tile
@@ -381,7 +379,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_wide_kernel(const __grid
     }
   }
 
-  if (threadIdx.x == 64) EPI_TRACE(6, globaltimer_ns());
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -396,12 +393,8 @@ namespace epi {
 
 // Host side: the persistent wide-tile launch, or EPILORA_ERR_UNSUPPORTED for
 // shapes it does not take (the caller then uses the two-CTAs-per-SM kernel).
-#ifndef EPILORA_GEMM_WIDE
-#define EPILORA_GEMM_WIDE 1
-#endif
-#ifndef EPILORA_GEMM_WIDE_MIN_TILES
-#define EPILORA_GEMM_WIDE_MIN_TILES 4   // tiles per SM below which the two-CTAs-per-SM kernel is used
-#endif
+// tiles per SM below which the two-CTAs-per-SM kernel is used instead
+constexpr int kWideMinTilesPerSm = 4;
 
 template <int KS>
 int launch_gemm_wide_ks(GemmParams& p, const GemmArgs& a, int tiles, int sms) {
@@ -445,7 +438,7 @@ int launch_gemm_wide_ks(GemmParams& p, const GemmArgs& a, int tiles, int sms) {
 
 template <int FMT>
 int launch_gemm_wide(const GemmArgs& a) {
-  if (!EPILORA_GEMM_WIDE || FMT != EPILORA_FMT_FP8_E4M3 || a.M <= 128) return EPILORA_ERR_UNSUPPORTED;
+  if (FMT != EPILORA_FMT_FP8_E4M3 || a.M <= 128) return EPILORA_ERR_UNSUPPORTED;
   const bool lora = a.S != nullptr && a.r > 0;
   if (lora && (a.r != 16 && a.r != 32 && a.r != 64)) return EPILORA_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(a.Y) & 15) != 0 || a.ldy % 8 != 0) return EPILORA_ERR_UNSUPPORTED;
@@ -454,7 +447,7 @@ int launch_gemm_wide(const GemmArgs& a) {
   const int t_tiles = (a.M + kWideBT - 1) / kWideBT;
   const long tiles = static_cast<long>(n_tiles) * t_tiles;
   // a tile or two per SM: nothing to overlap
-  if (tiles <= static_cast<long>(sms) * EPILORA_GEMM_WIDE_MIN_TILES || tiles <= sms || tiles > (1L << 30))
+  if (tiles <= static_cast<long>(sms) * kWideMinTilesPerSm || tiles <= sms || tiles > (1L << 30))
     return EPILORA_ERR_UNSUPPORTED;
 
   GemmParams p{};
@@ -469,9 +462,6 @@ int launch_gemm_wide(const GemmArgs& a) {
   p.fused = a.fused;
   p.pdl = !a.fused && a.pdl_dependent ? 1 : 0;
   p.perm = a.perm;
-#ifdef EPILORA_GEMM_TRACE
-  p.trace_slot = gemm_trace_launches()++ % kTraceSlots;
-#endif
   p.s_parts = a.s_parts < 1 ? 1 : a.s_parts;
   p.M = a.M;
   p.N = a.N;

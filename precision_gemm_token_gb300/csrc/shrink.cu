@@ -42,22 +42,6 @@ __device__ __forceinline__ float dot8(const uint4& xv, const uint4& av, float ac
   return acc;
 }
 
-#ifdef EPILORA_GEMM_TRACE
-// tuning builds only: per launch (round robin over 8), earliest entry,
-// earliest return from the dependency wait, latest quantizer exit, latest
-// rank-CTA exit
-static __device__ unsigned long long g_shrink_trace[8][8];
-int g_shrink_trace_launches = 0;
-#define SHRINK_TRACE_MIN(i) atomicMin(&g_shrink_trace[tslot][i], globaltimer_ns())
-#define SHRINK_TRACE_MAX(i) atomicMax(&g_shrink_trace[tslot][i], globaltimer_ns())
-#else
-#define SHRINK_TRACE_MIN(i) \
-  do {                      \
-  } while (0)
-#define SHRINK_TRACE_MAX(i) \
-  do {                      \
-  } while (0)
-#endif
 
 struct QuantSide {          // quantizer CTAs of the fused grid (fmt < 0: none)
   int fmt;
@@ -245,7 +229,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
                                                                     int L, int r, const int32_t* __restrict__ idx,
                                                                     const uint8_t* __restrict__ mask,
                                                                     float* __restrict__ S, int* status,
-                                                                    QuantSide qs, int parts, int kslice, int tslot,
+                                                                    QuantSide qs, int parts, int kslice,
                                                                     int early_release) {
   // Let the dependent GEMM launch at once: before it reads anything this grid
   // writes it waits for this grid's completion, and until then it only
@@ -253,13 +237,11 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   // (of the previous call's GEMM), wait for that grid's completion: x, idx,
   // mask and the workspace are only valid from here on (no-op for an
   // ordinary launch).
-  if (threadIdx.x == 0) SHRINK_TRACE_MIN(0);
   if (threadIdx.x == 0) prefetch_inputs(X, K, ldx, A, L, r, idx, qs.fmt >= 0 ? parts : 0, kslice);
   // early_release: the GEMM may launch as soon as every CTA of this grid has
   // started (else as they exit)
   if (early_release) pdl_allow_dependents();
   pdl_wait_primary();
-  if (threadIdx.x == 0) SHRINK_TRACE_MIN(1);
   __shared__ float red[kShrinkThreads / 32][kRanksPerCta];
 
   const size_t t = blockIdx.x;
@@ -269,7 +251,6 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
       quant_role<kShrinkQuantChunks>(X, K, ldx, idx, mask, L, static_cast<int>(gridDim.x), static_cast<int>(t), gy,
                                      parts, kslice, qs, status, &red[0][0]);
       __syncthreads();
-      if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
       return;
     }
     gy -= parts;
@@ -280,15 +261,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   const int part = gy / groups;
   rank_role(X, K, ldx, A, L, r, idx, mask, S, status, static_cast<int>(gridDim.x), t,
             (gy - part * groups) * kRanksPerCta, part, kslice, gy == 0, &red[0][0]);
-  if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
 }
-
-#ifndef EPILORA_SHRINK_BLOCK
-#define EPILORA_SHRINK_BLOCK 1       // wide batches: token-block CTAs on the tensor cores
-#endif
-#ifndef EPILORA_SHRINK_EARLY_ALL
-#define EPILORA_SHRINK_EARLY_ALL 0   // 1: grids of any size release the GEMM at CTA start
-#endif
 
 // Wide batches (M > 32): tokens in blocks of 16 consecutive tokens. A block
 // whose active tokens carry at most kBlockAdapters distinct adapters (the
@@ -327,11 +300,9 @@ __global__ void __launch_bounds__(kShrinkThreads, 6) shrink_block_kernel(const _
                                                                       const uint8_t* __restrict__ mask,
                                                                       float* __restrict__ S, int* status,
                                                                       QuantSide qs, int M, int parts, int kslice,
-                                                                      int tslot, int early_release) {
-  if (threadIdx.x == 0) SHRINK_TRACE_MIN(0);
+                                                                      int early_release) {
   if (early_release) pdl_allow_dependents();
   pdl_wait_primary();
-  if (threadIdx.x == 0) SHRINK_TRACE_MIN(1);
   extern __shared__ float red_dyn[];        // [4 warps][16 tokens][r] (at least 64 floats)
   __shared__ int lsh[kBlockTokens];
   const int nblk = r > 0 ? (M + kBlockTokens - 1) / kBlockTokens : 0;
@@ -347,7 +318,6 @@ __global__ void __launch_bounds__(kShrinkThreads, 6) shrink_block_kernel(const _
       // rows of up to 8192 elements stay in registers between the amax and the codes
       if (qs.fmt >= 0)
         quant_role<8>(X, K, ldx, idx, mask, L, M, static_cast<size_t>(t), 0, 1, K, qs, status, red_dyn);
-      if (threadIdx.x == 0) SHRINK_TRACE_MAX(2);
       return;
     }
     if (block_adapters(idx, mask, L, M, (t / kBlockTokens) * kBlockTokens) <= kBlockAdapters) return;
@@ -356,13 +326,11 @@ __global__ void __launch_bounds__(kShrinkThreads, 6) shrink_block_kernel(const _
       rank_role(X, K, ldx, A, L, r, idx, mask, S, status, M, static_cast<size_t>(t),
                 (role - 1) * 16 + gq * kRanksPerCta, 0, K, role == 1 && gq == 0, red_dyn);
     }
-    if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
     return;
   }
   const int blk = q / parts;
   const int part = q - blk * parts;
   const int t0 = blk * kBlockTokens;
-  if (threadIdx.x == 0) SHRINK_TRACE_MIN(5);
   if (block_adapters(idx, mask, L, M, t0) > kBlockAdapters) {
     // taken token by token (part 0): zero the other parts
     if (part > 0)
@@ -370,7 +338,6 @@ __global__ void __launch_bounds__(kShrinkThreads, 6) shrink_block_kernel(const _
         const int t = t0 + e / r;
         if (t < M) S[(static_cast<size_t>(part) * M + t) * r + (e % r)] = 0.0f;
       }
-    if (threadIdx.x == 0) SHRINK_TRACE_MAX(3);
     return;
   }
   if (threadIdx.x < kBlockTokens) {
@@ -469,7 +436,6 @@ __global__ void __launch_bounds__(kShrinkThreads, 6) shrink_block_kernel(const _
       S[(static_cast<size_t>(part) * M + t) * r + (e - tl * r)] = v;
     }
   }
-  if (threadIdx.x == 0) SHRINK_TRACE_MAX(4);
 }
 
 constexpr int kShrinkSliceTarget = 1024;   // elements of K per slice when splitting
@@ -482,14 +448,6 @@ int kslice_for(int K, int parts) {
 
 int shrink_carveout_done[64] = {0};
 
-int trace_slot_next() {
-#ifdef EPILORA_GEMM_TRACE
-  return g_shrink_trace_launches++ % 8;
-#else
-  return 0;
-#endif
-}
-
 }  // namespace
 
 int shrink_kslice(int K, int parts) { return kslice_for(K, parts); }
@@ -500,7 +458,6 @@ int shrink_parts_max(int K) {
 }
 
 int shrink_parts(int M, int K, int r) {
-  if (M > 32 && !EPILORA_SHRINK_BLOCK) return 1;
   if (M > 32) {
     // token-block CTAs: K slices of about 2048 (ranks <= 64; rank 128 keeps
     // one slice, the wide GEMM then reads S rows straight from memory)
@@ -536,7 +493,7 @@ int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, in
   dim3 grid(M, r / kRanksPerCta);
   shrink_kernel<<<grid, kShrinkThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), K, ldx,
                                                       static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S,
-                                                      status_dev, qs, 1, K, trace_slot_next(), 1);
+                                                      status_dev, qs, 1, K, 1);
   return cudaGetLastError() == cudaSuccess ? EPILORA_OK : EPILORA_ERR_CUDA;
 }
 
@@ -549,11 +506,11 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
     return EPILORA_ERR_INVALID_ARG;
   if (prefer_max_shared(reinterpret_cast<const void*>(shrink_kernel), shrink_carveout_done) != EPILORA_OK)
     return EPILORA_ERR_CUDA;
-  if (perm != nullptr && (M <= 32 || idx == nullptr || (s_parts != 1 && !EPILORA_SHRINK_BLOCK)))
+  if (perm != nullptr && (M <= 32 || idx == nullptr))
     return EPILORA_ERR_INVALID_ARG;
   QuantSide qs{fmt, static_cast<uint8_t*>(Xq), x_scale, x_block_scale, x_global_scale, perm};
   const int kslice = s_parts == 1 ? K : kslice_for(K, s_parts);
-  if (M > 32 && EPILORA_SHRINK_BLOCK) {
+  if (M > 32) {
     // wide batch: M quantizer CTAs, then token-block CTAs (block, K slice)
     const int nblk = r > 0 ? (M + kBlockTokens - 1) / kBlockTokens : 0;
     const long ctas = static_cast<long>(M) + static_cast<long>(nblk) * s_parts +
@@ -568,7 +525,7 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int early = EPILORA_SHRINK_EARLY_ALL || ctas <= num_sms() ? 1 : 0;
+    const int early = ctas <= num_sms() ? 1 : 0;
     // per-warp partial tiles of a token block (and the quantizers' scratch)
     cfg.dynamicSmemBytes = static_cast<size_t>(4) * kBlockTokens * (r > 4 ? r : 4) * sizeof(float);
     if (cfg.dynamicSmemBytes > 227 * 1024) return EPILORA_ERR_UNSUPPORTED;
@@ -585,7 +542,7 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
     }
     const cudaError_t e = cudaLaunchKernelEx(&cfg, shrink_block_kernel, static_cast<const __nv_bfloat16*>(X), K, ldx,
                                              static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S, status_dev, qs,
-                                             M, s_parts, kslice, trace_slot_next(), early);
+                                             M, s_parts, kslice, early);
     return e == cudaSuccess ? EPILORA_OK : EPILORA_ERR_CUDA;
   }
   // launched as a programmatic dependent of whatever precedes it on the
@@ -599,7 +556,7 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
   // release it at exit instead (their shrink is a small share of the layer,
   // and an early GEMM only competes with it for HBM).
   const int early_release =
-      EPILORA_SHRINK_EARLY_ALL || M <= 32 || static_cast<int>(cfg.gridDim.x * cfg.gridDim.y) <= num_sms() ? 1 : 0;
+      M <= 32 || static_cast<int>(cfg.gridDim.x * cfg.gridDim.y) <= num_sms() ? 1 : 0;
   cfg.blockDim = dim3(kShrinkThreads, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -609,7 +566,7 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, shrink_kernel, static_cast<const __nv_bfloat16*>(X), K, ldx,
                          static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S, status_dev, qs, s_parts,
-                         kslice, trace_slot_next(),
+                         kslice,
                          early_release) != cudaSuccess)
     return EPILORA_ERR_CUDA;
   return EPILORA_OK;
@@ -617,19 +574,3 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
 
 }  // namespace epi
 
-#ifdef EPILORA_GEMM_TRACE
-// tuning builds only: copy (and reset) the shrink launches' timestamps
-extern "C" EPILORA_API int epilora_debug_shrink_trace(void* host_out, int clear) {
-  if (cudaMemcpyFromSymbol(host_out, epi::g_shrink_trace, sizeof(epi::g_shrink_trace)) != cudaSuccess) return -3;
-  if (clear) {
-    static unsigned long long init[8][8];
-    for (auto& row : init) {
-      row[0] = row[1] = row[5] = ~0ull;   // earliest: entry, after the wait, block CTA start
-      row[2] = row[3] = row[4] = row[6] = row[7] = 0ull;   // latest: quantizer, rank, block CTA ends
-    }
-    if (cudaMemcpyToSymbol(epi::g_shrink_trace, init, sizeof(init)) != cudaSuccess) return -3;
-    epi::g_shrink_trace_launches = 0;
-  }
-  return 0;
-}
-#endif

@@ -168,3 +168,30 @@ def test_single_kernel_chain_shares_workspace(fmt):
         for c, Y in zip(cases, outs):
             assert torch.equal(Y, c[3])
     assert int(ws.buf[:SYNC_BYTES].count_nonzero().item()) == 0
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    """A wait that runs out, made on the host: the shrink-item counter at the
+    start of the workspace is set past every item before the call, so no
+    thread block claims any and the kernel's bounded wait for S gives up (about
+    a second). The call returns EPILORA_ERR_TIMEOUT in the status word, leaves
+    the counters zero again, and the next call on the same stream and
+    workspace is correct."""
+    M, K, N, L, r = 1, 2048, 1024, 1, 16
+    p = make_projection(M, K, N, L, r, seed=5, device="cuda")
+    w = T.quantize_weight(p.W, FP8)
+    ref = T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask)
+    ws = T.LayerWorkspace("cuda")
+    buf = ws.get(FP8, M, K, r)
+    torch.cuda.synchronize()
+    buf[:4].view(torch.int32).fill_(0x7FFFFFFF)          # the claim counter: every item taken already
+    st = status_buf()
+    T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, workspace=ws, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == E.EPILORA_ERR_TIMEOUT
+    assert int(buf[:SYNC_BYTES].count_nonzero().item()) == 0
+    st.zero_()
+    Y = T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, workspace=ws, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(Y, ref)
