@@ -192,9 +192,11 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
 /*
  * Number of kernels epilora_layer_forward (and _slices, _noalloc) enqueues
  * for (fmt, M, K): 1 when the single-kernel decode path takes the call (a few
- * tokens: M <= 8 and the quantized rows of all tokens within 16 KB, i.e.
- * M * K <= 16384 for FP8, M * K <= 32768 for NVFP4), else 2 (the shrink grid
- * with its quantizer blocks, then the GEMM as its programmatic dependent).
+ * tokens: M <= 8, the quantized rows of all tokens, each padded to a multiple
+ * of 256 bytes, within 16 KB, and for FP8 M * K <= 16384: e.g. one token up
+ * to K = 16384, four tokens at K = 4096; NVFP4 two tokens at K = 14336), else
+ * 2 (the shrink grid with its quantizer blocks, then the GEMM as its
+ * programmatic dependent).
  * Returns 0 for invalid arguments.
  */
 EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K);

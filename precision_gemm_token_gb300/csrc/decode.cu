@@ -54,8 +54,7 @@ constexpr int kDecMaxCtas = 256;
 constexpr int kDecXcBytes = 16384;         // compact quantized activations per CTA
 constexpr int kDecRanksPerItem = 4;
 constexpr int kDecHelperBar = 1;           // named barrier of the 4 helper warps
-constexpr int kDecUnitW = 128 * 128;       // weight codes per unit (bytes)
-constexpr int kDecXSlot = 16 * 128;        // activation rows of a stage (16-row MMA operand)
+constexpr int kDecAtomW = 128 * 128;       // weight codes of one 128-byte K atom of a tile (bytes)
 constexpr int kDecSmemBudget = 113 * 1024;
 constexpr int kDecMaxStages = 8;
 constexpr int kMaxRankBrow = 64;           // 32-bit words of a rank-128 bf16 B row
@@ -88,23 +87,25 @@ struct DecParams {
   int M, N, K, ldx, ldy, L, r, s_row, n_slices;
   int slice_end[4];
   int adapters, parts, kslice, n_items;
-  int kb_pad;          // bytes of one compact activation row (nkb * 128)
+  int kb_pad;          // code bytes of one token's row, padded to whole units
 };
 
-template <int FMT>
+// A unit is KA 128-byte K atoms of one 128-row weight tile (16 KB each).
+template <int FMT, int KA>
 struct DecCfg {
   static constexpr bool kFP4 = FMT == EPILORA_FMT_NVFP4;
-  static constexpr int kSfA = kFP4 ? 4 * 512 : 0;          // weight scale atoms of a stage (4 MMA k-steps)
-  static constexpr int kSfB = kFP4 ? 4 * 512 : 0;          // token scale atoms
-  static constexpr int kSfWRaw = kFP4 ? 128 * 16 : 0;      // TMA box of weight scales
-  static constexpr int kStage = kDecUnitW + kDecXSlot + kSfA + kSfB + kSfWRaw;
-  static constexpr int kStageTx = kDecUnitW + kSfWRaw;     // bytes TMA delivers per stage
-  static constexpr int kSfColsA = 16;                      // 4 k-steps x 4 columns
-  static constexpr int kSfColsB = 16;
-  static constexpr int kSfSlot = kSfColsA + kSfColsB;
-  static constexpr int kTmemCols = kFP4 ? 128 : 32;        // 2 accumulators of 16 (+ 2 scale slots)
+  static constexpr int kKSteps = 4 * KA;                    // MMAs per unit (32 bytes of K each)
+  static constexpr int kUnitW = KA * kDecAtomW;
+  static constexpr int kSfA = kFP4 ? kKSteps * 512 : 0;     // weight scales re-laid for tcgen05.cp
+  static constexpr int kSfWRaw = kFP4 ? 128 * 16 * KA : 0;  // TMA box of weight scales [128][16 KA]
+  static constexpr int kStageRaw = kUnitW + kSfA + kSfWRaw;
+  static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
+  static constexpr int kStageTx = kUnitW + kSfWRaw;         // bytes TMA delivers per stage
+  static constexpr int kSfCols = 4 * kKSteps;               // TMEM columns of one scale slot (A or B)
+  static constexpr int kSfSlot = 2 * kSfCols;
+  static constexpr int kTmemNeed = 32 + (kFP4 ? 2 * kSfSlot : 0);   // 2 accumulators of 16 (+ 2 scale slots)
+  static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : 256;
   static constexpr uint32_t kIdesc = kFP4 ? idesc_mxf4nvf4(128, 16) : idesc_f8f6f4_e4m3(128, 16);
-  static_assert(kStage % 1024 == 0, "stage alignment");
 };
 
 __device__ __forceinline__ void helper_sync() {
@@ -204,16 +205,25 @@ __device__ __forceinline__ int dec_slice_offset(const DecParams& p, int n0) {
   return off;
 }
 
-template <int FMT>
+template <int FMT, int KA>
 __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __grid_constant__ DecParams p) {
-  using C = DecCfg<FMT>;
+  using C = DecCfg<FMT, KA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stages = p.stages;
   const int M = p.M;
-  uint8_t* xc = smem + static_cast<size_t>(stages) * C::kStage;       // [M][kb_pad] swizzled codes
-  uint8_t* xsf = xc + M * p.kb_pad;                                   // NVFP4: [M][nkb * 16] block scales
-  float* s_stage = reinterpret_cast<float*>(xsf + (C::kFP4 ? (M * p.nkb * 16 + 127) / 128 * 128 : 0));
+  // Quantized activations, chunk-major: 16-byte K chunk j of token t at
+  // (j * M + t) * 16. The MMA reads them in place as its B operand (K-major,
+  // no swizzle, core matrices M * 16 bytes apart along K: rows t < M are the
+  // tokens, the other rows of a core matrix fall on the next chunk and only
+  // feed output columns that are never read), + 128 bytes of slack.
+  uint8_t* xc = smem + static_cast<size_t>(stages) * C::kStage;
+  // NVFP4 token block scales, one 16-byte line per (MMA k-step s, token t) at
+  // (s * M + t) * 16 holding the token's 4 scales of that k-step: read in
+  // place by tcgen05.cp, + 512 bytes of slack
+  uint8_t* xsf = xc + M * p.kb_pad + 128;
+  const int xsf_bytes = C::kFP4 ? (M * (p.kb_pad / 32) * 16 + 512 + 127) / 128 * 128 : 0;
+  float* s_stage = reinterpret_cast<float*>(xsf + xsf_bytes);
   uint8_t* misc = reinterpret_cast<uint8_t*>(s_stage) + (M * p.s_row * 4 + 127) / 128 * 128;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(misc);
   uint64_t* empty_bar = full_bar + kDecMaxStages;
@@ -273,9 +283,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         const int kb = static_cast<int>(u - static_cast<long long>(T) * p.nkb);
         uint8_t* st = smem + static_cast<size_t>(s) * C::kStage;
         mbar_arrive_expect_tx(&full_bar[s], C::kStageTx);
-        tma_load_2d(st, &p.tmW, &full_bar[s], kb * 128, T * 128);
-        if (C::kFP4) tma_load_2d(st + kDecUnitW + kDecXSlot + C::kSfA + C::kSfB, &p.tmSW, &full_bar[s], kb * 16,
-                                 T * 128);
+#pragma unroll
+        for (int a = 0; a < KA; ++a) tma_load_2d(st + a * kDecAtomW, &p.tmW, &full_bar[s], (kb * KA + a) * 128, T * 128);
+        if (C::kFP4) tma_load_2d(st + C::kUnitW + C::kSfA, &p.tmSW, &full_bar[s], kb * 16 * KA, T * 128);
         issued_mask |= 1u << s;
         parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
         if (it == stages - 1 || u + 1 == u_end) {
@@ -284,8 +294,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           for (long long v = u + 1; v < a_end; ++v) {
             const int T2 = static_cast<int>(v / p.nkb);
             const int kb2 = static_cast<int>(v - static_cast<long long>(T2) * p.nkb);
-            tma_prefetch_l2_2d(&p.tmW, kb2 * 128, T2 * 128);
-            if (C::kFP4) tma_prefetch_l2_2d(&p.tmSW, kb2 * 16, T2 * 128);
+#pragma unroll
+            for (int a = 0; a < KA; ++a) tma_prefetch_l2_2d(&p.tmW, (kb2 * KA + a) * 128, T2 * 128);
+            if (C::kFP4) tma_prefetch_l2_2d(&p.tmSW, kb2 * 16 * KA, T2 * 128);
           }
         }
       }
@@ -306,6 +317,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       *abort_flag = 1;
       record_status(p.status, EPILORA_ERR_TIMEOUT);
     }
+    const uint32_t xc_addr = smem_u32(xc);
+    const uint32_t xsf_addr = smem_u32(xsf);
+    const uint32_t x_lbo = static_cast<uint32_t>(16 * M);
     SegWalk walk(p, c);
     int T, kb0, kb1, j = 0;
     long long it = 0;
@@ -337,61 +351,56 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           break;
         }
         uint8_t* st = smem + static_cast<size_t>(s) * C::kStage;
-        uint8_t* xs = st + kDecUnitW;
-        // activation rows of this unit (row t of the 8-row group at t * 128;
-        // the compact rows already carry the swizzle of row t)
-        for (int q = lane; q < M * 8; q += 32) {
-          const int t = q >> 3, ch = q & 7;
-          *reinterpret_cast<uint4*>(xs + t * 128 + ch * 16) =
-              *reinterpret_cast<const uint4*>(xc + t * p.kb_pad + kb * 128 + ch * 16);
-        }
+        uint8_t* sfa = st + C::kUnitW;
         if (C::kFP4) {
-          // weight scales: canonical [128 rows][16 B] box -> one 512-B atom
-          // per K = 64 step (line r0 = 4 bytes of rows r0, r0+32, r0+64, r0+96);
-          // token scales from the compact copy the same way (rows < M)
-          uint8_t* sfa = xs + kDecXSlot;
-          uint8_t* sfb = sfa + C::kSfA;
-          const uint8_t* raw_w = sfb + C::kSfB;
-          uint4 v[4];
+          // weight scales: canonical [128 rows][16 KA bytes] box -> one 512-B
+          // atom per K = 64 step (line r0 = 4 bytes of rows r0, r0+32, r0+64,
+          // r0+96), the layout tcgen05.cp .32x128b.warpx4 takes
+          const uint8_t* raw_w = sfa + C::kSfA;
 #pragma unroll
-          for (int r1 = 0; r1 < 4; ++r1) v[r1] = *reinterpret_cast<const uint4*>(raw_w + (lane + 32 * r1) * 16);
+          for (int a = 0; a < KA; ++a) {
+            uint4 v[4];
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            uint4 o;
-            o.x = (&v[0].x)[kk];
-            o.y = (&v[1].x)[kk];
-            o.z = (&v[2].x)[kk];
-            o.w = (&v[3].x)[kk];
-            *reinterpret_cast<uint4*>(sfa + kk * 512 + lane * 16) = o;
+            for (int r1 = 0; r1 < 4; ++r1)
+              v[r1] = *reinterpret_cast<const uint4*>(raw_w + (lane + 32 * r1) * (16 * KA) + 16 * a);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              uint4 o;
+              o.x = (&v[0].x)[kk];
+              o.y = (&v[1].x)[kk];
+              o.z = (&v[2].x)[kk];
+              o.w = (&v[3].x)[kk];
+              *reinterpret_cast<uint4*>(sfa + (a * 4 + kk) * 512 + lane * 16) = o;
+            }
           }
-          uint4 tv4 = make_uint4(0u, 0u, 0u, 0u);
-          if (lane < M) tv4 = *reinterpret_cast<const uint4*>(xsf + (lane * p.nkb + kb) * 16);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            *reinterpret_cast<uint4*>(sfb + kk * 512 + lane * 16) = make_uint4((&tv4.x)[kk], 0u, 0u, 0u);
+          fence_proxy_async_smem();
+          __syncwarp();
         }
-        fence_proxy_async_smem();
-        __syncwarp();
         if (lane == 0) {
           tc_fence_after();
           const uint32_t w_addr = smem_u32(st);
-          const uint32_t x_addr = smem_u32(xs);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = make_smem_desc(w_addr + kk * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bdesc = make_smem_desc(x_addr + kk * 32, 16, 1024, kSwizzle128B);
-            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
-            if (C::kFP4) {
-              const uint32_t slot = 32u + static_cast<uint32_t>(it & 1) * C::kSfSlot;
-              const uint32_t sfa_col = slot + kk * 4;
-              const uint32_t sfb_col = slot + C::kSfColsA + kk * 4;
-              tc_cp_32x128b_warpx4(tmem_base + sfa_col,
-                                   make_smem_desc(smem_u32(xs + kDecXSlot) + kk * 512, 16, 128, kSwizzleNone));
-              tc_cp_32x128b_warpx4(tmem_base + sfb_col, make_smem_desc(smem_u32(xs + kDecXSlot + C::kSfA) + kk * 512,
-                                                                       16, 128, kSwizzleNone));
-              mma_mxf4nvf4(d_tmem, adesc, bdesc, C::kIdesc, tmem_base + sfa_col, tmem_base + sfb_col, accum);
-            } else {
-              mma_f8f6f4(d_tmem, adesc, bdesc, C::kIdesc, accum);
+          for (int a = 0; a < KA; ++a) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int jj = a * 4 + kk;                               // k-step within the unit
+              const int chunk = (kb * KA + a) * 8 + kk * 2;              // first 16-byte K chunk
+              const uint64_t adesc = make_smem_desc(w_addr + a * kDecAtomW + kk * 32, 16, 1024, kSwizzle128B);
+              const uint64_t bdesc = make_smem_desc(xc_addr + chunk * x_lbo, x_lbo, 0, kSwizzleNone);
+              const uint32_t accum = (kb > kb0 || jj > 0) ? 1u : 0u;
+              if (C::kFP4) {
+                const uint32_t slot = 32u + static_cast<uint32_t>(it & 1) * C::kSfSlot;
+                const uint32_t sfa_col = slot + jj * 4;
+                const uint32_t sfb_col = slot + C::kSfCols + jj * 4;
+                const int ks_glob = (kb * KA + a) * 4 + kk;              // k-step within the row
+                tc_cp_32x128b_warpx4(tmem_base + sfa_col,
+                                     make_smem_desc(smem_u32(sfa) + jj * 512, 16, 128, kSwizzleNone));
+                tc_cp_32x128b_warpx4(tmem_base + sfb_col,
+                                     make_smem_desc(xsf_addr + ks_glob * x_lbo, 16, 128, kSwizzleNone));
+                mma_mxf4nvf4(d_tmem, adesc, bdesc, C::kIdesc, tmem_base + sfa_col, tmem_base + sfb_col, accum);
+              } else {
+                mma_f8f6f4(d_tmem, adesc, bdesc, C::kIdesc, accum);
+              }
             }
           }
           tc_commit(&empty_bar[s]);   // frees the stage once these MMAs have read it
@@ -501,19 +510,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           const int t = q / nch;
           const int k0 = (q - t * nch) * 8;
           const uint2 code = quant8_e4m3(v[jj], meta_sx[t]);
-          const int a = k0 >> 7, ch = (k0 & 127) >> 4, half = (k0 & 15) >> 3;
-          *reinterpret_cast<uint2*>(xc + t * p.kb_pad + a * 128 + ((ch ^ (t & 7)) << 4) + half * 8) = code;
+          *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
           if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
         }
       }
-      // zero codes past K in the last unit (finite values against the
+      // zero codes past K up to the unit boundary (finite values against the
       // weight box's zero fill)
       for (int q = et; q < M * (p.kb_pad - p.K) / 8; q += 128) {
         const int per = (p.kb_pad - p.K) / 8;
         const int t = q / per;
         const int k0 = p.K + (q - t * per) * 8;
-        const int a = k0 >> 7, ch = (k0 & 127) >> 4, half = (k0 & 15) >> 3;
-        *reinterpret_cast<uint2*>(xc + t * p.kb_pad + a * 128 + ((ch ^ (t & 7)) << 4) + half * 8) = make_uint2(0, 0);
+        *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = make_uint2(0, 0);
       }
     } else {
       // NVFP4: per 16-element block, its scale and codes (block-local)
@@ -556,16 +563,29 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
             hi = by[4] | (by[5] << 8) | (by[6] << 16) | (by[7] << 24);
           }
         }
-        // byte k/2 of the packed row: atom b / 16, 16-byte chunk (b % 16) / 2, half b % 2
-        const int a = b >> 4, ch = (b & 15) >> 1, half = b & 1;
-        *reinterpret_cast<uint2*>(xc + t * p.kb_pad + a * 128 + ((ch ^ (t & 7)) << 4) + half * 8) = make_uint2(lo, hi);
-        xsf[t * p.nkb * 16 + b] = static_cast<uint8_t>(sb);
+        // block b is bytes [8 b, 8 b + 8) of the packed row: 16-byte chunk
+        // b / 2, half b % 2; its scale is byte b % 4 of the line of k-step b / 4
+        *reinterpret_cast<uint2*>(xc + ((b >> 1) * M + t) * 16 + (b & 1) * 8) = make_uint2(lo, hi);
+        xsf[((b >> 2) * M + t) * 16 + (b & 3)] = static_cast<uint8_t>(sb);
         if (c == 0) {
           *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * (p.K / 2) + b * 8) = make_uint2(lo, hi);
           p.xsb_out[static_cast<size_t>(t) * nb + b] = static_cast<uint8_t>(sb);
         }
       }
     }
+    if (C::kFP4) {
+      // codes and scales past K up to the unit boundary are zero (E4M3 scale
+      // bytes could otherwise read as NaN against the zero-filled weights)
+      const int nb = p.K / kNvfp4Block, nb_pad = 2 * p.kb_pad / kNvfp4Block;
+      for (int q = et; q < M * (nb_pad - nb); q += 128) {
+        const int t = q / (nb_pad - nb);
+        const int b = nb + (q - t * (nb_pad - nb));
+        *reinterpret_cast<uint2*>(xc + ((b >> 1) * M + t) * 16 + (b & 1) * 8) = make_uint2(0, 0);
+        xsf[((b >> 2) * M + t) * 16 + (b & 3)] = 0;
+      }
+    }
+    // the MMA reads the compact copy through the async proxy
+    fence_proxy_async_smem();
     helper_sync();
     if (et == 0) mbar_arrive(xrdy_bar);           // the MMA warp may start
     // ---- this CTA's finisher tiles: B slices of their adapters into L2 ----
@@ -588,12 +608,15 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     // ---- shrink items: (token, 4 ranks, K slice), claimed grid-wide ----
     const int groups = p.s_row / kDecRanksPerItem;
     if (p.adapters) {
+      unsigned* claim_box = reinterpret_cast<unsigned*>(bcast);
       while (true) {
-        if (et == 0) *bcast = static_cast<int>(atomicAdd(&p.sync[0], 1u));
+        // unsigned throughout: any counter value at or past n_items ends the loop
+        if (et == 0) *claim_box = atomicAdd(&p.sync[0], 1u);
         helper_sync();
-        const int item = *bcast;
+        const unsigned claimed = *claim_box;
         helper_sync();
-        if (item >= p.n_items) break;
+        if (claimed >= static_cast<unsigned>(p.n_items)) break;
+        const int item = static_cast<int>(claimed);
         const int t = item / (groups * p.parts);
         const int rem = item - t * groups * p.parts;
         const int part = rem / groups;
@@ -802,13 +825,23 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
 // Whether the single-kernel decode path takes (fmt, M, K): a few tokens whose
 // quantized rows fit the per-CTA compact copy (and, for FP8, the quantizer's
 // registers).
+// 128-byte K atoms per weight unit (a unit is KA atoms of one 128-row tile)
+constexpr int kDecKA = 2;
+
+// Whether the single-kernel decode path takes (fmt, M, K): a few tokens whose
+// quantized rows (padded to whole units) fit the per-CTA compact copy (and,
+// for FP8, the quantizer's registers).
 bool decode_path_eligible(int fmt, int M, int K) {
   if (M < 1 || M > kDecMaxTokens || K < 32 || K % 32 != 0) return false;
+  const long unit_k = 128L * kDecKA;
   if (fmt == EPILORA_FMT_FP8_E4M3) {
-    const long kb_pad = (static_cast<long>(K) + 127) / 128 * 128;
+    const long kb_pad = (static_cast<long>(K) + unit_k - 1) / unit_k * unit_k;
     return M * kb_pad <= kDecXcBytes && static_cast<long>(M) * (K / 8) <= 16L * 128;
   }
-  if (fmt == EPILORA_FMT_NVFP4) return K % 256 == 0 && static_cast<long>(M) * (K / 2) <= kDecXcBytes;
+  if (fmt == EPILORA_FMT_NVFP4) {
+    const long kb_pad = (static_cast<long>(K / 2) + unit_k - 1) / unit_k * unit_k;
+    return K % 256 == 0 && M * kb_pad <= kDecXcBytes;
+  }
   return false;
 }
 
@@ -817,9 +850,68 @@ static_assert((kDecSyncWords + kDecMaxCtas) * 4 == EPILORA_WORKSPACE_SYNC_BYTES,
 
 size_t decode_partial_bytes(int M) { return static_cast<size_t>(kDecMaxCtas) * M * 128 * 4; }
 
+namespace {
+
+template <int FMT, int KA>
+int launch_fused_decode_t(DecParams& p, const DecodeArgs& a) {
+  using C = DecCfg<FMT, KA>;
+  const int kbytes = C::kFP4 ? a.K / 2 : a.K;
+  p.nkb = (kbytes + 128 * KA - 1) / (128 * KA);
+  p.kb_pad = p.nkb * 128 * KA;
+  p.n_tiles = (a.N + 127) / 128;
+  p.U = static_cast<long long>(p.n_tiles) * p.nkb;
+  int G = num_sms();
+  if (G > kDecMaxCtas) G = kDecMaxCtas;
+  if (p.U < G) G = static_cast<int>(p.U);
+  p.G = G;
+  int rc = make_tma_2d_u8(&p.tmW, a.Wq, a.N, kbytes, kbytes, 128, 128, true);
+  if (rc != EPILORA_OK) return rc;
+  if (C::kFP4) {
+    rc = make_tma_2d_u8(&p.tmSW, a.w_block_scale, a.N, a.K / 16, a.K / 16, 128, 16 * KA, false);
+    if (rc != EPILORA_OK) return rc;
+  }
+  // [ring][compact codes + 128][token scale lines + 512][S rows][barriers, metadata]
+  const int xsf_bytes = C::kFP4 ? (a.M * (p.kb_pad / 32) * 16 + 512 + 127) / 128 * 128 : 0;
+  const int fixed = 1024 + a.M * p.kb_pad + 128 + xsf_bytes + (a.M * a.s_row * 4 + 127) / 128 * 128 + 1024;
+  int stages = (kDecSmemBudget - fixed) / C::kStage;
+  if (stages > kDecMaxStages) stages = kDecMaxStages;
+  if (stages < 2) return EPILORA_ERR_UNSUPPORTED;
+  p.stages = stages;
+  // L2 prefetch behind the ring: about 40 MB over the grid
+  p.l2_ahead = static_cast<int>((40L << 20) / (static_cast<long>(G) * C::kStageTx));
+  const int smem = fixed + stages * C::kStage;
+  if (smem > 227 * 1024) return EPILORA_ERR_UNSUPPORTED;
+
+  auto kern = fused_decode_kernel<FMT, KA>;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return EPILORA_ERR_CUDA;
+  if (attr_done[dev] < smem) {
+    // the largest shared-memory carveout: this CTA and the next projection's
+    // fit on one SM together
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+            cudaSuccess)
+      return EPILORA_ERR_CUDA;
+    attr_done[dev] = smem;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(G, 1, 1);
+  cfg.blockDim = dim3(kDecThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return EPILORA_ERR_CUDA;
+  return EPILORA_OK;
+}
+
+}  // namespace
+
 int launch_fused_decode(const DecodeArgs& a) {
-  const bool fp4 = a.fmt == EPILORA_FMT_NVFP4;
-  const int kbytes = fp4 ? a.K / 2 : a.K;
   DecParams p{};
   p.X = static_cast<const __nv_bfloat16*>(a.X);
   p.A = static_cast<const __nv_bfloat16*>(a.A);
@@ -851,59 +943,8 @@ int launch_fused_decode(const DecodeArgs& a) {
   p.parts = a.parts;
   p.kslice = a.kslice;
   p.n_items = p.adapters ? a.M * (a.s_row / kDecRanksPerItem) * a.parts : 0;
-  p.nkb = (kbytes + 127) / 128;
-  p.kb_pad = p.nkb * 128;
-  p.n_tiles = (a.N + 127) / 128;
-  p.U = static_cast<long long>(p.n_tiles) * p.nkb;
-  int G = num_sms();
-  if (G > kDecMaxCtas) G = kDecMaxCtas;
-  if (p.U < G) G = static_cast<int>(p.U);
-  p.G = G;
-
-  int rc = make_tma_2d_u8(&p.tmW, a.Wq, a.N, kbytes, kbytes, 128, 128, true);
-  if (rc != EPILORA_OK) return rc;
-  if (fp4) {
-    rc = make_tma_2d_u8(&p.tmSW, a.w_block_scale, a.N, a.K / 16, a.K / 16, 128, 16, false);
-    if (rc != EPILORA_OK) return rc;
-  }
-  const int stage = fp4 ? DecCfg<EPILORA_FMT_NVFP4>::kStage : DecCfg<EPILORA_FMT_FP8_E4M3>::kStage;
-  const int xsf_bytes = fp4 ? (a.M * p.nkb * 16 + 127) / 128 * 128 : 0;
-  const int fixed = 1024 + a.M * p.kb_pad + xsf_bytes + (a.M * a.s_row * 4 + 127) / 128 * 128 + 1024;
-  int stages = (kDecSmemBudget - fixed) / stage;
-  if (stages > kDecMaxStages) stages = kDecMaxStages;
-  if (stages < 2) return EPILORA_ERR_UNSUPPORTED;
-  p.stages = stages;
-  // L2 prefetch behind the ring: about 40 MB over the grid
-  {
-    const long per = (40L << 20) / (static_cast<long>(G) * (kDecUnitW + (fp4 ? 2048 : 0)));
-    p.l2_ahead = static_cast<int>(per);
-  }
-  const int smem = fixed + stages * stage;
-  if (smem > 227 * 1024) return EPILORA_ERR_UNSUPPORTED;
-
-  const void* kern = fp4 ? reinterpret_cast<const void*>(fused_decode_kernel<EPILORA_FMT_NVFP4>)
-                         : reinterpret_cast<const void*>(fused_decode_kernel<EPILORA_FMT_FP8_E4M3>);
-  static int attr_done[2][64] = {{0}};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return EPILORA_ERR_CUDA;
-  if (attr_done[fp4][dev] < smem) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return EPILORA_ERR_CUDA;
-    attr_done[fp4][dev] = smem;
-  }
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(G, 1, 1);
-  cfg.blockDim = dim3(kDecThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  void* args[] = {&p};
-  if (cudaLaunchKernelExC(&cfg, kern, args) != cudaSuccess) return EPILORA_ERR_CUDA;
-  return EPILORA_OK;
+  return a.fmt == EPILORA_FMT_NVFP4 ? launch_fused_decode_t<EPILORA_FMT_NVFP4, kDecKA>(p, a)
+                                    : launch_fused_decode_t<EPILORA_FMT_FP8_E4M3, kDecKA>(p, a);
 }
 
 }  // namespace epi
