@@ -242,6 +242,28 @@ def layer_nvfp4(x: np.ndarray, gx, wq: np.ndarray, sbw: np.ndarray, gw, A: np.nd
 
 
 # ---------------------------------------------------------------------------
+# Stored low-precision adapters (EpiLoRA, §Design › Multi-adapter kernels ›
+# K1 and K2: adapters may be stored in FP8 and dequantized in registers).
+# Reading P9: each row of A [L, r, K] (one rank over K) and of B [L, N, r] (one
+# output channel over r) is kept as E4M3 codes with one fp32 scale, quantized
+# with the arithmetic of the FP8 activation rows (readings O1, O2); the layer
+# is the plain layer on the dequantized tables.
+# ---------------------------------------------------------------------------
+def quant_adapter_fp8(T: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Adapter table [L, R, C] -> (E4M3 codes uint8 [L, R, C], fp32 scale [L, R])."""
+    T = np.asarray(T, dtype=F32)
+    L, R, C = T.shape
+    codes, scale = quant_fp8_rows(T.reshape(L * R, C))
+    return codes.reshape(L, R, C), scale.reshape(L, R)
+
+
+def dequant_adapter_fp8(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """float64 [L, R, C]: code value times its row's scale."""
+    L, R, C = codes.shape
+    return dequant_fp8_rows(codes.reshape(L * R, C), np.asarray(scale).reshape(L * R)).reshape(L, R, C)
+
+
+# ---------------------------------------------------------------------------
 # Acceptance bar for bf16 outputs (reading O13 of the stated 2e-2 bound)
 # ---------------------------------------------------------------------------
 def y_within_tolerance(y: np.ndarray, ref: np.ndarray, rel: float = 2e-2) -> tuple[bool, dict]:

@@ -316,3 +316,69 @@ def test_tolerance_helper():
     assert ok
     ok, _ = O.y_within_tolerance(ref * 1.05, ref)
     assert not ok
+
+
+# ------------------------------------------------------------------ stored FP8 adapters
+def test_adapter_fp8_integer_rows_exact():
+    """Rows whose amax is 448 get scale 1: small integers are their own codes,
+    the dequantized table equals the original, and the layer's adapter term on
+    integer activations is the exact integer product."""
+    rng = np.random.default_rng(31)
+    L, r, K, N, M = 3, 8, 64, 48, 5
+    A = rng.integers(-8, 9, (L, r, K)).astype(F32)
+    A[:, :, 0] = 448.0
+    B = rng.integers(-4, 5, (L, N, r)).astype(F32)
+    B[:, :, 1] = -448.0
+    for T in (A, B):
+        codes, sc = O.quant_adapter_fp8(T)
+        assert (sc == F32(1.0)).all()
+        assert (O.dequant_adapter_fp8(codes, sc) == T).all()
+    x = rng.integers(-3, 4, (M, K)).astype(F32)
+    idx = np.array([0, 2, -1, 1, 2], np.int32)
+    S = O.shrink(x, O.dequant_adapter_fp8(*O.quant_adapter_fp8(A)), idx, None)
+    d = O.expand(S, O.dequant_adapter_fp8(*O.quant_adapter_fp8(B)), idx, None)
+    xi, Ai, Bi = x.astype(np.int64), A.astype(np.int64), B.astype(np.int64)
+    for t in range(M):
+        if idx[t] < 0:
+            assert (d[t] == 0).all()
+            continue
+        want = Bi[idx[t]] @ (Ai[idx[t]] @ xi[t])
+        assert (d[t] == want.astype(np.float64)).all()
+
+
+def test_adapter_fp8_roundtrip_and_error_bound():
+    """Requantizing the dequantized table gives the same codes; every element
+    is within half an E4M3 step of the original (relative 2^-4 for normal
+    values, plus the subnormal step 2^-9 times the row scale)."""
+    rng = np.random.default_rng(32)
+    T = (rng.standard_normal((4, 16, 256)) / 16).astype(F32)
+    codes, sc = O.quant_adapter_fp8(T)
+    deq = O.dequant_adapter_fp8(codes, sc)
+    c2, s2 = O.quant_adapter_fp8(deq.astype(F32))
+    assert (s2 == sc).all()
+    assert ((c2 == codes) | (((c2 & 0x7F) == 0) & ((codes & 0x7F) == 0))).all()
+    err = np.abs(deq - T)
+    assert (err <= np.abs(T) / 16 + sc[:, :, None].astype(np.float64) * 2.0 ** -10).all()
+    # each row's amax element is exactly +-448 scaled
+    j = np.argmax(np.abs(T), axis=2)
+    assert ((np.take_along_axis(codes, j[:, :, None], 2) & 0x7F) == 0x7E).all()
+
+
+def test_adapter_fp8_layer_is_merged_update_of_dequantized_tables():
+    """The layer with stored adapters equals the base plus x (B^ A^)^T from the
+    explicit merged N x K matrix of the dequantized tables (tiny shapes)."""
+    p = make_projection(6, 64, 40, 3, 16, seed=33)
+    x, W = p.X.float().numpy(), p.W.float().numpy()
+    Ah = O.dequant_adapter_fp8(*O.quant_adapter_fp8(p.A.float().numpy()))
+    Bh = O.dequant_adapter_fp8(*O.quant_adapter_fp8(p.B.float().numpy()))
+    wq, sw = O.quant_fp8_rows(W)
+    ref = O.layer_fp8(x, wq, sw, Ah, Bh, p.idx.numpy(), p.mask.numpy())
+    act = O.active_tokens(p.idx.numpy(), p.mask.numpy(), 3)
+    for t in range(6):
+        merged = Bh[int(p.idx[t])] @ Ah[int(p.idx[t])] if act[t] else np.zeros((40, 64))
+        want = merged @ x[t].astype(np.float64)
+        assert np.allclose(ref["delta"][t], want, rtol=1e-12, atol=1e-15)
+    # zero adapters: codes 0, the floor scale, no adapter term
+    codes, sc = O.quant_adapter_fp8(np.zeros((2, 4, 32), F32))
+    assert ((codes & 0x7F) == 0).all() and (sc == F32(F32(1e-12) / F32(448.0))).all()
+
