@@ -158,6 +158,34 @@ __device__ __forceinline__ float dec_dot8(const uint4& xv, const uint4& av, floa
   return acc;
 }
 
+// x / s rounded to nearest float, from rs = 1/s rounded to nearest: P.
+// Markstein's correction of the reciprocal product ("Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990; also Muller et al., Handbook of Floating-Point Arithmetic, the
+// theorem on division by FMA): q0 = RN(x rs) is within one ulp of x / s, the
+// residual x - q0 s is then exact in one fma, and RN(q0 + residual rs) is the
+// correctly rounded quotient, provided the residual does not underflow.
+// Callers keep |x / s| <= 448 and s >= 2^-100, so the residual is a normal
+// number or x / s is far below the smallest E4M3 subnormal.
+__device__ __forceinline__ float div_rn_by_recip(float x, float s, float rs) {
+  const float q0 = __fmul_rn(x, rs);
+  const float e = __fmaf_rn(-q0, s, x);
+  return __fmaf_rn(e, rs, q0);
+}
+
+// E4M3 codes of 8 bf16 values divided by the row scale s (rs = 1/s rounded
+// to nearest); the IEEE division for scales below 2^-100.
+__device__ __forceinline__ uint2 quant8_e4m3_rs(const uint4& v, float s, float rs) {
+  if (s < 0x1p-100f) return quant8_e4m3(v, s);
+  float x[8];
+  unpack8(v, x);
+  uint32_t q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    q[i] = cvt_e4m3x2(div_rn_by_recip(x[2 * i], s, rs), div_rn_by_recip(x[2 * i + 1], s, rs));
+  return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
 // S[v] . B[l, n] with the B row in registers (R4 float4 chunks of S from
 // shared memory; two accumulators)
 template <int R4>
@@ -236,6 +264,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   float* red = reinterpret_cast<float*>(tmem_slot + 4);               // [4 warps][8]
   int* meta_idx = reinterpret_cast<int*>(red + 32);                   // [kDecMaxTokens] adapter or -1
   float* meta_sx = reinterpret_cast<float*>(meta_idx + kDecMaxTokens);   // FP8 activation scales
+  float* meta_rs = meta_sx + kDecMaxTokens;                           // their reciprocals
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -456,36 +485,23 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     // ---- activation quantization into the compact copy ----
     const int nch = p.K / 8;                      // 16-byte bf16 chunks per row
     if (!C::kFP4) {
-      // all M rows at once: chunk q = et + 128 j of the M x nch chunks is held
-      // in registers between the amax and the codes (M * K <= 16384)
-      constexpr int kHold = 16;
-      uint4 v[kHold];
+      // pass 1: every token's amax (a rolled loop over the M x nch chunks,
+      // loads kept in flight)
       float am[kDecMaxTokens];
 #pragma unroll
       for (int t = 0; t < kDecMaxTokens; ++t) am[t] = 0.0f;
       const int total = M * nch;
+#pragma unroll 4
+      for (int q = et; q < total; q += 128) {
+        const int t = q / nch;
+        float x[8];
+        unpack8(__ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch)), x);
+        float m = 0.0f;
 #pragma unroll
-      for (int jj = 0; jj < kHold; ++jj) {
-        const int q = et + 128 * jj;
-        if (q < total) {
-          const int t = q / nch;
-          v[jj] = __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch));
-        }
-      }
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
 #pragma unroll
-      for (int jj = 0; jj < kHold; ++jj) {
-        const int q = et + 128 * jj;
-        if (q < total) {
-          const int t = q / nch;
-          float x[8];
-          unpack8(v[jj], x);
-          float m = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
-#pragma unroll
-          for (int tt = 0; tt < kDecMaxTokens; ++tt)
-            if (tt == t) am[tt] = fmaxf(am[tt], m);
-        }
+        for (int tt = 0; tt < kDecMaxTokens; ++tt)
+          if (tt == t) am[tt] = fmaxf(am[tt], m);
       }
 #pragma unroll
       for (int tt = 0; tt < kDecMaxTokens; ++tt) {
@@ -500,19 +516,19 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
                               fmaxf(red[2 * kDecMaxTokens + et], red[3 * kDecMaxTokens + et]));
         const float sc = __fdiv_rn(fmaxf(m, kAmaxFloor), kE4M3Max);
         meta_sx[et] = sc;
+        meta_rs[et] = __frcp_rn(sc);
         if (c == 0) p.xs_out[et] = sc;
       }
       helper_sync();
-#pragma unroll
-      for (int jj = 0; jj < kHold; ++jj) {
-        const int q = et + 128 * jj;
-        if (q < total) {
-          const int t = q / nch;
-          const int k0 = (q - t * nch) * 8;
-          const uint2 code = quant8_e4m3(v[jj], meta_sx[t]);
-          *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
-          if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
-        }
+      // pass 2: the codes (the row again, from L2)
+#pragma unroll 4
+      for (int q = et; q < total; q += 128) {
+        const int t = q / nch;
+        const int k0 = (q - t * nch) * 8;
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch));
+        const uint2 code = quant8_e4m3_rs(v, meta_sx[t], meta_rs[t]);
+        *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
+        if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
       }
       // zero codes past K up to the unit boundary (finite values against the
       // weight box's zero fill)
@@ -605,9 +621,145 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         }
       }
     }
+    // ---- epilogue of one segment (T, kb0, kb1), the j-th of this CTA ----
+    const int q4 = warp & 3;                      // TMEM lane quadrant of this warp
+    const int m = q4 * 32 + lane;                 // weight row within the tile
+    bool s_ready = false;
+    uint32_t brow[kMaxRankBrow];
+    long long brow_key = -1;
+    auto epilogue_segment = [&](int T, int kb0, int kb1, int j) -> bool {
+      const int b = j & 1;
+      const int n = T * 128 + m;
+      const bool finisher = kb0 == 0;
+      float sw = 0.0f;
+      if (finisher && !C::kFP4 && n < p.N) sw = ldg_nc_f32_now(p.w_scale + n);
+      const bool ok = mbar_wait_bounded(&accf_bar[b], (j >> 1) & 1u, kWaitLimitNs);
+      if (helper_any(!ok || *abort_flag)) {
+        if (et == 0) {
+          *abort_flag = 1;
+          record_status(p.status, EPILORA_ERR_TIMEOUT);
+        }
+        return false;
+      }
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(b * 16), v);
+      tmem_ld_wait();
+      tc_fence_before();
+      helper_sync();
+      if (et == 0) mbar_arrive(&acce_bar[b]);     // the accumulator may take the next segment
+      float acc[kDecMaxTokens];
+#pragma unroll
+      for (int t = 0; t < kDecMaxTokens; ++t) acc[t] = __uint_as_float(v[t]);
+      if (!finisher) {
+        // publish this CTA's partial rows of tile T: slot c, [token][row]
+        float* dst = p.accp + static_cast<size_t>(c) * M * 128;
+#pragma unroll
+        for (int t = 0; t < kDecMaxTokens; ++t)
+          if (t < M) dst[t * 128 + m] = acc[t];
+        __threadfence();
+        helper_sync();
+        if (et == 0) st_release_u32(&p.sync[kDecSyncWords + c], 1u);
+        return true;
+      }
+      // finisher: add the partial rows of the CTAs holding the rest of tile T,
+      // in CTA order
+      if (kb1 < p.nkb) {
+        const int c_last = cta_of_unit(p, static_cast<long long>(T) * p.nkb + p.nkb - 1);
+        bool late = false;
+        for (int c2 = c + 1; c2 <= c_last; ++c2) {
+          if (et == 0) *bcast = spin_until_at_least(&p.sync[kDecSyncWords + c2], 1u) ? 1 : 0;
+          helper_sync();
+          if (*bcast == 0) {
+            late = true;
+            break;
+          }
+          const float* src = p.accp + static_cast<size_t>(c2) * M * 128;
+#pragma unroll
+          for (int t = 0; t < kDecMaxTokens; ++t)
+            if (t < M) acc[t] += __ldcg(src + t * 128 + m);
+          helper_sync();
+        }
+        if (late) {
+          if (et == 0) {
+            *abort_flag = 1;
+            record_status(p.status, EPILORA_ERR_TIMEOUT);
+          }
+          return false;
+        }
+      }
+      // S: every shrink item counted, partial sums added in part order
+      if (p.adapters && !s_ready) {
+        if (et == 0) *bcast = spin_until_at_least(&p.sync[1], static_cast<unsigned>(p.n_items)) ? 1 : 0;
+        helper_sync();
+        if (*bcast == 0) {
+          if (et == 0) {
+            *abort_flag = 1;
+            record_status(p.status, EPILORA_ERR_TIMEOUT);
+          }
+          return false;
+        }
+        const size_t part_stride = static_cast<size_t>(M) * p.s_row;
+        for (int e = et; e < M * p.s_row; e += 128) {
+          const int t = e / p.s_row;
+          float sum = 0.0f;
+          if (meta_idx[t] >= 0) {
+            sum = __ldcg(p.S + e);
+            for (int q = 1; q < p.parts; ++q) sum += __ldcg(p.S + q * part_stride + e);
+          }
+          s_stage[e] = sum;
+        }
+        helper_sync();
+        s_ready = true;
+      }
+      if (n < p.N) {
+        const int soff = p.adapters ? dec_slice_offset(p, T * 128) : 0;
+#pragma unroll
+        for (int t = 0; t < kDecMaxTokens; ++t) {
+          if (t >= M) break;
+          float y = C::kFP4 ? acc[t] * alpha : (acc[t] * meta_sx[t]) * sw;
+          const int l = meta_idx[t];
+          if (l >= 0) {
+            const long long key = static_cast<long long>(l) * p.n_tiles + T;
+            if (key != brow_key) {
+              const uint4* bsrc = reinterpret_cast<const uint4*>(p.B + (static_cast<size_t>(l) * p.N + n) * p.r);
+#pragma unroll
+              for (int cc = 0; cc < kMaxRankBrow / 4; ++cc)
+                if (cc < p.r / 8) {
+                  const uint4 bv = __ldg(bsrc + cc);
+                  brow[4 * cc] = bv.x;
+                  brow[4 * cc + 1] = bv.y;
+                  brow[4 * cc + 2] = bv.z;
+                  brow[4 * cc + 3] = bv.w;
+                }
+              brow_key = key;
+            }
+            const float4* srow = reinterpret_cast<const float4*>(s_stage + t * p.s_row + soff);
+            switch (p.r) {
+              case 16: y += dec_dot_row<4>(srow, brow); break;
+              case 32: y += dec_dot_row<8>(srow, brow); break;
+              case 64: y += dec_dot_row<16>(srow, brow); break;
+              default: y += dec_dot_row<32>(srow, brow); break;
+            }
+          }
+          p.Y[static_cast<size_t>(t) * p.ldy + n] = __float2bfloat16_rn(y);
+        }
+      }
+      return true;
+    };
+    SegWalk walk(p, c);
+    int T, kb0, kb1, j = 0;
+    bool have = walk.next(T, kb0, kb1);
+    bool alive = true;
+    // a first segment that another CTA finishes: publish its partial rows
+    // before the shrink items, so that CTA does not wait on them
+    if (have && kb0 > 0) {
+      alive = epilogue_segment(T, kb0, kb1, j++);
+      have = walk.next(T, kb0, kb1);
+    }
     // ---- shrink items: (token, 4 ranks, K slice), claimed grid-wide ----
     const int groups = p.s_row / kDecRanksPerItem;
-    if (p.adapters) {
+    if (p.adapters && alive) {
       unsigned* claim_box = reinterpret_cast<unsigned*>(bcast);
       while (true) {
         // unsigned throughout: any counter value at or past n_items ends the loop
@@ -666,134 +818,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         }
       }
     }
-    // ---- epilogue of each segment ----
-    const int q4 = warp & 3;                      // TMEM lane quadrant of this warp
-    const int m = q4 * 32 + lane;                 // weight row within the tile
-    bool s_ready = false;
-    uint32_t brow[kMaxRankBrow];
-    long long brow_key = -1;
-    SegWalk walk(p, c);
-    int T, kb0, kb1, j = 0;
-    while (walk.next(T, kb0, kb1)) {
-      const int b = j & 1;
-      const int n = T * 128 + m;
-      const bool finisher = kb0 == 0;
-      float sw = 0.0f;
-      if (finisher && !C::kFP4 && n < p.N) sw = ldg_nc_f32_now(p.w_scale + n);
-      const bool ok = mbar_wait_bounded(&accf_bar[b], (j >> 1) & 1u, kWaitLimitNs);
-      if (helper_any(!ok || *abort_flag)) {
-        if (et == 0) {
-          *abort_flag = 1;
-          record_status(p.status, EPILORA_ERR_TIMEOUT);
-        }
-        break;
-      }
-      tc_fence_after();
-      uint32_t v[16];
-      tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(b * 16), v);
-      tmem_ld_wait();
-      tc_fence_before();
-      helper_sync();
-      if (et == 0) mbar_arrive(&acce_bar[b]);     // the accumulator may take the next segment
-      float acc[kDecMaxTokens];
-#pragma unroll
-      for (int t = 0; t < kDecMaxTokens; ++t) acc[t] = __uint_as_float(v[t]);
-      if (!finisher) {
-        // publish this CTA's partial rows of tile T: slot c, [token][row]
-        float* dst = p.accp + static_cast<size_t>(c) * M * 128;
-#pragma unroll
-        for (int t = 0; t < kDecMaxTokens; ++t)
-          if (t < M) dst[t * 128 + m] = acc[t];
-        __threadfence();
-        helper_sync();
-        if (et == 0) st_release_u32(&p.sync[kDecSyncWords + c], 1u);
-        ++j;
-        continue;
-      }
-      // finisher: add the partial rows of the CTAs holding the rest of tile T,
-      // in CTA order
-      if (kb1 < p.nkb) {
-        const int c_last = cta_of_unit(p, static_cast<long long>(T) * p.nkb + p.nkb - 1);
-        bool late = false;
-        for (int c2 = c + 1; c2 <= c_last; ++c2) {
-          if (et == 0) *bcast = spin_until_at_least(&p.sync[kDecSyncWords + c2], 1u) ? 1 : 0;
-          helper_sync();
-          if (*bcast == 0) {
-            late = true;
-            break;
-          }
-          const float* src = p.accp + static_cast<size_t>(c2) * M * 128;
-#pragma unroll
-          for (int t = 0; t < kDecMaxTokens; ++t)
-            if (t < M) acc[t] += __ldcg(src + t * 128 + m);
-          helper_sync();
-        }
-        if (late) {
-          if (et == 0) {
-            *abort_flag = 1;
-            record_status(p.status, EPILORA_ERR_TIMEOUT);
-          }
-          break;
-        }
-      }
-      // S: every shrink item counted, partial sums added in part order
-      if (p.adapters && !s_ready) {
-        if (et == 0) *bcast = spin_until_at_least(&p.sync[1], static_cast<unsigned>(p.n_items)) ? 1 : 0;
-        helper_sync();
-        if (*bcast == 0) {
-          if (et == 0) {
-            *abort_flag = 1;
-            record_status(p.status, EPILORA_ERR_TIMEOUT);
-          }
-          break;
-        }
-        const size_t part_stride = static_cast<size_t>(M) * p.s_row;
-        for (int e = et; e < M * p.s_row; e += 128) {
-          const int t = e / p.s_row;
-          float sum = 0.0f;
-          if (meta_idx[t] >= 0) {
-            sum = __ldcg(p.S + e);
-            for (int q = 1; q < p.parts; ++q) sum += __ldcg(p.S + q * part_stride + e);
-          }
-          s_stage[e] = sum;
-        }
-        helper_sync();
-        s_ready = true;
-      }
-      if (n < p.N) {
-        const int soff = p.adapters ? dec_slice_offset(p, T * 128) : 0;
-#pragma unroll
-        for (int t = 0; t < kDecMaxTokens; ++t) {
-          if (t >= M) break;
-          float y = C::kFP4 ? acc[t] * alpha : (acc[t] * meta_sx[t]) * sw;
-          const int l = meta_idx[t];
-          if (l >= 0) {
-            const long long key = static_cast<long long>(l) * p.n_tiles + T;
-            if (key != brow_key) {
-              const uint4* bsrc = reinterpret_cast<const uint4*>(p.B + (static_cast<size_t>(l) * p.N + n) * p.r);
-#pragma unroll
-              for (int cc = 0; cc < kMaxRankBrow / 4; ++cc)
-                if (cc < p.r / 8) {
-                  const uint4 bv = __ldg(bsrc + cc);
-                  brow[4 * cc] = bv.x;
-                  brow[4 * cc + 1] = bv.y;
-                  brow[4 * cc + 2] = bv.z;
-                  brow[4 * cc + 3] = bv.w;
-                }
-              brow_key = key;
-            }
-            const float4* srow = reinterpret_cast<const float4*>(s_stage + t * p.s_row + soff);
-            switch (p.r) {
-              case 16: y += dec_dot_row<4>(srow, brow); break;
-              case 32: y += dec_dot_row<8>(srow, brow); break;
-              case 64: y += dec_dot_row<16>(srow, brow); break;
-              default: y += dec_dot_row<32>(srow, brow); break;
-            }
-          }
-          p.Y[static_cast<size_t>(t) * p.ldy + n] = __float2bfloat16_rn(y);
-        }
-      }
-      ++j;
+    while (alive && have) {
+      alive = epilogue_segment(T, kb0, kb1, j++);
+      have = walk.next(T, kb0, kb1);
     }
   }
 

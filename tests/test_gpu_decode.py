@@ -195,3 +195,43 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable():
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert torch.equal(Y, ref)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_single_kernel_fp8_codes_bit_exact_over_magnitudes(seed):
+    """The single kernel's FP8 activation codes and scales against the
+    oracle's IEEE-division quantizer, bit for bit, on rows whose values span
+    many binades (log-uniform magnitudes, random signs, exact zeros, values
+    that land on E4M3 rounding ties), including a row whose scale is below
+    2^-100."""
+    rng = np.random.default_rng(100 + seed)
+    M, K, N = 4, 4096, 256
+    mag = np.exp2(rng.uniform(-30, 12, (M, K)))
+    x = (np.sign(rng.standard_normal((M, K))) * mag).astype(np.float32)
+    x[1] *= np.float32(1e-3)
+    x[2, ::7] = 0.0
+    # row 3: tiny values (amax ~ 1e-33: scale < 2^-100)
+    x[3] = (rng.standard_normal(K) * 1e-34).astype(np.float32)
+    X = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    xr = X.float().cpu().numpy()
+    # ties: half-way values between E4M3 neighbours after the scale
+    amax0 = float(np.abs(xr[0]).max())
+    s0 = np.float32(np.float32(amax0) / np.float32(448.0))
+    for j, code_mid in enumerate((1.0625, 2.125, 9.0 / 8 * 3, 0.5 + 1.0 / 32)):
+        v = torch.tensor([code_mid * float(s0)], dtype=torch.float32).to(torch.bfloat16)
+        X[0, 10 + j] = v.item()
+    xr = X.float().cpu().numpy()
+    assert E.epilora_layer_forward_kernels(FP8, M, K) == 1
+    W = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+    w = T.quantize_weight(W, FP8)
+    ws = T.LayerWorkspace("cuda")
+    buf = ws.get(FP8, M, K, 0)
+    T.layer_forward(X, w, workspace=ws)
+    torch.cuda.synchronize()
+    codes, sc = O.quant_fp8_rows(xr)
+    off = SYNC_BYTES
+    r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    got = npu8(buf[off:off + M * K].view(M, K))
+    got_s = np32(buf[off + r256(M * K):off + r256(M * K) + 4 * M].view(torch.float32))
+    assert (got_s == sc).all()
+    assert same_codes_e4m3(got, codes).all(), np.argwhere(~same_codes_e4m3(got, codes))[:5]
