@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   uint64_t* accf_bar = empty_bar + kDecMaxStages;    // [2] accumulator complete
   uint64_t* acce_bar = accf_bar + 2;                 // [2] accumulator read out
   uint64_t* xrdy_bar = acce_bar + 2;                 // compact activations written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xrdy_bar + 1);
+  uint64_t* pref_bar = xrdy_bar + 1;                 // the helpers' L2 hints are issued
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pref_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bcast = reinterpret_cast<int*>(tmem_slot + 2);                 // helper broadcast word
   float* red = reinterpret_cast<float*>(tmem_slot + 4);               // [4 warps][8]
@@ -280,6 +281,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       mbar_init(&acce_bar[b], 1);
     }
     mbar_init(xrdy_bar, 1);
+    mbar_init(pref_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&p.tmW);
@@ -297,6 +299,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   if (warp == 0) {
     // ===== TMA producer: the run's weight units, in order =====
     if (lane == 0) {
+      // behind the helpers' L2 hints (they never wait before issuing them)
+      if (!mbar_wait_bounded(pref_bar, 0, kWaitLimitNs)) {
+        *abort_flag = 1;
+        record_status(p.status, EPILORA_ERR_TIMEOUT);
+      }
       uint32_t issued_mask = 0, parity_mask = 0;
       long long it = 0;
       const long long u_begin = (p.U * c) / p.G, u_end = (p.U * (c + 1)) / p.G;
@@ -450,8 +457,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     // ===== helpers =====
     const int et = threadIdx.x - 64;
     const int hw = warp - 2;                      // helper warp 0..3
-    // hints before the wait: the activation rows and this CTA's share of the
-    // adapters' A rows into L2 (the index read here may still change)
+    // hints before the wait, issued ahead of the weight ring (the producer
+    // waits for them): the activation rows, this CTA's share of the adapters'
+    // A rows and the B slices of the tiles it finishes go to L2 first, so the
+    // loads on the critical path after the wait do not queue behind the
+    // weight stream (the index read here may still change: hints only)
     if (et == 0) {
       for (int t = 0; t < M; ++t)
         prefetch_l2_bulk(p.X + static_cast<size_t>(t) * p.ldx, static_cast<uint32_t>(p.K * 2));
@@ -459,15 +469,26 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         const size_t abytes = static_cast<size_t>(p.s_row) * p.K * 2;
         const size_t share = ((abytes + p.G - 1) / p.G + 255) / 256 * 256;
         const size_t lo = share * c;
-        for (int t = 0; t < M && lo < abytes; ++t) {
+        int prev = -1;
+        for (int t = 0; t < M; ++t) {
           int l;
           asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(l) : "l"(p.idx + t));
-          if (l < 0 || l >= p.L) continue;
-          const size_t n = min(share, abytes - lo);
-          prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.A) + static_cast<size_t>(l) * abytes + lo,
-                           static_cast<uint32_t>(n));
+          if (l < 0 || l >= p.L || l == prev) continue;
+          prev = l;
+          if (lo < abytes)
+            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.A) + static_cast<size_t>(l) * abytes + lo,
+                             static_cast<uint32_t>(min(share, abytes - lo)));
+          SegWalk w2(p, c);
+          int T, kb0, kb1;
+          while (w2.next(T, kb0, kb1)) {
+            if (kb0 != 0) continue;
+            const int rows = min(128, p.N - T * 128);
+            prefetch_l2_bulk(p.B + (static_cast<size_t>(l) * p.N + T * 128) * p.r,
+                             static_cast<uint32_t>(rows * p.r * 2));
+          }
         }
       }
+      mbar_arrive(pref_bar);
     }
     // the preceding kernel on the stream has completed: X, idx, mask and the
     // workspace are valid from here on
@@ -604,23 +625,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     fence_proxy_async_smem();
     helper_sync();
     if (et == 0) mbar_arrive(xrdy_bar);           // the MMA warp may start
-    // ---- this CTA's finisher tiles: B slices of their adapters into L2 ----
-    if (p.adapters && et == 0) {
-      SegWalk w2(p, c);
-      int T, kb0, kb1;
-      while (w2.next(T, kb0, kb1)) {
-        if (kb0 != 0) continue;
-        const int rows = min(128, p.N - T * 128);
-        int prev = -1;
-        for (int t = 0; t < M; ++t) {
-          const int l = meta_idx[t];
-          if (l < 0 || l == prev) continue;
-          prefetch_l2_bulk(p.B + (static_cast<size_t>(l) * p.N + T * 128) * p.r,
-                           static_cast<uint32_t>(rows * p.r * 2));
-          prev = l;
-        }
-      }
-    }
     // ---- epilogue of one segment (T, kb0, kb1), the j-th of this CTA ----
     const int q4 = warp & 3;                      // TMEM lane quadrant of this warp
     const int m = q4 * 32 + lane;                 // weight row within the tile
