@@ -174,9 +174,9 @@ __device__ __forceinline__ float div_rn_by_recip(float x, float s, float rs) {
 }
 
 // E4M3 codes of 8 bf16 values divided by the row scale s (rs = 1/s rounded
-// to nearest); the IEEE division for scales below 2^-100.
+// to nearest); for scales of at least 2^-100 (callers take the IEEE division
+// below that).
 __device__ __forceinline__ uint2 quant8_e4m3_rs(const uint4& v, float s, float rs) {
-  if (s < 0x1p-100f) return quant8_e4m3(v, s);
   float x[8];
   unpack8(v, x);
   uint32_t q[4];
@@ -493,36 +493,53 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     // the preceding kernel on the stream has completed: X, idx, mask and the
     // workspace are valid from here on
     pdl_wait_primary();
-    if (et < M) {
-      int l = -1;
-      if (p.adapters) {
-        const int li = p.idx[et];
-        if (li >= p.L) record_status(p.status, EPILORA_ERR_INVALID_ARG);
-        l = (li >= 0 && li < p.L && (p.mask == nullptr || p.mask[et] != 0)) ? li : -1;
-      }
-      meta_idx[et] = l;
+    // Every load below that does not depend on another is issued before any
+    // is used: on this two-die GPU each dependent round trip to L2 costs about
+    // a microsecond, and this path has a handful of them.
+    int li = -1, mk = 1;
+    if (et < M && p.adapters) {
+      li = p.idx[et];
+      if (p.mask != nullptr) mk = p.mask[et];
     }
     float alpha = 1.0f;
-    // ---- activation quantization into the compact copy ----
     const int nch = p.K / 8;                      // 16-byte bf16 chunks per row
+    const int total = M * nch;
+    constexpr int kHold = 16;                     // FP8: M x nch <= 16 x 128 chunks held in registers
+    uint4 xv[kHold];
     if (!C::kFP4) {
-      // pass 1: every token's amax (a rolled loop over the M x nch chunks,
-      // loads kept in flight)
+#pragma unroll
+      for (int jj = 0; jj < kHold; ++jj) {
+        const int q = et + 128 * jj;
+        if (q < total) {
+          const int t = q / nch;
+          xv[jj] = __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch));
+        }
+      }
+    }
+    if (et < M) {
+      if (li >= p.L) record_status(p.status, EPILORA_ERR_INVALID_ARG);
+      meta_idx[et] = (li >= 0 && li < p.L && mk != 0) ? li : -1;
+    }
+    // ---- activation quantization into the compact copy ----
+    if (!C::kFP4) {
+      // the amax of every token, from the chunks held in registers
       float am[kDecMaxTokens];
 #pragma unroll
       for (int t = 0; t < kDecMaxTokens; ++t) am[t] = 0.0f;
-      const int total = M * nch;
-#pragma unroll 4
-      for (int q = et; q < total; q += 128) {
-        const int t = q / nch;
-        float x[8];
-        unpack8(__ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch)), x);
-        float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+      for (int jj = 0; jj < kHold; ++jj) {
+        const int q = et + 128 * jj;
+        if (q < total) {
+          const int t = q / nch;
+          float x[8];
+          unpack8(xv[jj], x);
+          float m = 0.0f;
 #pragma unroll
-        for (int tt = 0; tt < kDecMaxTokens; ++tt)
-          if (tt == t) am[tt] = fmaxf(am[tt], m);
+          for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+#pragma unroll
+          for (int tt = 0; tt < kDecMaxTokens; ++tt)
+            if (tt == t) am[tt] = fmaxf(am[tt], m);
+        }
       }
 #pragma unroll
       for (int tt = 0; tt < kDecMaxTokens; ++tt) {
@@ -541,15 +558,36 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         if (c == 0) p.xs_out[et] = sc;
       }
       helper_sync();
-      // pass 2: the codes (the row again, from L2)
-#pragma unroll 4
-      for (int q = et; q < total; q += 128) {
-        const int t = q / nch;
-        const int k0 = (q - t * nch) * 8;
-        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch));
-        const uint2 code = quant8_e4m3_rs(v, meta_sx[t], meta_rs[t]);
-        *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
-        if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+      // the codes, from the same registers (rows whose scale is below 2^-100
+      // take the IEEE division in a loop of their own below)
+      bool slow = false;
+#pragma unroll
+      for (int jj = 0; jj < kHold; ++jj) {
+        const int q = et + 128 * jj;
+        if (q < total) {
+          const int t = q / nch;
+          const int k0 = (q - t * nch) * 8;
+          const float sc = meta_sx[t];
+          if (sc < 0x1p-100f) {
+            slow = true;
+            continue;
+          }
+          const uint2 code = quant8_e4m3_rs(xv[jj], sc, meta_rs[t]);
+          *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
+          if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+        }
+      }
+      if (slow) {
+#pragma unroll 1
+        for (int q = et; q < total; q += 128) {
+          const int t = q / nch;
+          if (meta_sx[t] >= 0x1p-100f) continue;
+          const int k0 = (q - t * nch) * 8;
+          const uint2 code = quant8_e4m3(
+              __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch)), meta_sx[t]);
+          *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
+          if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+        }
       }
       // zero codes past K up to the unit boundary (finite values against the
       // weight box's zero fill)
@@ -631,20 +669,46 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     bool s_ready = false;
     uint32_t brow[kMaxRankBrow];
     long long brow_key = -1;
+    auto load_brow = [&](int l, int T, int n) {
+      const uint4* bsrc = reinterpret_cast<const uint4*>(p.B + (static_cast<size_t>(l) * p.N + n) * p.r);
+#pragma unroll
+      for (int cc = 0; cc < kMaxRankBrow / 4; ++cc)
+        if (cc < p.r / 8) {
+          const uint4 bv = ldg_nc_v4_now(bsrc + cc);
+          brow[4 * cc] = bv.x;
+          brow[4 * cc + 1] = bv.y;
+          brow[4 * cc + 2] = bv.z;
+          brow[4 * cc + 3] = bv.w;
+        }
+      brow_key = static_cast<long long>(l) * p.n_tiles + T;
+    };
+    auto fail = [&]() {
+      if (et == 0) {
+        *abort_flag = 1;
+        record_status(p.status, EPILORA_ERR_TIMEOUT);
+      }
+      return false;
+    };
     auto epilogue_segment = [&](int T, int kb0, int kb1, int j) -> bool {
       const int b = j & 1;
       const int n = T * 128 + m;
       const bool finisher = kb0 == 0;
       float sw = 0.0f;
-      if (finisher && !C::kFP4 && n < p.N) sw = ldg_nc_f32_now(p.w_scale + n);
-      const bool ok = mbar_wait_bounded(&accf_bar[b], (j >> 1) & 1u, kWaitLimitNs);
-      if (helper_any(!ok || *abort_flag)) {
-        if (et == 0) {
-          *abort_flag = 1;
-          record_status(p.status, EPILORA_ERR_TIMEOUT);
+      if (finisher && n < p.N) {
+        // loads of this row's scale and B row go out before the accumulator
+        // is ready (the B row of the first token that carries an adapter)
+        if (!C::kFP4) sw = ldg_nc_f32_now(p.w_scale + n);
+        if (p.adapters) {
+          for (int t = 0; t < M; ++t) {
+            const int l = meta_idx[t];
+            if (l < 0) continue;
+            if (static_cast<long long>(l) * p.n_tiles + T != brow_key) load_brow(l, T, n);
+            break;
+          }
         }
-        return false;
       }
+      const bool ok = mbar_wait_bounded(&accf_bar[b], (j >> 1) & 1u, kWaitLimitNs);
+      if (helper_any(!ok || *abort_flag)) return fail();
       tc_fence_after();
       uint32_t v[16];
       tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(b * 16), v);
@@ -666,43 +730,21 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         if (et == 0) st_release_u32(&p.sync[kDecSyncWords + c], 1u);
         return true;
       }
-      // finisher: add the partial rows of the CTAs holding the rest of tile T,
-      // in CTA order
-      if (kb1 < p.nkb) {
-        const int c_last = cta_of_unit(p, static_cast<long long>(T) * p.nkb + p.nkb - 1);
-        bool late = false;
-        for (int c2 = c + 1; c2 <= c_last; ++c2) {
-          if (et == 0) *bcast = spin_until_at_least(&p.sync[kDecSyncWords + c2], 1u) ? 1 : 0;
-          helper_sync();
-          if (*bcast == 0) {
-            late = true;
-            break;
-          }
-          const float* src = p.accp + static_cast<size_t>(c2) * M * 128;
-#pragma unroll
-          for (int t = 0; t < kDecMaxTokens; ++t)
-            if (t < M) acc[t] += __ldcg(src + t * 128 + m);
-          helper_sync();
-        }
-        if (late) {
-          if (et == 0) {
-            *abort_flag = 1;
-            record_status(p.status, EPILORA_ERR_TIMEOUT);
-          }
-          return false;
-        }
+      // finisher: one thread waits (bounded) until the CTAs holding the rest
+      // of tile T have published their partial rows and, the first time,
+      // until every shrink item is counted; then all loads go out together
+      const int c_last = kb1 < p.nkb ? cta_of_unit(p, static_cast<long long>(T) * p.nkb + p.nkb - 1) : c;
+      const bool need_s = p.adapters && !s_ready;
+      if (et == 0) {
+        bool all = true;
+        for (int c2 = c + 1; c2 <= c_last && all; ++c2) all = spin_until_at_least(&p.sync[kDecSyncWords + c2], 1u);
+        if (all && need_s) all = spin_until_at_least(&p.sync[1], static_cast<unsigned>(p.n_items));
+        *bcast = all ? 1 : 0;
       }
-      // S: every shrink item counted, partial sums added in part order
-      if (p.adapters && !s_ready) {
-        if (et == 0) *bcast = spin_until_at_least(&p.sync[1], static_cast<unsigned>(p.n_items)) ? 1 : 0;
-        helper_sync();
-        if (*bcast == 0) {
-          if (et == 0) {
-            *abort_flag = 1;
-            record_status(p.status, EPILORA_ERR_TIMEOUT);
-          }
-          return false;
-        }
+      helper_sync();
+      if (*bcast == 0) return fail();
+      if (need_s) {
+        // S: the partial sums over K slices added in part order
         const size_t part_stride = static_cast<size_t>(M) * p.s_row;
         for (int e = et; e < M * p.s_row; e += 128) {
           const int t = e / p.s_row;
@@ -713,9 +755,16 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           }
           s_stage[e] = sum;
         }
-        helper_sync();
-        s_ready = true;
       }
+      // partial rows of the other CTAs, added in CTA order
+      for (int c2 = c + 1; c2 <= c_last; ++c2) {
+        const float* src = p.accp + static_cast<size_t>(c2) * M * 128;
+#pragma unroll
+        for (int t = 0; t < kDecMaxTokens; ++t)
+          if (t < M) acc[t] += __ldcg(src + t * 128 + m);
+      }
+      helper_sync();                              // S staged; bcast free again
+      s_ready = s_ready || need_s;
       if (n < p.N) {
         const int soff = p.adapters ? dec_slice_offset(p, T * 128) : 0;
 #pragma unroll
@@ -724,20 +773,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           float y = C::kFP4 ? acc[t] * alpha : (acc[t] * meta_sx[t]) * sw;
           const int l = meta_idx[t];
           if (l >= 0) {
-            const long long key = static_cast<long long>(l) * p.n_tiles + T;
-            if (key != brow_key) {
-              const uint4* bsrc = reinterpret_cast<const uint4*>(p.B + (static_cast<size_t>(l) * p.N + n) * p.r);
-#pragma unroll
-              for (int cc = 0; cc < kMaxRankBrow / 4; ++cc)
-                if (cc < p.r / 8) {
-                  const uint4 bv = __ldg(bsrc + cc);
-                  brow[4 * cc] = bv.x;
-                  brow[4 * cc + 1] = bv.y;
-                  brow[4 * cc + 2] = bv.z;
-                  brow[4 * cc + 3] = bv.w;
-                }
-              brow_key = key;
-            }
+            if (static_cast<long long>(l) * p.n_tiles + T != brow_key) load_brow(l, T, n);
             const float4* srow = reinterpret_cast<const float4*>(s_stage + t * p.s_row + soff);
             switch (p.r) {
               case 16: y += dec_dot_row<4>(srow, brow); break;
@@ -761,17 +797,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       alive = epilogue_segment(T, kb0, kb1, j++);
       have = walk.next(T, kb0, kb1);
     }
-    // ---- shrink items: (token, 4 ranks, K slice), claimed grid-wide ----
+    // ---- shrink items: (token, 4 ranks, K slice). Item c is this CTA's;
+    // items from G on are claimed from the counter at the start of the
+    // workspace (unsigned throughout: any counter value at or past the end
+    // stops the claims) ----
     const int groups = p.s_row / kDecRanksPerItem;
     if (p.adapters && alive) {
       unsigned* claim_box = reinterpret_cast<unsigned*>(bcast);
-      while (true) {
-        // unsigned throughout: any counter value at or past n_items ends the loop
-        if (et == 0) *claim_box = atomicAdd(&p.sync[0], 1u);
-        helper_sync();
-        const unsigned claimed = *claim_box;
-        helper_sync();
-        if (claimed >= static_cast<unsigned>(p.n_items)) break;
+      const unsigned n_items = static_cast<unsigned>(p.n_items);
+      const unsigned G = static_cast<unsigned>(p.G);
+      unsigned claimed = static_cast<unsigned>(c);
+      while (claimed < n_items) {
         const int item = static_cast<int>(claimed);
         const int t = item / (groups * p.parts);
         const int rem = item - t * groups * p.parts;
@@ -784,24 +820,24 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           const uint4* xr = reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx);
           const uint4* ar =
               reinterpret_cast<const uint4*>(p.A + (static_cast<size_t>(l) * p.s_row + j0) * static_cast<size_t>(p.K));
-          float acc[kDecRanksPerItem];
+          float accs[kDecRanksPerItem];
 #pragma unroll
-          for (int jr = 0; jr < kDecRanksPerItem; ++jr) acc[jr] = 0.0f;
+          for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = 0.0f;
 #pragma unroll 2
           for (int ch = c0 + et; ch < c1; ch += 128) {
-            const uint4 xv = __ldcg(xr + ch);
+            const uint4 xw = __ldcg(xr + ch);
             uint4 av[kDecRanksPerItem];
 #pragma unroll
             for (int jr = 0; jr < kDecRanksPerItem; ++jr) av[jr] = __ldg(ar + static_cast<size_t>(jr) * nch + ch);
 #pragma unroll
-            for (int jr = 0; jr < kDecRanksPerItem; ++jr) acc[jr] = dec_dot8(xv, av[jr], acc[jr]);
+            for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = dec_dot8(xw, av[jr], accs[jr]);
           }
 #pragma unroll
           for (int jr = 0; jr < kDecRanksPerItem; ++jr) {
-            float s = acc[jr];
+            float sv = accs[jr];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) red[hw * kDecRanksPerItem + jr] = s;
+            for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
+            if (lane == 0) red[hw * kDecRanksPerItem + jr] = sv;
           }
           helper_sync();
           if (et == 0) {
@@ -820,6 +856,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           __threadfence();
           atomicAdd(&p.sync[1], 1u);
         }
+        // the next item: past the statically assigned ones, from the counter
+        if (n_items <= G) break;
+        if (et == 0) *claim_box = atomicAdd(&p.sync[0], 1u);
+        helper_sync();
+        const unsigned k = *claim_box;
+        helper_sync();
+        claimed = k < n_items - G ? G + k : n_items;
       }
     }
     while (alive && have) {

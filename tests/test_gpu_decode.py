@@ -171,13 +171,15 @@ def test_single_kernel_chain_shares_workspace(fmt):
 
 
 def test_bounded_wait_runs_out_and_the_context_stays_usable():
-    """A wait that runs out, made on the host: the shrink-item counter at the
-    start of the workspace is set past every item before the call, so no
-    thread block claims any and the kernel's bounded wait for S gives up (about
-    a second). The call returns EPILORA_ERR_TIMEOUT in the status word, leaves
-    the counters zero again, and the next call on the same stream and
-    workspace is correct."""
-    M, K, N, L, r = 1, 2048, 1024, 1, 16
+    """A wait that runs out, made on the host: 2 tokens at rank 128 over 8 K
+    slices make 512 shrink items, more than thread blocks, so those past the
+    grid are claimed from the counter at the start of the workspace; that
+    counter is set past every item before the call, so they are never done and
+    the kernel's bounded wait for S gives up (about a second). The call
+    returns EPILORA_ERR_TIMEOUT in the status word, leaves the counters zero
+    again, and the next call on the same stream and workspace is correct."""
+    M, K, N, L, r = 2, 8192, 1024, 2, 128
+    assert E.epilora_layer_forward_kernels(FP8, M, K) == 1
     p = make_projection(M, K, N, L, r, seed=5, device="cuda")
     w = T.quantize_weight(p.W, FP8)
     ref = T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask)
