@@ -252,7 +252,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   uint8_t* xsf = xc + M * p.kb_pad + 128;
   const int xsf_bytes = C::kFP4 ? (M * (p.kb_pad / 32) * 16 + 512 + 127) / 128 * 128 : 0;
   float* s_stage = reinterpret_cast<float*>(xsf + xsf_bytes);
-  uint8_t* misc = reinterpret_cast<uint8_t*>(s_stage) + (M * p.s_row * 4 + 127) / 128 * 128;
+  float* yacc = s_stage + (M * p.s_row + 31) / 32 * 32;             // [M][128] a finisher's row sums
+  uint8_t* misc = reinterpret_cast<uint8_t*>(yacc + M * 128);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(misc);
   uint64_t* empty_bar = full_bar + kDecMaxStages;
   uint64_t* accf_bar = empty_bar + kDecMaxStages;    // [2] accumulator complete
@@ -504,7 +505,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     float alpha = 1.0f;
     const int nch = p.K / 8;                      // 16-byte bf16 chunks per row
     const int total = M * nch;
-    constexpr int kHold = 16;                     // FP8: M x nch <= 16 x 128 chunks held in registers
+    // FP8: a thread's first kHold chunks (all of them for one token up to
+    // K = 4096) stay in registers between the amax and the codes; the rest
+    // are read again from L2. Short loops: this code runs once per call, so
+    // its instruction fetch is on the critical path.
+    constexpr int kHold = 4;
     uint4 xv[kHold];
     if (!C::kFP4) {
 #pragma unroll
@@ -522,72 +527,68 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     }
     // ---- activation quantization into the compact copy ----
     if (!C::kFP4) {
-      // the amax of every token, from the chunks held in registers
       float am[kDecMaxTokens];
 #pragma unroll
       for (int t = 0; t < kDecMaxTokens; ++t) am[t] = 0.0f;
+      auto amax_chunk = [&](const uint4& v, int t) {
+        float x[8];
+        unpack8(v, x);
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(x[i]));
+#pragma unroll
+        for (int tt = 0; tt < kDecMaxTokens; ++tt)
+          if (tt == t) am[tt] = fmaxf(am[tt], mx);
+      };
 #pragma unroll
       for (int jj = 0; jj < kHold; ++jj) {
         const int q = et + 128 * jj;
-        if (q < total) {
-          const int t = q / nch;
-          float x[8];
-          unpack8(xv[jj], x);
-          float m = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
-#pragma unroll
-          for (int tt = 0; tt < kDecMaxTokens; ++tt)
-            if (tt == t) am[tt] = fmaxf(am[tt], m);
-        }
+        if (q < total) amax_chunk(xv[jj], q / nch);
+      }
+#pragma unroll 1
+      for (int q = et + 128 * kHold; q < total; q += 128) {
+        const int t = q / nch;
+        amax_chunk(__ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch)), t);
       }
 #pragma unroll
       for (int tt = 0; tt < kDecMaxTokens; ++tt) {
-        float m = am[tt];
+        float mx = am[tt];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) red[hw * kDecMaxTokens + tt] = m;
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) red[hw * kDecMaxTokens + tt] = mx;
       }
       helper_sync();
       if (et < M) {
-        const float m = fmaxf(fmaxf(red[et], red[kDecMaxTokens + et]),
-                              fmaxf(red[2 * kDecMaxTokens + et], red[3 * kDecMaxTokens + et]));
-        const float sc = __fdiv_rn(fmaxf(m, kAmaxFloor), kE4M3Max);
+        const float mx = fmaxf(fmaxf(red[et], red[kDecMaxTokens + et]),
+                               fmaxf(red[2 * kDecMaxTokens + et], red[3 * kDecMaxTokens + et]));
+        const float sc = __fdiv_rn(fmaxf(mx, kAmaxFloor), kE4M3Max);
         meta_sx[et] = sc;
         meta_rs[et] = __frcp_rn(sc);
         if (c == 0) p.xs_out[et] = sc;
       }
       helper_sync();
-      // the codes, from the same registers (rows whose scale is below 2^-100
-      // take the IEEE division in a loop of their own below)
-      bool slow = false;
+      // the codes: the held chunks of rows whose scale is at least 2^-100
+      // from registers; every other chunk in one short loop (read again from
+      // L2; the IEEE division for rows whose scale is below 2^-100)
+      auto store_code = [&](uint2 code, int t, int k0) {
+        *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
+        if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+      };
 #pragma unroll
       for (int jj = 0; jj < kHold; ++jj) {
         const int q = et + 128 * jj;
         if (q < total) {
           const int t = q / nch;
-          const int k0 = (q - t * nch) * 8;
-          const float sc = meta_sx[t];
-          if (sc < 0x1p-100f) {
-            slow = true;
-            continue;
-          }
-          const uint2 code = quant8_e4m3_rs(xv[jj], sc, meta_rs[t]);
-          *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
-          if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+          if (meta_sx[t] >= 0x1p-100f) store_code(quant8_e4m3_rs(xv[jj], meta_sx[t], meta_rs[t]), t, (q - t * nch) * 8);
         }
       }
-      if (slow) {
 #pragma unroll 1
-        for (int q = et; q < total; q += 128) {
-          const int t = q / nch;
-          if (meta_sx[t] >= 0x1p-100f) continue;
-          const int k0 = (q - t * nch) * 8;
-          const uint2 code = quant8_e4m3(
-              __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch)), meta_sx[t]);
-          *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
-          if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
-        }
+      for (int q = et; q < total; q += 128) {
+        const int t = q / nch;
+        const float sc = meta_sx[t];
+        if (q < et + 128 * kHold && sc >= 0x1p-100f) continue;
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch));
+        store_code(sc >= 0x1p-100f ? quant8_e4m3_rs(v, sc, meta_rs[t]) : quant8_e4m3(v, sc), t, (q - t * nch) * 8);
       }
       // zero codes past K up to the unit boundary (finite values against the
       // weight box's zero fill)
@@ -605,7 +606,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       alpha = 1.0f / (g * *p.w_gs);
       const int nb = p.K / kNvfp4Block;
       const int total = M * nb;
-#pragma unroll 4
+#pragma unroll 2
       for (int q = et; q < total; q += 128) {
         const int t = q / nb;
         const int b = q - t * nb;
@@ -767,10 +768,14 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       s_ready = s_ready || need_s;
       if (n < p.N) {
         const int soff = p.adapters ? dec_slice_offset(p, T * 128) : 0;
+        // a rolled loop over the tokens (this thread's sums through shared
+        // memory): one copy of the adapter dot in the code
 #pragma unroll
-        for (int t = 0; t < kDecMaxTokens; ++t) {
-          if (t >= M) break;
-          float y = C::kFP4 ? acc[t] * alpha : (acc[t] * meta_sx[t]) * sw;
+        for (int t = 0; t < kDecMaxTokens; ++t)
+          if (t < M) yacc[t * 128 + m] = acc[t];
+#pragma unroll 1
+        for (int t = 0; t < M; ++t) {
+          float y = C::kFP4 ? yacc[t * 128 + m] * alpha : (yacc[t * 128 + m] * meta_sx[t]) * sw;
           const int l = meta_idx[t];
           if (l >= 0) {
             if (static_cast<long long>(l) * p.n_tiles + T != brow_key) load_brow(l, T, n);
@@ -787,82 +792,82 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       }
       return true;
     };
-    SegWalk walk(p, c);
-    int T, kb0, kb1, j = 0;
-    bool have = walk.next(T, kb0, kb1);
-    bool alive = true;
-    // a first segment that another CTA finishes: publish its partial rows
-    // before the shrink items, so that CTA does not wait on them
-    if (have && kb0 > 0) {
-      alive = epilogue_segment(T, kb0, kb1, j++);
-      have = walk.next(T, kb0, kb1);
-    }
     // ---- shrink items: (token, 4 ranks, K slice). Item c is this CTA's;
     // items from G on are claimed from the counter at the start of the
     // workspace (unsigned throughout: any counter value at or past the end
     // stops the claims) ----
     const int groups = p.s_row / kDecRanksPerItem;
-    if (p.adapters && alive) {
-      unsigned* claim_box = reinterpret_cast<unsigned*>(bcast);
-      const unsigned n_items = static_cast<unsigned>(p.n_items);
-      const unsigned G = static_cast<unsigned>(p.G);
-      unsigned claimed = static_cast<unsigned>(c);
-      while (claimed < n_items) {
-        const int item = static_cast<int>(claimed);
-        const int t = item / (groups * p.parts);
-        const int rem = item - t * groups * p.parts;
-        const int part = rem / groups;
-        const int j0 = (rem - part * groups) * kDecRanksPerItem;
-        const int l = meta_idx[t];
-        if (l >= 0) {
-          const int c0 = part * p.kslice / 8;
-          const int c1 = min(p.K, (part + 1) * p.kslice) / 8;
-          const uint4* xr = reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx);
-          const uint4* ar =
-              reinterpret_cast<const uint4*>(p.A + (static_cast<size_t>(l) * p.s_row + j0) * static_cast<size_t>(p.K));
-          float accs[kDecRanksPerItem];
+    auto do_item = [&](int item) {
+      const int t = item / (groups * p.parts);
+      const int rem = item - t * groups * p.parts;
+      const int part = rem / groups;
+      const int j0 = (rem - part * groups) * kDecRanksPerItem;
+      const int l = meta_idx[t];
+      if (l >= 0) {
+        const int c0 = part * p.kslice / 8;
+        const int c1 = min(p.K, (part + 1) * p.kslice) / 8;
+        const uint4* xr = reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx);
+        const uint4* ar =
+            reinterpret_cast<const uint4*>(p.A + (static_cast<size_t>(l) * p.s_row + j0) * static_cast<size_t>(p.K));
+        float accs[kDecRanksPerItem];
 #pragma unroll
-          for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = 0.0f;
+        for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = 0.0f;
 #pragma unroll 2
-          for (int ch = c0 + et; ch < c1; ch += 128) {
-            const uint4 xw = __ldcg(xr + ch);
-            uint4 av[kDecRanksPerItem];
+        for (int ch = c0 + et; ch < c1; ch += 128) {
+          const uint4 xw = __ldcg(xr + ch);
+          uint4 av[kDecRanksPerItem];
 #pragma unroll
-            for (int jr = 0; jr < kDecRanksPerItem; ++jr) av[jr] = __ldg(ar + static_cast<size_t>(jr) * nch + ch);
+          for (int jr = 0; jr < kDecRanksPerItem; ++jr) av[jr] = __ldg(ar + static_cast<size_t>(jr) * nch + ch);
 #pragma unroll
-            for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = dec_dot8(xw, av[jr], accs[jr]);
-          }
+          for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = dec_dot8(xw, av[jr], accs[jr]);
+        }
+#pragma unroll
+        for (int jr = 0; jr < kDecRanksPerItem; ++jr) {
+          float sv = accs[jr];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
+          if (lane == 0) red[hw * kDecRanksPerItem + jr] = sv;
+        }
+        helper_sync();
+        if (et == 0) {
+          float4 o;
+          float* ov = &o.x;
 #pragma unroll
           for (int jr = 0; jr < kDecRanksPerItem; ++jr) {
-            float sv = accs[jr];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
-            if (lane == 0) red[hw * kDecRanksPerItem + jr] = sv;
+            float sum = 0.0f;
+            for (int w = 0; w < 4; ++w) sum += red[w * kDecRanksPerItem + jr];
+            ov[jr] = sum;
           }
-          helper_sync();
-          if (et == 0) {
-            float4 o;
-            float* ov = &o.x;
-#pragma unroll
-            for (int jr = 0; jr < kDecRanksPerItem; ++jr) {
-              float sum = 0.0f;
-              for (int w = 0; w < 4; ++w) sum += red[w * kDecRanksPerItem + jr];
-              ov[jr] = sum;
-            }
-            *reinterpret_cast<float4*>(p.S + (static_cast<size_t>(part) * M + t) * p.s_row + j0) = o;
-          }
+          *reinterpret_cast<float4*>(p.S + (static_cast<size_t>(part) * M + t) * p.s_row + j0) = o;
         }
-        if (et == 0) {
-          __threadfence();
-          atomicAdd(&p.sync[1], 1u);
-        }
-        // the next item: past the statically assigned ones, from the counter
-        if (n_items <= G) break;
+      }
+      if (et == 0) {
+        __threadfence();
+        atomicAdd(&p.sync[1], 1u);
+      }
+    };
+    const unsigned n_items = static_cast<unsigned>(p.n_items);
+    const unsigned G = static_cast<unsigned>(p.G);
+    if (p.adapters && static_cast<unsigned>(c) < n_items) do_item(c);
+    SegWalk walk(p, c);
+    int T, kb0, kb1, j = 0;
+    bool have = walk.next(T, kb0, kb1);
+    bool alive = true;
+    // a first segment that another CTA finishes: its partial rows next, so
+    // that CTA does not wait on them
+    if (have && kb0 > 0) {
+      alive = epilogue_segment(T, kb0, kb1, j++);
+      have = walk.next(T, kb0, kb1);
+    }
+    if (p.adapters && alive && n_items > G) {
+      unsigned* claim_box = reinterpret_cast<unsigned*>(bcast);
+      while (true) {
         if (et == 0) *claim_box = atomicAdd(&p.sync[0], 1u);
         helper_sync();
         const unsigned k = *claim_box;
         helper_sync();
-        claimed = k < n_items - G ? G + k : n_items;
+        if (k >= n_items - G) break;
+        do_item(static_cast<int>(G + k));
       }
     }
     while (alive && have) {
@@ -946,7 +951,7 @@ int launch_fused_decode_t(DecParams& p, const DecodeArgs& a) {
   }
   // [ring][compact codes + 128][token scale lines + 512][S rows][barriers, metadata]
   const int xsf_bytes = C::kFP4 ? (a.M * (p.kb_pad / 32) * 16 + 512 + 127) / 128 * 128 : 0;
-  const int fixed = 1024 + a.M * p.kb_pad + 128 + xsf_bytes + (a.M * a.s_row * 4 + 127) / 128 * 128 + 1024;
+  const int fixed = 1024 + a.M * p.kb_pad + 128 + xsf_bytes + (a.M * a.s_row + 31) / 32 * 128 + a.M * 512 + 1024;
   int stages = (kDecSmemBudget - fixed) / C::kStage;
   if (stages > kDecMaxStages) stages = kDecMaxStages;
   if (stages < 2) return EPILORA_ERR_UNSUPPORTED;
