@@ -529,7 +529,7 @@ def run_ours(args, rank, world, local):
         "e2e": e2e,
         # per projection: one persistent kernel (single-kernel decode path) or
         # the shrink grid and the GEMM, as the library reports for the shape
-        "gpu_launches": args.steps * sum(E.epilora_layer_forward_kernels(fmt, M, K) for _, K, _ in PROJ8B),
+        "gpu_launches": args.steps * sum(E.epilora_layer_forward_kernels(fmt, M, K, r) for _, K, _ in PROJ8B),
         "clocks": clocks,
         "median_ms_per_step": round(ms_med, 5),
     }
@@ -678,7 +678,7 @@ def run_profile_fused(args):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     print(json.dumps({"profile": args.workload, "kernel": f"fused gate_up {K}->{N} M={M}",
-                      "kernels_per_call": E.epilora_layer_forward_kernels(fmt, M, K), "ok": True}))
+                      "kernels_per_call": E.epilora_layer_forward_kernels(fmt, M, K, r), "ok": True}))
 
 
 def run_profile_wide(args):

@@ -191,15 +191,16 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
 
 /*
  * Number of kernels epilora_layer_forward (and _slices, _noalloc) enqueues
- * for (fmt, M, K): 1 when the single-kernel decode path takes the call (a few
- * tokens: M <= 8, the quantized rows of all tokens, each padded to a multiple
- * of 256 bytes, within 16 KB, and for FP8 M * K <= 16384: e.g. one token up
- * to K = 16384, four tokens at K = 4096; NVFP4 two tokens at K = 14336), else
- * 2 (the shrink grid with its quantizer blocks, then the GEMM as its
- * programmatic dependent).
- * Returns 0 for invalid arguments.
+ * for (fmt, M, K, r), r as for epilora_workspace_bytes (rank times slices, 0
+ * without adapters): 1 when the single-kernel decode path takes the call, 2
+ * otherwise (the shrink grid with its quantizer blocks, then the GEMM as its
+ * programmatic dependent). The single kernel takes a few tokens: M <= 8,
+ * FP8 with M * K <= 16384 (one token up to K = 16384, four at K = 4096),
+ * NVFP4 with the bf16 rows within 40 KB (one token up to K = 16384, two at
+ * K = 8192), as long as the shared memory of the call leaves room for two
+ * weight stages (large M * r excludes it). Returns 0 for invalid arguments.
  */
-EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K);
+EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K, int r);
 
 /*
  * Fused one-call layer (the decode path of the EpiLoRA page, §Design ›

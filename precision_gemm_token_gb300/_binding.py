@@ -36,7 +36,7 @@ SIGNATURES = {
     "epilora_gemm_lora_epilogue": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                             _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp]),
     "epilora_workspace_bytes": (_sz, [_c_int, _c_int, _c_int, _c_int]),
-    "epilora_layer_forward_kernels": (_c_int, [_c_int, _c_int, _c_int]),
+    "epilora_layer_forward_kernels": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
     "epilora_layer_forward": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _sz, _vp, _vp]),
     "epilora_layer_forward_noalloc": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp,
@@ -138,8 +138,8 @@ def epilora_workspace_bytes(fmt, M, K, r) -> int:
     return load().epilora_workspace_bytes(fmt, M, K, r)
 
 
-def epilora_layer_forward_kernels(fmt, M, K) -> int:
-    return load().epilora_layer_forward_kernels(fmt, M, K)
+def epilora_layer_forward_kernels(fmt, M, K, r) -> int:
+    return load().epilora_layer_forward_kernels(fmt, M, K, r)
 
 
 def epilora_layer_forward(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale, x_global_scale, A, B,

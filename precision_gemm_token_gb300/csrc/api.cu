@@ -222,10 +222,10 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K, const v
   return fmt == EPILORA_FMT_FP8_E4M3 ? launch_gemm_fp8(a) : launch_gemm_nvfp4(a);
 }
 
-EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K) {
-  if (!fmt_ok(fmt) || M < 0 || !k_ok(K)) return 0;
+EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K, int r) {
+  if (!fmt_ok(fmt) || M < 0 || !k_ok(K) || r < 0) return 0;
   if (M == 0) return 0;
-  return decode_path_eligible(fmt, M, K) ? 1 : 2;
+  return decode_path_eligible(fmt, M, K, r) ? 1 : 2;
 }
 
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
@@ -246,7 +246,7 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   // more than one decode tile of tokens with adapters: the adapter-sorted row order
   if (r > 0 && M > 32) bytes += round256(m * 4);
   // single-kernel decode path: partial rows of weight tiles split over CTAs
-  if (decode_path_eligible(fmt, M, K)) bytes += round256(decode_partial_bytes(M));
+  if (decode_path_eligible(fmt, M, K, r)) bytes += round256(decode_partial_bytes(M));
   return bytes;
 }
 
@@ -305,7 +305,7 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
   if (!quant_args_ok(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale)) return EPILORA_ERR_INVALID_ARG;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (decode_path_eligible(fmt, M, K)) {
+  if (decode_path_eligible(fmt, M, K, rr)) {
     // a few tokens: quantizer, shrink and GEMM in one persistent launch
     DecodeArgs d{};
     d.fmt = fmt;

@@ -118,7 +118,7 @@ struct DecodeArgs {
   float* x_scale;
   uint8_t* x_block_scale;
 };
-bool decode_path_eligible(int fmt, int M, int K);
+bool decode_path_eligible(int fmt, int M, int K, int s_row);
 size_t decode_sync_bytes();
 size_t decode_partial_bytes(int M);
 int launch_fused_decode(const DecodeArgs& a);

@@ -88,6 +88,7 @@ struct DecParams {
   int slice_end[4];
   int adapters, parts, kslice, n_items;
   int kb_pad;          // code bytes of one token's row, padded to whole units
+  int xslots;          // last ring slots that first hold the bf16 activation rows
 };
 
 // A unit is KA 128-byte K atoms of one 128-row weight tile (16 KB each).
@@ -260,7 +261,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   uint64_t* acce_bar = accf_bar + 2;                 // [2] accumulator read out
   uint64_t* xrdy_bar = acce_bar + 2;                 // compact activations written
   uint64_t* pref_bar = xrdy_bar + 1;                 // the helpers' L2 hints are issued
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pref_bar + 1);
+  uint64_t* xst_bar = pref_bar + 1;                  // the bf16 activation rows have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xst_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bcast = reinterpret_cast<int*>(tmem_slot + 2);                 // helper broadcast word
   float* red = reinterpret_cast<float*>(tmem_slot + 4);               // [4 warps][8]
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     }
     mbar_init(xrdy_bar, 1);
     mbar_init(pref_bar, 1);
+    mbar_init(xst_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&p.tmW);
@@ -312,6 +315,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         const int s = static_cast<int>(it % stages);
         const uint32_t ph = static_cast<uint32_t>(it / stages) & 1u;
         if (*abort_flag || !mbar_wait_bounded(&empty_bar[s], ph ^ 1u, kWaitLimitNs)) {
+          *abort_flag = 1;
+          record_status(p.status, EPILORA_ERR_TIMEOUT);
+          break;
+        }
+        // the last xslots slots hold the activation rows until the quantized
+        // copy is published
+        if (it == stages - p.xslots && !mbar_wait_bounded(xrdy_bar, 0, kWaitLimitNs)) {
           *abort_flag = 1;
           record_status(p.status, EPILORA_ERR_TIMEOUT);
           break;
@@ -494,9 +504,20 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     // the preceding kernel on the stream has completed: X, idx, mask and the
     // workspace are valid from here on
     pdl_wait_primary();
-    // Every load below that does not depend on another is issued before any
-    // is used: on this two-die GPU each dependent round trip to L2 costs about
-    // a microsecond, and this path has a handful of them.
+    // The activation rows come in one bulk copy into the last ring slots
+    // (one round trip for any K), and the quantizers read them from there:
+    // on this two-die GPU a dependent round trip to L2 costs about a
+    // microsecond, so loads that do not depend on each other are issued
+    // together.
+    const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(smem + static_cast<size_t>(stages - p.xslots) *
+                                                                     C::kStage);
+    if (et == 0) {
+      fence_proxy_async_global();       // the preceding kernel's writes of X, for the copy engine
+      mbar_arrive_expect_tx(xst_bar, static_cast<uint32_t>(M * p.K * 2));
+      for (int t = 0; t < M; ++t)
+        bulk_copy_g2s(const_cast<__nv_bfloat16*>(xs) + static_cast<size_t>(t) * p.K,
+                      p.X + static_cast<size_t>(t) * p.ldx, static_cast<uint32_t>(p.K * 2), xst_bar);
+    }
     int li = -1, mk = 1;
     if (et < M && p.adapters) {
       li = p.idx[et];
@@ -505,50 +526,31 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     float alpha = 1.0f;
     const int nch = p.K / 8;                      // 16-byte bf16 chunks per row
     const int total = M * nch;
-    // FP8: a thread's first kHold chunks (all of them for one token up to
-    // K = 4096) stay in registers between the amax and the codes; the rest
-    // are read again from L2. Short loops: this code runs once per call, so
-    // its instruction fetch is on the critical path.
-    constexpr int kHold = 4;
-    uint4 xv[kHold];
-    if (!C::kFP4) {
-#pragma unroll
-      for (int jj = 0; jj < kHold; ++jj) {
-        const int q = et + 128 * jj;
-        if (q < total) {
-          const int t = q / nch;
-          xv[jj] = __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch));
-        }
-      }
-    }
     if (et < M) {
       if (li >= p.L) record_status(p.status, EPILORA_ERR_INVALID_ARG);
       meta_idx[et] = (li >= 0 && li < p.L && mk != 0) ? li : -1;
     }
+    if (!mbar_wait_bounded(xst_bar, 0, kWaitLimitNs)) {
+      *abort_flag = 1;
+      record_status(p.status, EPILORA_ERR_TIMEOUT);
+    }
+    const uint4* xs4 = reinterpret_cast<const uint4*>(xs);   // chunk q of the M x nch chunks
     // ---- activation quantization into the compact copy ----
     if (!C::kFP4) {
       float am[kDecMaxTokens];
 #pragma unroll
       for (int t = 0; t < kDecMaxTokens; ++t) am[t] = 0.0f;
-      auto amax_chunk = [&](const uint4& v, int t) {
+#pragma unroll 4
+      for (int q = et; q < total; q += 128) {
+        const int t = q / nch;
         float x[8];
-        unpack8(v, x);
+        unpack8(xs4[q], x);
         float mx = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(x[i]));
 #pragma unroll
         for (int tt = 0; tt < kDecMaxTokens; ++tt)
           if (tt == t) am[tt] = fmaxf(am[tt], mx);
-      };
-#pragma unroll
-      for (int jj = 0; jj < kHold; ++jj) {
-        const int q = et + 128 * jj;
-        if (q < total) amax_chunk(xv[jj], q / nch);
-      }
-#pragma unroll 1
-      for (int q = et + 128 * kHold; q < total; q += 128) {
-        const int t = q / nch;
-        amax_chunk(__ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch)), t);
       }
 #pragma unroll
       for (int tt = 0; tt < kDecMaxTokens; ++tt) {
@@ -567,28 +569,15 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         if (c == 0) p.xs_out[et] = sc;
       }
       helper_sync();
-      // the codes: the held chunks of rows whose scale is at least 2^-100
-      // from registers; every other chunk in one short loop (read again from
-      // L2; the IEEE division for rows whose scale is below 2^-100)
-      auto store_code = [&](uint2 code, int t, int k0) {
-        *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
-        if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
-      };
-#pragma unroll
-      for (int jj = 0; jj < kHold; ++jj) {
-        const int q = et + 128 * jj;
-        if (q < total) {
-          const int t = q / nch;
-          if (meta_sx[t] >= 0x1p-100f) store_code(quant8_e4m3_rs(xv[jj], meta_sx[t], meta_rs[t]), t, (q - t * nch) * 8);
-        }
-      }
-#pragma unroll 1
+      // the codes (the IEEE division for rows whose scale is below 2^-100)
+#pragma unroll 2
       for (int q = et; q < total; q += 128) {
         const int t = q / nch;
+        const int k0 = (q - t * nch) * 8;
         const float sc = meta_sx[t];
-        if (q < et + 128 * kHold && sc >= 0x1p-100f) continue;
-        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx) + (q - t * nch));
-        store_code(sc >= 0x1p-100f ? quant8_e4m3_rs(v, sc, meta_rs[t]) : quant8_e4m3(v, sc), t, (q - t * nch) * 8);
+        const uint2 code = sc >= 0x1p-100f ? quant8_e4m3_rs(xs4[q], sc, meta_rs[t]) : quant8_e4m3(xs4[q], sc);
+        *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
+        if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
       }
       // zero codes past K up to the unit boundary (finite values against the
       // weight box's zero fill)
@@ -610,12 +599,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       for (int q = et; q < total; q += 128) {
         const int t = q / nb;
         const int b = q - t * nb;
-        const uint4* row = reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx);
+        const uint4* row = xs4 + static_cast<size_t>(t) * nch;
         float x[16];
         {
           float a0[8], a1[8];
-          unpack8(__ldcg(row + 2 * b), a0);
-          unpack8(__ldcg(row + 2 * b + 1), a1);
+          unpack8(row[2 * b], a0);
+          unpack8(row[2 * b + 1], a1);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             x[i] = a0[i];
@@ -907,20 +896,47 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
 // 128-byte K atoms per weight unit (a unit is KA atoms of one 128-row tile)
 constexpr int kDecKA = 2;
 
-// Whether the single-kernel decode path takes (fmt, M, K): a few tokens whose
-// quantized rows (padded to whole units) fit the per-CTA compact copy (and,
-// for FP8, the quantizer's registers).
-bool decode_path_eligible(int fmt, int M, int K) {
-  if (M < 1 || M > kDecMaxTokens || K < 32 || K % 32 != 0) return false;
-  const long unit_k = 128L * kDecKA;
-  if (fmt == EPILORA_FMT_FP8_E4M3) {
-    const long kb_pad = (static_cast<long>(K) + unit_k - 1) / unit_k * unit_k;
-    return M * kb_pad <= kDecXcBytes && static_cast<long>(M) * (K / 8) <= 16L * 128;
-  }
-  if (fmt == EPILORA_FMT_NVFP4) {
-    const long kb_pad = (static_cast<long>(K / 2) + unit_k - 1) / unit_k * unit_k;
-    return K % 256 == 0 && M * kb_pad <= kDecXcBytes;
-  }
+namespace {
+
+// Shared-memory plan of one call: ring stages, the slots that first hold the
+// bf16 activation rows, and the bytes outside the ring.
+struct DecPlan {
+  int nkb, kb_pad, stages, xslots, fixed, stage_bytes;
+};
+
+template <int FMT, int KA>
+bool decode_plan_t(int M, int K, int s_row, DecPlan* pl) {
+  using C = DecCfg<FMT, KA>;
+  const int kbytes = C::kFP4 ? K / 2 : K;
+  pl->nkb = (kbytes + 128 * KA - 1) / (128 * KA);
+  pl->kb_pad = pl->nkb * 128 * KA;
+  pl->stage_bytes = C::kStage;
+  // [ring][compact codes + 128][token scale lines + 512][S rows][row sums][barriers, metadata]
+  const int xsf_bytes = C::kFP4 ? (M * (pl->kb_pad / 32) * 16 + 512 + 127) / 128 * 128 : 0;
+  pl->fixed = 1024 + M * pl->kb_pad + 128 + xsf_bytes + (M * s_row + 31) / 32 * 128 + M * 512 + 1024;
+  int stages = (kDecSmemBudget - pl->fixed) / C::kStage;
+  if (stages > kDecMaxStages) stages = kDecMaxStages;
+  pl->stages = stages;
+  pl->xslots = (M * K * 2 + C::kStage - 1) / C::kStage;
+  // at least one slot streams weights while the rows are quantized
+  return stages >= 2 && pl->xslots <= stages - 1 && pl->fixed + stages * C::kStage <= 227 * 1024;
+}
+
+}  // namespace
+
+// Whether the single-kernel decode path takes (fmt, M, K) with S rows of
+// s_row floats (rank x slices, 0 without adapters): a few tokens whose
+// quantized rows (padded to whole units) fit the per-CTA compact copy, whose
+// bf16 rows fit the ring slots that stage them, and, for FP8, M * K <= 16384.
+bool decode_path_eligible(int fmt, int M, int K, int s_row) {
+  if (M < 1 || M > kDecMaxTokens || K < 32 || K % 32 != 0 || s_row < 0) return false;
+  DecPlan pl{};
+  if (fmt == EPILORA_FMT_FP8_E4M3)
+    return M * K <= 16384 && decode_plan_t<EPILORA_FMT_FP8_E4M3, kDecKA>(M, K, s_row, &pl) &&
+           M * pl.kb_pad <= kDecXcBytes;
+  if (fmt == EPILORA_FMT_NVFP4)
+    return K % 256 == 0 && decode_plan_t<EPILORA_FMT_NVFP4, kDecKA>(M, K, s_row, &pl) &&
+           M * pl.kb_pad <= kDecXcBytes;
   return false;
 }
 
@@ -934,9 +950,13 @@ namespace {
 template <int FMT, int KA>
 int launch_fused_decode_t(DecParams& p, const DecodeArgs& a) {
   using C = DecCfg<FMT, KA>;
+  DecPlan pl{};
+  if (!decode_plan_t<FMT, KA>(a.M, a.K, a.s_row, &pl)) return EPILORA_ERR_UNSUPPORTED;
   const int kbytes = C::kFP4 ? a.K / 2 : a.K;
-  p.nkb = (kbytes + 128 * KA - 1) / (128 * KA);
-  p.kb_pad = p.nkb * 128 * KA;
+  p.nkb = pl.nkb;
+  p.kb_pad = pl.kb_pad;
+  p.stages = pl.stages;
+  p.xslots = pl.xslots;
   p.n_tiles = (a.N + 127) / 128;
   p.U = static_cast<long long>(p.n_tiles) * p.nkb;
   int G = num_sms();
@@ -949,17 +969,9 @@ int launch_fused_decode_t(DecParams& p, const DecodeArgs& a) {
     rc = make_tma_2d_u8(&p.tmSW, a.w_block_scale, a.N, a.K / 16, a.K / 16, 128, 16 * KA, false);
     if (rc != EPILORA_OK) return rc;
   }
-  // [ring][compact codes + 128][token scale lines + 512][S rows][barriers, metadata]
-  const int xsf_bytes = C::kFP4 ? (a.M * (p.kb_pad / 32) * 16 + 512 + 127) / 128 * 128 : 0;
-  const int fixed = 1024 + a.M * p.kb_pad + 128 + xsf_bytes + (a.M * a.s_row + 31) / 32 * 128 + a.M * 512 + 1024;
-  int stages = (kDecSmemBudget - fixed) / C::kStage;
-  if (stages > kDecMaxStages) stages = kDecMaxStages;
-  if (stages < 2) return EPILORA_ERR_UNSUPPORTED;
-  p.stages = stages;
   // L2 prefetch behind the ring: about 40 MB over the grid
   p.l2_ahead = static_cast<int>((40L << 20) / (static_cast<long>(G) * C::kStageTx));
-  const int smem = fixed + stages * C::kStage;
-  if (smem > 227 * 1024) return EPILORA_ERR_UNSUPPORTED;
+  const int smem = pl.fixed + pl.stages * C::kStage;
 
   auto kern = fused_decode_kernel<FMT, KA>;
   static int attr_done[64] = {0};

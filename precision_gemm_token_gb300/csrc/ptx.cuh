@@ -110,6 +110,14 @@ __device__ __forceinline__ float ldg_nc_f32_now(const float* ptr) {
   return v;
 }
 
+// Untiled bulk copy global -> shared memory of this CTA, completing on `bar`
+// (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Bring [ptr, ptr + bytes) into L2 (bytes a multiple of 16, ptr 16-B aligned).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)

@@ -79,14 +79,17 @@ def test_workspace_bytes(lib):
 
 
 def test_layer_forward_kernels(lib):
-    """One persistent kernel for a few tokens whose quantized rows fit 16 KB
-    (FP8: M * K <= 16384, NVFP4: M * K <= 32768, M <= 8), else two."""
+    """One persistent kernel for a few tokens (FP8: M * K <= 16384; NVFP4:
+    bf16 rows within one 40 KB ring slot; M <= 8) while two weight stages
+    still fit beside the per-call buffers; else two."""
     k = E.epilora_layer_forward_kernels
-    assert k(0, 1, 14336) == 1 and k(0, 1, 16384) == 1 and k(0, 1, 16416) == 2
-    assert k(0, 4, 4096) == 1 and k(0, 5, 4096) == 2 and k(0, 8, 2048) == 1 and k(0, 9, 512) == 2
-    assert k(1, 2, 14336) == 1 and k(1, 8, 4096) == 1 and k(1, 3, 14336) == 2
-    assert k(1, 1, 4128) == 2            # NVFP4 wants K % 256 == 0
-    assert k(0, 32, 4096) == 2 and k(0, 0, 4096) == 0 and k(2, 1, 4096) == 0 and k(0, 1, 100) == 0
+    assert k(0, 1, 14336, 0) == 1 and k(0, 1, 16384, 64) == 1 and k(0, 1, 16416, 0) == 2
+    assert k(0, 4, 4096, 64) == 1 and k(0, 5, 4096, 0) == 2 and k(0, 8, 2048, 16) == 1 and k(0, 9, 512, 0) == 2
+    assert k(1, 1, 14336, 64) == 1 and k(1, 2, 8192, 64) == 1 and k(1, 8, 2048, 16) == 1
+    assert k(1, 2, 14336, 64) == 2 and k(1, 8, 4096, 16) == 2           # bf16 rows beyond one ring slot
+    assert k(0, 8, 2048, 512) == 1 and k(1, 8, 2048, 512) == 2          # S rows crowd out a weight stage
+    assert k(1, 1, 4128, 0) == 2                                         # NVFP4 wants K % 256 == 0
+    assert k(0, 32, 4096, 0) == 2 and k(0, 0, 4096, 0) == 0 and k(2, 1, 4096, 0) == 0 and k(0, 1, 100, 0) == 0
 
 
 # ---------------------------------------------------------------------------

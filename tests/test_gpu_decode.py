@@ -42,7 +42,7 @@ CASES = [
 @pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
 @pytest.mark.parametrize("M,K,N,L,r,idx_mode,mask_mode", CASES)
 def test_single_kernel_matches_oracle(fmt, M, K, N, L, r, idx_mode, mask_mode):
-    assert E.epilora_layer_forward_kernels(fmt, M, K) == 1
+    assert E.epilora_layer_forward_kernels(fmt, M, K, r) == 1
     y, ref, bound, _ = run_case(fmt, M, K, N, L, r, seed=M * 31 + K + N, idx_mode=idx_mode, mask_mode=mask_mode)
     assert_y_close(y, ref, bound, what=(fmt, M, K, N, r))
 
@@ -51,7 +51,7 @@ def test_single_kernel_fp8_k_tail():
     """FP8 with K not a multiple of 128: the last weight unit is zero-filled
     past K by the copy engine and the quantized rows are zero there."""
     for K in (160, 416):
-        assert E.epilora_layer_forward_kernels(FP8, 3, K) == 1
+        assert E.epilora_layer_forward_kernels(FP8, 3, K, 16) == 1
         y, ref, bound, _ = run_case(FP8, 3, K, 384, 2, 16, seed=K)
         assert_y_close(y, ref, bound, what=K)
 
@@ -179,7 +179,7 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable():
     returns EPILORA_ERR_TIMEOUT in the status word, leaves the counters zero
     again, and the next call on the same stream and workspace is correct."""
     M, K, N, L, r = 2, 8192, 1024, 2, 128
-    assert E.epilora_layer_forward_kernels(FP8, M, K) == 1
+    assert E.epilora_layer_forward_kernels(FP8, M, K, r) == 1
     p = make_projection(M, K, N, L, r, seed=5, device="cuda")
     w = T.quantize_weight(p.W, FP8)
     ref = T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask)
@@ -223,7 +223,7 @@ def test_single_kernel_fp8_codes_bit_exact_over_magnitudes(seed):
         v = torch.tensor([code_mid * float(s0)], dtype=torch.float32).to(torch.bfloat16)
         X[0, 10 + j] = v.item()
     xr = X.float().cpu().numpy()
-    assert E.epilora_layer_forward_kernels(FP8, M, K) == 1
+    assert E.epilora_layer_forward_kernels(FP8, M, K, 0) == 1
     W = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
     w = T.quantize_weight(W, FP8)
     ws = T.LayerWorkspace("cuda")

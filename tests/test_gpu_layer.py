@@ -220,7 +220,7 @@ def test_gemm_with_h_given_matches_fused():
     two-kernel fused call bit for bit (12 tokens: more than the single-kernel
     path takes)."""
     import precision_gemm_token_gb300 as E
-    assert E.epilora_layer_forward_kernels(FP8, 12, 1024) == 2
+    assert E.epilora_layer_forward_kernels(FP8, 12, 1024, 32) == 2
     p = make_projection(12, 1024, 512, 4, 32, seed=10)
     X, W = p.X.cuda(), p.W.cuda()
     w = T.quantize_weight(W, FP8)
