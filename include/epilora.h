@@ -178,15 +178,15 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
 
 /*
  * Bytes of device workspace epilora_layer_forward needs for (fmt, M, K, r):
- * EPILORA_WORKSPACE_SYNC_BYTES of grid-wide counters first, then the
- * quantized activations, their scales, S (r = 0: no adapters; S is held as
- * up to ceil(K / 1024) partial sums over K slices, capped at 8), for more
- * than 32 tokens with adapters a row-to-token map, and for the single-kernel
- * decode path (see epilora_layer_forward_kernels) partial rows of weight
- * tiles split between thread blocks; each region 256-byte aligned. Returns 0
- * for M == 0 or invalid arguments.
+ * a head of EPILORA_WORKSPACE_SYNC_BYTES (2.25 MiB: the single-kernel decode
+ * path's grid-wide counters and the regions where its thread blocks exchange
+ * partial results, see epilora_layer_forward_kernels), then the quantized
+ * activations, their scales, S (r = 0: no adapters; S is held as up to
+ * ceil(K / 1024) partial sums over K slices, capped at 8) and, for more than
+ * 32 tokens with adapters, a row-to-token map; each region 256-byte aligned.
+ * Returns 0 for M == 0 or invalid arguments.
  */
-#define EPILORA_WORKSPACE_SYNC_BYTES 1280
+#define EPILORA_WORKSPACE_SYNC_BYTES 2360576
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
 
 /*
@@ -230,12 +230,14 @@ EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K, int r);
  *      it starts streaming Wq (and w_block_scale) as soon as it is resident,
  *      and reads everything else only after the shrink grid has completed;
  * using `workspace` (>= epilora_workspace_bytes, 256-byte aligned) for the
- * counters, Xq, scales, S, the row map and partial rows. The first
- * EPILORA_WORKSPACE_SYNC_BYTES of the workspace must be zero before the
- * first call that uses it (zero-fill a workspace once after allocating it);
- * every call leaves them zero again, and nothing else in the workspace needs
- * an initial value. Y is the same whatever the row order. Calls that share a
- * workspace must be ordered on one stream.
+ * head, Xq, scales, S and the row map. The head (the first
+ * EPILORA_WORKSPACE_SYNC_BYTES) must be zero before the first call that uses
+ * the workspace: zero-fill a workspace once after allocating it. Calls keep
+ * the head valid for the next call (counters back to zero, an epoch moved on
+ * that tags every value the thread blocks exchange, so older values are
+ * never taken for new ones); nothing else needs an initial value. Y is the
+ * same whatever the row order. Calls that share a workspace must be ordered
+ * on one stream.
  * Because the GEMM may start while the kernel that precedes this call on the
  * stream is still running, that kernel must not write Wq or w_block_scale
  * (every other input, X included, may be its output).
@@ -296,11 +298,11 @@ EPILORA_API int epilora_layer_forward_slices(int fmt, int M, int N, int K,
  * epilora_workspace_bytes(fmt, M, K, A && B ? r : 0) exceeds
  * EPILORA_NOALLOC_SCRATCH_BYTES (8 MiB); the test is exactly that size query,
  * whose S term grows with the number of K slices of the shrink (e.g. FP8,
- * r = 64: M up to 1635 at K = 4096); EPILORA_ERR_CUDA if the address lookup
+ * r = 64: M up to 1175 at K = 4096); EPILORA_ERR_CUDA if the address lookup
  * fails.
  * Otherwise it enqueues what epilora_layer_forward enqueues (the scratch
- * starts zeroed when the library is loaded, and every call leaves its
- * counters zero again, as epilora_layer_forward requires).
+ * starts zeroed when the library is loaded, which is what
+ * epilora_layer_forward requires of a workspace's head).
  *
  * All calls on one device share the one scratch array: calls that overlap in
  * time (on different streams, or from host threads that do not order their

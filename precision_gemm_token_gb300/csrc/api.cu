@@ -232,8 +232,9 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   if (!fmt_ok(fmt) || M < 0 || K < 0 || r < 0) return 0;
   const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
   if (M == 0) return 0;
-  // counters of the single-kernel decode path, at a fixed place
-  size_t bytes = round256(decode_sync_bytes());
+  // the head: counters and tagged exchange regions of the single-kernel
+  // decode path, at a fixed place
+  size_t bytes = EPILORA_WORKSPACE_SYNC_BYTES;
   if (fmt == EPILORA_FMT_FP8_E4M3) {
     bytes += round256(m * k);          // Xq
     bytes += round256(m * 4);          // x_scale
@@ -245,8 +246,6 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   bytes += round256(m * static_cast<size_t>(r) * 4 * static_cast<size_t>(r > 0 ? shrink_parts_max(K) : 1));
   // more than one decode tile of tokens with adapters: the adapter-sorted row order
   if (r > 0 && M > 32) bytes += round256(m * 4);
-  // single-kernel decode path: partial rows of weight tiles split over CTAs
-  if (decode_path_eligible(fmt, M, K, r)) bytes += round256(decode_partial_bytes(M));
   return bytes;
 }
 
@@ -273,7 +272,9 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t m = static_cast<size_t>(M), k = static_cast<size_t>(K);
   void* sync = ws;
-  size_t off = round256(decode_sync_bytes());
+  void* accp = ws + decode_sync_bytes();
+  void* S_tagged = ws + decode_sync_bytes() + decode_partial_bytes();
+  size_t off = EPILORA_WORKSPACE_SYNC_BYTES;
   void* Xq = ws + off;
   float* x_scale = nullptr;
   uint8_t* x_block_scale = nullptr;
@@ -296,7 +297,6 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
       off += round256(m * 4);
     }
   }
-  float* accp = reinterpret_cast<float*>(ws + off);   // decode path only
 
   int rc = gemm_validate(fmt, M, N, K, Xq, x_scale, x_block_scale, x_global_scale, Wq, w_scale, w_block_scale,
                          w_global_scale, S, B, L, r, idx, Y, ldy);
@@ -337,7 +337,7 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
     d.status_dev = status_dev;
     d.stream = st;
     d.sync = sync;
-    d.S = S;
+    d.S = S_tagged;
     d.accp = accp;
     d.Xq = Xq;
     d.x_scale = x_scale;

@@ -110,17 +110,18 @@ struct DecodeArgs {
   void* Y;
   int* status_dev;
   cudaStream_t stream;
-  // workspace regions
-  void* sync;           // decode_sync_bytes(), zero before the call, zero after it
-  float* S;             // [parts][M][s_row]
-  float* accp;          // decode_partial_bytes(M)
+  // workspace regions (the head: counters, tagged partial rows, tagged S)
+  void* sync;           // decode_sync_bytes()
+  void* S;              // decode_s_bytes(): tagged [parts][M][s_row]
+  void* accp;           // decode_partial_bytes(): tagged [CTA][M][128]
   void* Xq;             // the quantized activations as used (written by one CTA)
   float* x_scale;
   uint8_t* x_block_scale;
 };
 bool decode_path_eligible(int fmt, int M, int K, int s_row);
 size_t decode_sync_bytes();
-size_t decode_partial_bytes(int M);
+size_t decode_partial_bytes();
+size_t decode_s_bytes();
 int launch_fused_decode(const DecodeArgs& a);
 // K slice length of a shrink split into `parts` slices (multiple of 256)
 int shrink_kslice(int K, int parts);

@@ -59,9 +59,11 @@ constexpr int kDecSmemBudget = 113 * 1024;
 constexpr int kDecMaxStages = 8;
 constexpr int kMaxRankBrow = 64;           // 32-bit words of a rank-128 bf16 B row
 
-// sync block at the start of the workspace: [0] claim, [1] done, [2] exit;
-// flags of the partial-row slots from word 64 on
+// sync block at the start of the workspace: [0] claim counter, [2] exit
+// counter, [3] epoch; then the tagged region (partial rows, then S)
 constexpr int kDecSyncWords = 64;
+constexpr int kDecSParts = 8;              // K slices of the shrink at most
+constexpr int kDecMaxSRow = 512;           // rank 128 x 4 slices
 
 struct DecParams {
   CUtensorMap tmW;     // uint8 [N, Kb], box 128 rows x 128 B, 128-B swizzle
@@ -76,9 +78,12 @@ struct DecParams {
   const float* x_gs;
   __nv_bfloat16* Y;
   int* status;
-  unsigned* sync;      // [claim, done, exit, ..., flags from kDecSyncWords]
-  float* S;            // [parts][M][s_row] partial sums of the shrink
-  float* accp;         // [G][M][128] fp32 partial rows of split weight tiles
+  unsigned* sync;      // [0] claim counter, [2] exit counter, [3] launch epoch
+  // Published values carry the launch epoch in the same 64-bit word (value
+  // bits low, epoch high): a reader retries until the tag is this launch's,
+  // so no flag or counter has to be polled before the data.
+  uint2* S;            // [parts][M][s_row] partial sums of the shrink
+  uint2* accp;         // [G][M][128] partial rows of split weight tiles
   uint8_t* xq_out;     // CTA 0 also stores the quantized activations here
   float* xs_out;       // FP8 scales
   uint8_t* xsb_out;    // NVFP4 block scales
@@ -127,23 +132,30 @@ __device__ __forceinline__ bool helper_any(bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
+// Tag of the launch whose epoch word is e: an odd multiplicative mix (never
+// zero, distinct for distinct e).
+__device__ __forceinline__ unsigned launch_tag(unsigned e) { return ((e + 1u) * 0x9E3779B1u) | 1u; }
 
-// Bounded spin of one thread until *p >= target (1 s limit); false on timeout.
-__device__ __forceinline__ bool spin_until_at_least(const unsigned* p, unsigned target) {
-  if (ld_acquire_u32(p) >= target) return true;
+// One tagged 64-bit value, read again until its tag is `epoch` (1 s limit);
+// false on timeout.
+__device__ __forceinline__ bool read_tagged(const uint2* p, unsigned epoch, uint2* out) {
+  uint2 w = __ldcg(p);
+  if (w.y == epoch) {
+    *out = w;
+    return true;
+  }
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (ld_acquire_u32(p) >= target) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    __nanosleep(64);
+    __nanosleep(32);
+    w = __ldcg(p);
+    if (w.y == epoch) {
+      *out = w;
+      return true;
+    }
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *out = w;
+      return false;
+    }
   }
 }
 
@@ -523,6 +535,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       li = p.idx[et];
       if (p.mask != nullptr) mk = p.mask[et];
     }
+    // this launch's tag: a mix of the epoch word (which the previous launch on
+    // this workspace moved on), never zero, so zero-filled or older memory
+    // never reads as this launch's data
+    const unsigned epoch = launch_tag(__ldcg(p.sync + 3));
     float alpha = 1.0f;
     const int nch = p.K / 8;                      // 16-byte bf16 chunks per row
     const int total = M * nch;
@@ -710,50 +726,47 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
 #pragma unroll
       for (int t = 0; t < kDecMaxTokens; ++t) acc[t] = __uint_as_float(v[t]);
       if (!finisher) {
-        // publish this CTA's partial rows of tile T: slot c, [token][row]
-        float* dst = p.accp + static_cast<size_t>(c) * M * 128;
+        // publish this CTA's partial rows of tile T: slot c, [token][row],
+        // each value tagged with the launch epoch
+        uint2* dst = p.accp + static_cast<size_t>(c) * M * 128;
 #pragma unroll
         for (int t = 0; t < kDecMaxTokens; ++t)
-          if (t < M) dst[t * 128 + m] = acc[t];
-        __threadfence();
-        helper_sync();
-        if (et == 0) st_release_u32(&p.sync[kDecSyncWords + c], 1u);
+          if (t < M) __stcg(dst + t * 128 + m, make_uint2(__float_as_uint(acc[t]), epoch));
         return true;
       }
-      // finisher: one thread waits (bounded) until the CTAs holding the rest
-      // of tile T have published their partial rows and, the first time,
-      // until every shrink item is counted; then all loads go out together
+      // finisher: the partial rows of the CTAs holding the rest of tile T
+      // (added in CTA order) and, the first time, S (its K-slice partial sums
+      // added in part order), each value read until it carries this launch's
+      // epoch (bounded)
       const int c_last = kb1 < p.nkb ? cta_of_unit(p, static_cast<long long>(T) * p.nkb + p.nkb - 1) : c;
       const bool need_s = p.adapters && !s_ready;
-      if (et == 0) {
-        bool all = true;
-        for (int c2 = c + 1; c2 <= c_last && all; ++c2) all = spin_until_at_least(&p.sync[kDecSyncWords + c2], 1u);
-        if (all && need_s) all = spin_until_at_least(&p.sync[1], static_cast<unsigned>(p.n_items));
-        *bcast = all ? 1 : 0;
-      }
-      helper_sync();
-      if (*bcast == 0) return fail();
+      bool late = false;
       if (need_s) {
-        // S: the partial sums over K slices added in part order
         const size_t part_stride = static_cast<size_t>(M) * p.s_row;
         for (int e = et; e < M * p.s_row; e += 128) {
           const int t = e / p.s_row;
           float sum = 0.0f;
           if (meta_idx[t] >= 0) {
-            sum = __ldcg(p.S + e);
-            for (int q = 1; q < p.parts; ++q) sum += __ldcg(p.S + q * part_stride + e);
+            for (int q = 0; q < p.parts; ++q) {
+              uint2 w;
+              if (!read_tagged(p.S + q * part_stride + e, epoch, &w)) late = true;
+              sum = q == 0 ? __uint_as_float(w.x) : sum + __uint_as_float(w.x);
+            }
           }
           s_stage[e] = sum;
         }
       }
-      // partial rows of the other CTAs, added in CTA order
       for (int c2 = c + 1; c2 <= c_last; ++c2) {
-        const float* src = p.accp + static_cast<size_t>(c2) * M * 128;
+        const uint2* src = p.accp + static_cast<size_t>(c2) * M * 128;
 #pragma unroll
         for (int t = 0; t < kDecMaxTokens; ++t)
-          if (t < M) acc[t] += __ldcg(src + t * 128 + m);
+          if (t < M) {
+            uint2 w;
+            if (!read_tagged(src + t * 128 + m, epoch, &w)) late = true;
+            acc[t] += __uint_as_float(w.x);
+          }
       }
-      helper_sync();                              // S staged; bcast free again
+      if (helper_any(late)) return fail();        // (also: S staged for every thread)
       s_ready = s_ready || need_s;
       if (n < p.N) {
         const int soff = p.adapters ? dec_slice_offset(p, T * 128) : 0;
@@ -827,12 +840,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
             for (int w = 0; w < 4; ++w) sum += red[w * kDecRanksPerItem + jr];
             ov[jr] = sum;
           }
-          *reinterpret_cast<float4*>(p.S + (static_cast<size_t>(part) * M + t) * p.s_row + j0) = o;
+          uint4* dst = reinterpret_cast<uint4*>(p.S + (static_cast<size_t>(part) * M + t) * p.s_row + j0);
+          __stcg(dst, make_uint4(__float_as_uint(o.x), epoch, __float_as_uint(o.y), epoch));
+          __stcg(dst + 1, make_uint4(__float_as_uint(o.z), epoch, __float_as_uint(o.w), epoch));
         }
-      }
-      if (et == 0) {
-        __threadfence();
-        atomicAdd(&p.sync[1], 1u);
       }
     };
     const unsigned n_items = static_cast<unsigned>(p.n_items);
@@ -874,10 +885,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     __threadfence();
     const unsigned old = atomicAdd(&p.sync[2], 1u);
     if (old == static_cast<unsigned>(p.G - 1)) {
+      // the next launch on this workspace tags its values with the next epoch
       __threadfence();
       p.sync[0] = 0u;
-      p.sync[1] = 0u;
-      for (int q = 0; q < p.G; ++q) p.sync[kDecSyncWords + q] = 0u;
+      p.sync[3] = p.sync[3] + 1u;
       __threadfence();
       p.sync[2] = 0u;
     }
@@ -929,7 +940,7 @@ bool decode_plan_t(int M, int K, int s_row, DecPlan* pl) {
 // quantized rows (padded to whole units) fit the per-CTA compact copy, whose
 // bf16 rows fit the ring slots that stage them, and, for FP8, M * K <= 16384.
 bool decode_path_eligible(int fmt, int M, int K, int s_row) {
-  if (M < 1 || M > kDecMaxTokens || K < 32 || K % 32 != 0 || s_row < 0) return false;
+  if (M < 1 || M > kDecMaxTokens || K < 32 || K % 32 != 0 || s_row < 0 || s_row > kDecMaxSRow) return false;
   DecPlan pl{};
   if (fmt == EPILORA_FMT_FP8_E4M3)
     return M * K <= 16384 && decode_plan_t<EPILORA_FMT_FP8_E4M3, kDecKA>(M, K, s_row, &pl) &&
@@ -940,10 +951,17 @@ bool decode_path_eligible(int fmt, int M, int K, int s_row) {
   return false;
 }
 
+// The workspace head: the counters, then the tagged partial rows (every CTA,
+// every token) and the tagged S partial sums, at fixed places that only this
+// path writes, so that every tagged word there was written by an earlier
+// launch (an older epoch) or is still zero.
 size_t decode_sync_bytes() { return static_cast<size_t>(kDecSyncWords + kDecMaxCtas) * 4; }
-static_assert((kDecSyncWords + kDecMaxCtas) * 4 == EPILORA_WORKSPACE_SYNC_BYTES, "sync block size");
-
-size_t decode_partial_bytes(int M) { return static_cast<size_t>(kDecMaxCtas) * M * 128 * 4; }
+size_t decode_partial_bytes() { return static_cast<size_t>(kDecMaxCtas) * kDecMaxTokens * 128 * 8; }
+size_t decode_s_bytes() { return static_cast<size_t>(kDecSParts) * kDecMaxTokens * kDecMaxSRow * 8; }
+static_assert((kDecSyncWords + kDecMaxCtas) * 4 + static_cast<size_t>(kDecMaxCtas) * kDecMaxTokens * 128 * 8 +
+                      static_cast<size_t>(kDecSParts) * kDecMaxTokens * kDecMaxSRow * 8 ==
+                  EPILORA_WORKSPACE_SYNC_BYTES,
+              "workspace head size");
 
 namespace {
 
@@ -1015,8 +1033,8 @@ int launch_fused_decode(const DecodeArgs& a) {
   p.Y = static_cast<__nv_bfloat16*>(a.Y);
   p.status = a.status_dev;
   p.sync = static_cast<unsigned*>(a.sync);
-  p.S = a.S;
-  p.accp = a.accp;
+  p.S = reinterpret_cast<uint2*>(a.S);
+  p.accp = reinterpret_cast<uint2*>(a.accp);
   p.xq_out = static_cast<uint8_t*>(a.Xq);
   p.xs_out = a.x_scale;
   p.xsb_out = a.x_block_scale;

@@ -119,3 +119,27 @@ def run_case(fmt, M, K, N, L, r, seed=0, idx_mode="uniform", mask_mode="all", n_
     assert int(st.item()) == 0
     bound = tight_bound(ref, xv, wv, B if use_adapter else np.zeros_like(B), idx, mask)
     return np32(Y), ref, bound, (p, w, gx)
+
+
+HEAD_BYTES = 2360576          # EPILORA_WORKSPACE_SYNC_BYTES
+HEAD_S_OFFSET = 1280 + 256 * 8 * 128 * 8   # tagged S partial sums of the single-kernel path in the head
+
+
+def _r256(v):
+    return (v + 255) // 256 * 256
+
+
+def fused_s_partials(buf: torch.Tensor, fmt: int, M: int, K: int, r: int) -> torch.Tensor:
+    """The partial sums of S over K slices [n_parts, M, r] that a fused call
+    left in its workspace `buf` (zero where a slice was not used, if the
+    workspace was zero-filled): in the head as (value, tag) pairs for the
+    single-kernel path, else as floats after the quantized activations."""
+    n_parts = min(8, -(-K // 1024))
+    if E.epilora_layer_forward_kernels(fmt, M, K, r) == 1:
+        w = buf[HEAD_S_OFFSET:HEAD_S_OFFSET + n_parts * M * r * 8].view(torch.int32).view(n_parts, M, r, 2)
+        return w[..., 0].contiguous().view(torch.float32)
+    xq_bytes = M * K if fmt == FP8 else M * K // 2
+    sc_bytes = 4 * M if fmt == FP8 else M * K // 16
+    off = HEAD_BYTES + _r256(xq_bytes) + _r256(sc_bytes)
+    return buf[off:off + n_parts * M * r * 4].view(torch.float32).view(n_parts, M, r)
+

@@ -59,17 +59,14 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    sync = 1280                   # grid-wide counters of the single-kernel decode path, first
-    part = 256 * 128 * 4          # per token: partial rows of split weight tiles (single-kernel path)
+    sync = 2360576                # the head: counters and exchange regions of the single-kernel path
     # counters, Xq, scales, then S with room for ceil(K / 1024) partial sums (at most 8)
-    assert E.epilora_workspace_bytes(0, 4, 512, 16) == sync + r256(4 * 512) + r256(16) + r256(4 * 16 * 4) + 4 * part
-    assert E.epilora_workspace_bytes(1, 4, 512, 16) == sync + r256(4 * 256) + r256(4 * 32) + r256(4 * 16 * 4) + \
-        4 * part
-    assert E.epilora_workspace_bytes(0, 4, 512, 0) == sync + r256(4 * 512) + r256(16) + 4 * part
+    assert E.epilora_workspace_bytes(0, 4, 512, 16) == sync + r256(4 * 512) + r256(16) + r256(4 * 16 * 4)
+    assert E.epilora_workspace_bytes(1, 4, 512, 16) == sync + r256(4 * 256) + r256(4 * 32) + r256(4 * 16 * 4)
+    assert E.epilora_workspace_bytes(0, 4, 512, 0) == sync + r256(4 * 512) + r256(16)
     assert E.epilora_workspace_bytes(0, 2, 14336, 64) == sync + r256(2 * 14336) + r256(8) + r256(2 * 64 * 4 * 8)
     assert E.epilora_workspace_bytes(0, 1, 40960, 16) == sync + r256(40960) + r256(4) + r256(16 * 4 * 8)
-    assert E.epilora_workspace_bytes(0, 3, 4096, 32) == sync + r256(3 * 4096) + r256(12) + r256(3 * 32 * 4 * 4) + \
-        3 * part
+    assert E.epilora_workspace_bytes(0, 3, 4096, 32) == sync + r256(3 * 4096) + r256(12) + r256(3 * 32 * 4 * 4)
     # more than 32 tokens with adapters: plus the adapter-sorted row order (int32 per token)
     assert E.epilora_workspace_bytes(0, 64, 512, 16) == sync + r256(64 * 512) + r256(256) + r256(64 * 16 * 4) + \
         r256(256)

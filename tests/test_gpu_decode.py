@@ -14,12 +14,12 @@ from oracle import epilora_oracle as O
 from precision_gemm_token_gb300 import tensors as T
 from synth import make_projection
 
-from .gpu_util import (FP8, NVFP4, assert_y_close, ensure_lib, np32, npu8, run_case, same_codes_e2m1_packed,
-                       same_codes_e4m3, status_buf)
+from .gpu_util import (FP8, NVFP4, assert_y_close, ensure_lib, fused_s_partials, np32, npu8, run_case,
+                       same_codes_e2m1_packed, same_codes_e4m3, status_buf)
 
 pytestmark = pytest.mark.gpu
 
-SYNC_BYTES = 1280      # EPILORA_WORKSPACE_SYNC_BYTES
+SYNC_BYTES = 2360576   # EPILORA_WORKSPACE_SYNC_BYTES: the head (counters, tagged exchange regions)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -82,7 +82,8 @@ def test_single_kernel_workspace_contents(fmt, M, K, N, r):
     """The activation codes and scales the kernel used (stored by one thread
     block) are the oracle's bit for bit; the shrink's partial sums over K
     slices, added in part order, are the oracle's S within fp32 rounding; the
-    counters at the start of the workspace are zero again."""
+    counters at the start of the workspace are zero again and the epoch has
+    moved on by one."""
     L = 3
     p = make_projection(M, K, N, L, r, seed=M + K, idx_mode="uniform", device="cuda")
     w = T.quantize_weight(p.W, fmt)
@@ -94,7 +95,8 @@ def test_single_kernel_workspace_contents(fmt, M, K, N, r):
     T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx_t, workspace=ws, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    assert int(buf[:SYNC_BYTES].count_nonzero().item()) == 0
+    assert int(buf[:12].count_nonzero().item()) == 0          # claim and exit counters back to zero
+    assert int(buf[12:16].view(torch.int32).item()) == 1      # the epoch moved on by one launch
     x, A, B = p.X.float().cpu().numpy(), p.A.float().cpu().numpy(), p.B.float().cpu().numpy()
     idx, mask = p.idx.cpu().numpy(), p.mask.cpu().numpy()
     r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
@@ -105,7 +107,6 @@ def test_single_kernel_workspace_contents(fmt, M, K, N, r):
         assert same_codes_e4m3(npu8(buf[off:off + M * K].view(M, K)), ref["xq"]).all()
         o2 = off + r256(M * K)
         assert (np32(buf[o2:o2 + 4 * M].view(torch.float32)) == ref["sx"]).all()
-        off_s = o2 + r256(4 * M)
     else:
         Wn = p.W.float().cpu().numpy()
         gw = O.nvfp4_global_scale(Wn)
@@ -114,9 +115,8 @@ def test_single_kernel_workspace_contents(fmt, M, K, N, r):
         assert same_codes_e2m1_packed(npu8(buf[off:off + M * K // 2].view(M, K // 2)), ref["xq"]).all()
         o2 = off + r256(M * K // 2)
         assert (npu8(buf[o2:o2 + M * K // 16].view(M, K // 16)) == ref["sbx"]).all()
-        off_s = o2 + r256(M * K // 16)
     n_parts = min(8, -(-K // 1024))
-    parts = buf[off_s:off_s + n_parts * M * r * 4].view(torch.float32).view(n_parts, M, r)
+    parts = fused_s_partials(buf, fmt, M, K, r)
     S = parts.sum(dim=0) if n_parts == 1 else parts[0].clone()
     for q in range(1, n_parts):
         S += parts[q]
@@ -167,7 +167,7 @@ def test_single_kernel_chain_shares_workspace(fmt):
         torch.cuda.synchronize()
         for c, Y in zip(cases, outs):
             assert torch.equal(Y, c[3])
-    assert int(ws.buf[:SYNC_BYTES].count_nonzero().item()) == 0
+    assert int(ws.buf[:12].count_nonzero().item()) == 0       # claim and exit counters back to zero
 
 
 def test_bounded_wait_runs_out_and_the_context_stays_usable():
@@ -191,7 +191,7 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable():
     T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, workspace=ws, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == E.EPILORA_ERR_TIMEOUT
-    assert int(buf[:SYNC_BYTES].count_nonzero().item()) == 0
+    assert int(buf[:12].count_nonzero().item()) == 0          # claim and exit counters back to zero
     st.zero_()
     Y = T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, workspace=ws, status=st)
     torch.cuda.synchronize()

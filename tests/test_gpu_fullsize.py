@@ -23,7 +23,8 @@ from oracle import epilora_oracle as O
 from precision_gemm_token_gb300 import tensors as T
 from synth import LLAMA8B_PROJECTIONS, LLAMA70B_PROJECTIONS, make_projection
 
-from .gpu_util import FP8, NVFP4, ensure_lib, np32, npu8, same_codes_e2m1_packed, same_codes_e4m3, status_buf
+from .gpu_util import (FP8, NVFP4, ensure_lib, fused_s_partials, np32, npu8, same_codes_e2m1_packed, same_codes_e4m3,
+                       status_buf)
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +37,7 @@ def _lib():
     ensure_lib()
 
 
-SYNC_BYTES = 1280      # EPILORA_WORKSPACE_SYNC_BYTES
+SYNC_BYTES = 2360576   # EPILORA_WORKSPACE_SYNC_BYTES: the head (counters, tagged exchange regions)
 
 
 def _r256(v):
@@ -93,7 +94,7 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
     # for min(8, ceil(K / 1024)) partial sums), and for more than 32 tokens
     # the adapter-sorted row order: row q holds token perm[q]
     off_xq = SYNC_BYTES
-    assert int(buf[:SYNC_BYTES].count_nonzero().item()) == 0
+    assert int(buf[:12].count_nonzero().item()) == 0          # claim and exit counters back to zero
     xq_bytes = M * K if fmt == FP8 else M * K // 2
     sc_bytes = 4 * M if fmt == FP8 else M * K // 16
     off_perm = off_xq + _r256(xq_bytes) + _r256(sc_bytes) + _r256(M * r * 4 * min(8, -(-K // 1024)))
@@ -134,8 +135,7 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
     # GEMM adds them; and from the standalone shrink
     S_ref = ref["S"]
     n_parts = min(8, -(-K // 1024))
-    off_s = off_xq + _r256(xq_bytes) + _r256(sc_bytes)
-    parts = buf[off_s:off_s + n_parts * M * r * 4].view(torch.float32).view(n_parts, M, r)[:, rows_t, :]
+    parts = fused_s_partials(buf, fmt, M, K, r)[:, rows_t, :]
     S_fused = parts[0].clone()
     for q in range(1, n_parts):
         S_fused += parts[q]
