@@ -347,10 +347,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         if (C::kFP4) tma_load_2d(st + C::kUnitW + C::kSfA, &p.tmSW, &full_bar[s], kb * 16 * KA, T * 128);
         issued_mask |= 1u << s;
         parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
-        if (it == stages - 1 || u + 1 == u_end) {
-          // the ring is primed: the units behind it go to L2 now
+        // L2 prefetch window: once the ring is primed, the next l2_ahead
+        // units go to L2, and from then on each issued unit moves the window
+        // by one, so every ring fill finds its unit in L2
+        if (p.l2_ahead > 0 && it >= stages - 1) {
+          const long long a_begin = it == stages - 1 ? u + 1 : u + p.l2_ahead;
           const long long a_end = min(u_end, u + 1 + p.l2_ahead);
-          for (long long v = u + 1; v < a_end; ++v) {
+          for (long long v = a_begin; v < a_end; ++v) {
             const int T2 = static_cast<int>(v / p.nkb);
             const int kb2 = static_cast<int>(v - static_cast<long long>(T2) * p.nkb);
 #pragma unroll
