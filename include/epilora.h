@@ -116,8 +116,10 @@ EPILORA_API const char* epilora_status_string(int status);
  *        code = E2M1_rn_satfinite(fl32(X * fl32(g / sb)));
  *        x_block_scale[t,b] = sb (E4M3 byte)          (x_scale ignored)
  * Applied to a weight matrix (M := N rows) this also produces the FP8
- * per-output-channel weight scales and the NVFP4 weight codes.
- * Codes and scales are bit-exact functions of the inputs.
+ * per-output-channel weight scales and the NVFP4 weight codes, and applied to
+ * the rows of adapter tables the stored FP8 adapters of
+ * epilora_layer_forward_fp8_adapters (FP8 takes any K % 16 == 0, so rank-16
+ * rows too). Codes and scales are bit-exact functions of the inputs.
  */
 EPILORA_API int epilora_quant_act(int fmt, const void* X, int M, int K, int ldx,
                       void* Xq, float* x_scale, uint8_t* x_block_scale,
@@ -275,6 +277,35 @@ EPILORA_API int epilora_layer_forward_slices(int fmt, int M, int N, int K,
                           const float* x_global_scale,
                           const void* A, const void* B, int L, int r,
                           int n_slices, const int* slice_end,
+                          const int32_t* idx, const uint8_t* mask,
+                          void* Y, int ldy,
+                          void* workspace, size_t workspace_bytes,
+                          int* status_dev, void* stream);
+
+/*
+ * Stored FP8 adapters (EpiLoRA page, §Design › Multi-adapter kernels › K1
+ * and K2: adapters may be kept in FP8 and are dequantized in registers):
+ * epilora_layer_forward with the adapter tables as E4M3 codes and one fp32
+ * scale per row,
+ *   Aq uint8 [L, r, K], a_scale fp32 [L, r]   (rank j of adapter l over K)
+ *   Bq uint8 [L, N, r], b_scale fp32 [L, N]   (output n of adapter l over r)
+ *   S[t, j] = a_scale[l, j] * sum_k X[t, k] * E4M3(Aq[l, j, k])   (l = idx_t)
+ *   d[t, n] = b_scale[l, n] * sum_j S[t, j] * E4M3(Bq[l, n, j])
+ * (the codes and scales of each row as epilora_quant_act gives them for the
+ * row). About half the adapter bytes of bf16 tables; the page reports that
+ * part of its accuracy checks with stored adapters failed, so this is an
+ * option for the caller, not a default. Decode batches only: M <= 32, else
+ * EPILORA_ERR_UNSUPPORTED. Workspace as epilora_layer_forward (r as given);
+ * other arguments, results and errors as there (all four adapter pointers
+ * required).
+ */
+EPILORA_API int epilora_layer_forward_fp8_adapters(int fmt, int M, int N, int K,
+                          const void* X, int ldx,
+                          const void* Wq, const float* w_scale,
+                          const uint8_t* w_block_scale, const float* w_global_scale,
+                          const float* x_global_scale,
+                          const uint8_t* Aq, const float* a_scale,
+                          const uint8_t* Bq, const float* b_scale, int L, int r,
                           const int32_t* idx, const uint8_t* mask,
                           void* Y, int ldy,
                           void* workspace, size_t workspace_bytes,

@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     epilora_abi_version,
     epilora_gemm_lora_epilogue,
     epilora_layer_forward,
+    epilora_layer_forward_fp8_adapters,
     epilora_layer_forward_kernels,
     epilora_layer_forward_noalloc,
     epilora_layer_forward_slices,

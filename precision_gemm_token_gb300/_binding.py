@@ -39,6 +39,9 @@ SIGNATURES = {
     "epilora_layer_forward_kernels": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
     "epilora_layer_forward": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _sz, _vp, _vp]),
+    "epilora_layer_forward_fp8_adapters": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp,
+                                                    _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int,
+                                                    _vp, _sz, _vp, _vp]),
     "epilora_layer_forward_noalloc": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp,
                                                _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp]),
     "epilora_layer_forward_slices": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp, _vp,
@@ -160,6 +163,15 @@ def epilora_layer_forward_slices(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scal
                                                n_slices, ctypes.cast(ends, ctypes.c_void_p), _p(idx), _p(mask),
                                                _p(Y), ldy, _p(workspace), workspace_bytes, _p(status_dev),
                                                _stream(stream))
+
+
+def epilora_layer_forward_fp8_adapters(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale,
+                                       x_global_scale, Aq, a_scale, Bq, b_scale, L, r, idx, mask, Y, ldy, workspace,
+                                       workspace_bytes, status_dev=None, stream=None) -> int:
+    return load().epilora_layer_forward_fp8_adapters(fmt, M, N, K, _p(X), ldx, _p(Wq), _p(w_scale), _p(w_block_scale),
+                                                     _p(w_global_scale), _p(x_global_scale), _p(Aq), _p(a_scale),
+                                                     _p(Bq), _p(b_scale), L, r, _p(idx), _p(mask), _p(Y), ldy,
+                                                     _p(workspace), workspace_bytes, _p(status_dev), _stream(stream))
 
 
 def epilora_layer_forward_noalloc(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale,

@@ -36,7 +36,9 @@ inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 bool quant_args_ok(int fmt, const void* X, int M, int K, int ldx, const void* Xq, const float* x_scale,
                    const uint8_t* x_block_scale, const float* x_global_scale) {
-  if (!fmt_ok(fmt) || M < 0 || !k_ok(K) || ldx < K || ldx % 8 != 0) return false;
+  // FP8 rows need only whole 16-element groups (rank-16 rows of adapter tables)
+  const bool kq = fmt == EPILORA_FMT_FP8_E4M3 ? (K >= 16 && K % 16 == 0) : k_ok(K);
+  if (!fmt_ok(fmt) || M < 0 || !kq || ldx < K || ldx % 8 != 0) return false;
   if (M == 0) return true;
   if (X == nullptr || Xq == nullptr || !al16(X) || !al16(Xq)) return false;
   if (fmt == EPILORA_FMT_FP8_E4M3) return x_scale != nullptr && al4(x_scale);
@@ -256,8 +258,14 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
                               const float* x_global_scale, const void* A, const void* B, int L, int r,
                               const int32_t* idx, const uint8_t* mask, void* Y, int ldy, void* workspace,
                               size_t workspace_bytes, int* status_dev, void* stream, int n_slices,
-                              const int* slice_end) {
+                              const int* slice_end, const float* a_scale = nullptr, const float* b_scale = nullptr) {
   const bool adapters = A != nullptr && B != nullptr;
+  // stored FP8 adapters (both scales given): decode batches of at most 32 tokens
+  if ((a_scale == nullptr) != (b_scale == nullptr)) return EPILORA_ERR_INVALID_ARG;
+  if (a_scale != nullptr) {
+    if (!adapters || !al4(a_scale) || !al4(b_scale)) return EPILORA_ERR_INVALID_ARG;
+    if (M > 32) return EPILORA_ERR_UNSUPPORTED;
+  }
   // S rows: n_slices rank-r blocks (the shrink runs with rank r * n_slices)
   const int rs = r * n_slices;
   if (!fmt_ok(fmt) || M < 0 || !k_ok(K) || ldx < K || ldx % 8 != 0) return EPILORA_ERR_INVALID_ARG;
@@ -331,6 +339,8 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
     d.x_global_scale = x_global_scale;
     d.A = adapters ? A : nullptr;
     d.B = adapters ? B : nullptr;
+    d.a_scale = a_scale;
+    d.b_scale = b_scale;
     d.idx = idx;
     d.mask = mask;
     d.Y = Y;
@@ -351,7 +361,7 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
   // the token metadata) only after that grid has completed.
   const int parts = adapters ? shrink_parts(M, K, rs) : shrink_parts(M, K, 0);
   rc = launch_shrink_quant(X, M, K, ldx, A, adapters ? L : 1, adapters ? rs : 0, idx, mask, S, parts, fmt, Xq,
-                           x_scale, x_block_scale, x_global_scale, perm, status_dev, st);
+                           x_scale, x_block_scale, x_global_scale, perm, status_dev, st, a_scale);
   if (rc != EPILORA_OK) return rc;
   GemmArgs a{};
   a.fmt = fmt;
@@ -368,6 +378,7 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
   a.w_global_scale = w_global_scale;
   a.S = S;
   a.B = B;
+  a.b_scale = b_scale;
   a.L = adapters ? L : 1;
   a.r = adapters ? r : 16;
   a.idx = idx;
@@ -418,6 +429,19 @@ EPILORA_API int epilora_layer_forward_slices(int fmt, int M, int N, int K, const
   return layer_forward_impl(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale, x_global_scale, A, B,
                             L, r, idx, mask, Y, ldy, workspace, workspace_bytes, status_dev, stream, n_slices,
                             slice_end);
+}
+
+EPILORA_API int epilora_layer_forward_fp8_adapters(int fmt, int M, int N, int K, const void* X, int ldx,
+                                                   const void* Wq, const float* w_scale, const uint8_t* w_block_scale,
+                                                   const float* w_global_scale, const float* x_global_scale,
+                                                   const uint8_t* Aq, const float* a_scale, const uint8_t* Bq,
+                                                   const float* b_scale, int L, int r, const int32_t* idx,
+                                                   const uint8_t* mask, void* Y, int ldy, void* workspace,
+                                                   size_t workspace_bytes, int* status_dev, void* stream) {
+  if (Aq == nullptr || Bq == nullptr || a_scale == nullptr || b_scale == nullptr) return EPILORA_ERR_INVALID_ARG;
+  return layer_forward_impl(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale, x_global_scale, Aq,
+                            Bq, L, r, idx, mask, Y, ldy, workspace, workspace_bytes, status_dev, stream, 1, nullptr,
+                            a_scale, b_scale);
 }
 
 }  // extern "C"

@@ -43,6 +43,7 @@ struct GemmArgs {
   const float* w_global_scale;
   const float* S;
   const void* B;
+  const float* b_scale = nullptr;   // stored FP8 B (E4M3 [L, N, r] bytes, fp32 scale per row [L, N])
   int L, r;
   const int32_t* idx;
   const uint8_t* mask;
@@ -80,10 +81,12 @@ int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, in
 // perm != nullptr (s_parts == 1 only): the quantized rows and their scales are
 // written in adapter-sorted order (key idx[t] if the token carries an adapter,
 // else L; ties by token), and perm[row] = token.
+// a_scale != nullptr: A holds E4M3 codes [L, r, K] bytes with one fp32 scale
+// per row [L, r] (stored FP8 adapters; at most 32 tokens).
 int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
                         const uint8_t* mask, float* S, int s_parts, int fmt, void* Xq, float* x_scale,
                         uint8_t* x_block_scale, const float* x_global_scale, int32_t* perm, int* status_dev,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const float* a_scale = nullptr);
 // Number of K slices launch_shrink_quant uses for (M, K, r) (1 when M > 32),
 // and the largest it can use for K (sizes the workspace).
 int shrink_parts(int M, int K, int r);
@@ -105,6 +108,8 @@ struct DecodeArgs {
   const float* x_global_scale;
   const void* A;        // NULL with B: no adapters
   const void* B;
+  const float* a_scale; // stored FP8 adapters: row scales of A [L, s_row] and B [L, N]; NULL: bf16
+  const float* b_scale;
   const int32_t* idx;
   const uint8_t* mask;
   void* Y;

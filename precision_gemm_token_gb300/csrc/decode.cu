@@ -14,34 +14,38 @@
 //
 // GB300 design: one persistent CTA per SM (about 113 KB of shared memory, so
 // the next projection's CTA fits beside it and streams its weights while this
-// one finishes). The weight matrix is cut into units (128 rows x 128 bytes of
-// K, 16 KB of codes) in tile-major order and every CTA takes an equal
+// one finishes). The weight matrix is cut into units (128 rows x 256 bytes of
+// K, 32 KB of codes) in tile-major order and every CTA takes an equal
 // contiguous run of units (stream-K), so no SM streams more than its share.
 // Roles (192 threads):
 //   warp 0      TMA producer: the CTA's weight units (and NVFP4 weight scale
 //               boxes) through a ring, started before the dependency wait
-//               (weights are never written by the preceding kernel), plus an
-//               L2 prefetch of the units behind the ring;
-//   warp 1      MMA issuer: copies the unit's quantized activation rows from
-//               shared memory into the stage, then tcgen05.mma (kind::f8f6f4,
-//               or kind::mxf4nvf4 with scales copied into TMEM) into one of
-//               two TMEM accumulators (one per segment of the run that falls
-//               in one weight tile);
-//   warps 2..5  helpers: wait for the preceding kernel (griddepcontrol.wait),
-//               quantize the activations of all tokens into shared memory
-//               (every CTA does it for itself: at most 16 KB of codes), then
-//               take shrink work items from a grid-wide counter (token x 4
-//               ranks x K slice, the arithmetic of the standalone shrink),
-//               publish each partial sum of S and count it done; then the
-//               epilogue of each segment.
+//               (weights are never written by the preceding kernel) and
+//               behind the helpers' L2 hints;
+//   warp 1      MMA issuer: tcgen05.mma (kind::f8f6f4, or kind::mxf4nvf4 with
+//               scales copied into TMEM) into one of two TMEM accumulators
+//               (one per segment of the run that falls in one weight tile),
+//               the activations read in place from the compact quantized
+//               copy (a no-swizzle operand whose core matrices are M x 16
+//               bytes apart along K);
+//   warps 2..5  helpers: L2 hints (activations, A rows, B slices), the
+//               dependency wait (griddepcontrol.wait), one bulk copy of the
+//               bf16 activation rows into the last ring slots, quantization
+//               of every token into shared memory (each CTA for itself: FP8
+//               divisions by Markstein's correction of the reciprocal
+//               product), shrink work items (token x 4 ranks x K slice, the
+//               arithmetic of the standalone shrink: item c is CTA c's, items
+//               past the grid are claimed from a counter), then the epilogue
+//               of each segment.
 // A weight tile split over several CTAs is finished by the CTA that holds its
-// first K unit (it reaches that tile last): the other CTAs store their fp32
-// partial rows and raise a flag; the finisher adds them in CTA order
-// (deterministic), then the scales, then the adapter term once every shrink
-// item is counted, and writes Y. Every wait is bounded (an error status, then
-// an orderly exit), and waits only on work already claimed by running CTAs.
-// The grid-wide counters live in the first bytes of the workspace; the last
-// CTA to exit returns them to zero.
+// first K unit (it reaches that tile last): the others store their fp32
+// partial rows, and the shrink items their partial sums of S, each value in a
+// 64-bit word with this launch's tag (a mix of an epoch the previous launch
+// moved on); the finisher reads them until the tags match, adds the partial
+// rows in CTA order and S's slices in part order (deterministic), applies the
+// scales, adds the adapter term and writes Y. Every wait is bounded (an error
+// status, then an orderly exit) and waits only on work already claimed by
+// running CTAs; the last CTA to exit resets the counters and moves the epoch.
 #include "quant_row.cuh"
 
 namespace epi {
@@ -71,6 +75,10 @@ struct DecParams {
   const __nv_bfloat16* X;
   const __nv_bfloat16* A;
   const __nv_bfloat16* B;
+  // stored FP8 adapters: A and B hold E4M3 codes ([L, s_row, K] and [L, N, r]
+  // bytes) with one fp32 scale per row; null: bf16 tables
+  const float* a_scale;
+  const float* b_scale;
   const int32_t* idx;
   const uint8_t* mask;
   const float* w_scale;
@@ -88,7 +96,7 @@ struct DecParams {
   float* xs_out;       // FP8 scales
   uint8_t* xsb_out;    // NVFP4 block scales
   long long U;         // units in total
-  int G, nkb, n_tiles, stages, l2_ahead;
+  int G, nkb, n_tiles, stages;
   int M, N, K, ldx, ldy, L, r, s_row, n_slices;
   int slice_end[4];
   int adapters, parts, kslice, n_items;
@@ -201,6 +209,49 @@ __device__ __forceinline__ uint2 quant8_e4m3_rs(const uint4& v, float s, float r
 
 // S[v] . B[l, n] with the B row in registers (R4 float4 chunks of S from
 // shared memory; two accumulators)
+// Two E4M3 codes (the low 16 bits of c, low byte first) as floats.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t c) {
+  uint32_t h2;
+  const uint16_t c16 = static_cast<uint16_t>(c & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c16));
+  __half2_raw hr;
+  hr.x = static_cast<unsigned short>(h2 & 0xFFFFu);
+  hr.y = static_cast<unsigned short>(h2 >> 16);
+  return __half22float2(__half2(hr));
+}
+
+// x (8 bf16) . a (8 E4M3 codes), accumulated into acc in element order
+__device__ __forceinline__ float dec_dot8_e4m3(const uint4& xv, const uint2& av, float acc) {
+  const float2 a01 = e4m3x2_to_f32x2(av.x), a23 = e4m3x2_to_f32x2(av.x >> 16);
+  const float2 a45 = e4m3x2_to_f32x2(av.y), a67 = e4m3x2_to_f32x2(av.y >> 16);
+  acc = fmaf(bf16_lo(xv.x), a01.x, acc);
+  acc = fmaf(bf16_hi(xv.x), a01.y, acc);
+  acc = fmaf(bf16_lo(xv.y), a23.x, acc);
+  acc = fmaf(bf16_hi(xv.y), a23.y, acc);
+  acc = fmaf(bf16_lo(xv.z), a45.x, acc);
+  acc = fmaf(bf16_hi(xv.z), a45.y, acc);
+  acc = fmaf(bf16_lo(xv.w), a67.x, acc);
+  acc = fmaf(bf16_hi(xv.w), a67.y, acc);
+  return acc;
+}
+
+// S[v] . codes of an E4M3 B row held 4 per 32-bit word (R4 float4 chunks)
+template <int R4>
+__device__ __forceinline__ float dec_dot_row_e4m3(const float4* srow, const uint32_t* brow) {
+  float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+  for (int c = 0; c < R4; ++c) {
+    const float4 s4 = srow[c];
+    const float2 lo = e4m3x2_to_f32x2(brow[c]), hi = e4m3x2_to_f32x2(brow[c] >> 16);
+    float& d = (c & 1) ? d1 : d0;
+    d = fmaf(s4.x, lo.x, d);
+    d = fmaf(s4.y, lo.y, d);
+    d = fmaf(s4.z, hi.x, d);
+    d = fmaf(s4.w, hi.y, d);
+  }
+  return d0 + d1;
+}
+
 template <int R4>
 __device__ __forceinline__ float dec_dot_row(const float4* srow, const uint32_t* brow) {
   float d0 = 0.0f, d1 = 0.0f;
@@ -347,20 +398,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         if (C::kFP4) tma_load_2d(st + C::kUnitW + C::kSfA, &p.tmSW, &full_bar[s], kb * 16 * KA, T * 128);
         issued_mask |= 1u << s;
         parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
-        // L2 prefetch window: once the ring is primed, the next l2_ahead
-        // units go to L2, and from then on each issued unit moves the window
-        // by one, so every ring fill finds its unit in L2
-        if (p.l2_ahead > 0 && it >= stages - 1) {
-          const long long a_begin = it == stages - 1 ? u + 1 : u + p.l2_ahead;
-          const long long a_end = min(u_end, u + 1 + p.l2_ahead);
-          for (long long v = a_begin; v < a_end; ++v) {
-            const int T2 = static_cast<int>(v / p.nkb);
-            const int kb2 = static_cast<int>(v - static_cast<long long>(T2) * p.nkb);
-#pragma unroll
-            for (int a = 0; a < KA; ++a) tma_prefetch_l2_2d(&p.tmW, (kb2 * KA + a) * 128, T2 * 128);
-            if (C::kFP4) tma_prefetch_l2_2d(&p.tmSW, kb2 * 16 * KA, T2 * 128);
-          }
-        }
       }
       // every weight byte of this CTA is requested: the next kernel on the
       // stream may start its CTAs (they wait for this grid before reading
@@ -492,7 +529,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       for (int t = 0; t < M; ++t)
         prefetch_l2_bulk(p.X + static_cast<size_t>(t) * p.ldx, static_cast<uint32_t>(p.K * 2));
       if (p.adapters) {
-        const size_t abytes = static_cast<size_t>(p.s_row) * p.K * 2;
+        const size_t abytes = static_cast<size_t>(p.s_row) * p.K * (p.a_scale != nullptr ? 1 : 2);
         const size_t share = ((abytes + p.G - 1) / p.G + 255) / 256 * 256;
         const size_t lo = share * c;
         int prev = -1;
@@ -509,8 +546,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           while (w2.next(T, kb0, kb1)) {
             if (kb0 != 0) continue;
             const int rows = min(128, p.N - T * 128);
-            prefetch_l2_bulk(p.B + (static_cast<size_t>(l) * p.N + T * 128) * p.r,
-                             static_cast<uint32_t>(rows * p.r * 2));
+            const int bb = p.a_scale != nullptr ? p.r : 2 * p.r;   // bytes of one B row
+            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.B) + (static_cast<size_t>(l) * p.N + T * 128) * bb,
+                             static_cast<uint32_t>(rows * bb));
           }
         }
       }
@@ -678,11 +716,14 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     bool s_ready = false;
     uint32_t brow[kMaxRankBrow];
     long long brow_key = -1;
+    const bool qa = p.a_scale != nullptr;         // stored FP8 adapters
+    const int brow_bytes = qa ? p.r : 2 * p.r;
     auto load_brow = [&](int l, int T, int n) {
-      const uint4* bsrc = reinterpret_cast<const uint4*>(p.B + (static_cast<size_t>(l) * p.N + n) * p.r);
+      const uint4* bsrc = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.B) +
+                                                         (static_cast<size_t>(l) * p.N + n) * brow_bytes);
 #pragma unroll
       for (int cc = 0; cc < kMaxRankBrow / 4; ++cc)
-        if (cc < p.r / 8) {
+        if (cc < brow_bytes / 16) {
           const uint4 bv = ldg_nc_v4_now(bsrc + cc);
           brow[4 * cc] = bv.x;
           brow[4 * cc + 1] = bv.y;
@@ -785,11 +826,22 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           if (l >= 0) {
             if (static_cast<long long>(l) * p.n_tiles + T != brow_key) load_brow(l, T, n);
             const float4* srow = reinterpret_cast<const float4*>(s_stage + t * p.s_row + soff);
-            switch (p.r) {
-              case 16: y += dec_dot_row<4>(srow, brow); break;
-              case 32: y += dec_dot_row<8>(srow, brow); break;
-              case 64: y += dec_dot_row<16>(srow, brow); break;
-              default: y += dec_dot_row<32>(srow, brow); break;
+            if (qa) {
+              float d;
+              switch (p.r) {
+                case 16: d = dec_dot_row_e4m3<4>(srow, brow); break;
+                case 32: d = dec_dot_row_e4m3<8>(srow, brow); break;
+                case 64: d = dec_dot_row_e4m3<16>(srow, brow); break;
+                default: d = dec_dot_row_e4m3<32>(srow, brow); break;
+              }
+              y += d * __ldg(p.b_scale + static_cast<size_t>(l) * p.N + n);
+            } else {
+              switch (p.r) {
+                case 16: y += dec_dot_row<4>(srow, brow); break;
+                case 32: y += dec_dot_row<8>(srow, brow); break;
+                case 64: y += dec_dot_row<16>(srow, brow); break;
+                default: y += dec_dot_row<32>(srow, brow); break;
+              }
             }
           }
           p.Y[static_cast<size_t>(t) * p.ldy + n] = __float2bfloat16_rn(y);
@@ -812,19 +864,33 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         const int c0 = part * p.kslice / 8;
         const int c1 = min(p.K, (part + 1) * p.kslice) / 8;
         const uint4* xr = reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(t) * p.ldx);
-        const uint4* ar =
-            reinterpret_cast<const uint4*>(p.A + (static_cast<size_t>(l) * p.s_row + j0) * static_cast<size_t>(p.K));
+        const size_t arow = (static_cast<size_t>(l) * p.s_row + j0) * static_cast<size_t>(p.K);   // first A row
         float accs[kDecRanksPerItem];
 #pragma unroll
         for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = 0.0f;
+        if (!qa) {
+          const uint4* ar = reinterpret_cast<const uint4*>(p.A + arow);
 #pragma unroll 2
-        for (int ch = c0 + et; ch < c1; ch += 128) {
-          const uint4 xw = __ldcg(xr + ch);
-          uint4 av[kDecRanksPerItem];
+          for (int ch = c0 + et; ch < c1; ch += 128) {
+            const uint4 xw = __ldcg(xr + ch);
+            uint4 av[kDecRanksPerItem];
 #pragma unroll
-          for (int jr = 0; jr < kDecRanksPerItem; ++jr) av[jr] = __ldg(ar + static_cast<size_t>(jr) * nch + ch);
+            for (int jr = 0; jr < kDecRanksPerItem; ++jr) av[jr] = __ldg(ar + static_cast<size_t>(jr) * nch + ch);
 #pragma unroll
-          for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = dec_dot8(xw, av[jr], accs[jr]);
+            for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = dec_dot8(xw, av[jr], accs[jr]);
+          }
+        } else {
+          // E4M3 rows: 8 codes (8 bytes) per 8 activations
+          const uint2* ar = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(p.A) + arow);
+#pragma unroll 2
+          for (int ch = c0 + et; ch < c1; ch += 128) {
+            const uint4 xw = __ldcg(xr + ch);
+            uint2 av[kDecRanksPerItem];
+#pragma unroll
+            for (int jr = 0; jr < kDecRanksPerItem; ++jr) av[jr] = __ldg(ar + static_cast<size_t>(jr) * nch + ch);
+#pragma unroll
+            for (int jr = 0; jr < kDecRanksPerItem; ++jr) accs[jr] = dec_dot8_e4m3(xw, av[jr], accs[jr]);
+          }
         }
 #pragma unroll
         for (int jr = 0; jr < kDecRanksPerItem; ++jr) {
@@ -841,7 +907,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           for (int jr = 0; jr < kDecRanksPerItem; ++jr) {
             float sum = 0.0f;
             for (int w = 0; w < 4; ++w) sum += red[w * kDecRanksPerItem + jr];
-            ov[jr] = sum;
+            // stored FP8 rows: the row's scale applied to the slice's sum
+            ov[jr] = qa ? sum * __ldg(p.a_scale + static_cast<size_t>(l) * p.s_row + j0 + jr) : sum;
           }
           uint4* dst = reinterpret_cast<uint4*>(p.S + (static_cast<size_t>(part) * M + t) * p.s_row + j0);
           __stcg(dst, make_uint4(__float_as_uint(o.x), epoch, __float_as_uint(o.y), epoch));
@@ -990,8 +1057,6 @@ int launch_fused_decode_t(DecParams& p, const DecodeArgs& a) {
     rc = make_tma_2d_u8(&p.tmSW, a.w_block_scale, a.N, a.K / 16, a.K / 16, 128, 16 * KA, false);
     if (rc != EPILORA_OK) return rc;
   }
-  // L2 prefetch behind the ring: about 40 MB over the grid
-  p.l2_ahead = static_cast<int>((40L << 20) / (static_cast<long>(G) * C::kStageTx));
   const int smem = pl.fixed + pl.stages * C::kStage;
 
   auto kern = fused_decode_kernel<FMT, KA>;
@@ -1028,6 +1093,8 @@ int launch_fused_decode(const DecodeArgs& a) {
   p.X = static_cast<const __nv_bfloat16*>(a.X);
   p.A = static_cast<const __nv_bfloat16*>(a.A);
   p.B = static_cast<const __nv_bfloat16*>(a.B);
+  p.a_scale = a.a_scale;
+  p.b_scale = a.b_scale;
   p.idx = a.idx;
   p.mask = a.mask;
   p.w_scale = a.w_scale;

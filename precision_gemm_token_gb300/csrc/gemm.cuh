@@ -78,6 +78,7 @@ struct GemmParams {
   const float* w_gs;
   const float* S;
   const __nv_bfloat16* B;
+  const float* b_scale;  // stored FP8 B: E4M3 codes [L, N, r] bytes with one fp32 scale per row [L, N]; null: bf16
   const int32_t* idx;
   const uint8_t* mask;
   __nv_bfloat16* Y;
@@ -231,6 +232,41 @@ __device__ __forceinline__ float dot_srow_brow(const float4* srow, const uint32_
 // S[t] . B_g[row] for a B row of NC 16-byte chunks held in a swizzled ring
 // box (chunk c in atom c >> cpa_log, at position (c & mask) ^ xr), S in
 // shared memory; loads independent, two accumulators.
+// The same for an E4M3 B row (16 codes per 16-byte chunk, S in chunks of 16).
+__device__ __forceinline__ float2 e4m3x2_f32(uint32_t c) {
+  uint32_t h2;
+  const uint16_t c16 = static_cast<uint16_t>(c & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c16));
+  __half2_raw hr;
+  hr.x = static_cast<unsigned short>(h2 & 0xFFFFu);
+  hr.y = static_cast<unsigned short>(h2 >> 16);
+  return __half22float2(__half2(hr));
+}
+template <int NC>
+__device__ __forceinline__ float dot_b_row_e4m3(const uint8_t* gb, int atom_stride, int cpa_log, int mask, int xr,
+                                                const float4* srow) {
+  float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(gb + (c >> cpa_log) * atom_stride + (((c & mask) ^ xr) << 4));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float& d = (c & 1) ? d1 : d0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 s4 = srow[4 * c + q];
+      const float2 lo = e4m3x2_f32(w[q]), hi = e4m3x2_f32(w[q] >> 16);
+      d = fmaf(s4.x, lo.x, d);
+      d = fmaf(s4.y, lo.y, d);
+      d = fmaf(s4.z, hi.x, d);
+      d = fmaf(s4.w, hi.y, d);
+    }
+  }
+  return d0 + d1;
+}
+// S[t] . B_g[row] for the row at gb (bf16 or E4M3 per b_scale), rank r
+__device__ __forceinline__ float dot_b_row_any(const uint8_t* gb, int atom_stride, int cpa_log, int mask, int xr,
+                                               const float4* srow, int r, bool fp8);
+
 template <int NC>
 __device__ __forceinline__ float dot_b_row(const uint8_t* gb, int atom_stride, int cpa_log, int mask, int xr,
                                            const float4* srow) {
@@ -250,6 +286,24 @@ __device__ __forceinline__ float dot_b_row(const uint8_t* gb, int atom_stride, i
     d = fmaf(s1.w, bf16_hi(v.w), d);
   }
   return d0 + d1;
+}
+
+__device__ __forceinline__ float dot_b_row_any(const uint8_t* gb, int atom_stride, int cpa_log, int mask, int xr,
+                                               const float4* srow, int r, bool fp8) {
+  if (fp8) {
+    switch (r) {
+      case 16: return dot_b_row_e4m3<1>(gb, atom_stride, cpa_log, mask, xr, srow);
+      case 32: return dot_b_row_e4m3<2>(gb, atom_stride, cpa_log, mask, xr, srow);
+      case 64: return dot_b_row_e4m3<4>(gb, atom_stride, cpa_log, mask, xr, srow);
+      default: return dot_b_row_e4m3<8>(gb, atom_stride, cpa_log, mask, xr, srow);
+    }
+  }
+  switch (r) {   // rank 16 / 32 / 64 / 128: a loop without guards per chunk
+    case 16: return dot_b_row<2>(gb, atom_stride, cpa_log, mask, xr, srow);
+    case 32: return dot_b_row<4>(gb, atom_stride, cpa_log, mask, xr, srow);
+    case 64: return dot_b_row<8>(gb, atom_stride, cpa_log, mask, xr, srow);
+    default: return dot_b_row<16>(gb, atom_stride, cpa_log, mask, xr, srow);
+  }
 }
 
 template <int FMT, int BT, int KA>
@@ -895,7 +949,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       const int sw_mask = sw_span / 16 - 1;
       const int sw_shift = sw_span == 128 ? 0 : sw_span == 64 ? 1 : 2;   // row >> shift = (row * span) / 128
       const int cpa_log = 3 - sw_shift;                    // log2 of the 16-byte chunks per atom
-      const int nchunk = p.r / 8;                          // 16-byte chunks of a B row
+      const bool bq = p.b_scale != nullptr;                // stored FP8 B rows (r bytes each)
       const int atom_stride = RR * sw_span;                // bytes between a group's atoms
       if (b_early_on) {
         // the only group's slice is in its own buffer
@@ -906,13 +960,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
             const int tl = g_order[k];
             const uint8_t* gb = b_early_buf + i * sw_span;
             const float4* srow = reinterpret_cast<const float4*>(s_stage + tl * p.r);
-            float d;
-            switch (nchunk) {
-              case 2: d = dot_b_row<2>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
-              case 4: d = dot_b_row<4>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
-              case 8: d = dot_b_row<8>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
-              default: d = dot_b_row<16>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
-            }
+            float d = dot_b_row_any(gb, atom_stride, cpa_log, sw_mask, xr, srow, p.r, bq);
+            if (bq) d *= __ldg(p.b_scale + static_cast<size_t>(g_adapter[0]) * p.N + n0 + row_lo + i);
             y_tile[tl * RR + i] += d;
           }
           asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
@@ -943,13 +992,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
           const int tl = g_order[k];
           const uint8_t* gb = st + (g_of[k] - g0) * p.b_group_bytes + i * sw_span;
           const float4* srow = reinterpret_cast<const float4*>(s_stage + tl * p.r);
-          float d;
-          switch (nchunk) {   // rank 16 / 32 / 64 / 128: a loop without guards per chunk
-            case 2: d = dot_b_row<2>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
-            case 4: d = dot_b_row<4>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
-            case 8: d = dot_b_row<8>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
-            default: d = dot_b_row<16>(gb, atom_stride, cpa_log, sw_mask, xr, srow); break;
-          }
+          float d = dot_b_row_any(gb, atom_stride, cpa_log, sw_mask, xr, srow, p.r, bq);
+          if (bq) d *= __ldg(p.b_scale + static_cast<size_t>(g_adapter[g_of[k]]) * p.N + n0 + row_lo + i);
           y_tile[tl * RR + i] += d;
         }
         asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
@@ -1256,8 +1300,10 @@ int launch_gemm_tiled(const GemmArgs& a) {
   const int RR = gemm_red_rows(ks);
 
   // streamed B (decode tiles): one TMA box of the tile's rows per adapter,
-  // its inner extent the row of B (2r bytes, in atoms of at most 128 B)
-  const int brow_bytes = 2 * a.r;
+  // its inner extent the row of B (2r bytes, or r for stored FP8 rows, in
+  // atoms of at most 128 B)
+  p.b_scale = a.b_scale;
+  const int brow_bytes = a.b_scale != nullptr ? a.r : 2 * a.r;
   p.b_box_bytes = brow_bytes >= 128 ? 128 : brow_bytes;
   p.b_atoms = brow_bytes > 128 ? brow_bytes / 128 : 1;
   p.stream_b = 0;
@@ -1307,6 +1353,8 @@ int launch_gemm_tiled(const GemmArgs& a) {
   }
   // wide tiles read a split shrink's partial sums only from the staged rows
   if (!C::kDecode && a.S != nullptr && p.s_parts > 1 && !p.stage_s) return EPILORA_ERR_UNSUPPORTED;
+  // stored FP8 B rows are read only by the streamed-B decode epilogue
+  if (a.b_scale != nullptr && (!C::kDecode || !p.stream_b)) return EPILORA_ERR_UNSUPPORTED;
   p.stages = stages;
   // wide tiles without split K: output rows leave through a 5 KB staging
   // block placed after the staged S (16-byte stores need aligned rows)
@@ -1372,6 +1420,7 @@ namespace epi {
 
 template <int FMT>
 int launch_gemm_by_m(const GemmArgs& a) {
+  if (a.b_scale != nullptr && a.M > kDecodeBT) return EPILORA_ERR_UNSUPPORTED;   // stored FP8 B: decode tiles only
   // decode tiles of 16 tokens: two 128-byte K atoms per stage (NVFP4 stages
   // also carry scale boxes: one atom keeps three or more stages in flight at
   // two CTAs per SM); 32-token decode tiles also keep output-tile and S

@@ -168,11 +168,29 @@ __device__ __forceinline__ void quant_role(const __nv_bfloat16* __restrict__ X, 
 // Rank CTA: ranks j0 .. j0 + 3 of token t over K slice `part` (kslice
 // elements), written to S[part][t][j0 ..]; zeros for a token without an
 // active adapter. `red` holds (blockDim.x / 32) * 4 floats.
+// x (8 bf16) . a (8 E4M3 codes), accumulated in element order
+__device__ __forceinline__ float dot8_e4m3(const uint4& xv, const uint2& av, float acc) {
+  const uint32_t w[2] = {av.x, av.y};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float f0 = e4m3_to_f32(w[h] & 0xFFu), f1 = e4m3_to_f32((w[h] >> 8) & 0xFFu);
+    const float f2 = e4m3_to_f32((w[h] >> 16) & 0xFFu), f3 = e4m3_to_f32(w[h] >> 24);
+    const uint32_t xa = h == 0 ? xv.x : xv.z, xb = h == 0 ? xv.y : xv.w;
+    acc = fmaf(bf16_lo(xa), f0, acc);
+    acc = fmaf(bf16_hi(xa), f1, acc);
+    acc = fmaf(bf16_lo(xb), f2, acc);
+    acc = fmaf(bf16_hi(xb), f3, acc);
+  }
+  return acc;
+}
+
+// a_scale != nullptr: A holds E4M3 codes (K bytes per row) and each row's
+// fp32 scale multiplies the slice's sum.
 __device__ __forceinline__ void rank_role(const __nv_bfloat16* __restrict__ X, int K, int ldx,
                                           const __nv_bfloat16* __restrict__ A, int L, int r,
                                           const int32_t* __restrict__ idx, const uint8_t* __restrict__ mask,
                                           float* __restrict__ S, int* status, int M, size_t t, int j0, int part,
-                                          int kslice, bool report, float* red) {
+                                          int kslice, bool report, float* red, const float* a_scale = nullptr) {
   const int l = idx[t];
   bool act = (l >= 0) && (mask == nullptr || mask[t] != 0);
   if (l >= L) {
@@ -188,20 +206,34 @@ __device__ __forceinline__ void rank_role(const __nv_bfloat16* __restrict__ X, i
   const int c1 = min(K, (part + 1) * kslice) / 8;
   const int nch = K / 8;
   const uint4* xr = reinterpret_cast<const uint4*>(X + t * static_cast<size_t>(ldx));
-  const uint4* ar = reinterpret_cast<const uint4*>(A + (static_cast<size_t>(l) * r + j0) * static_cast<size_t>(K));
+  const size_t arow = (static_cast<size_t>(l) * r + j0) * static_cast<size_t>(K);   // first A row (elements)
 
   float acc[kRanksPerCta];
 #pragma unroll
   for (int j = 0; j < kRanksPerCta; ++j) acc[j] = 0.0f;
 
+  if (a_scale == nullptr) {
+    const uint4* ar = reinterpret_cast<const uint4*>(A + arow);
 #pragma unroll 2
-  for (int c = c0 + static_cast<int>(threadIdx.x); c < c1; c += blockDim.x) {
-    const uint4 xv = __ldg(xr + c);
-    uint4 av[kRanksPerCta];
+    for (int c = c0 + static_cast<int>(threadIdx.x); c < c1; c += blockDim.x) {
+      const uint4 xv = __ldg(xr + c);
+      uint4 av[kRanksPerCta];
 #pragma unroll
-    for (int j = 0; j < kRanksPerCta; ++j) av[j] = __ldg(ar + static_cast<size_t>(j) * nch + c);
+      for (int j = 0; j < kRanksPerCta; ++j) av[j] = __ldg(ar + static_cast<size_t>(j) * nch + c);
 #pragma unroll
-    for (int j = 0; j < kRanksPerCta; ++j) acc[j] = dot8(xv, av[j], acc[j]);
+      for (int j = 0; j < kRanksPerCta; ++j) acc[j] = dot8(xv, av[j], acc[j]);
+    }
+  } else {
+    const uint2* ar = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(A) + arow);
+#pragma unroll 2
+    for (int c = c0 + static_cast<int>(threadIdx.x); c < c1; c += blockDim.x) {
+      const uint4 xv = __ldg(xr + c);
+      uint2 av[kRanksPerCta];
+#pragma unroll
+      for (int j = 0; j < kRanksPerCta; ++j) av[j] = __ldg(ar + static_cast<size_t>(j) * nch + c);
+#pragma unroll
+      for (int j = 0; j < kRanksPerCta; ++j) acc[j] = dot8_e4m3(xv, av[j], acc[j]);
+    }
   }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -216,7 +248,7 @@ __device__ __forceinline__ void rank_role(const __nv_bfloat16* __restrict__ X, i
   if (threadIdx.x < kRanksPerCta) {
     float sum = 0.0f;
     for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) sum += red[w * kRanksPerCta + threadIdx.x];
-    srow[threadIdx.x] = sum;
+    srow[threadIdx.x] = a_scale != nullptr ? sum * __ldg(a_scale + static_cast<size_t>(l) * r + j0 + threadIdx.x) : sum;
   }
 }
 
@@ -230,7 +262,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
                                                                     const uint8_t* __restrict__ mask,
                                                                     float* __restrict__ S, int* status,
                                                                     QuantSide qs, int parts, int kslice,
-                                                                    int early_release) {
+                                                                    int early_release, const float* a_scale) {
   // Let the dependent GEMM launch at once: before it reads anything this grid
   // writes it waits for this grid's completion, and until then it only
   // streams weights. Then, when this grid is itself a programmatic dependent
@@ -260,7 +292,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 8) shrink_kernel(const __nv_bf
   if (groups == 0) return;
   const int part = gy / groups;
   rank_role(X, K, ldx, A, L, r, idx, mask, S, status, static_cast<int>(gridDim.x), t,
-            (gy - part * groups) * kRanksPerCta, part, kslice, gy == 0, &red[0][0]);
+            (gy - part * groups) * kRanksPerCta, part, kslice, gy == 0, &red[0][0], a_scale);
 }
 
 // Wide batches (M > 32): tokens in blocks of 16 consecutive tokens. A block
@@ -493,14 +525,14 @@ int launch_shrink(const void* X, int M, int K, int ldx, const void* A, int L, in
   dim3 grid(M, r / kRanksPerCta);
   shrink_kernel<<<grid, kShrinkThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), K, ldx,
                                                       static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S,
-                                                      status_dev, qs, 1, K, 1);
+                                                      status_dev, qs, 1, K, 1, nullptr);
   return cudaGetLastError() == cudaSuccess ? EPILORA_OK : EPILORA_ERR_CUDA;
 }
 
 int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int L, int r, const int32_t* idx,
                         const uint8_t* mask, float* S, int s_parts, int fmt, void* Xq, float* x_scale,
                         uint8_t* x_block_scale, const float* x_global_scale, int32_t* perm, int* status_dev,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const float* a_scale) {
   if (M == 0) return EPILORA_OK;
   if (s_parts < 1 || s_parts > shrink_parts_max(K) || (s_parts > 1 && kslice_for(K, s_parts) * (s_parts - 1) >= K))
     return EPILORA_ERR_INVALID_ARG;
@@ -511,6 +543,7 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
   QuantSide qs{fmt, static_cast<uint8_t*>(Xq), x_scale, x_block_scale, x_global_scale, perm};
   const int kslice = s_parts == 1 ? K : kslice_for(K, s_parts);
   if (M > 32) {
+    if (a_scale != nullptr) return EPILORA_ERR_UNSUPPORTED;   // stored FP8 adapters: decode batches only
     // wide batch: M quantizer CTAs, then token-block CTAs (block, K slice)
     const int nblk = r > 0 ? (M + kBlockTokens - 1) / kBlockTokens : 0;
     const long ctas = static_cast<long>(M) + static_cast<long>(nblk) * s_parts +
@@ -566,8 +599,7 @@ int launch_shrink_quant(const void* X, int M, int K, int ldx, const void* A, int
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, shrink_kernel, static_cast<const __nv_bfloat16*>(X), K, ldx,
                          static_cast<const __nv_bfloat16*>(A), L, r, idx, mask, S, status_dev, qs, s_parts,
-                         kslice,
-                         early_release) != cudaSuccess)
+                         kslice, early_release, a_scale) != cudaSuccess)
     return EPILORA_ERR_CUDA;
   return EPILORA_OK;
 }

@@ -77,6 +77,42 @@ def lora_shrink(X, A, idx, mask=None, status=None, stream=None) -> torch.Tensor:
     return S
 
 
+@dataclass
+class Fp8Adapters:
+    """Adapter tables stored as E4M3 codes with one fp32 scale per row."""
+    Aq: torch.Tensor        # uint8 [L, r, K]
+    a_scale: torch.Tensor   # fp32 [L, r]
+    Bq: torch.Tensor        # uint8 [L, N, r]
+    b_scale: torch.Tensor   # fp32 [L, N]
+
+
+def quantize_adapters_fp8(A: torch.Tensor, B: torch.Tensor, stream=None) -> Fp8Adapters:
+    """Load-time quantization of bf16 adapter tables A [L, r, K] and B [L, N, r]
+    with the FP8 row quantizer (one scale per row of each table)."""
+    L, r, K = A.shape
+    N = B.shape[1]
+    Aq, sa = quant_act(A.reshape(L * r, K), E.FMT_FP8, stream=stream)
+    Bq, sb = quant_act(B.reshape(L * N, r), E.FMT_FP8, stream=stream)
+    return Fp8Adapters(Aq.view(L, r, K), sa.view(L, r), Bq.view(L, N, r), sb.view(L, N))
+
+
+def layer_forward_fp8_adapters(X, w: QuantWeight, ad: Fp8Adapters, idx, mask=None, x_global_scale=None,
+                               workspace: Optional[LayerWorkspace] = None, status=None, stream=None, Y=None):
+    """epilora_layer_forward_fp8_adapters: the layer with stored FP8 adapters."""
+    M, K = X.shape
+    N = w.N
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    L, r = ad.Aq.shape[0], ad.Aq.shape[1]
+    ws = workspace or LayerWorkspace(X.device)
+    buf = ws.get(w.fmt, M, K, r)
+    rc = E.epilora_layer_forward_fp8_adapters(w.fmt, M, N, K, X, X.stride(0), w.codes, w.scale, w.block_scale,
+                                              w.global_scale, x_global_scale, ad.Aq, ad.a_scale, ad.Bq, ad.b_scale,
+                                              L, r, idx, mask, Y, Y.stride(0), buf, buf.numel(), status, stream)
+    E.check(rc, "layer_forward_fp8_adapters")
+    return Y
+
+
 def lora_shrink_into(X, A, idx, mask, S, status=None, stream=None):
     """lora_shrink into a caller-owned S [M, r] fp32."""
     M, K = X.shape

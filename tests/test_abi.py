@@ -106,7 +106,8 @@ INVALID, UNSUP, WS = -1, -2, -5
 @pytest.mark.skipif(not _no_gpu(), reason="fake-pointer validation runs only where nothing can launch")
 @pytest.mark.parametrize("kw,want", [
     (dict(fmt=2), INVALID),
-    (dict(K=48), INVALID),             # K % 32
+    (dict(K=40), INVALID),             # FP8: K % 16
+    (dict(fmt=1, K=48, x_scale=None, x_block_scale=FAKE, x_global_scale=FAKE), INVALID),   # NVFP4: K % 32
     (dict(K=0), INVALID),
     (dict(M=-1), INVALID),
     (dict(ldx=500), INVALID),          # ldx < K
