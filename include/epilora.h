@@ -181,7 +181,7 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
 /*
  * Bytes of device workspace epilora_layer_forward needs for (fmt, M, K, r):
  * a head of EPILORA_WORKSPACE_SYNC_BYTES (2.25 MiB: the single-kernel decode
- * path's grid-wide counters and the regions where its thread blocks exchange
+ * path's launch counter and the regions where its thread blocks exchange
  * partial results, see epilora_layer_forward_kernels), then the quantized
  * activations, their scales, S (r = 0: no adapters; S is held as up to
  * ceil(K / 1024) partial sums over K slices, capped at 8) and, for more than
@@ -211,13 +211,14 @@ EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K, int r);
  * A few tokens (epilora_layer_forward_kernels == 1) run as ONE persistent
  * kernel, a programmatic dependent of the previous kernel on the stream: it
  * streams Wq (and w_block_scale) at once, waits for that kernel, then every
- * thread block quantizes the activations of all tokens for itself (the
- * arithmetic of epilora_quant_act), takes shrink work items (token, 4 ranks,
- * K slice: the arithmetic of epilora_lora_shrink split into partial sums)
- * from a counter in the workspace, and finishes its share of the output; the
- * weight stream is split evenly over the SMs, a weight tile split between
- * thread blocks being summed in a fixed order. Otherwise it enqueues two
- * kernels,
+ * thread block quantizes the activations (the arithmetic of
+ * epilora_quant_act) over the K range of its own weight units, takes a fixed
+ * share of the shrink work items (token, 4 ranks, K slice: the arithmetic of
+ * epilora_lora_shrink split into partial sums), and finishes its share of
+ * the output; the weight stream is split evenly over the SMs, a weight tile
+ * split between thread blocks being summed in a fixed order. It lets the
+ * next kernel on the stream launch as soon as all its thread blocks run.
+ * Otherwise it enqueues two kernels,
  *   1. the shrink grid (the arithmetic of epilora_lora_shrink, split over K
  *      slices into partial sums; for more than 32 tokens, blocks of 16
  *      consecutive tokens carrying at most two adapters on the tensor
@@ -235,9 +236,10 @@ EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K, int r);
  * head, Xq, scales, S and the row map. The head (the first
  * EPILORA_WORKSPACE_SYNC_BYTES) must be zero before the first call that uses
  * the workspace: zero-fill a workspace once after allocating it. Calls keep
- * the head valid for the next call (counters back to zero, an epoch moved on
- * that tags every value the thread blocks exchange, so older values are
- * never taken for new ones); nothing else needs an initial value. Y is the
+ * the head valid for the next call (each adds 256 to a 64-bit launch
+ * counter at bytes [16, 24) of the head, whose value at the start of a call
+ * gives the tag of every value its thread blocks exchange, so older values
+ * are never taken for new ones); nothing else needs an initial value. Y is the
  * same whatever the row order. Calls that share a workspace must be ordered
  * on one stream.
  * Because the GEMM may start while the kernel that precedes this call on the
@@ -310,6 +312,16 @@ EPILORA_API int epilora_layer_forward_fp8_adapters(int fmt, int M, int N, int K,
                           void* Y, int ldy,
                           void* workspace, size_t workspace_bytes,
                           int* status_dev, void* stream);
+
+/*
+ * Test hook of the single-kernel decode path: with on != 0, later calls that
+ * take that path (in this process) have their shrink work items publish
+ * nothing, so every finishing thread block that needs S waits until its
+ * bounded wait runs out (1 s), records EPILORA_ERR_TIMEOUT in the status
+ * word and returns in order (Y is then unspecified). on = 0 restores normal
+ * operation. Not for production use; returns EPILORA_OK.
+ */
+EPILORA_API int epilora_test_drop_shrink_results(int on);
 
 /*
  * epilora_layer_forward without a caller workspace. The EpiLoRA page has no

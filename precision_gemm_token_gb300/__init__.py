@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     epilora_layer_forward,
     epilora_layer_forward_fp8_adapters,
     epilora_layer_forward_kernels,
+    epilora_test_drop_shrink_results,
     epilora_layer_forward_noalloc,
     epilora_layer_forward_slices,
     epilora_lora_shrink,

@@ -37,6 +37,7 @@ SIGNATURES = {
                                             _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp]),
     "epilora_workspace_bytes": (_sz, [_c_int, _c_int, _c_int, _c_int]),
     "epilora_layer_forward_kernels": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
+    "epilora_test_drop_shrink_results": (_c_int, [_c_int]),
     "epilora_layer_forward": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _sz, _vp, _vp]),
     "epilora_layer_forward_fp8_adapters": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp,
@@ -143,6 +144,12 @@ def epilora_workspace_bytes(fmt, M, K, r) -> int:
 
 def epilora_layer_forward_kernels(fmt, M, K, r) -> int:
     return load().epilora_layer_forward_kernels(fmt, M, K, r)
+
+
+def epilora_test_drop_shrink_results(on: bool) -> None:
+    """Test hook: the single-kernel path's shrink items publish nothing
+    while on (finishers then time out with EPILORA_ERR_TIMEOUT)."""
+    load().epilora_test_drop_shrink_results(1 if on else 0)
 
 
 def epilora_layer_forward(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale, x_global_scale, A, B,

@@ -57,6 +57,12 @@ bool shrink_args_ok(const void* X, int M, int K, int ldx, const void* A, int L, 
 
 }  // namespace
 
+namespace {
+std::atomic<int> g_test_drop_s{0};
+}  // namespace
+
+int decode_test_drop_s() { return g_test_drop_s.load(); }
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -352,6 +358,7 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
     d.Xq = Xq;
     d.x_scale = x_scale;
     d.x_block_scale = x_block_scale;
+    d.drop_s = decode_test_drop_s();
     return launch_fused_decode(d);
   }
 
@@ -429,6 +436,11 @@ EPILORA_API int epilora_layer_forward_slices(int fmt, int M, int N, int K, const
   return layer_forward_impl(fmt, M, N, K, X, ldx, Wq, w_scale, w_block_scale, w_global_scale, x_global_scale, A, B,
                             L, r, idx, mask, Y, ldy, workspace, workspace_bytes, status_dev, stream, n_slices,
                             slice_end);
+}
+
+EPILORA_API int epilora_test_drop_shrink_results(int on) {
+  g_test_drop_s.store(on != 0 ? 1 : 0);
+  return EPILORA_OK;
 }
 
 EPILORA_API int epilora_layer_forward_fp8_adapters(int fmt, int M, int N, int K, const void* X, int ldx,

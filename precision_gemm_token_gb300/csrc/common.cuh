@@ -119,10 +119,13 @@ struct DecodeArgs {
   void* sync;           // decode_sync_bytes()
   void* S;              // decode_s_bytes(): tagged [parts][M][s_row]
   void* accp;           // decode_partial_bytes(): tagged [CTA][M][128]
-  void* Xq;             // the quantized activations as used (written by one CTA)
+  void* Xq;             // the quantized activations as used (each CTA writes its K range)
   float* x_scale;
   uint8_t* x_block_scale;
+  int drop_s = 0;       // test hook: the shrink items publish nothing
 };
+// test hook of the single-kernel path (epilora_test_drop_shrink_results)
+int decode_test_drop_s();
 bool decode_path_eligible(int fmt, int M, int K, int s_row);
 size_t decode_sync_bytes();
 size_t decode_partial_bytes();

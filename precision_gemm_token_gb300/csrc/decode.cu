@@ -33,19 +33,24 @@
 //               bf16 activation rows into the last ring slots, quantization
 //               of every token into shared memory (each CTA for itself: FP8
 //               divisions by Markstein's correction of the reciprocal
-//               product), shrink work items (token x 4 ranks x K slice, the
-//               arithmetic of the standalone shrink: item c is CTA c's, items
-//               past the grid are claimed from a counter), then the epilogue
-//               of each segment.
+//               product; each CTA quantizes the K range of its own units),
+//               shrink work items (token x 4 ranks x K slice, the arithmetic
+//               of the standalone shrink; CTA c takes items c, c + G, ...),
+//               then the epilogue of each segment.
 // A weight tile split over several CTAs is finished by the CTA that holds its
 // first K unit (it reaches that tile last): the others store their fp32
 // partial rows, and the shrink items their partial sums of S, each value in a
-// 64-bit word with this launch's tag (a mix of an epoch the previous launch
-// moved on); the finisher reads them until the tags match, adds the partial
-// rows in CTA order and S's slices in part order (deterministic), applies the
-// scales, adds the adapter term and writes Y. Every wait is bounded (an error
-// status, then an orderly exit) and waits only on work already claimed by
-// running CTAs; the last CTA to exit resets the counters and moves the epoch.
+// 64-bit word with this launch's tag; the finisher reads them until the tags
+// match (all of a row's words requested at once), adds the partial rows in
+// CTA order and S's slices in part order (deterministic), applies the scales,
+// adds the adapter term and writes Y. The tag comes from a launch counter in
+// the workspace to which every launch adds 256 in all as its CTAs exit (one
+// reduction each, nothing waited for), so a launch reads 256 j plus less
+// than 256 and takes j as its epoch. Every wait is bounded (an error status,
+// then an orderly exit) and waits only on work of running CTAs. The next
+// kernel on the stream is released as soon as every CTA has started: it
+// streams its first weight units while this one works and waits for this
+// grid's completion before it reads anything else.
 #include "quant_row.cuh"
 
 namespace epi {
@@ -63,9 +68,10 @@ constexpr int kDecSmemBudget = 113 * 1024;
 constexpr int kDecMaxStages = 8;
 constexpr int kMaxRankBrow = 64;           // 32-bit words of a rank-128 bf16 B row
 
-// sync block at the start of the workspace: [0] claim counter, [2] exit
-// counter, [3] epoch; then the tagged region (partial rows, then S)
+// sync block at the start of the workspace: words [4, 6) hold the 64-bit
+// launch counter; then the tagged region (partial rows, then S)
 constexpr int kDecSyncWords = 64;
+constexpr int kDecCounterWord = 4;
 constexpr int kDecSParts = 8;              // K slices of the shrink at most
 constexpr int kDecMaxSRow = 512;           // rank 128 x 4 slices
 
@@ -86,13 +92,13 @@ struct DecParams {
   const float* x_gs;
   __nv_bfloat16* Y;
   int* status;
-  unsigned* sync;      // [0] claim counter, [2] exit counter, [3] launch epoch
+  unsigned long long* counter;   // launch counter (256 per launch)
   // Published values carry the launch epoch in the same 64-bit word (value
   // bits low, epoch high): a reader retries until the tag is this launch's,
   // so no flag or counter has to be polled before the data.
   uint2* S;            // [parts][M][s_row] partial sums of the shrink
   uint2* accp;         // [G][M][128] partial rows of split weight tiles
-  uint8_t* xq_out;     // CTA 0 also stores the quantized activations here
+  uint8_t* xq_out;     // the quantized activations also go here (each CTA its K range)
   float* xs_out;       // FP8 scales
   uint8_t* xsb_out;    // NVFP4 block scales
   long long U;         // units in total
@@ -100,6 +106,7 @@ struct DecParams {
   int M, N, K, ldx, ldy, L, r, s_row, n_slices;
   int slice_end[4];
   int adapters, parts, kslice, n_items;
+  int drop_s;          // test hook: the shrink items publish nothing (finishers time out)
   int kb_pad;          // code bytes of one token's row, padded to whole units
   int xslots;          // last ring slots that first hold the bf16 activation rows
 };
@@ -140,31 +147,61 @@ __device__ __forceinline__ bool helper_any(bool v) {
   return r != 0;
 }
 
-// Tag of the launch whose epoch word is e: an odd multiplicative mix (never
-// zero, distinct for distinct e).
-__device__ __forceinline__ unsigned launch_tag(unsigned e) { return ((e + 1u) * 0x9E3779B1u) | 1u; }
+// Tag of the launch with epoch e: odd (never the zero of fresh memory) and
+// distinct for epochs less than 2^31 apart.
+__device__ __forceinline__ unsigned launch_tag(unsigned long long e) {
+  return (static_cast<unsigned>(e) << 1) | 1u;
+}
 
-// One tagged 64-bit value, read again until its tag is `epoch` (1 s limit);
-// false on timeout.
-__device__ __forceinline__ bool read_tagged(const uint2* p, unsigned epoch, uint2* out) {
-  uint2 w = __ldcg(p);
-  if (w.y == epoch) {
-    *out = w;
-    return true;
-  }
+// One tagged 64-bit value, read again until its tag is `epoch` (1 s limit;
+// on timeout the last word read, whose tag is then another). `w` holds a
+// first read already made.
+__device__ __forceinline__ uint2 reread_tagged(const uint2* p, unsigned epoch, uint2 w) {
+  if (w.y == epoch) return w;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     __nanosleep(32);
     w = __ldcg(p);
-    if (w.y == epoch) {
-      *out = w;
-      return true;
-    }
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *out = w;
-      return false;
-    }
+    if (w.y == epoch || globaltimer_ns() - t0 > kWaitLimitNs) return w;
   }
+}
+
+// n <= N tagged values p[0], p[stride], ... whose first reads are in w:
+// late ones read again, none after a timeout. The values go to v[0..n);
+// false if one timed out.
+template <int N>
+__device__ __forceinline__ bool check_tagged_n(const uint2* p, size_t stride, int n, unsigned epoch, uint2 (&w)[N],
+                                               float (&v)[N]) {
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (i < n) {
+      if (w[i].y != epoch && ok) {
+        w[i] = reread_tagged(p + i * stride, epoch, w[i]);
+        ok = w[i].y == epoch;
+      }
+      v[i] = __uint_as_float(w[i].x);
+    }
+  return ok;
+}
+
+// First reads of n <= N tagged values p[0], p[stride], ..., all issued before
+// any is used (one round trip when they are all there).
+template <int N>
+__device__ __forceinline__ void load_tagged_n(const uint2* p, size_t stride, int n, uint2 (&w)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (i < n) w[i] = __ldcg(p + i * stride);
+}
+
+// |x| max of a 16-byte chunk of 8 bf16 values as a bf16 pair (the max of
+// bf16 magnitudes is one of them: exact).
+__device__ __forceinline__ __nv_bfloat162 absmax8_bf16(const uint4& v) {
+  const __nv_bfloat162 a = __hmax2(__habs2(*reinterpret_cast<const __nv_bfloat162*>(&v.x)),
+                                   __habs2(*reinterpret_cast<const __nv_bfloat162*>(&v.y)));
+  const __nv_bfloat162 b = __hmax2(__habs2(*reinterpret_cast<const __nv_bfloat162*>(&v.z)),
+                                   __habs2(*reinterpret_cast<const __nv_bfloat162*>(&v.w)));
+  return __hmax2(a, b);
 }
 
 __device__ __forceinline__ float dec_dot8(const uint4& xv, const uint4& av, float acc) {
@@ -327,7 +364,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   uint64_t* xst_bar = pref_bar + 1;                  // the bf16 activation rows have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xst_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* bcast = reinterpret_cast<int*>(tmem_slot + 2);                 // helper broadcast word
   float* red = reinterpret_cast<float*>(tmem_slot + 4);               // [4 warps][8]
   int* meta_idx = reinterpret_cast<int*>(red + 32);                   // [kDecMaxTokens] adapter or -1
   float* meta_sx = reinterpret_cast<float*>(meta_idx + kDecMaxTokens);   // FP8 activation scales
@@ -362,6 +398,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // every CTA of this grid is running: the next kernel on the stream may
+  // start its CTAs (they stream weights, never written here, and wait for
+  // this grid's completion before they read anything else)
+  if (threadIdx.x == 0) pdl_allow_dependents();
 
   if (warp == 0) {
     // ===== TMA producer: the run's weight units, in order =====
@@ -399,10 +439,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         issued_mask |= 1u << s;
         parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
       }
-      // every weight byte of this CTA is requested: the next kernel on the
-      // stream may start its CTAs (they wait for this grid before reading
-      // anything it writes)
-      pdl_allow_dependents();
       if (*abort_flag) {
         for (int s = 0; s < stages; ++s)
           if (issued_mask & (1u << s)) (void)mbar_wait_bounded(&full_bar[s], (parity_mask >> s) & 1u, kWaitLimitNs);
@@ -411,19 +447,20 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     __syncwarp();
   } else if (warp == 1) {
     // ===== MMA issuer =====
-    const bool xok = __all_sync(0xffffffffu, mbar_wait_bounded(xrdy_bar, 0, kWaitLimitNs));
-    if (!xok && lane == 0) {
-      *abort_flag = 1;
-      record_status(p.status, EPILORA_ERR_TIMEOUT);
-    }
     const uint32_t xc_addr = smem_u32(xc);
     const uint32_t xsf_addr = smem_u32(xsf);
     const uint32_t x_lbo = static_cast<uint32_t>(16 * M);
     SegWalk walk(p, c);
     int T, kb0, kb1, j = 0;
     long long it = 0;
+    bool have = walk.next(T, kb0, kb1);           // (the first segment before the wait)
+    const bool xok = __all_sync(0xffffffffu, mbar_wait_bounded(xrdy_bar, 0, kWaitLimitNs));
+    if (!xok && lane == 0) {
+      *abort_flag = 1;
+      record_status(p.status, EPILORA_ERR_TIMEOUT);
+    }
     bool stop = !xok;
-    while (!stop && walk.next(T, kb0, kb1)) {
+    for (; !stop && have; have = walk.next(T, kb0, kb1)) {
       const int b = j & 1;
       // the helpers have read this accumulator's previous segment
       const bool oke = __all_sync(0xffffffffu, mbar_wait_bounded(&acce_bar[b], ((j >> 1) & 1) ^ 1u, kWaitLimitNs));
@@ -576,13 +613,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       li = p.idx[et];
       if (p.mask != nullptr) mk = p.mask[et];
     }
-    // this launch's tag: a mix of the epoch word (which the previous launch on
-    // this workspace moved on), never zero, so zero-filled or older memory
-    // never reads as this launch's data
-    const unsigned epoch = launch_tag(__ldcg(p.sync + 3));
+    // this launch's tag: earlier launches on this workspace have added 256
+    // each to the counter, CTAs of this one that already exited less than 256
+    const unsigned epoch = launch_tag(__ldcg(p.counter) >> 8);
     float alpha = 1.0f;
     const int nch = p.K / 8;                      // 16-byte bf16 chunks per row
-    const int total = M * nch;
     if (et < M) {
       if (li >= p.L) record_status(p.status, EPILORA_ERR_INVALID_ARG);
       meta_idx[et] = (li >= 0 && li < p.L && mk != 0) ? li : -1;
@@ -592,29 +627,33 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       record_status(p.status, EPILORA_ERR_TIMEOUT);
     }
     const uint4* xs4 = reinterpret_cast<const uint4*>(xs);   // chunk q of the M x nch chunks
+    // Quantization steps (FP8: 8-element chunks; NVFP4: 16-element blocks;
+    // 16 KA of either per weight unit) that this CTA's MMAs read: those of
+    // the K atoms its units cover, [lo, hi] or, wrapping around a tile end,
+    // [lo, end) and [0, hi]; the whole row when it covers a tile.
+    const int nsteps = C::kFP4 ? p.K / kNvfp4Block : nch;
+    int rb0, re0, rb1 = 0, re1 = 0;
+    {
+      const long long ub = (p.U * c) / p.G, ue = (p.U * (c + 1)) / p.G;
+      const int lo = static_cast<int>(ub % p.nkb) * 16 * KA;
+      const int hi = min(nsteps, (static_cast<int>((ue - 1) % p.nkb) + 1) * 16 * KA);
+      rb0 = ue - ub >= p.nkb ? 0 : lo;
+      re0 = ue - ub >= p.nkb || lo >= hi ? nsteps : hi;
+      if (ue - ub < p.nkb && lo >= hi) re1 = hi;
+    }
     // ---- activation quantization into the compact copy ----
     if (!C::kFP4) {
-      float am[kDecMaxTokens];
-#pragma unroll
-      for (int t = 0; t < kDecMaxTokens; ++t) am[t] = 0.0f;
+      // per-token amax over the whole row, on bf16 pairs
+#pragma unroll 1
+      for (int t = 0; t < M; ++t) {
+        const uint4* row = xs4 + static_cast<size_t>(t) * nch;
+        __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
 #pragma unroll 4
-      for (int q = et; q < total; q += 128) {
-        const int t = q / nch;
-        float x[8];
-        unpack8(xs4[q], x);
-        float mx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(x[i]));
-#pragma unroll
-        for (int tt = 0; tt < kDecMaxTokens; ++tt)
-          if (tt == t) am[tt] = fmaxf(am[tt], mx);
-      }
-#pragma unroll
-      for (int tt = 0; tt < kDecMaxTokens; ++tt) {
-        float mx = am[tt];
+        for (int q = et; q < nch; q += 128) m2 = __hmax2(m2, absmax8_bf16(row[q]));
+        float mx = fmaxf(__low2float(m2), __high2float(m2));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) red[hw * kDecMaxTokens + tt] = mx;
+        if (lane == 0) red[hw * kDecMaxTokens + t] = mx;
       }
       helper_sync();
       if (et < M) {
@@ -626,15 +665,22 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         if (c == 0) p.xs_out[et] = sc;
       }
       helper_sync();
-      // the codes (the IEEE division for rows whose scale is below 2^-100)
+      // the codes of this CTA's steps (the IEEE division for rows whose scale
+      // is below 2^-100), also stored to the workspace copy
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        const int rbg = g == 0 ? rb0 : rb1;
+        const int n = (g == 0 ? re0 : re1) - rbg;
 #pragma unroll 2
-      for (int q = et; q < total; q += 128) {
-        const int t = q / nch;
-        const int k0 = (q - t * nch) * 8;
-        const float sc = meta_sx[t];
-        const uint2 code = sc >= 0x1p-100f ? quant8_e4m3_rs(xs4[q], sc, meta_rs[t]) : quant8_e4m3(xs4[q], sc);
-        *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
-        if (c == 0) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+        for (int q = et; q < M * n; q += 128) {
+          const int t = q / n;
+          const int k0 = (rbg + q - t * n) * 8;
+          const float sc = meta_sx[t];
+          const uint4 v = xs4[static_cast<size_t>(t) * nch + k0 / 8];
+          const uint2 code = sc >= 0x1p-100f ? quant8_e4m3_rs(v, sc, meta_rs[t]) : quant8_e4m3(v, sc);
+          *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
+          *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+        }
       }
       // zero codes past K up to the unit boundary (finite values against the
       // weight box's zero fill)
@@ -645,51 +691,54 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = make_uint2(0, 0);
       }
     } else {
-      // NVFP4: per 16-element block, its scale and codes (block-local)
+      // NVFP4: per 16-element block, its scale and codes (block-local), for
+      // this CTA's blocks
       const float g = *p.x_gs;
       const bool g_ok = (g > 0.0f) && isfinite(g);
       if (!g_ok && et == 0) record_status(p.status, EPILORA_ERR_INVALID_ARG);
       alpha = 1.0f / (g * *p.w_gs);
-      const int nb = p.K / kNvfp4Block;
-      const int total = M * nb;
+      const int nb = nsteps;
+#pragma unroll 1
+      for (int gi = 0; gi < 2; ++gi) {
+        const int rbg = gi == 0 ? rb0 : rb1;
+        const int n = (gi == 0 ? re0 : re1) - rbg;
 #pragma unroll 2
-      for (int q = et; q < total; q += 128) {
-        const int t = q / nb;
-        const int b = q - t * nb;
-        const uint4* row = xs4 + static_cast<size_t>(t) * nch;
-        float x[16];
-        {
-          float a0[8], a1[8];
-          unpack8(row[2 * b], a0);
-          unpack8(row[2 * b + 1], a1);
+        for (int q = et; q < M * n; q += 128) {
+          const int t = q / n;
+          const int b = rbg + q - t * n;
+          const uint4* row = xs4 + static_cast<size_t>(t) * nch;
+          float x[16];
+          {
+            float a0[8], a1[8];
+            unpack8(row[2 * b], a0);
+            unpack8(row[2 * b + 1], a1);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            x[i] = a0[i];
-            x[8 + i] = a1[i];
+            for (int i = 0; i < 8; ++i) {
+              x[i] = a0[i];
+              x[8 + i] = a1[i];
+            }
           }
-        }
-        float amax = 0.0f;
+          float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-        uint32_t sb = 0, lo = 0, hi = 0;
-        if (g_ok) {
-          const float t2 = __fmul_rn(__fdiv_rn(amax, kE2M1Max), g);
-          sb = cvt_e4m3x2(t2, 0.0f) & 0xFFu;
-          const float sbf = e4m3_to_f32(sb);
-          if (sbf > 0.0f) {
-            const float inv = __fdiv_rn(g, sbf);
-            uint32_t by[8];
+          for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+          uint32_t sb = 0, lo = 0, hi = 0;
+          if (g_ok) {
+            const float t2 = __fmul_rn(__fdiv_rn(amax, kE2M1Max), g);
+            sb = cvt_e4m3x2(t2, 0.0f) & 0xFFu;
+            const float sbf = e4m3_to_f32(sb);
+            if (sbf > 0.0f) {
+              const float inv = __fdiv_rn(g, sbf);
+              uint32_t by[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) by[i] = cvt_e2m1x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
-            lo = by[0] | (by[1] << 8) | (by[2] << 16) | (by[3] << 24);
-            hi = by[4] | (by[5] << 8) | (by[6] << 16) | (by[7] << 24);
+              for (int i = 0; i < 8; ++i) by[i] = cvt_e2m1x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
+              lo = by[0] | (by[1] << 8) | (by[2] << 16) | (by[3] << 24);
+              hi = by[4] | (by[5] << 8) | (by[6] << 16) | (by[7] << 24);
+            }
           }
-        }
-        // block b is bytes [8 b, 8 b + 8) of the packed row: 16-byte chunk
-        // b / 2, half b % 2; its scale is byte b % 4 of the line of k-step b / 4
-        *reinterpret_cast<uint2*>(xc + ((b >> 1) * M + t) * 16 + (b & 1) * 8) = make_uint2(lo, hi);
-        xsf[((b >> 2) * M + t) * 16 + (b & 3)] = static_cast<uint8_t>(sb);
-        if (c == 0) {
+          // block b is bytes [8 b, 8 b + 8) of the packed row: 16-byte chunk
+          // b / 2, half b % 2; its scale is byte b % 4 of the line of k-step b / 4
+          *reinterpret_cast<uint2*>(xc + ((b >> 1) * M + t) * 16 + (b & 1) * 8) = make_uint2(lo, hi);
+          xsf[((b >> 2) * M + t) * 16 + (b & 3)] = static_cast<uint8_t>(sb);
           *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * (p.K / 2) + b * 8) = make_uint2(lo, hi);
           p.xsb_out[static_cast<size_t>(t) * nb + b] = static_cast<uint8_t>(sb);
         }
@@ -785,29 +834,50 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       const int c_last = kb1 < p.nkb ? cta_of_unit(p, static_cast<long long>(T) * p.nkb + p.nkb - 1) : c;
       const bool need_s = p.adapters && !s_ready;
       bool late = false;
+      // first round, all in flight together: up to 8 partial-row values of
+      // this thread's row (the other CTAs' rows in CTA order, tokens
+      // innermost: one run with a stride of 128 words) and the S parts of
+      // this thread's first S element
+      const int np = (c_last - c) * M;
+      const uint2* pp = p.accp + static_cast<size_t>(c + 1) * M * 128 + m;
+      const size_t part_stride = static_cast<size_t>(M) * p.s_row;
+      uint2 wp[8], wsp[kDecSParts];
+      load_tagged_n<8>(pp, 128, min(8, np), wp);
+      if (need_s && et < M * p.s_row && meta_idx[et / p.s_row] >= 0)
+        load_tagged_n<kDecSParts>(p.S + et, part_stride, p.parts, wsp);
       if (need_s) {
-        const size_t part_stride = static_cast<size_t>(M) * p.s_row;
         for (int e = et; e < M * p.s_row; e += 128) {
           const int t = e / p.s_row;
           float sum = 0.0f;
-          if (meta_idx[t] >= 0) {
-            for (int q = 0; q < p.parts; ++q) {
-              uint2 w;
-              if (!read_tagged(p.S + q * part_stride + e, epoch, &w)) late = true;
-              sum = q == 0 ? __uint_as_float(w.x) : sum + __uint_as_float(w.x);
+          if (meta_idx[t] >= 0 && !late) {
+            if (e != et) load_tagged_n<kDecSParts>(p.S + e, part_stride, p.parts, wsp);
+            float v[kDecSParts];
+            if (check_tagged_n<kDecSParts>(p.S + e, part_stride, p.parts, epoch, wsp, v)) {
+              sum = v[0];
+#pragma unroll
+              for (int q = 1; q < kDecSParts; ++q)
+                if (q < p.parts) sum += v[q];
+            } else {
+              late = true;
             }
           }
           s_stage[e] = sum;
         }
       }
-      for (int c2 = c + 1; c2 <= c_last; ++c2) {
-        const uint2* src = p.accp + static_cast<size_t>(c2) * M * 128;
+      for (int i0 = 0; i0 < np && !late; i0 += 8) {
+        if (i0 > 0) load_tagged_n<8>(pp + static_cast<size_t>(i0) * 128, 128, min(8, np - i0), wp);
+        float v[8];
+        if (!check_tagged_n<8>(pp + static_cast<size_t>(i0) * 128, 128, min(8, np - i0), epoch, wp, v)) {
+          late = true;
+          break;
+        }
 #pragma unroll
-        for (int t = 0; t < kDecMaxTokens; ++t)
-          if (t < M) {
-            uint2 w;
-            if (!read_tagged(src + t * 128 + m, epoch, &w)) late = true;
-            acc[t] += __uint_as_float(w.x);
+        for (int i = 0; i < 8; ++i)
+          if (i0 + i < np) {
+            const int t = (i0 + i) % M;
+#pragma unroll
+            for (int tt = 0; tt < kDecMaxTokens; ++tt)
+              if (tt == t) acc[tt] += v[i];
           }
       }
       if (helper_any(late)) return fail();        // (also: S staged for every thread)
@@ -849,10 +919,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       }
       return true;
     };
-    // ---- shrink items: (token, 4 ranks, K slice). Item c is this CTA's;
-    // items from G on are claimed from the counter at the start of the
-    // workspace (unsigned throughout: any counter value at or past the end
-    // stops the claims) ----
+    // ---- shrink items: (token, 4 ranks, K slice); CTA c takes items c,
+    // c + G, c + 2 G, ... ----
     const int groups = p.s_row / kDecRanksPerItem;
     auto do_item = [&](int item) {
       const int t = item / (groups * p.parts);
@@ -911,14 +979,14 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
             ov[jr] = qa ? sum * __ldg(p.a_scale + static_cast<size_t>(l) * p.s_row + j0 + jr) : sum;
           }
           uint4* dst = reinterpret_cast<uint4*>(p.S + (static_cast<size_t>(part) * M + t) * p.s_row + j0);
-          __stcg(dst, make_uint4(__float_as_uint(o.x), epoch, __float_as_uint(o.y), epoch));
-          __stcg(dst + 1, make_uint4(__float_as_uint(o.z), epoch, __float_as_uint(o.w), epoch));
+          if (!p.drop_s) {
+            __stcg(dst, make_uint4(__float_as_uint(o.x), epoch, __float_as_uint(o.y), epoch));
+            __stcg(dst + 1, make_uint4(__float_as_uint(o.z), epoch, __float_as_uint(o.w), epoch));
+          }
         }
       }
     };
-    const unsigned n_items = static_cast<unsigned>(p.n_items);
-    const unsigned G = static_cast<unsigned>(p.G);
-    if (p.adapters && static_cast<unsigned>(c) < n_items) do_item(c);
+    if (p.adapters && c < p.n_items) do_item(c);
     SegWalk walk(p, c);
     int T, kb0, kb1, j = 0;
     bool have = walk.next(T, kb0, kb1);
@@ -929,17 +997,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       alive = epilogue_segment(T, kb0, kb1, j++);
       have = walk.next(T, kb0, kb1);
     }
-    if (p.adapters && alive && n_items > G) {
-      unsigned* claim_box = reinterpret_cast<unsigned*>(bcast);
-      while (true) {
-        if (et == 0) *claim_box = atomicAdd(&p.sync[0], 1u);
-        helper_sync();
-        const unsigned k = *claim_box;
-        helper_sync();
-        if (k >= n_items - G) break;
-        do_item(static_cast<int>(G + k));
-      }
-    }
+    if (p.adapters && alive)
+      for (int item = c + p.G; item < p.n_items; item += p.G) do_item(item);
     while (alive && have) {
       alive = epilogue_segment(T, kb0, kb1, j++);
       have = walk.next(T, kb0, kb1);
@@ -950,18 +1009,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 64) {
-    // (a helper thread: it has passed the dependency wait)
-    // the last CTA out returns the grid-wide counters and flags to zero
-    __threadfence();
-    const unsigned old = atomicAdd(&p.sync[2], 1u);
-    if (old == static_cast<unsigned>(p.G - 1)) {
-      // the next launch on this workspace tags its values with the next epoch
-      __threadfence();
-      p.sync[0] = 0u;
-      p.sync[3] = p.sync[3] + 1u;
-      __threadfence();
-      p.sync[2] = 0u;
-    }
+    // (a helper thread: it has read this launch's epoch) 256 in all per
+    // launch: 1 per CTA, CTA 0 the rest; nothing waits for the reduction
+    const unsigned long long add = c == 0 ? static_cast<unsigned long long>(kDecMaxCtas + 1 - p.G) : 1ull;
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p.counter), "l"(add) : "memory");
   }
   if (warp == 1) {
     tc_fence_after();
@@ -1102,7 +1153,7 @@ int launch_fused_decode(const DecodeArgs& a) {
   p.x_gs = a.x_global_scale;
   p.Y = static_cast<__nv_bfloat16*>(a.Y);
   p.status = a.status_dev;
-  p.sync = static_cast<unsigned*>(a.sync);
+  p.counter = reinterpret_cast<unsigned long long*>(static_cast<unsigned*>(a.sync) + kDecCounterWord);
   p.S = reinterpret_cast<uint2*>(a.S);
   p.accp = reinterpret_cast<uint2*>(a.accp);
   p.xq_out = static_cast<uint8_t*>(a.Xq);
@@ -1122,6 +1173,7 @@ int launch_fused_decode(const DecodeArgs& a) {
   p.parts = a.parts;
   p.kslice = a.kslice;
   p.n_items = p.adapters ? a.M * (a.s_row / kDecRanksPerItem) * a.parts : 0;
+  p.drop_s = a.drop_s;
   return a.fmt == EPILORA_FMT_NVFP4 ? launch_fused_decode_t<EPILORA_FMT_NVFP4, kDecKA>(p, a)
                                     : launch_fused_decode_t<EPILORA_FMT_FP8_E4M3, kDecKA>(p, a);
 }

@@ -79,11 +79,12 @@ def test_single_kernel_no_adapter_cases_are_bit_exact_base(fmt):
 @pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
 @pytest.mark.parametrize("M,K,N,r", [(1, 4096, 2048, 64), (6, 2048, 1024, 32)])
 def test_single_kernel_workspace_contents(fmt, M, K, N, r):
-    """The activation codes and scales the kernel used (stored by one thread
-    block) are the oracle's bit for bit; the shrink's partial sums over K
-    slices, added in part order, are the oracle's S within fp32 rounding; the
-    counters at the start of the workspace are zero again and the epoch has
-    moved on by one."""
+    """The activation codes and scales the kernel used (each thread block
+    stores the K range it quantized; together they cover the rows) are the
+    oracle's bit for bit; the shrink's partial sums over K slices, added in
+    part order, are the oracle's S within fp32 rounding; the launch counter
+    at bytes [16, 24) of the workspace has moved on by 256 and the rest of
+    the counter block is untouched."""
     L = 3
     p = make_projection(M, K, N, L, r, seed=M + K, idx_mode="uniform", device="cuda")
     w = T.quantize_weight(p.W, fmt)
@@ -95,8 +96,8 @@ def test_single_kernel_workspace_contents(fmt, M, K, N, r):
     T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx_t, workspace=ws, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    assert int(buf[:12].count_nonzero().item()) == 0          # claim and exit counters back to zero
-    assert int(buf[12:16].view(torch.int32).item()) == 1      # the epoch moved on by one launch
+    assert int(buf[16:24].view(torch.int64).item()) == 256    # one launch
+    assert int(buf[:16].count_nonzero().item()) == 0 and int(buf[24:256].count_nonzero().item()) == 0
     x, A, B = p.X.float().cpu().numpy(), p.A.float().cpu().numpy(), p.B.float().cpu().numpy()
     idx, mask = p.idx.cpu().numpy(), p.mask.cpu().numpy()
     r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
@@ -131,7 +132,7 @@ def test_single_kernel_chain_shares_workspace(fmt):
     """Single-kernel calls of different shapes back to back on one stream
     (each a programmatic dependent of the one before, sharing the workspace
     counters), eagerly and replayed from a CUDA graph three times: bitwise
-    equal to isolated calls, and the counters end at zero."""
+    equal to isolated calls; the launch counter ends at 256 per launch."""
     shapes = [(1, 4096, 6144, 1, 64), (1, 4096, 4096, 1, 64), (1, 4096, 28672, 1, 64), (1, 14336, 4096, 1, 64),
               (4, 2048, 1024, 3, 16)]
     cases = []
@@ -167,17 +168,18 @@ def test_single_kernel_chain_shares_workspace(fmt):
         torch.cuda.synchronize()
         for c, Y in zip(cases, outs):
             assert torch.equal(Y, c[3])
-    assert int(ws.buf[:12].count_nonzero().item()) == 0       # claim and exit counters back to zero
+    assert int(ws.buf[16:24].view(torch.int64).item()) == 256 * 4 * len(shapes)   # 1 eager run + 3 replays
 
 
 def test_bounded_wait_runs_out_and_the_context_stays_usable():
-    """A wait that runs out, made on the host: 2 tokens at rank 128 over 8 K
-    slices make 512 shrink items, more than thread blocks, so those past the
-    grid are claimed from the counter at the start of the workspace; that
-    counter is set past every item before the call, so they are never done and
-    the kernel's bounded wait for S gives up (about a second). The call
-    returns EPILORA_ERR_TIMEOUT in the status word, leaves the counters zero
-    again, and the next call on the same stream and workspace is correct."""
+    """A wait that runs out, made on the host: with the library's test hook on,
+    the shrink items of the single kernel publish nothing, so every thread
+    block that finishes a tile waits for S until its bounded wait gives up
+    (about a second). 2 tokens at rank 128 over 8 K slices make 512 items,
+    more than thread blocks (every block takes several). The call returns
+    EPILORA_ERR_TIMEOUT in the status word, every block still exits (the
+    launch counter moves on by 256), and with the hook off the next call on
+    the same stream and workspace is correct."""
     M, K, N, L, r = 2, 8192, 1024, 2, 128
     assert E.epilora_layer_forward_kernels(FP8, M, K, r) == 1
     p = make_projection(M, K, N, L, r, seed=5, device="cuda")
@@ -185,13 +187,16 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable():
     ref = T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask)
     ws = T.LayerWorkspace("cuda")
     buf = ws.get(FP8, M, K, r)
-    torch.cuda.synchronize()
-    buf[:4].view(torch.int32).fill_(0x7FFFFFFF)          # the claim counter: every item taken already
     st = status_buf()
-    T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, workspace=ws, status=st)
     torch.cuda.synchronize()
+    E.epilora_test_drop_shrink_results(True)
+    try:
+        T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, workspace=ws, status=st)
+        torch.cuda.synchronize()
+    finally:
+        E.epilora_test_drop_shrink_results(False)
     assert int(st.item()) == E.EPILORA_ERR_TIMEOUT
-    assert int(buf[:12].count_nonzero().item()) == 0          # claim and exit counters back to zero
+    assert int(buf[16:24].view(torch.int64).item()) == 256
     st.zero_()
     Y = T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, workspace=ws, status=st)
     torch.cuda.synchronize()

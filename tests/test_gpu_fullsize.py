@@ -90,11 +90,13 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
     cols_t = torch.from_numpy(cols).cuda()
     rows_t = torch.from_numpy(rows).cuda()
     buf = ws.buf
-    # workspace: the counters (zero again after the call), Xq, scales, S (room
-    # for min(8, ceil(K / 1024)) partial sums), and for more than 32 tokens
-    # the adapter-sorted row order: row q holds token perm[q]
+    # workspace: the head (a launch counter that grows by 256 per single-kernel
+    # call, nothing else in its first 256 bytes), Xq, scales, S (room for
+    # min(8, ceil(K / 1024)) partial sums), and for more than 32 tokens the
+    # adapter-sorted row order: row q holds token perm[q]
     off_xq = SYNC_BYTES
-    assert int(buf[:12].count_nonzero().item()) == 0          # claim and exit counters back to zero
+    assert int(buf[16:24].view(torch.int64).item()) % 256 == 0
+    assert int(buf[:16].count_nonzero().item()) == 0 and int(buf[24:256].count_nonzero().item()) == 0
     xq_bytes = M * K if fmt == FP8 else M * K // 2
     sc_bytes = 4 * M if fmt == FP8 else M * K // 16
     off_perm = off_xq + _r256(xq_bytes) + _r256(sc_bytes) + _r256(M * r * 4 * min(8, -(-K // 1024)))
