@@ -20,20 +20,21 @@
 // Roles (192 threads):
 //   warp 0      TMA producer: the CTA's weight units (and NVFP4 weight scale
 //               boxes) through a ring, started before the dependency wait
-//               (weights are never written by the preceding kernel) and
-//               behind the helpers' L2 hints;
+//               (weights are never written by the preceding kernel), L2
+//               hints (activations first, adapter rows behind the first
+//               units);
 //   warp 1      MMA issuer: tcgen05.mma (kind::f8f6f4, or kind::mxf4nvf4 with
 //               scales copied into TMEM) into one of two TMEM accumulators
 //               (one per segment of the run that falls in one weight tile),
 //               the activations read in place from the compact quantized
 //               copy (a no-swizzle operand whose core matrices are M x 16
 //               bytes apart along K);
-//   warps 2..5  helpers: L2 hints (activations, A rows, B slices), the
-//               dependency wait (griddepcontrol.wait), one bulk copy of the
-//               bf16 activation rows into the last ring slots, quantization
-//               of every token into shared memory (each CTA for itself: FP8
-//               divisions by Markstein's correction of the reciprocal
-//               product; each CTA quantizes the K range of its own units),
+//   warps 2..5  helpers: the dependency wait (griddepcontrol.wait), one
+//               bulk copy of the bf16 activation rows into the last ring
+//               slots, quantization of every token into shared memory (each
+//               CTA for itself: FP8 divisions by Markstein's correction of
+//               the reciprocal product; each CTA encodes the K range of its
+//               own units),
 //               shrink work items (token x 4 ranks x K slice, the arithmetic
 //               of the standalone shrink; CTA c takes items c, c + G, ...),
 //               then the epilogue of each segment.
@@ -360,8 +361,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   uint64_t* accf_bar = empty_bar + kDecMaxStages;    // [2] accumulator complete
   uint64_t* acce_bar = accf_bar + 2;                 // [2] accumulator read out
   uint64_t* xrdy_bar = acce_bar + 2;                 // compact activations written
-  uint64_t* pref_bar = xrdy_bar + 1;                 // the helpers' L2 hints are issued
-  uint64_t* xst_bar = pref_bar + 1;                  // the bf16 activation rows have landed
+  uint64_t* xst_bar = xrdy_bar + 1;                  // the bf16 activation rows have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xst_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);               // [4 warps][8]
@@ -383,7 +383,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       mbar_init(&acce_bar[b], 1);
     }
     mbar_init(xrdy_bar, 1);
-    mbar_init(pref_bar, 1);
     mbar_init(xst_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -406,11 +405,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
   if (warp == 0) {
     // ===== TMA producer: the run's weight units, in order =====
     if (lane == 0) {
-      // behind the helpers' L2 hints (they never wait before issuing them)
-      if (!mbar_wait_bounded(pref_bar, 0, kWaitLimitNs)) {
-        *abort_flag = 1;
-        record_status(p.status, EPILORA_ERR_TIMEOUT);
-      }
+      // the activation rows go to L2 first (a hint: the preceding kernel may
+      // still be writing them)
+      for (int t = 0; t < M; ++t)
+        prefetch_l2_bulk(p.X + static_cast<size_t>(t) * p.ldx, static_cast<uint32_t>(p.K * 2));
       uint32_t issued_mask = 0, parity_mask = 0;
       long long it = 0;
       const long long u_begin = (p.U * c) / p.G, u_end = (p.U * (c + 1)) / p.G;
@@ -423,7 +421,33 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           break;
         }
         // the last xslots slots hold the activation rows until the quantized
-        // copy is published
+        // copy is published; meanwhile, with the first units requested, this
+        // CTA's share of the adapters' A rows and the B slices of the tiles
+        // it finishes go to L2 (the index read here may still change: hints)
+        if (it == stages - p.xslots && p.adapters) {
+          const size_t abytes = static_cast<size_t>(p.s_row) * p.K * (p.a_scale != nullptr ? 1 : 2);
+          const size_t share = ((abytes + p.G - 1) / p.G + 255) / 256 * 256;
+          const size_t lo = share * c;
+          int prev = -1;
+          for (int t = 0; t < M; ++t) {
+            int l;
+            asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(l) : "l"(p.idx + t));
+            if (l < 0 || l >= p.L || l == prev) continue;
+            prev = l;
+            if (lo < abytes)
+              prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.A) + static_cast<size_t>(l) * abytes + lo,
+                               static_cast<uint32_t>(min(share, abytes - lo)));
+            SegWalk w2(p, c);
+            int T2, kb0, kb1;
+            while (w2.next(T2, kb0, kb1)) {
+              if (kb0 != 0) continue;
+              const int rows = min(128, p.N - T2 * 128);
+              const int bb = p.a_scale != nullptr ? p.r : 2 * p.r;   // bytes of one B row
+              prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.B) + (static_cast<size_t>(l) * p.N + T2 * 128) * bb,
+                               static_cast<uint32_t>(rows * bb));
+            }
+          }
+        }
         if (it == stages - p.xslots && !mbar_wait_bounded(xrdy_bar, 0, kWaitLimitNs)) {
           *abort_flag = 1;
           record_status(p.status, EPILORA_ERR_TIMEOUT);
@@ -557,40 +581,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     // ===== helpers =====
     const int et = threadIdx.x - 64;
     const int hw = warp - 2;                      // helper warp 0..3
-    // hints before the wait, issued ahead of the weight ring (the producer
-    // waits for them): the activation rows, this CTA's share of the adapters'
-    // A rows and the B slices of the tiles it finishes go to L2 first, so the
-    // loads on the critical path after the wait do not queue behind the
-    // weight stream (the index read here may still change: hints only)
-    if (et == 0) {
-      for (int t = 0; t < M; ++t)
-        prefetch_l2_bulk(p.X + static_cast<size_t>(t) * p.ldx, static_cast<uint32_t>(p.K * 2));
-      if (p.adapters) {
-        const size_t abytes = static_cast<size_t>(p.s_row) * p.K * (p.a_scale != nullptr ? 1 : 2);
-        const size_t share = ((abytes + p.G - 1) / p.G + 255) / 256 * 256;
-        const size_t lo = share * c;
-        int prev = -1;
-        for (int t = 0; t < M; ++t) {
-          int l;
-          asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(l) : "l"(p.idx + t));
-          if (l < 0 || l >= p.L || l == prev) continue;
-          prev = l;
-          if (lo < abytes)
-            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.A) + static_cast<size_t>(l) * abytes + lo,
-                             static_cast<uint32_t>(min(share, abytes - lo)));
-          SegWalk w2(p, c);
-          int T, kb0, kb1;
-          while (w2.next(T, kb0, kb1)) {
-            if (kb0 != 0) continue;
-            const int rows = min(128, p.N - T * 128);
-            const int bb = p.a_scale != nullptr ? p.r : 2 * p.r;   // bytes of one B row
-            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.B) + (static_cast<size_t>(l) * p.N + T * 128) * bb,
-                             static_cast<uint32_t>(rows * bb));
-          }
-        }
-      }
-      mbar_arrive(pref_bar);
-    }
     // the preceding kernel on the stream has completed: X, idx, mask and the
     // workspace are valid from here on
     pdl_wait_primary();
