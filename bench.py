@@ -804,6 +804,35 @@ def run_profile_fused(args):
                       "kernels_per_call": E.epilora_layer_forward_kernels(fmt, M, K, r), "ok": True}))
 
 
+def run_profile_large(args):
+    """The 8B NVFP4 M = 512 layer's gate_up projection alone, for ncu: three
+    fused layer calls (shrink grid + wide-tile GEMM) on Zipf-indexed rank-64
+    adapters out of 128."""
+    import torch
+
+    import precision_gemm_token_gb300 as E
+    from precision_gemm_token_gb300 import tensors as T
+    from synth import make_projection
+
+    E.build()
+    E.load()
+    _, plist, M, fmt, L, r, idx_mode, mask_mode, n_decode, _ = LARGE_WORKLOADS[1]
+    _, K, N = plist[2]
+    p = make_projection(M, K, N, L, r, seed=302, idx_mode=idx_mode, mask_mode=mask_mode, n_decode=n_decode,
+                        device="cuda")
+    w = T.quantize_weight(p.W, fmt)
+    del p.W
+    gx = T.nvfp4_global_scale(p.X)
+    ws = T.LayerWorkspace("cuda")
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx, workspace=ws, status=st, Y=Y)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    print(json.dumps({"profile": "8b_m512_nvfp4", "kernel": f"gate_up {K}->{N} M={M}", "ok": True}))
+
+
 def run_profile_wide(args):
     """A wide-tile fused layer call alone, for ncu: the Llama-3.1-70B gate_up
     projection's quarter column slice (K 8192 -> N 14336: 1008 tiles of
@@ -846,6 +875,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true", help="run the dominant kernel alone (for ncu)")
     ap.add_argument("--profile-wide", action="store_true", help="run one wide-tile fused layer call alone (for ncu)")
+    ap.add_argument("--profile-large", action="store_true",
+                    help="run the 8B NVFP4 M=512 gate_up fused call alone (for ncu)")
     ap.add_argument("--profile-fused", action="store_true",
                     help="run the workload's fused gate_up layer call alone (for ncu)")
     args = ap.parse_args()
@@ -859,6 +890,9 @@ def main():
         return
     if args.profile_fused:
         run_profile_fused(args)
+        return
+    if args.profile_large:
+        run_profile_large(args)
         return
     rank, world, local = dist_setup()
     if args.impl == "reference":
