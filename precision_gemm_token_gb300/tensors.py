@@ -139,8 +139,8 @@ def gemm_lora_epilogue(Xq, x_scale, w: QuantWeight, M, K, S=None, B=None, idx=No
 
 class LayerWorkspace:
     """Caller-owned workspace for epilora_layer_forward (grown on demand).
-    Zero-filled when (re)allocated: the library wants the counters at its
-    start zero before the first call and leaves them zero after each."""
+    Zero-filled when (re)allocated: the library wants the head of the
+    workspace zero before the first call and keeps it valid after each."""
 
     def __init__(self, device):
         self.device = torch.device(device)
