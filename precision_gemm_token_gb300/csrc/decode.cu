@@ -552,11 +552,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
                 const uint32_t slot = 32u + static_cast<uint32_t>(it & 1) * C::kSfSlot;
                 const uint32_t sfa_col = slot + jj * 4;
                 const uint32_t sfb_col = slot + C::kSfCols + jj * 4;
-                const int ks_glob = (kb * KA + a) * 4 + kk;              // k-step within the row
-                tc_cp_32x128b_warpx4(tmem_base + sfa_col,
-                                     make_smem_desc(smem_u32(sfa) + jj * 512, 16, 128, kSwizzleNone));
-                tc_cp_32x128b_warpx4(tmem_base + sfb_col,
-                                     make_smem_desc(xsf_addr + ks_glob * x_lbo, 16, 128, kSwizzleNone));
+                if (jj == 0) {
+                  // the unit's scale copies first (weight atoms and token lines
+                  // of its k-steps), then its MMAs
+#pragma unroll
+                  for (int j2 = 0; j2 < 4 * KA; ++j2) {
+                    tc_cp_32x128b_warpx4(tmem_base + slot + j2 * 4,
+                                         make_smem_desc(smem_u32(sfa) + j2 * 512, 16, 128, kSwizzleNone));
+                    tc_cp_32x128b_warpx4(tmem_base + slot + C::kSfCols + j2 * 4,
+                                         make_smem_desc(xsf_addr + (kb * KA * 4 + j2) * x_lbo, 16, 128, kSwizzleNone));
+                  }
+                }
                 mma_mxf4nvf4(d_tmem, adesc, bdesc, C::kIdesc, tmem_base + sfa_col, tmem_base + sfb_col, accum);
               } else {
                 mma_f8f6f4(d_tmem, adesc, bdesc, C::kIdesc, accum);
