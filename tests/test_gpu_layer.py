@@ -36,6 +36,7 @@ SHAPES = [
     (100, 512, 384, 5, 32),     # BT 128, no split
     (130, 256, 256, 3, 16),     # BT 256
     (300, 512, 272, 7, 64),     # two 256-token tiles, ragged both ways
+    (160, 512, 384, 9, 128),    # wide tiles at rank 128
 ]
 
 
@@ -56,7 +57,7 @@ def test_layer_mask_prefill_chunk(fmt):
 
 
 @pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
-@pytest.mark.parametrize("r", [16, 32, 64])
+@pytest.mark.parametrize("r", [16, 32, 64, 128])
 def test_wide_tiles_prefill_chunk_one_adapter_runs(fmt, r):
     """Wide (256-token) tiles whose columns are long one-adapter runs, mask-0
     decode tokens and a ragged last tile: the one-adapter, no-adapter and
@@ -72,6 +73,7 @@ WIDE_PERSISTENT = [
     (520, 256, 7168, 8, 16, "uniform", "all"),           # mixed-adapter chunks, ragged token tile
     (520, 256, 7152, 64, 32, "zipf", "prefill_chunk"),   # one-adapter runs, mask-0 tokens, ragged weight tile
     (1000, 512, 5120, 16, 64, "zipf", "all"),            # rank 64
+    (520, 256, 3072, 24, 128, "zipf", "all"),            # rank 128 (the two-CTA kernel for both formats)
     (520, 256, 7168, 8, 0, "uniform", "all"),            # no adapter
 ]
 
