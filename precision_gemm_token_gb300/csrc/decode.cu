@@ -99,7 +99,7 @@ struct DecParams {
   // so no flag or counter has to be polled before the data.
   uint2* S;            // [parts][M][s_row] partial sums of the shrink
   uint2* accp;         // [G][M][128] partial rows of split weight tiles
-  uint8_t* xq_out;     // the quantized activations also go here (each CTA its K range)
+  uint8_t* xq_out;     // the quantized activations also go here (each code by one CTA)
   float* xs_out;       // FP8 scales
   uint8_t* xsb_out;    // NVFP4 block scales
   long long U;         // units in total
@@ -157,32 +157,35 @@ __device__ __forceinline__ unsigned launch_tag(unsigned long long e) {
 // One tagged 64-bit value, read again until its tag is `epoch` (1 s limit;
 // on timeout the last word read, whose tag is then another). `w` holds a
 // first read already made.
-__device__ __forceinline__ uint2 reread_tagged(const uint2* p, unsigned epoch, uint2 w) {
-  if (w.y == epoch) return w;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    __nanosleep(32);
-    w = __ldcg(p);
-    if (w.y == epoch || globaltimer_ns() - t0 > kWaitLimitNs) return w;
-  }
-}
-
 // n <= N tagged values p[0], p[stride], ... whose first reads are in w:
-// late ones read again, none after a timeout. The values go to v[0..n);
-// false if one timed out.
+// the late ones are read again, all of them in each round (one round trip
+// per round however many are late), until every tag is this launch's or
+// the wait limit has passed. The values go to v[0..n); false on a timeout.
 template <int N>
 __device__ __forceinline__ bool check_tagged_n(const uint2* p, size_t stride, int n, unsigned epoch, uint2 (&w)[N],
                                                float (&v)[N]) {
-  bool ok = true;
+  auto all_here = [&]() {
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (i < n && w[i].y != epoch) ok = false;
+    return ok;
+  };
+  bool ok = all_here();
+  if (!ok) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      __nanosleep(32);
+#pragma unroll
+      for (int i = 0; i < N; ++i)
+        if (i < n && w[i].y != epoch) w[i] = __ldcg(p + i * stride);
+      ok = all_here();
+      if (ok || globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
 #pragma unroll
   for (int i = 0; i < N; ++i)
-    if (i < n) {
-      if (w[i].y != epoch && ok) {
-        w[i] = reread_tagged(p + i * stride, epoch, w[i]);
-        ok = w[i].y == epoch;
-      }
-      v[i] = __uint_as_float(w[i].x);
-    }
+    if (i < n) v[i] = __uint_as_float(w[i].x);
   return ok;
 }
 
@@ -411,6 +414,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         prefetch_l2_bulk(p.X + static_cast<size_t>(t) * p.ldx, static_cast<uint32_t>(p.K * 2));
       uint32_t issued_mask = 0, parity_mask = 0;
       long long it = 0;
+      // every weight byte is read once per call: streamed with the first
+      // eviction priority, so that the activations, the adapter rows and the
+      // exchanged partial sums stay in L2 beside the stream
+      const uint64_t wpol = l2_policy_evict_first();
       const long long u_begin = (p.U * c) / p.G, u_end = (p.U * (c + 1)) / p.G;
       for (long long u = u_begin; u < u_end; ++u, ++it) {
         const int s = static_cast<int>(it % stages);
@@ -458,8 +465,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         uint8_t* st = smem + static_cast<size_t>(s) * C::kStage;
         mbar_arrive_expect_tx(&full_bar[s], C::kStageTx);
 #pragma unroll
-        for (int a = 0; a < KA; ++a) tma_load_2d(st + a * kDecAtomW, &p.tmW, &full_bar[s], (kb * KA + a) * 128, T * 128);
-        if (C::kFP4) tma_load_2d(st + C::kUnitW + C::kSfA, &p.tmSW, &full_bar[s], kb * 16 * KA, T * 128);
+        for (int a = 0; a < KA; ++a)
+          tma_load_2d_hint(st + a * kDecAtomW, &p.tmW, &full_bar[s], (kb * KA + a) * 128, T * 128, wpol);
+        if (C::kFP4) tma_load_2d_hint(st + C::kUnitW + C::kSfA, &p.tmSW, &full_bar[s], kb * 16 * KA, T * 128, wpol);
         issued_mask |= 1u << s;
         parity_mask = (parity_mask & ~(1u << s)) | (ph << s);
       }
@@ -587,6 +595,27 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     // ===== helpers =====
     const int et = threadIdx.x - 64;
     const int hw = warp - 2;                      // helper warp 0..3
+    // (launch parameters only: worked out while the preceding kernel runs)
+    const int nch = p.K / 8;                      // 16-byte bf16 chunks per row
+    // Quantization steps (FP8: 8-element chunks; NVFP4: 16-element blocks;
+    // 16 KA of either per weight unit) that this CTA's MMAs read: those of
+    // the K atoms its units cover, [lo, hi] or, wrapping around a tile end,
+    // [lo, end) and [0, hi]; the whole row when it covers a tile.
+    const int nsteps = C::kFP4 ? p.K / kNvfp4Block : nch;
+    int rb0, re0, rb1 = 0, re1 = 0;
+    // the K units of tile 0 in this CTA's run [own_lo, own_hi): the codes of
+    // those steps go to the workspace copy from this CTA only (one writer each)
+    int own_lo, own_hi;
+    {
+      const long long ub = (p.U * c) / p.G, ue = (p.U * (c + 1)) / p.G;
+      own_lo = static_cast<int>(min(ub, static_cast<long long>(p.nkb)));
+      own_hi = static_cast<int>(min(ue, static_cast<long long>(p.nkb)));
+      const int lo = static_cast<int>(ub % p.nkb) * 16 * KA;
+      const int hi = min(nsteps, (static_cast<int>((ue - 1) % p.nkb) + 1) * 16 * KA);
+      rb0 = ue - ub >= p.nkb ? 0 : lo;
+      re0 = ue - ub >= p.nkb || lo >= hi ? nsteps : hi;
+      if (ue - ub < p.nkb && lo >= hi) re1 = hi;
+    }
     // the preceding kernel on the stream has completed: X, idx, mask and the
     // workspace are valid from here on
     pdl_wait_primary();
@@ -613,7 +642,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
     // each to the counter, CTAs of this one that already exited less than 256
     const unsigned epoch = launch_tag(__ldcg(p.counter) >> 8);
     float alpha = 1.0f;
-    const int nch = p.K / 8;                      // 16-byte bf16 chunks per row
     if (et < M) {
       if (li >= p.L) record_status(p.status, EPILORA_ERR_INVALID_ARG);
       meta_idx[et] = (li >= 0 && li < p.L && mk != 0) ? li : -1;
@@ -623,20 +651,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
       record_status(p.status, EPILORA_ERR_TIMEOUT);
     }
     const uint4* xs4 = reinterpret_cast<const uint4*>(xs);   // chunk q of the M x nch chunks
-    // Quantization steps (FP8: 8-element chunks; NVFP4: 16-element blocks;
-    // 16 KA of either per weight unit) that this CTA's MMAs read: those of
-    // the K atoms its units cover, [lo, hi] or, wrapping around a tile end,
-    // [lo, end) and [0, hi]; the whole row when it covers a tile.
-    const int nsteps = C::kFP4 ? p.K / kNvfp4Block : nch;
-    int rb0, re0, rb1 = 0, re1 = 0;
-    {
-      const long long ub = (p.U * c) / p.G, ue = (p.U * (c + 1)) / p.G;
-      const int lo = static_cast<int>(ub % p.nkb) * 16 * KA;
-      const int hi = min(nsteps, (static_cast<int>((ue - 1) % p.nkb) + 1) * 16 * KA);
-      rb0 = ue - ub >= p.nkb ? 0 : lo;
-      re0 = ue - ub >= p.nkb || lo >= hi ? nsteps : hi;
-      if (ue - ub < p.nkb && lo >= hi) re1 = hi;
-    }
     // ---- activation quantization into the compact copy ----
     if (!C::kFP4) {
       // per-token amax over the whole row, on bf16 pairs
@@ -661,21 +675,47 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
         if (c == 0) p.xs_out[et] = sc;
       }
       helper_sync();
-      // the codes of this CTA's steps (the IEEE division for rows whose scale
-      // is below 2^-100), also stored to the workspace copy
+      // the codes of this CTA's steps, also stored to the workspace copy:
+      // four independent chunks per thread and round (the division by the
+      // reciprocal product; the IEEE division for rows whose scale is below
+      // 2^-100)
+      bool tiny = false;
+      for (int t = 0; t < M; ++t) tiny = tiny || !(meta_sx[t] >= 0x1p-100f);
+      const int kown0 = own_lo * 128 * KA, kown1 = own_hi * 128 * KA;
+      auto put = [&](int t, int k0, uint2 code) {
+        *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
+        if (k0 >= kown0 && k0 < kown1) *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+      };
 #pragma unroll 1
       for (int g = 0; g < 2; ++g) {
         const int rbg = g == 0 ? rb0 : rb1;
         const int n = (g == 0 ? re0 : re1) - rbg;
-#pragma unroll 2
-        for (int q = et; q < M * n; q += 128) {
-          const int t = q / n;
-          const int k0 = (rbg + q - t * n) * 8;
-          const float sc = meta_sx[t];
-          const uint4 v = xs4[static_cast<size_t>(t) * nch + k0 / 8];
-          const uint2 code = sc >= 0x1p-100f ? quant8_e4m3_rs(v, sc, meta_rs[t]) : quant8_e4m3(v, sc);
-          *reinterpret_cast<uint2*>(xc + ((k0 >> 4) * M + t) * 16 + ((k0 >> 3) & 1) * 8) = code;
-          *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * p.K + k0) = code;
+        if (!tiny) {
+#pragma unroll 1
+          for (int q0 = et; q0 < M * n; q0 += 4 * 128) {
+            int t4[4], k4[4];
+            uint4 v4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int q = q0 + u * 128;
+              t4[u] = q / n;
+              k4[u] = (rbg + q - t4[u] * n) * 8;
+              if (q < M * n) v4[u] = xs4[static_cast<size_t>(t4[u]) * nch + k4[u] / 8];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (q0 + u * 128 < M * n)
+                put(t4[u], k4[u], quant8_e4m3_rs(v4[u], meta_sx[t4[u]], meta_rs[t4[u]]));
+          }
+        } else {
+#pragma unroll 1
+          for (int q = et; q < M * n; q += 128) {
+            const int t = q / n;
+            const int k0 = (rbg + q - t * n) * 8;
+            const float sc = meta_sx[t];
+            const uint4 v = xs4[static_cast<size_t>(t) * nch + k0 / 8];
+            put(t, k0, sc >= 0x1p-100f ? quant8_e4m3_rs(v, sc, meta_rs[t]) : quant8_e4m3(v, sc));
+          }
         }
       }
       // zero codes past K up to the unit boundary (finite values against the
@@ -735,8 +775,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) fused_decode_kernel(const __gr
           // b / 2, half b % 2; its scale is byte b % 4 of the line of k-step b / 4
           *reinterpret_cast<uint2*>(xc + ((b >> 1) * M + t) * 16 + (b & 1) * 8) = make_uint2(lo, hi);
           xsf[((b >> 2) * M + t) * 16 + (b & 3)] = static_cast<uint8_t>(sb);
-          *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * (p.K / 2) + b * 8) = make_uint2(lo, hi);
-          p.xsb_out[static_cast<size_t>(t) * nb + b] = static_cast<uint8_t>(sb);
+          if (b >= own_lo * 16 * KA && b < own_hi * 16 * KA) {
+            *reinterpret_cast<uint2*>(p.xq_out + static_cast<size_t>(t) * (p.K / 2) + b * 8) = make_uint2(lo, hi);
+            p.xsb_out[static_cast<size_t>(t) * nb + b] = static_cast<uint8_t>(sb);
+          }
         }
       }
     }

@@ -364,17 +364,29 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     if (kb >= nkb) kb -= nkb;
     return kb + kb_begin;
   };
+  // A single token tile reads every weight byte once: the weights then
+  // stream with the first eviction priority, so that the activations, S and
+  // the adapters' B slices stay in L2 beside them (several token tiles
+  // re-read them and keep the default).
+  const bool w_once = gridDim.y == 1;
+  const uint64_t wpol = l2_policy_evict_first();
   // TMA loads of ring slot s for loop iteration i: weights (+ their scales)
   auto issue_w = [&](int i, int s) {
     uint8_t* st = smem + static_cast<size_t>(s) * C::kStageBytes;
     const int kb = stage_kb(i);
     mbar_arrive_expect_tx(&full_bar[s], C::kStageTx);
+    uint8_t* sfw = st + C::kWBytes + C::kXBytes + C::kSfABytes + C::kSfBBytes;
+    if (w_once) {
 #pragma unroll
-    for (int a = 0; a < KA; ++a)
-      tma_load_2d(st + a * C::kWAtom, &p.tmW, &full_bar[s], (kb * KA + a) * kAtomBytes, n0);
-    if (C::kFP4)
-      tma_load_2d(st + C::kWBytes + C::kXBytes + C::kSfABytes + C::kSfBBytes, &p.tmSW, &full_bar[s],
-                  kb * C::kSfRow, n0);
+      for (int a = 0; a < KA; ++a)
+        tma_load_2d_hint(st + a * C::kWAtom, &p.tmW, &full_bar[s], (kb * KA + a) * kAtomBytes, n0, wpol);
+      if (C::kFP4) tma_load_2d_hint(sfw, &p.tmSW, &full_bar[s], kb * C::kSfRow, n0, wpol);
+    } else {
+#pragma unroll
+      for (int a = 0; a < KA; ++a)
+        tma_load_2d(st + a * C::kWAtom, &p.tmW, &full_bar[s], (kb * KA + a) * kAtomBytes, n0);
+      if (C::kFP4) tma_load_2d(sfw, &p.tmSW, &full_bar[s], kb * C::kSfRow, n0);
+    }
   };
   // ... and activations (+ their scales)
   auto issue_x = [&](int i, int s) {
