@@ -266,11 +266,12 @@ def run_ours(args, rank, world, local):
                 T.layer_forward(p.X, q["w"], p.A, p.B, p.idx, p.mask, x_global_scale=q["gx"], workspace=q["ws"],
                                 status=q["st"], stream=stream, Y=q["Y"])
 
-    def layer_line(projs, fmt, steps, warmup, desc, M):
+    def layer_line(projs, fmt, steps, warmup, desc, M, layers=1):
         """Layer time (graph replay, L2 flushed) and the layer's HBM
-        fraction over its algorithmic bytes."""
+        fraction over its algorithmic bytes; `layers` layers of distinct
+        weights in one graph are reported per layer."""
         ms, _, _, _ = time_graph(projs, steps, warmup)
-        ms = max_over_ranks(ms, world, dev)
+        ms = max_over_ranks(ms, world, dev) / layers
         byts = 0
         for q in projs:
             pq = q["p"]
@@ -280,11 +281,13 @@ def run_ours(args, rank, world, local):
             if q["ad"] is not None:       # stored FP8 tables: 1 byte per element + a scale per row
                 b -= nd * (q["r"] * q["K"] + q["N"] * q["r"]) - nd * (q["r"] + q["N"]) * 4
             byts += b
+        byts //= layers
         gbs = byts / (ms / 1000) / 1e9
         return {"workload": desc, "M": M, "layer_us": round(ms * 1000, 2),
                 "tokens_per_s": round(world * M / (ms / 1000), 1), "algorithmic_bytes": int(byts),
                 "hbm_gbs": round(gbs, 1), "hbm_frac_of_measured": round(gbs / peaks.get("hbm_gbs", 6800.0), 4),
-                "kernels_per_projection": [E.epilora_layer_forward_kernels(fmt, M, q["K"], q["r"]) for q in projs]}
+                "kernels_per_projection": [E.epilora_layer_forward_kernels(fmt, M, q["K"], q["r"])
+                                           for q in projs[:len(projs) // layers]]}
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
@@ -422,7 +425,7 @@ def run_ours(args, rank, world, local):
     # more decode layers of the configurations: 32 tenants (FP8 base with bf16
     # adapters, the same with stored FP8 adapters, an NVFP4 base), the NVFP4
     # layer over M and rank, and multi-slice projections
-    t32 = t32_fp8ad = t32_nv = nv = slices_line = None
+    t32 = t32_fp8ad = t32_nv = nv = slices_line = chain_line = None
     nv_sweep = []
     xsteps = max(args.steps // 4, 5)
     if not args.skip_tenants:
@@ -462,6 +465,17 @@ def run_ours(args, rank, world, local):
         slices_line = layer_line(pr, 0, xsteps, args.warmup,
                                  "Llama-3.1-8B layer, M=1, FP8, qkv as three slices (q, k, v) and gate_up as two "
                                  "(gate, up), one rank-64 adapter pair per slice", 1)
+        del pr
+        torch.cuda.empty_cache()
+        # four layers of distinct weights in one graph, as a decode step runs
+        # them (0.9 GB, far larger than L2; the flush stays outside the
+        # events): the cost of one layer inside a chain
+        pr = []
+        for li in range(4):
+            pr += make_layer("8b_m1_fp8", seed=600 + 10 * li)
+        chain_line = layer_line(pr, 0, xsteps, args.warmup,
+                                "four Llama-3.1-8B decode layers of distinct weights in one graph, M=1, FP8, one "
+                                "rank-64 adapter each; per layer", 1, layers=4)
         del pr
         torch.cuda.empty_cache()
 
@@ -598,6 +612,7 @@ def run_ours(args, rank, world, local):
         "nvfp4_m1": nv,
         "nvfp4_sweep": nv_sweep,
         "multi_slice": slices_line,
+        "layers_chained": chain_line,
         "large_m": large,
         "e2e": e2e,
         # per projection: one persistent kernel (single-kernel decode path) or
