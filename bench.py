@@ -69,10 +69,12 @@ WORKLOADS = {
 }
 
 
-def csrc_sha256() -> str:
+def csrc_sha256(files=None) -> str:
+    """sha256 over the named files of the kernel sources (all of them by
+    default), in name order."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "precision_gemm_token_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(files or os.listdir(d)):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()
@@ -86,8 +88,12 @@ def read_profile_traffic(workload: str, kernel: str = "gemm_gate_up"):
         return None
     txt = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    s = re.search(r"csrc_sha256:\s*([0-9a-f]+)", txt)
-    if not m or not s or s.group(1) != csrc_sha256():
+    # the hash of the files the kernel is compiled from (listed), else of all
+    # kernel sources
+    srcs = re.search(r"kernel_sources:\s*([\w. ]+)", txt)
+    s = re.search(r"sources_sha256:\s*([0-9a-f]+)", txt) or re.search(r"csrc_sha256:\s*([0-9a-f]+)", txt)
+    files = srcs.group(1).split() if srcs else None
+    if not m or not s or s.group(1) != csrc_sha256(files):
         return None
     return float(m.group(1))
 
@@ -794,7 +800,8 @@ def run_profile(args):
 def run_profile_fused(args):
     """One fused layer call alone, for ncu: the workload's gate_up projection
     (4096 -> 28672) through epilora_layer_forward five times on one
-    workspace (for a few tokens this is the single-kernel decode path)."""
+    workspace, on the single-kernel decode path (for a few tokens; both
+    formats)."""
     import torch
 
     import precision_gemm_token_gb300 as E
@@ -803,6 +810,7 @@ def run_profile_fused(args):
 
     E.build()
     E.load()
+    E.epilora_set_decode_path(E.DECODE_PATH_SINGLE)
     M, fmt, L, r, idx_mode, _ = WORKLOADS[args.workload]
     _, K, N = PROJ8B[2]
     p = make_projection(M, K, N, L, r, seed=102, idx_mode=idx_mode, device="cuda")

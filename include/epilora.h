@@ -192,17 +192,38 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
 
 /*
- * Number of kernels epilora_layer_forward (and _slices, _noalloc) enqueues
- * for (fmt, M, K, r), r as for epilora_workspace_bytes (rank times slices, 0
- * without adapters): 1 when the single-kernel decode path takes the call, 2
- * otherwise (the shrink grid with its quantizer blocks, then the GEMM as its
- * programmatic dependent). The single kernel takes a few tokens: M <= 8,
- * FP8 with M * K <= 16384 (one token up to K = 16384, four at K = 4096),
- * NVFP4 with the bf16 rows within 40 KB (one token up to K = 16384, two at
- * K = 8192), as long as the shared memory of the call leaves room for two
- * weight stages (large M * r excludes it). Returns 0 for invalid arguments.
+ * Number of kernels epilora_layer_forward (and _slices, _fp8_adapters,
+ * _noalloc) enqueues for (fmt, M, K, r), r as for epilora_workspace_bytes
+ * (rank times slices, 0 without adapters), under the current decode-path
+ * policy (epilora_set_decode_path): 1 when the single-kernel decode path takes
+ * the call, 2 otherwise (the shrink grid with its quantizer blocks, then the
+ * GEMM as its programmatic dependent). The single kernel can take a few
+ * tokens: M <= 8, FP8 with M * K <= 16384 (one token up to K = 16384, four at
+ * K = 4096), NVFP4 with the bf16 rows within 40 KB (one token up to
+ * K = 16384, two at K = 8192), as long as the shared memory of the call
+ * leaves room for two weight stages (large M * r excludes it); the automatic
+ * policy gives it the FP8 calls only. Returns 0 for invalid arguments.
  */
 EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K, int r);
+
+/*
+ * Decode-path policy for all later calls in the process (calls already
+ * enqueued are not affected): which path epilora_layer_forward (and _slices,
+ * _fp8_adapters, _noalloc) takes for calls the single kernel can run.
+ *   EPILORA_DECODE_PATH_AUTO (the default): the single kernel for FP8 bases,
+ *     the shrink grid and the GEMM for NVFP4 bases (on GB300 each is the
+ *     faster of the two for its format at one token on the 8B layer);
+ *   EPILORA_DECODE_PATH_SINGLE: the single kernel wherever it can run;
+ *   EPILORA_DECODE_PATH_TWO: the shrink grid and the GEMM always.
+ * Results agree between the paths within the arithmetic bound of the
+ * method (the adapter term and the split-K sums are added in a different
+ * order). Returns the previous policy, or EPILORA_ERR_INVALID_ARG (policy
+ * unchanged) for another value.
+ */
+#define EPILORA_DECODE_PATH_AUTO 0
+#define EPILORA_DECODE_PATH_SINGLE 1
+#define EPILORA_DECODE_PATH_TWO 2
+EPILORA_API int epilora_set_decode_path(int policy);
 
 /*
  * Fused one-call layer (the decode path of the EpiLoRA page, §Design ›

@@ -15,6 +15,9 @@ from ._binding import (  # noqa: F401
     EPILORA_ERR_TIMEOUT,
     EPILORA_ERR_UNSUPPORTED,
     EPILORA_ERR_WORKSPACE,
+    DECODE_PATH_AUTO,
+    DECODE_PATH_SINGLE,
+    DECODE_PATH_TWO,
     EPILORA_OK,
     FMT_FP8,
     FMT_NVFP4,
@@ -31,6 +34,7 @@ from ._binding import (  # noqa: F401
     epilora_lora_shrink,
     epilora_nvfp4_global_scale,
     epilora_quant_act,
+    epilora_set_decode_path,
     epilora_status_string,
     epilora_workspace_bytes,
     load,

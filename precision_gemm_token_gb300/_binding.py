@@ -38,6 +38,7 @@ SIGNATURES = {
     "epilora_workspace_bytes": (_sz, [_c_int, _c_int, _c_int, _c_int]),
     "epilora_layer_forward_kernels": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
     "epilora_test_drop_shrink_results": (_c_int, [_c_int]),
+    "epilora_set_decode_path": (_c_int, [_c_int]),
     "epilora_layer_forward": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _sz, _vp, _vp]),
     "epilora_layer_forward_fp8_adapters": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp,
@@ -144,6 +145,18 @@ def epilora_workspace_bytes(fmt, M, K, r) -> int:
 
 def epilora_layer_forward_kernels(fmt, M, K, r) -> int:
     return load().epilora_layer_forward_kernels(fmt, M, K, r)
+
+
+DECODE_PATH_AUTO, DECODE_PATH_SINGLE, DECODE_PATH_TWO = 0, 1, 2
+
+
+def epilora_set_decode_path(policy: int) -> int:
+    """Decode-path policy for later calls (DECODE_PATH_AUTO: the single kernel
+    for FP8, the shrink grid and GEMM for NVFP4; _SINGLE: the single kernel
+    wherever it can run; _TWO: never). Returns the previous policy."""
+    rc = load().epilora_set_decode_path(policy)
+    check(rc if rc < 0 else 0, "set_decode_path")
+    return rc
 
 
 def epilora_test_drop_shrink_results(on: bool) -> None:

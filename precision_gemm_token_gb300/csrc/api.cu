@@ -59,6 +59,18 @@ bool shrink_args_ok(const void* X, int M, int K, int ldx, const void* A, int L, 
 
 namespace {
 std::atomic<int> g_test_drop_s{0};
+std::atomic<int> g_decode_path{EPILORA_DECODE_PATH_AUTO};
+
+// Whether the single-kernel decode path takes a call: eligible, and chosen by
+// the policy (automatic: FP8 only; for NVFP4 the shrink grid and the GEMM
+// are the faster pair on GB300 at one token, the 8B layer 73.5-74 against
+// 77.5 us).
+bool single_kernel_takes(int fmt, int M, int K, int r) {
+  const int pol = g_decode_path.load(std::memory_order_relaxed);
+  if (pol == EPILORA_DECODE_PATH_TWO) return false;
+  if (pol == EPILORA_DECODE_PATH_AUTO && fmt != EPILORA_FMT_FP8_E4M3) return false;
+  return decode_path_eligible(fmt, M, K, r);
+}
 }  // namespace
 
 int decode_test_drop_s() { return g_test_drop_s.load(); }
@@ -233,7 +245,13 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K, const v
 EPILORA_API int epilora_layer_forward_kernels(int fmt, int M, int K, int r) {
   if (!fmt_ok(fmt) || M < 0 || !k_ok(K) || r < 0) return 0;
   if (M == 0) return 0;
-  return decode_path_eligible(fmt, M, K, r) ? 1 : 2;
+  return single_kernel_takes(fmt, M, K, r) ? 1 : 2;
+}
+
+EPILORA_API int epilora_set_decode_path(int policy) {
+  if (policy != EPILORA_DECODE_PATH_AUTO && policy != EPILORA_DECODE_PATH_SINGLE && policy != EPILORA_DECODE_PATH_TWO)
+    return EPILORA_ERR_INVALID_ARG;
+  return g_decode_path.exchange(policy);
 }
 
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
@@ -319,7 +337,7 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
   if (!quant_args_ok(fmt, X, M, K, ldx, Xq, x_scale, x_block_scale, x_global_scale)) return EPILORA_ERR_INVALID_ARG;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (decode_path_eligible(fmt, M, K, rr)) {
+  if (single_kernel_takes(fmt, M, K, rr)) {
     // a few tokens: quantizer, shrink and GEMM in one persistent launch
     DecodeArgs d{};
     d.fmt = fmt;

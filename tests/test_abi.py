@@ -78,8 +78,16 @@ def test_workspace_bytes(lib):
 def test_layer_forward_kernels(lib):
     """One persistent kernel for a few tokens (FP8: M * K <= 16384; NVFP4:
     bf16 rows within one 40 KB ring slot; M <= 8) while two weight stages
-    still fit beside the per-call buffers; else two."""
+    still fit beside the per-call buffers; else two. The automatic policy
+    gives the single kernel the FP8 calls only."""
     k = E.epilora_layer_forward_kernels
+    assert E.epilora_set_decode_path(E.DECODE_PATH_AUTO) == E.DECODE_PATH_AUTO
+    assert k(0, 1, 4096, 64) == 1 and k(1, 1, 4096, 64) == 2
+    assert E.epilora_set_decode_path(E.DECODE_PATH_TWO) == E.DECODE_PATH_AUTO
+    assert k(0, 1, 4096, 64) == 2 and k(1, 1, 4096, 64) == 2
+    with pytest.raises(E.EpiloraError):
+        E.epilora_set_decode_path(3)
+    assert E.epilora_set_decode_path(E.DECODE_PATH_SINGLE) == E.DECODE_PATH_TWO
     assert k(0, 1, 14336, 0) == 1 and k(0, 1, 16384, 64) == 1 and k(0, 1, 16416, 0) == 2
     assert k(0, 4, 4096, 64) == 1 and k(0, 5, 4096, 0) == 2 and k(0, 8, 2048, 16) == 1 and k(0, 9, 512, 0) == 2
     assert k(1, 1, 14336, 64) == 1 and k(1, 2, 8192, 64) == 1 and k(1, 8, 2048, 16) == 1
@@ -87,6 +95,7 @@ def test_layer_forward_kernels(lib):
     assert k(0, 8, 2048, 512) == 1 and k(1, 8, 2048, 512) == 2          # S rows crowd out a weight stage
     assert k(1, 1, 4128, 0) == 2                                         # NVFP4 wants K % 256 == 0
     assert k(0, 32, 4096, 0) == 2 and k(0, 0, 4096, 0) == 0 and k(2, 1, 4096, 0) == 0 and k(0, 1, 100, 0) == 0
+    E.epilora_set_decode_path(E.DECODE_PATH_AUTO)
 
 
 # ---------------------------------------------------------------------------

@@ -25,6 +25,11 @@ SYNC_BYTES = 2360576   # EPILORA_WORKSPACE_SYNC_BYTES: the head (counters, tagge
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     ensure_lib()
+    # the single kernel for both formats (the automatic policy gives NVFP4
+    # calls to the shrink grid and the GEMM)
+    prev = E.epilora_set_decode_path(E.DECODE_PATH_SINGLE)
+    yield
+    E.epilora_set_decode_path(prev)
 
 
 CASES = [

@@ -22,6 +22,10 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     ensure_lib()
+    # the cases marked "single kernel" take it in both formats
+    prev = E.epilora_set_decode_path(E.DECODE_PATH_SINGLE)
+    yield
+    E.epilora_set_decode_path(prev)
 
 
 CASES = [
