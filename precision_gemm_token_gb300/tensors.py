@@ -145,9 +145,13 @@ class LayerWorkspace:
     def __init__(self, device):
         self.device = torch.device(device)
         self.buf = torch.zeros(0, dtype=torch.uint8, device=self.device)
+        self._need = {}     # (fmt, M, K, r) -> bytes, asked of the library once per shape
 
     def get(self, fmt, M, K, r) -> torch.Tensor:
-        need = E.epilora_workspace_bytes(fmt, M, K, r)
+        key = (fmt, M, K, r)
+        need = self._need.get(key)
+        if need is None:
+            need = self._need[key] = E.epilora_workspace_bytes(fmt, M, K, r)
         if self.buf.numel() < need:
             self.buf = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
         return self.buf
@@ -186,3 +190,37 @@ def layer_forward(X, w: QuantWeight, A=None, B=None, idx=None, mask=None, x_glob
                                  stream)
     E.check(rc, "layer_forward")
     return Y
+
+
+class PreparedLayer:
+    """epilora_layer_forward with every argument bound once (the device
+    addresses of the given tensors, the sizes, the workspace and the stream):
+    each call enqueues the same layer again with a single C call, no per-call
+    argument conversion. The tensors must stay alive and in place (a caller
+    refreshes X's contents, e.g. with one copy per step, and reads Y)."""
+
+    def __init__(self, X, w: QuantWeight, A=None, B=None, idx=None, mask=None, x_global_scale=None,
+                 workspace: Optional[LayerWorkspace] = None, status=None, stream=None, Y=None):
+        M, K = X.shape
+        N = w.N
+        if Y is None:
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+        L, r = (A.shape[0], A.shape[1]) if A is not None else (1, 16)
+        ws = workspace or LayerWorkspace(X.device)
+        buf = ws.get(w.fmt, M, K, r if A is not None else 0)
+        p = lambda t: None if t is None else t.data_ptr()   # noqa: E731
+        if stream is None:
+            stream = torch.cuda.current_stream(X.device)
+        s = stream if isinstance(stream, int) else stream.cuda_stream
+        self.Y = Y
+        self._keep = (X, w, A, B, idx, mask, x_global_scale, buf, status, Y)
+        self._fn = E.load().epilora_layer_forward
+        self._args = (w.fmt, M, N, K, p(X), X.stride(0), p(w.codes), p(w.scale), p(w.block_scale), p(w.global_scale),
+                      p(x_global_scale), p(A), p(B), L, r, p(idx), p(mask), p(Y), Y.stride(0), p(buf), buf.numel(),
+                      p(status), s)
+
+    def __call__(self):
+        rc = self._fn(*self._args)
+        if rc != E.EPILORA_OK:
+            E.check(rc, "layer_forward")
+        return self.Y

@@ -332,3 +332,30 @@ def test_back_to_back_calls_share_workspace_and_replay_in_a_graph(fmt):
         torch.cuda.synchronize()
         for (_, ref), Y in zip(cases, outs):
             assert torch.equal(Y, ref)
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+@pytest.mark.parametrize("M", [1, 40])
+def test_prepared_layer_equals_layer_forward(fmt, M):
+    """tensors.PreparedLayer (arguments bound once) re-enqueues the same call:
+    with X's contents refreshed in place between calls, Y equals a fresh
+    layer_forward call bit for bit, on the single-kernel and the two-kernel
+    paths."""
+    p = make_projection(M, 2048, 1024, 3, 16, seed=11 + M, device="cuda")
+    w = T.quantize_weight(p.W, fmt)
+    X = p.X.clone()
+    gx = T.nvfp4_global_scale(X) if fmt == NVFP4 else None
+    Y = torch.empty((M, 1024), dtype=torch.bfloat16, device="cuda")
+    st = status_buf()
+    call = T.PreparedLayer(X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx, workspace=T.LayerWorkspace("cuda"),
+                           status=st, Y=Y)
+    g = torch.Generator(device="cuda").manual_seed(M)
+    for step in range(3):
+        X.copy_(torch.randn(X.shape, generator=g, device="cuda").to(torch.bfloat16))
+        if gx is not None:
+            gx.copy_(T.nvfp4_global_scale(X))
+        call()
+        ref = T.layer_forward(X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.equal(Y, ref), (fmt, M, step)
