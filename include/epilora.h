@@ -192,12 +192,36 @@ EPILORA_API int epilora_gemm_lora_epilogue(int fmt, int M, int N, int K,
 EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r);
 
 /*
+ * Bytes of device workspace with which epilora_layer_forward (and _slices,
+ * _noalloc) computes the adapter term of a batch of more than 32 tokens in a
+ * pass of its own (the adapter kernels the EpiLoRA page runs after the base
+ * GEMM above the decode batch sizes, §Design › Timed dispatch):
+ * epilora_workspace_bytes(fmt, M, K, r) plus, for M > 32 and r >= 32, an
+ * fp32 buffer of M x N (256-byte rounded) placed right after the regions
+ * listed there. A call with more than 32 tokens and bf16 adapters of rank 32
+ * or more (per slice) whose workspace_bytes reaches this size enqueues three
+ * kernels instead of two: the shrink grid, the expand pass (S . B_l for
+ * every sorted row with an adapter, 128 output columns per tile, each tile
+ * inside one slice) as its programmatic dependent, and the GEMM as the
+ * expand pass's programmatic dependent, whose epilogue adds the fp32 term to
+ * the base value before the one rounding to bf16 (the term: bf16 tensor-core
+ * MMAs of the B rows with S split exactly into three bf16 parts, fp32
+ * accumulation). Otherwise (rank 16, or a smaller workspace) the GEMM's
+ * epilogue computes the term itself; the two agree within the arithmetic
+ * bound of the method. Other shapes: the same as epilora_workspace_bytes.
+ * Returns 0 for M == 0 or invalid arguments.
+ */
+EPILORA_API size_t epilora_layer_workspace_bytes(int fmt, int M, int N, int K, int r);
+
+/*
  * Number of kernels epilora_layer_forward (and _slices, _fp8_adapters,
  * _noalloc) enqueues for (fmt, M, K, r), r as for epilora_workspace_bytes
  * (rank times slices, 0 without adapters), under the current decode-path
  * policy (epilora_set_decode_path): 1 when the single-kernel decode path takes
  * the call, 2 otherwise (the shrink grid with its quantizer blocks, then the
- * GEMM as its programmatic dependent). The single kernel can take a few
+ * GEMM as its programmatic dependent), for a workspace of
+ * epilora_workspace_bytes; a workspace of epilora_layer_workspace_bytes adds
+ * the expand pass (3) where that size exceeds epilora_workspace_bytes. The single kernel can take a few
  * tokens: M <= 8, FP8 with M * K <= 16384 (one token up to K = 16384, four at
  * K = 4096), NVFP4 with the bf16 rows within 40 KB (one token up to
  * K = 16384, two at K = 8192), as long as the shared memory of the call
@@ -254,7 +278,9 @@ EPILORA_API int epilora_set_decode_path(int policy);
  *      it starts streaming Wq (and w_block_scale) as soon as it is resident,
  *      and reads everything else only after the shrink grid has completed;
  * using `workspace` (>= epilora_workspace_bytes, 256-byte aligned) for the
- * head, Xq, scales, S and the row map. The head (the first
+ * head, Xq, scales, S and the row map; with more than 32 tokens, adapters and
+ * a workspace of epilora_layer_workspace_bytes, the expand pass runs between
+ * the two (see there). The head (the first
  * EPILORA_WORKSPACE_SYNC_BYTES) must be zero before the first call that uses
  * the workspace: zero-fill a workspace once after allocating it. Calls keep
  * the head valid for the next call (each adds 256 to a 64-bit launch
@@ -289,7 +315,9 @@ EPILORA_API int epilora_layer_forward(int fmt, int M, int N, int K,
  * [L, N, r] (row n belongs to its column's slice). n_slices in 1..4;
  * slice_end (host memory, read during the call) ascending, every end but the
  * last a multiple of 128, the last == N. The workspace must hold
- * epilora_workspace_bytes(fmt, M, K, n_slices * r) bytes. idx / mask select
+ * epilora_workspace_bytes(fmt, M, K, n_slices * r) bytes (with
+ * epilora_layer_workspace_bytes(fmt, M, N, K, n_slices * r), batches of more
+ * than 32 tokens take the expand pass). idx / mask select
  * one adapter slot per token for all slices. Other arguments and errors as
  * epilora_layer_forward (A and B are required).
  */

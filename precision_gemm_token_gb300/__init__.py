@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     epilora_test_drop_shrink_results,
     epilora_layer_forward_noalloc,
     epilora_layer_forward_slices,
+    epilora_layer_workspace_bytes,
     epilora_lora_shrink,
     epilora_nvfp4_global_scale,
     epilora_quant_act,

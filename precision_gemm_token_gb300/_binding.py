@@ -36,6 +36,7 @@ SIGNATURES = {
     "epilora_gemm_lora_epilogue": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                             _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp]),
     "epilora_workspace_bytes": (_sz, [_c_int, _c_int, _c_int, _c_int]),
+    "epilora_layer_workspace_bytes": (_sz, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "epilora_layer_forward_kernels": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
     "epilora_test_drop_shrink_results": (_c_int, [_c_int]),
     "epilora_set_decode_path": (_c_int, [_c_int]),
@@ -141,6 +142,10 @@ def epilora_gemm_lora_epilogue(fmt, M, N, K, Xq, x_scale, x_block_scale, x_globa
 
 def epilora_workspace_bytes(fmt, M, K, r) -> int:
     return load().epilora_workspace_bytes(fmt, M, K, r)
+
+
+def epilora_layer_workspace_bytes(fmt, M, N, K, r) -> int:
+    return load().epilora_layer_workspace_bytes(fmt, M, N, K, r)
 
 
 def epilora_layer_forward_kernels(fmt, M, K, r) -> int:

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libepilora.so")
-SOURCES = ("api.cu", "quant.cu", "shrink.cu", "gemm_fp8.cu", "gemm_nvfp4.cu", "decode.cu", "noalloc.cu")
+SOURCES = ("api.cu", "quant.cu", "shrink.cu", "gemm_fp8.cu", "gemm_nvfp4.cu", "decode.cu", "noalloc.cu", "expand.cu")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -275,6 +275,12 @@ EPILORA_API size_t epilora_workspace_bytes(int fmt, int M, int K, int r) {
   return bytes;
 }
 
+EPILORA_API size_t epilora_layer_workspace_bytes(int fmt, int M, int N, int K, int r) {
+  const size_t base = epilora_workspace_bytes(fmt, M, K, r);
+  if (base == 0 || N < 0) return 0;
+  return r >= kExpandMinRank && M > 32 ? base + expand_yadd_bytes(M, N) : base;
+}
+
 }  // extern "C"
 
 static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int ldx, const void* Wq,
@@ -329,6 +335,15 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
       off += round256(m * 4);
     }
   }
+  // more than 32 tokens with bf16 adapters of rank 32 or more and room for
+  // the fp32 term: the expand pass computes the adapter term between the
+  // shrink grid and the GEMM (rank 16 stays in the GEMM's epilogue, whose
+  // tensor-core term costs little there, while the pass would add the fp32
+  // term's round trip through memory)
+  float* yadd = nullptr;
+  if (adapters && M > 32 && r >= kExpandMinRank && a_scale == nullptr &&
+      workspace_bytes >= off + expand_yadd_bytes(M, N))
+    yadd = reinterpret_cast<float*>(ws + off);
 
   int rc = gemm_validate(fmt, M, N, K, Xq, x_scale, x_block_scale, x_global_scale, Wq, w_scale, w_block_scale,
                          w_global_scale, S, B, L, r, idx, Y, ldy);
@@ -388,6 +403,28 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
   rc = launch_shrink_quant(X, M, K, ldx, A, adapters ? L : 1, adapters ? rs : 0, idx, mask, S, parts, fmt, Xq,
                            x_scale, x_block_scale, x_global_scale, perm, status_dev, st, a_scale);
   if (rc != EPILORA_OK) return rc;
+  if (yadd != nullptr) {
+    ExpandArgs e{};
+    e.M = M;
+    e.N = N;
+    e.L = L;
+    e.r = r;
+    e.s_row = rs;
+    e.s_parts = parts;
+    e.n_slices = n_slices;
+    for (int q = 0; q < 4; ++q) e.slice_end[q] = q < n_slices && slice_end != nullptr ? slice_end[q] : N;
+    e.S = S;
+    e.B = B;
+    e.perm = perm;
+    e.idx = idx;
+    e.mask = mask;
+    e.yadd = yadd;
+    e.status_dev = status_dev;
+    e.stream = st;
+    e.pdl_dependent = 1;
+    rc = launch_expand(e);
+    if (rc != EPILORA_OK) return rc;
+  }
   GemmArgs a{};
   a.fmt = fmt;
   a.M = M;
@@ -416,6 +453,7 @@ static int layer_forward_impl(int fmt, int M, int N, int K, const void* X, int l
   a.fused = 1;
   a.s_parts = parts;
   a.perm = perm;
+  a.yadd = yadd;
   a.s_row = adapters ? rs : 0;
   a.n_slices = n_slices;
   for (int q = 0; q < n_slices && q < 4; ++q) a.slice_end[q] = slice_end != nullptr ? slice_end[q] : N;

@@ -66,6 +66,11 @@ struct GemmArgs {
   int s_row = 0;
   int n_slices = 1;
   int slice_end[4] = {0, 0, 0, 0};
+  // wide tiles (more than 32 tokens): the adapter term of every sorted row
+  // with an adapter, computed by launch_expand, fp32 [M][N] (row = row of Xq);
+  // the epilogue adds it instead of computing S[t] . B[l][n] itself. null:
+  // the epilogue computes the term.
+  const float* yadd = nullptr;
 };
 
 int launch_quant(int fmt, const void* X, int M, int K, int ldx, void* Xq, float* x_scale,
@@ -133,6 +138,32 @@ size_t decode_s_bytes();
 int launch_fused_decode(const DecodeArgs& a);
 // K slice length of a shrink split into `parts` slices (multiple of 256)
 int shrink_kslice(int K, int parts);
+
+// Adapter term of a batch of more than 32 tokens as a pass of its own
+// (expand.cu): yadd[row][n] = S[perm[row]] . B[l][n] for the sorted rows whose
+// token carries an adapter l (mask on); other rows are not written. Launched
+// as a programmatic dependent of the shrink grid when pdl_dependent is set; it
+// releases its own dependent (the GEMM) at once and reads S, perm, idx and
+// mask only after that grid has completed.
+struct ExpandArgs {
+  int M, N, L, r;
+  int s_row, s_parts, n_slices;
+  int slice_end[4];
+  const float* S;          // [s_parts][M][s_row] fp32, rows by token
+  const void* B;           // bf16 [L, N, r], 16-byte aligned
+  const int32_t* perm;     // sorted row -> token, or null (identity)
+  const int32_t* idx;
+  const uint8_t* mask;
+  float* yadd;             // fp32 [M][N]
+  int* status_dev;
+  cudaStream_t stream;
+  int pdl_dependent;
+};
+int launch_expand(const ExpandArgs& a);
+// smallest adapter rank (per slice) for which a layer call takes the expand pass
+constexpr int kExpandMinRank = 32;
+// bytes of the fp32 [M][N] buffer launch_expand writes (a multiple of 256)
+size_t expand_yadd_bytes(int M, int N);
 
 int launch_gemm_fp8(const GemmArgs& a);
 int launch_gemm_nvfp4(const GemmArgs& a);

@@ -116,6 +116,9 @@ struct GemmParams {
   int n_slices;
   int slice_end[4];
   int y_stage;        // wide tiles: ring byte offset of the per-warp output staging (-1: 2-byte stores)
+  // wide tiles: the adapter term of each sorted row with an adapter, fp32
+  // [M][N] (written by the expand pass); null: the epilogue computes it
+  const float* yadd;
 };
 
 template <int FMT, int BT, int KA>
@@ -470,6 +473,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       meta_sx[i] = sx;
       meta_idx[i] = l;
       meta_tok[i] = tok;
+      // the expand pass's term of this row and weight tile: into L2 while the
+      // main loop runs (bulk prefetch needs 16-byte aligned rows)
+      if (!C::kDecode && p.yadd != nullptr && l >= 0 && (p.N & 3) == 0)
+        prefetch_l2_bulk(p.yadd + static_cast<size_t>(row) * p.N + n0, static_cast<uint32_t>(min(kTileN, p.N - n0) * 4));
     }
     asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
     if (C::kDecode) {
@@ -864,7 +871,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
     if (n >= p.N || t >= p.M) return;
     float y = base_value(mm, tl, acc, sw);
     const int l = meta_idx[tl];
-    if (l >= 0) {
+    if (l >= 0 && p.yadd != nullptr) {
+      y += __ldcg(p.yadd + static_cast<size_t>(t) * p.N + n);     // the expand pass's term
+    } else if (l >= 0) {
       if (l * kTileN + mm != cached_key) load_brow(l, mm);
       const bool s_smem = C::kDecode || p.stage_s;
       const float4* srow =
@@ -1183,11 +1192,51 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
           }
         }
       };
-      switch (p.r) {
-        case 16: run(std::integral_constant<int, 4>{}); break;
-        case 32: run(std::integral_constant<int, 8>{}); break;
-        case 64: run(std::integral_constant<int, 16>{}); break;
-        default: run(std::integral_constant<int, 32>{}); break;
+      if (p.yadd != nullptr) {
+        // the adapter term comes from the expand pass: one fp32 per (sorted
+        // row, output column), added to the base value as the CUDA-core term
+        // below would be
+#pragma unroll 1
+        for (int c = 0; c < BT / 16; ++c) {
+          if (c * 16 >= tv) break;
+          uint32_t v[16];
+          float ya[16];
+          tmem_ld_32x32b_x16(lane_base + c * 16, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tl = c * 16 + j;
+            ya[j] = tl < tv && n < p.N && meta_idx[tl] >= 0
+                        ? __ldcg(p.yadd + static_cast<size_t>(t0 + tl) * p.N + n)
+                        : 0.0f;
+          }
+          tmem_ld_wait();
+          float yv[16] = {};
+          if (n < p.N) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int tl = c * 16 + j;
+              if (tl < tv) {
+                float y = base_value(m, tl, __uint_as_float(v[j]), sw);
+                if (meta_idx[tl] >= 0) y += ya[j];
+                yv[j] = y;
+              }
+            }
+          }
+          if (p.y_stage >= 0) {
+            emit16(c, yv);
+          } else if (n < p.N) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c * 16 + j < tv) p.Y[static_cast<size_t>(meta_tok[c * 16 + j]) * p.ldy + n] = __float2bfloat16_rn(yv[j]);
+          }
+        }
+      } else {
+        switch (p.r) {
+          case 16: run(std::integral_constant<int, 4>{}); break;
+          case 32: run(std::integral_constant<int, 8>{}); break;
+          case 64: run(std::integral_constant<int, 16>{}); break;
+          default: run(std::integral_constant<int, 32>{}); break;
+        }
       }
     } else if (ks == 1) {
       const int q = warp & 3;
@@ -1271,6 +1320,8 @@ int launch_gemm_tiled(const GemmArgs& a) {
   p.fused = a.fused;
   p.pdl = !a.fused && a.pdl_dependent ? 1 : 0;
   p.perm = a.perm;
+  p.yadd = a.yadd;
+  if (a.yadd != nullptr && (C::kDecode || a.S == nullptr)) return EPILORA_ERR_UNSUPPORTED;
   p.s_parts = a.s_parts < 1 ? 1 : a.s_parts;
   p.M = a.M;
   p.N = a.N;
@@ -1354,7 +1405,7 @@ int launch_gemm_tiled(const GemmArgs& a) {
   // non-decode tiles stage S of their tokens in the ring once the main loop
   // is over (one fp32 row of r per token column); deepen the ring if needed
   p.stage_s = 0;
-  if (!C::kDecode && a.S != nullptr) {
+  if (!C::kDecode && a.S != nullptr && a.yadd == nullptr) {
     const int need = BT * (a.r + 4) * 4 + 5 * 1024;     // padded S rows + the output staging
     int st_need = (need + C::kStageBytes - 1) / C::kStageBytes;
     if (st_need < stages) st_need = stages;
@@ -1364,7 +1415,8 @@ int launch_gemm_tiled(const GemmArgs& a) {
     }
   }
   // wide tiles read a split shrink's partial sums only from the staged rows
-  if (!C::kDecode && a.S != nullptr && p.s_parts > 1 && !p.stage_s) return EPILORA_ERR_UNSUPPORTED;
+  if (!C::kDecode && a.S != nullptr && a.yadd == nullptr && p.s_parts > 1 && !p.stage_s)
+    return EPILORA_ERR_UNSUPPORTED;
   // stored FP8 B rows are read only by the streamed-B decode epilogue
   if (a.b_scale != nullptr && (!C::kDecode || !p.stream_b)) return EPILORA_ERR_UNSUPPORTED;
   p.stages = stages;

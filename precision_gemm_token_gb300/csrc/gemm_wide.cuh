@@ -12,7 +12,8 @@
 //               j % 2 while the MMAs of tile j + 1 fill the other buffer.
 // The adapter term comes from TF32 mma.sync passes in the accumulator layout
 // of tcgen05.ld.16x256b (one pass per adapter present in a 16-column chunk,
-// S split hi + lo, the adapter rows exact in TF32).
+// S split hi + lo, the adapter rows exact in TF32), or, when the expand pass
+// has computed it (KS = -1), from its fp32 buffer.
 //
 // Every wait is bounded: on a timeout the CTA records EPILORA_ERR_TIMEOUT,
 // stops issuing, waits (bounded) for its copies and MMAs in flight and frees
@@ -24,7 +25,9 @@ namespace epi {
 constexpr int kWideBT = 256;
 constexpr int kWideTmemCols = 512;         // two 256-column accumulators
 
-template <int KS>   // k-steps of 8 in the adapter rank (r = 8 KS), 0: no adapters
+// KS: k-steps of 8 in the adapter rank (r = 8 KS); 0: no adapters; -1: the
+// adapter term is read from p.yadd
+template <int KS>
 __device__ __forceinline__ void wide_load_afrag(uint32_t (&af)[2 * (KS > 0 ? KS : 1)][4], const GemmParams& p,
                                                 int l, int rbase, int g, int tq) {
   const uint16_t* bl = reinterpret_cast<const uint16_t*>(p.B) + static_cast<size_t>(l) * p.N * p.r;
@@ -46,7 +49,8 @@ __device__ __forceinline__ void wide_load_afrag(uint32_t (&af)[2 * (KS > 0 ? KS 
 template <int KS>
 __device__ __forceinline__ void wide_epilogue_tile(const GemmParams& p, uint32_t tmem_acc, const float* meta_sx,
                                                    const int* meta_idx, const int* meta_tok, const float* s_big,
-                                                   int s_ld, __nv_bfloat16* ys, int n0, int tv, int warp, int lane) {
+                                                   int s_ld, __nv_bfloat16* ys, int t0, int n0, int tv, int warp,
+                                                   int lane) {
   constexpr int kYsLd = 40;
   const int q = warp & 3;
   const int g = lane >> 2, tq = lane & 3;
@@ -65,7 +69,7 @@ __device__ __forceinline__ void wide_epilogue_tile(const GemmParams& p, uint32_t
   for (int c = 0; c < kWideBT / 16; ++c) {
     if (c * 16 >= tv) break;
     const int jl = c * 16 + (lane & 15);
-    const int lj = KS > 0 && jl < tv ? meta_idx[jl] : -1;
+    const int lj = KS != 0 && jl < tv ? meta_idx[jl] : -1;
     const uint32_t actm = __ballot_sync(0xffffffffu, lj >= 0) & 0xffffu;
     uint32_t va[2][8];
     tmem_ld_16x256b_x2(lane_base + c * 16, va[0]);
@@ -106,6 +110,19 @@ __device__ __forceinline__ void wide_epilogue_tile(const GemmParams& p, uint32_t
             }
           }
       }
+    } else if constexpr (KS < 0) {
+      // the expand pass's term of element (mt, nt, i) (layout below)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int col = nt * 8 + 2 * tq + (i & 1);
+            const int row = n0 + q * 32 + mt * 16 + g + 8 * (i >> 1);
+            if (((actm >> col) & 1u) && row < p.N)
+              d[mt][nt][i] = __ldcg(p.yadd + static_cast<size_t>(t0 + c * 16 + col) * p.N + row);
+          }
     }
     tmem_ld_wait();
     // element (mt, nt, i): row q*32 + mt*16 + g + 8*(i/2), column
@@ -331,7 +348,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_wide_kernel(const __grid
         if (row < p.M) {
           if (p.perm != nullptr) tok = p.perm[row];
           sx = p.x_scale[row];
-          if (KS > 0) {
+          if (KS != 0) {
             const int li = p.idx[tok];
             const bool on = li >= 0 && li < p.L && (p.mask == nullptr || p.mask[tok] != 0);
             if (li >= p.L) record_status(p.status, EPILORA_ERR_INVALID_ARG);
@@ -341,6 +358,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_wide_kernel(const __grid
         meta_sx[i] = sx;
         meta_idx[i] = l;
         meta_tok[i] = tok;
+        // the expand pass's term of this row and weight tile: into L2 while
+        // the tile's MMAs run (bulk prefetch needs 16-byte aligned rows)
+        if (KS < 0 && l >= 0 && (p.N & 3) == 0)
+          prefetch_l2_bulk(p.yadd + static_cast<size_t>(row) * p.N + n0,
+                           static_cast<uint32_t>(min(kTileN, p.N - n0) * 4));
       }
       asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
       if (KS > 0) {
@@ -371,7 +393,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_wide_kernel(const __grid
       if (epi_bar_any(*abort_flag != 0)) break;
       tc_fence_after();
       wide_epilogue_tile<KS>(p, tmem_base + static_cast<uint32_t>(b * kWideBT), meta_sx, meta_idx, meta_tok, s_big,
-                             s_ld, ys, n0, tv, warp, lane);
+                             s_ld, ys, t0, n0, tv, warp, lane);
       // accumulator b may take the next tile
       tc_fence_before();
       asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
@@ -440,7 +462,7 @@ template <int FMT>
 int launch_gemm_wide(const GemmArgs& a) {
   if (FMT != EPILORA_FMT_FP8_E4M3 || a.M <= 128) return EPILORA_ERR_UNSUPPORTED;
   const bool lora = a.S != nullptr && a.r > 0;
-  if (lora && (a.r != 16 && a.r != 32 && a.r != 64)) return EPILORA_ERR_UNSUPPORTED;
+  if (lora && a.yadd == nullptr && (a.r != 16 && a.r != 32 && a.r != 64)) return EPILORA_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(a.Y) & 15) != 0 || a.ldy % 8 != 0) return EPILORA_ERR_UNSUPPORTED;
   const int sms = num_sms();
   const int n_tiles = (a.N + kTileN - 1) / kTileN;
@@ -462,6 +484,7 @@ int launch_gemm_wide(const GemmArgs& a) {
   p.fused = a.fused;
   p.pdl = !a.fused && a.pdl_dependent ? 1 : 0;
   p.perm = a.perm;
+  p.yadd = lora ? a.yadd : nullptr;
   p.s_parts = a.s_parts < 1 ? 1 : a.s_parts;
   p.M = a.M;
   p.N = a.N;
@@ -480,6 +503,7 @@ int launch_gemm_wide(const GemmArgs& a) {
   if (rc != EPILORA_OK) return rc;
   rc = make_tma_2d_u8(&p.tmX, a.Xq, a.M, a.K, a.K, kWideBT, kAtomBytes, true);
   if (rc != EPILORA_OK) return rc;
+  if (p.yadd != nullptr) return launch_gemm_wide_ks<-1>(p, a, static_cast<int>(tiles), sms);
   switch (p.r) {
     case 0: return launch_gemm_wide_ks<0>(p, a, static_cast<int>(tiles), sms);
     case 16: return launch_gemm_wide_ks<2>(p, a, static_cast<int>(tiles), sms);

@@ -108,7 +108,8 @@ def layer_forward_fp8_adapters(X, w: QuantWeight, ad: Fp8Adapters, idx, mask=Non
     buf = ws.get(w.fmt, M, K, r)
     rc = E.epilora_layer_forward_fp8_adapters(w.fmt, M, N, K, X, X.stride(0), w.codes, w.scale, w.block_scale,
                                               w.global_scale, x_global_scale, ad.Aq, ad.a_scale, ad.Bq, ad.b_scale,
-                                              L, r, idx, mask, Y, Y.stride(0), buf, buf.numel(), status, stream)
+                                              L, r, idx, mask, Y, Y.stride(0), buf, ws.need(w.fmt, M, K, r), status,
+                                              stream)
     E.check(rc, "layer_forward_fp8_adapters")
     return Y
 
@@ -145,13 +146,22 @@ class LayerWorkspace:
     def __init__(self, device):
         self.device = torch.device(device)
         self.buf = torch.zeros(0, dtype=torch.uint8, device=self.device)
-        self._need = {}     # (fmt, M, K, r) -> bytes, asked of the library once per shape
+        self._need = {}     # (fmt, M, N, K, r) -> bytes, asked of the library once per shape
 
-    def get(self, fmt, M, K, r) -> torch.Tensor:
-        key = (fmt, M, K, r)
+    def need(self, fmt, M, K, r, N=None) -> int:
+        """Bytes a call of this shape uses: epilora_layer_workspace_bytes
+        when N is given (batches of more than 32 tokens with adapters then
+        take the expand pass), else epilora_workspace_bytes."""
+        key = (fmt, M, N, K, r)
         need = self._need.get(key)
         if need is None:
-            need = self._need[key] = E.epilora_workspace_bytes(fmt, M, K, r)
+            need = E.epilora_workspace_bytes(fmt, M, K, r) if N is None else \
+                E.epilora_layer_workspace_bytes(fmt, M, N, K, r)
+            self._need[key] = need
+        return need
+
+    def get(self, fmt, M, K, r, N=None) -> torch.Tensor:
+        need = self.need(fmt, M, K, r, N)
         if self.buf.numel() < need:
             self.buf = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
         return self.buf
@@ -168,10 +178,10 @@ def layer_forward_slices(X, w: QuantWeight, A, B, idx, slice_end, mask=None, x_g
     n = len(slice_end)
     L, r = A.shape[0], B.shape[2]
     ws = workspace or LayerWorkspace(X.device)
-    buf = ws.get(w.fmt, M, K, n * r)
+    buf = ws.get(w.fmt, M, K, n * r, N)
     rc = E.epilora_layer_forward_slices(w.fmt, M, N, K, X, X.stride(0), w.codes, w.scale, w.block_scale,
                                         w.global_scale, x_global_scale, A, B, L, r, n, slice_end, idx, mask, Y,
-                                        Y.stride(0), buf, buf.numel(), status, stream)
+                                        Y.stride(0), buf, ws.need(w.fmt, M, K, n * r, N), status, stream)
     E.check(rc, "layer_forward_slices")
     return Y
 
@@ -184,10 +194,11 @@ def layer_forward(X, w: QuantWeight, A=None, B=None, idx=None, mask=None, x_glob
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     L, r = (A.shape[0], A.shape[1]) if A is not None else (1, 16)
     ws = workspace or LayerWorkspace(X.device)
-    buf = ws.get(w.fmt, M, K, r if A is not None else 0)
+    rr = r if A is not None else 0
+    buf = ws.get(w.fmt, M, K, rr, N)
     rc = E.epilora_layer_forward(w.fmt, M, N, K, X, X.stride(0), w.codes, w.scale, w.block_scale, w.global_scale,
-                                 x_global_scale, A, B, L, r, idx, mask, Y, Y.stride(0), buf, buf.numel(), status,
-                                 stream)
+                                 x_global_scale, A, B, L, r, idx, mask, Y, Y.stride(0), buf,
+                                 ws.need(w.fmt, M, K, rr, N), status, stream)
     E.check(rc, "layer_forward")
     return Y
 
@@ -207,7 +218,8 @@ class PreparedLayer:
             Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
         L, r = (A.shape[0], A.shape[1]) if A is not None else (1, 16)
         ws = workspace or LayerWorkspace(X.device)
-        buf = ws.get(w.fmt, M, K, r if A is not None else 0)
+        rr = r if A is not None else 0
+        buf = ws.get(w.fmt, M, K, rr, N)
         p = lambda t: None if t is None else t.data_ptr()   # noqa: E731
         if stream is None:
             stream = torch.cuda.current_stream(X.device)
@@ -216,8 +228,8 @@ class PreparedLayer:
         self._keep = (X, w, A, B, idx, mask, x_global_scale, buf, status, Y)
         self._fn = E.load().epilora_layer_forward
         self._args = (w.fmt, M, N, K, p(X), X.stride(0), p(w.codes), p(w.scale), p(w.block_scale), p(w.global_scale),
-                      p(x_global_scale), p(A), p(B), L, r, p(idx), p(mask), p(Y), Y.stride(0), p(buf), buf.numel(),
-                      p(status), s)
+                      p(x_global_scale), p(A), p(B), L, r, p(idx), p(mask), p(Y), Y.stride(0), p(buf),
+                      ws.need(w.fmt, M, K, rr, N), p(status), s)
 
     def __call__(self):
         rc = self._fn(*self._args)

@@ -81,9 +81,25 @@ def assert_y_close(y: np.ndarray, ref: dict, bound: np.ndarray | None = None, wh
         assert not bad.any(), (what, np.argwhere(bad)[:5], float((err / bound).max()))
 
 
+def layer_forward_epilogue_term(X, w, A, B, idx, mask, x_global_scale=None, status=None):
+    """epilora_layer_forward with a workspace of epilora_workspace_bytes: the
+    GEMM's epilogue computes the adapter term itself (no expand pass)."""
+    M, K = X.shape
+    L, r = A.shape[0], A.shape[1]
+    need = E.epilora_workspace_bytes(w.fmt, M, K, r)
+    buf = torch.zeros(need, dtype=torch.uint8, device=X.device)
+    Y = torch.empty((M, w.N), dtype=torch.bfloat16, device=X.device)
+    E.check(E.epilora_layer_forward(w.fmt, M, w.N, K, X, X.stride(0), w.codes, w.scale, w.block_scale,
+                                    w.global_scale, x_global_scale, A, B, L, r, idx, mask, Y, Y.stride(0), buf,
+                                    need, status, None), "layer_forward")
+    return Y
+
+
 def run_case(fmt, M, K, N, L, r, seed=0, idx_mode="uniform", mask_mode="all", n_decode=0, zero_w=False,
-             use_adapter=True):
-    """Run GPU and oracle on the same inputs; returns (Y_gpu np, ref dict, bound, inputs)."""
+             use_adapter=True, epilogue_term=False):
+    """Run GPU and oracle on the same inputs; returns (Y_gpu np, ref dict, bound, inputs).
+    epilogue_term: the workspace leaves no room for the expand pass, so that
+    wide tiles compute the adapter term in the GEMM's epilogue."""
     p = make_projection(M, K, N, L, r, seed=seed, idx_mode=idx_mode, mask_mode=mask_mode, n_decode=n_decode)
     W = torch.zeros_like(p.W) if zero_w else p.W
     Xg, Wg = p.X.cuda(), W.cuda()
@@ -111,7 +127,10 @@ def run_case(fmt, M, K, N, L, r, seed=0, idx_mode="uniform", mask_mode="all", n_
         xv = O.dequant_nvfp4_rows(ref["xq"], ref["sbx"], gxv)
         wv = O.dequant_nvfp4_rows(wq, sbw, gw)
     st = status_buf()
-    if use_adapter:
+    if use_adapter and epilogue_term:
+        Y = layer_forward_epilogue_term(Xg, w, p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda(), x_global_scale=gx,
+                                        status=st)
+    elif use_adapter:
         Y = T.layer_forward(Xg, w, p.A.cuda(), p.B.cuda(), p.idx.cuda(), p.mask.cuda(), x_global_scale=gx, status=st)
     else:
         Y = T.layer_forward(Xg, w, x_global_scale=gx, status=st)

@@ -75,6 +75,21 @@ def test_workspace_bytes(lib):
     assert E.epilora_workspace_bytes(7, 4, 512, 16) == 0
 
 
+def test_layer_workspace_bytes(lib):
+    r256 = lambda v: (v + 255) // 256 * 256   # noqa: E731
+    # more than 32 tokens with adapters of rank >= 32: plus the expand pass's fp32 [M, N] term
+    for fmt, M, N, K, r in [(0, 64, 512, 512, 32), (1, 300, 272, 512, 64), (0, 33, 130, 256, 128)]:
+        assert E.epilora_layer_workspace_bytes(fmt, M, N, K, r) == \
+            E.epilora_workspace_bytes(fmt, M, K, r) + r256(M * N * 4)
+    # decode batches, rank 16 and base-only calls: the same as epilora_workspace_bytes
+    for fmt, M, N, K, r in [(0, 32, 512, 512, 16), (1, 4, 4096, 4096, 64), (0, 64, 512, 512, 0),
+                            (0, 64, 512, 512, 16)]:
+        assert E.epilora_layer_workspace_bytes(fmt, M, N, K, r) == E.epilora_workspace_bytes(fmt, M, K, r)
+    assert E.epilora_layer_workspace_bytes(0, 0, 512, 512, 16) == 0
+    assert E.epilora_layer_workspace_bytes(7, 64, 512, 512, 16) == 0
+    assert E.epilora_layer_workspace_bytes(0, 64, -1, 512, 16) == 0
+
+
 def test_layer_forward_kernels(lib):
     """One persistent kernel for a few tokens (FP8: M * K <= 16384; NVFP4:
     bf16 rows within one 40 KB ring slot; M <= 8) while two weight stages

@@ -65,7 +65,7 @@ def run_fullsize(fmt, K, N, M, L, r, idx_mode, seed, mask_mode="all", n_decode=0
     gx_t = T.nvfp4_global_scale(p.X) if fmt == NVFP4 else None
     ws = T.LayerWorkspace(p.X.device)
     # zero-filled: partial-sum slots the shrink leaves unused then read as 0
-    ws.get(fmt, M, K, r).zero_()
+    ws.get(fmt, M, K, r, N).zero_()
     st = status_buf()
     Y = T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx_t, workspace=ws, status=st)
     torch.cuda.synchronize()

@@ -88,6 +88,52 @@ def test_wide_grids_larger_than_the_gpu(fmt, M, K, N, L, r, idx_mode, mask_mode)
     assert_y_close(y, ref, bound, what=(fmt, M, N, r))
 
 
+EPILOGUE_TERM = [
+    # M, K, N, L, r, idx_mode, mask_mode    (wide tiles whose epilogue computes the
+    # adapter term: a workspace without room for the expand pass)
+    (100, 512, 384, 5, 32, "uniform", "all"),            # 128-token tiles, TF32 tensor-core term
+    (300, 512, 272, 7, 64, "uniform", "all"),            # CUDA-core term, ragged both ways
+    (160, 512, 384, 9, 128, "zipf", "all"),              # rank 128
+    (600, 512, 384, 64, 16, "zipf", "prefill_chunk"),    # one-adapter runs, mask-0 tokens
+    (1000, 512, 5120, 16, 64, "zipf", "all"),            # persistent FP8 kernel, rank 64
+    (80, 6144, 128, 6, 64, "zipf", "prefill_chunk"),     # shrink split over K slices
+]
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+@pytest.mark.parametrize("M,K,N,L,r,idx_mode,mask_mode", EPILOGUE_TERM)
+def test_wide_epilogue_term_matches_oracle(fmt, M, K, N, L, r, idx_mode, mask_mode):
+    """The adapter term computed in the GEMM's epilogue (the path a call
+    takes when its workspace has no room for the expand pass's fp32 term)."""
+    if fmt == NVFP4 and K % 256:
+        pytest.skip("NVFP4 GEMM needs K % 256 == 0")
+    y, ref, bound, _ = run_case(fmt, M, K, N, L, r, seed=17 + M + r, idx_mode=idx_mode, mask_mode=mask_mode,
+                                n_decode=8 if mask_mode == "prefill_chunk" else 0, epilogue_term=True)
+    assert_y_close(y, ref, bound, what=(fmt, M, N, r))
+
+
+@pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
+@pytest.mark.parametrize("M,K,N,L,r,idx_mode", [
+    (300, 512, 272, 7, 64, "uniform"),     # 128-token tiles (NVFP4), ragged weight tile
+    (100, 512, 384, 5, 64, "zipf"),        # 128-token tiles, both formats
+    (160, 512, 384, 9, 128, "zipf"),       # rank 128
+    (40, 4096, 256, 3, 64, "uniform"),     # few tiles: split-K clusters, the element-wise epilogue
+    (33, 512, 208, 40, 32, "uniform"),     # one-token runs, ragged weight tile
+    (700, 256, 384, 3, 32, "zipf"),        # runs longer than a round of 32 rows
+])
+def test_expand_pass_and_epilogue_term_both_match_oracle(fmt, M, K, N, L, r, idx_mode):
+    """The same inputs through the expand pass (workspace of
+    epilora_layer_workspace_bytes) and through the epilogue's own term: both
+    within the arithmetic bound of the oracle, and every element of Y the
+    same to within that bound of each other."""
+    y_x, ref, bound, _ = run_case(fmt, M, K, N, L, r, seed=M + N + r, idx_mode=idx_mode)
+    y_e, ref_e, _, _ = run_case(fmt, M, K, N, L, r, seed=M + N + r, idx_mode=idx_mode, epilogue_term=True)
+    assert np.array_equal(ref["Y"], ref_e["Y"])
+    assert_y_close(y_x, ref, bound, what=("expand", fmt, M, r))
+    assert_y_close(y_e, ref, bound, what=("epilogue", fmt, M, r))
+    assert (np.abs(y_x.astype(np.float64) - y_e) <= 2 * bound).all()
+
+
 @pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
 @pytest.mark.parametrize("M,K,N,L,r,idx_mode,mask_mode", [
     (48, 4096, 256, 4, 16, "zipf", "prefill_chunk"),      # token blocks over 2 K slices
@@ -307,7 +353,7 @@ def test_back_to_back_calls_share_workspace_and_replay_in_a_graph(fmt):
         cases.append((args, ref))
     ws = T.LayerWorkspace("cuda")
     for M, K, N, L, r in shapes:
-        ws.get(fmt, M, K, r)
+        ws.get(fmt, M, K, r, N)
     outs = [torch.empty_like(ref) for _, ref in cases]
 
     def run(stream=None):
