@@ -34,6 +34,7 @@ constexpr int kExpandThreads = 256;   // two per output column
 constexpr int kExpandRows = 32;       // sorted rows staged per round
 constexpr int kExpandMinRows = 16;    // smallest row range of a work item
 constexpr int kExpandItemRows = 256;  // largest row range of a work item
+constexpr int kExpandItemCost = 16;   // set-up of a work item, in rows' worth of time
 
 // Ring of B slices (one adapter's 128 rows of the weight tile) in shared
 // memory, filled with 16-byte asynchronous copies kDepth - 1 adapter runs
@@ -250,19 +251,20 @@ __global__ void __launch_bounds__(kExpandThreads, ExpandCfg<R4>::kCtas)
         const int i = seg_start[k] - c0;
         const int jr = seg_start[k + 1] - c0;
         // Yadd[token t][column n] = sum over the rank of B[n][k] S[t][k]: one
-        // m16n8k16 MMA per 8 tokens, k-step and S part (lo, mid, hi), tokens
-        // outside the segment zero
+        // m16n8k16 MMA per 8 tokens, k-step and S part (lo, mid, hi). A token
+        // column of the MMA depends on that token's S row alone: the columns
+        // past the segment (other rows of the round, or none) are computed
+        // but not stored.
         for (int t0 = i; t0 < jr; t0 += 8) {
-          const bool on = t0 + g < jr;
-          const int t = on ? t0 + g : i;    // rows past the segment read as zero
+          const int t = min(t0 + g, kExpandRows - 1);
           float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
           for (int ks = 0; ks < kKSteps; ++ks)
 #pragma unroll
             for (int part = 2; part >= 0; --part) {
               const uint8_t* sp = s_planes + part * C::kSPlaneBytes + t * C::kSRowBytes + (16 * ks + 2 * tq) * 2;
-              const uint32_t b0 = on ? *reinterpret_cast<const uint32_t*>(sp) : 0u;
-              const uint32_t b1 = on ? *reinterpret_cast<const uint32_t*>(sp + 16) : 0u;
+              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(sp);
+              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(sp + 16);
               mma_bf16_m16n8k16(acc, af[ks], b0, b1);
             }
           // c0: (column g, token 2 tq), c1: (g, 2 tq + 1), c2/c3: column g + 8
@@ -331,17 +333,27 @@ int launch_expand(const ExpandArgs& a) {
   p.n_slices = a.n_slices < 1 ? 1 : a.n_slices;
   for (int q = 0; q < 4; ++q) p.slice_end[q] = a.slice_end[q];
   p.n_tiles = (a.N + 127) / 128;
-  // row groups per weight tile: at least one item per CTA slot of the grid,
-  // each of kExpandMinRows to kExpandItemRows rows (fewer, longer items read
-  // each B slice fewer times)
+  // row groups per weight tile, items of kExpandMinRows to kExpandItemRows
+  // rows: the count that minimises (waves of items over the grid's CTA
+  // slots) x (rows per item + a fixed cost per item, counted in rows), fewer
+  // items on a tie (each item reads its runs' B slices once)
   const int ctas = a.r >= 128 ? ExpandCfg<32>::kCtas : ExpandCfg<16>::kCtas;
-  const int slots = num_sms() * ctas;
-  int groups = (slots + p.n_tiles - 1) / p.n_tiles;
-  const int max_groups = (a.M + kExpandMinRows - 1) / kExpandMinRows;
-  if (groups > max_groups) groups = max_groups;
-  const int min_groups = (a.M + kExpandItemRows - 1) / kExpandItemRows;
-  if (groups < min_groups) groups = min_groups;
-  if (groups < 1) groups = 1;
+  const long slots = static_cast<long>(num_sms()) * ctas;
+  int max_groups = (a.M + kExpandMinRows - 1) / kExpandMinRows;
+  int min_groups = (a.M + kExpandItemRows - 1) / kExpandItemRows;
+  if (min_groups < 1) min_groups = 1;
+  if (max_groups < min_groups) max_groups = min_groups;
+  int groups = min_groups;
+  long best = -1;
+  for (int g = min_groups; g <= max_groups; ++g) {
+    const long rows = (a.M + g - 1) / g;
+    const long items = static_cast<long>(p.n_tiles) * ((a.M + rows - 1) / rows);
+    const long cost = (items + slots - 1) / slots * (rows + kExpandItemCost);
+    if (best < 0 || cost < best) {
+      best = cost;
+      groups = g;
+    }
+  }
   p.rows_per_group = (a.M + groups - 1) / groups;
   p.row_groups = (a.M + p.rows_per_group - 1) / p.rows_per_group;
 

@@ -1195,13 +1195,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       if (p.yadd != nullptr) {
         // the adapter term comes from the expand pass: one fp32 per (sorted
         // row, output column), added to the base value as the CUDA-core term
-        // below would be
-#pragma unroll 1
-        for (int c = 0; c < BT / 16; ++c) {
-          if (c * 16 >= tv) break;
-          uint32_t v[16];
-          float ya[16];
-          tmem_ld_32x32b_x16(lane_base + c * 16, v);
+        // below would be; the next chunk's values are requested before this
+        // chunk is finished
+        auto load_ya = [&](int c, float (&ya)[16]) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tl = c * 16 + j;
@@ -1209,6 +1205,18 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
                         ? __ldcg(p.yadd + static_cast<size_t>(t0 + tl) * p.N + n)
                         : 0.0f;
           }
+        };
+        float ya_next[16];
+        load_ya(0, ya_next);
+#pragma unroll 1
+        for (int c = 0; c < BT / 16; ++c) {
+          if (c * 16 >= tv) break;
+          uint32_t v[16];
+          float ya[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) ya[j] = ya_next[j];
+          tmem_ld_32x32b_x16(lane_base + c * 16, v);
+          if ((c + 1) * 16 < tv) load_ya(c + 1, ya_next);
           tmem_ld_wait();
           float yv[16] = {};
           if (n < p.N) {
