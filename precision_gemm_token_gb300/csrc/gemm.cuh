@@ -473,10 +473,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_lora_kernel(const __grid
       meta_sx[i] = sx;
       meta_idx[i] = l;
       meta_tok[i] = tok;
-      // the expand pass's term of this row and weight tile: into L2 while the
-      // main loop runs (bulk prefetch needs 16-byte aligned rows)
-      if (!C::kDecode && p.yadd != nullptr && l >= 0 && (p.N & 3) == 0)
-        prefetch_l2_bulk(p.yadd + static_cast<size_t>(row) * p.N + n0, static_cast<uint32_t>(min(kTileN, p.N - n0) * 4));
     }
     asm volatile("bar.sync %0, 128;" ::"r"(kEpiBarrier) : "memory");
     if (C::kDecode) {
