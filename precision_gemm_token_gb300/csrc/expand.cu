@@ -15,11 +15,11 @@
 // Work item: one weight tile of 128 output columns and a range of at most 256
 // adapter-sorted rows. The item's adapter per row is staged once and cut into
 // segments (runs of one adapter, also cut every 32 rows, where a round of S
-// rows is staged in shared memory). The B slices of the adapter runs (128
-// rows of 2r bytes) stream through a ring in shared memory with 16-byte
-// asynchronous copies issued two or three runs ahead. Each of the 8 warps
-// owns 16 output columns: per run it loads the A fragments of its B rows
-// once, then per 8 tokens of the segment runs one bf16 m16n8k16 MMA per
+// rows is staged in shared memory). Each of the 8 warps owns 16 output
+// columns: the 16 B rows of every adapter run that they use stream through
+// the warp's own ring in shared memory with 16-byte asynchronous copies
+// issued two or three runs ahead (no CTA-wide barrier per run). Per run the
+// warp loads the A fragments of its B rows once, then per 8 tokens of the segment runs one bf16 m16n8k16 MMA per
 // k-step of 16 and per part of S, S being split into three bf16 parts
 // (hi + mid + lo == S exactly): every product is exact and the sum is
 // accumulated in fp32, the precision the epilogue's own term has.
@@ -36,19 +36,21 @@ constexpr int kExpandMinRows = 16;    // smallest row range of a work item
 constexpr int kExpandItemRows = 256;  // largest row range of a work item
 constexpr int kExpandItemCost = 16;   // set-up of a work item, in rows' worth of time
 
-// Ring of B slices (one adapter's 128 rows of the weight tile) in shared
-// memory, filled with 16-byte asynchronous copies kDepth - 1 adapter runs
-// ahead; 16-byte unit u of row n sits at unit u ^ (n & kSwMask) of its row,
-// so that the 16 rows a warp reads at once fall into different banks.
+// Rings of B rows in shared memory, one per warp (the 16 rows of one
+// adapter's B slice that the warp's columns use, per slot), filled by the
+// warp's own 16-byte asynchronous copies kDepth - 1 adapter runs ahead, so
+// that a warp waits for nothing but its own copies; 16-byte unit u of row n
+// sits at unit u ^ (n & kSwMask) of its row, so that the rows a fragment load
+// reads fall into different banks.
 template <int R4>
 struct ExpandCfg {
   static constexpr int kRowBytes = 8 * R4;                  // r = 4 R4 bf16 values
   static constexpr int kUnits = kRowBytes / 16;
   static constexpr int kSwMask = kUnits - 1 < 7 ? kUnits - 1 : 7;
-  static constexpr int kSlotBytes = 128 * kRowBytes;
+  static constexpr int kSlotBytes = 16 * kRowBytes;        // one warp's rows of a slice
   static constexpr int kDepth = R4 >= 32 ? 2 : R4 >= 16 ? 3 : 4;
   static constexpr int kCtas = R4 >= 32 ? 2 : 3;            // resident CTAs per SM
-  static constexpr int kRingBytes = kDepth * kSlotBytes;
+  static constexpr int kRingBytes = 8 * kDepth * kSlotBytes;   // 8 warps
   // S rows of a round as three bf16 planes (hi, mid, lo), rows padded by 16
   // bytes so that the 8 token rows of an MMA fragment fall into different banks
   static constexpr int kSRowBytes = kRowBytes + 16;
@@ -170,16 +172,18 @@ __global__ void __launch_bounds__(kExpandThreads, ExpandCfg<R4>::kCtas)
     __syncthreads();
     const int nseg = nseg_s;
     const int nload = nload_s;
-    // B slice j into ring slot j % kDepth (rows past N zero-filled); one
-    // commit group per call, empty past the last load
+    // this warp's 16 rows of B slice j into its ring slot j % kDepth (rows
+    // past N zero-filled); one commit group per call, empty past the last load
+    uint8_t* wring = ring + warp * C::kDepth * C::kSlotBytes;
     auto issue_load = [&](int j) {
       if (j < nload) {
-        uint8_t* slot = ring + (j % C::kDepth) * C::kSlotBytes;
-        const uint8_t* src = p.B + (static_cast<size_t>(load_l[j]) * p.N + n0) * C::kRowBytes;
-        for (int e = tid; e < 128 * C::kUnits; e += kExpandThreads) {
+        uint8_t* slot = wring + (j % C::kDepth) * C::kSlotBytes;
+        const int nw = n0 + warp * 16;
+        const uint8_t* src = p.B + (static_cast<size_t>(load_l[j]) * p.N + nw) * C::kRowBytes;
+        for (int e = lane; e < 16 * C::kUnits; e += 32) {
           const int row = e / C::kUnits;
           const int u = e - row * C::kUnits;
-          const bool ok = n0 + row < p.N;
+          const bool ok = nw + row < p.N;
           cp_async_16(slot + row * C::kRowBytes + ((u ^ (row & C::kSwMask)) << 4),
                       ok ? src + row * C::kRowBytes + (u << 4) : p.B, ok ? 16 : 0);
         }
@@ -228,20 +232,21 @@ __global__ void __launch_bounds__(kExpandThreads, ExpandCfg<R4>::kCtas)
         const int j = seg_load[k];
         if (j < 0) continue;
         if (j != cur_j) {
-          // a new adapter run: slot (j - 1) % kDepth has been read by every
-          // thread, so it may take load j + kDepth - 1; then load j is awaited
-          __syncthreads();
+          // a new adapter run: every lane of the warp has read slot
+          // (j - 1) % kDepth, so it may take load j + kDepth - 1; then the
+          // warp's copies of load j are awaited and made visible to its lanes
+          __syncwarp();
           issue_load(j + C::kDepth - 1);
           cp_async_wait<C::kDepth - 1>();
-          __syncthreads();
+          __syncwarp();
           // A fragments of this warp's 16 B rows (rows g and g + 8, ranks
           // 2 tq, 2 tq + 1 and + 8 of each k-step of 16)
-          const uint8_t* slot = ring + (j % C::kDepth) * C::kSlotBytes;
+          const uint8_t* slot = wring + (j % C::kDepth) * C::kSlotBytes;
 #pragma unroll
           for (int ks = 0; ks < kKSteps; ++ks)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int row = warp * 16 + g + 8 * (e & 1);
+              const int row = g + 8 * (e & 1);
               const int unit = 2 * ks + (e >> 1);
               af[ks][e] = *reinterpret_cast<const uint32_t*>(slot + row * C::kRowBytes +
                                                              ((unit ^ (row & C::kSwMask)) << 4) + 4 * tq);
