@@ -18,7 +18,7 @@
 // rows is staged in shared memory). Each of the 8 warps owns 16 output
 // columns: the 16 B rows of every adapter run that they use stream through
 // the warp's own ring in shared memory with 16-byte asynchronous copies
-// issued two or three runs ahead (no CTA-wide barrier per run). Per run the
+// issued one to three runs ahead (no CTA-wide barrier per run). Per run the
 // warp loads the A fragments of its B rows once, then per 8 tokens of the segment runs one bf16 m16n8k16 MMA per
 // k-step of 16 and per part of S, S being split into three bf16 parts
 // (hi + mid + lo == S exactly): every product is exact and the sum is
@@ -48,8 +48,8 @@ struct ExpandCfg {
   static constexpr int kUnits = kRowBytes / 16;
   static constexpr int kSwMask = kUnits - 1 < 7 ? kUnits - 1 : 7;
   static constexpr int kSlotBytes = 16 * kRowBytes;        // one warp's rows of a slice
-  static constexpr int kDepth = R4 >= 32 ? 2 : R4 >= 16 ? 3 : 4;
-  static constexpr int kCtas = R4 >= 32 ? 2 : 3;            // resident CTAs per SM
+  static constexpr int kDepth = R4 >= 16 ? 2 : 4;
+  static constexpr int kCtas = R4 >= 32 ? 2 : R4 >= 16 ? 4 : 3;   // resident CTAs per SM
   static constexpr int kRingBytes = 8 * kDepth * kSlotBytes;   // 8 warps
   // S rows of a round as three bf16 planes (hi, mid, lo), rows padded by 16
   // bytes so that the 8 token rows of an MMA fragment fall into different banks
@@ -342,7 +342,10 @@ int launch_expand(const ExpandArgs& a) {
   // rows: the count that minimises (waves of items over the grid's CTA
   // slots) x (rows per item + a fixed cost per item, counted in rows), fewer
   // items on a tie (each item reads its runs' B slices once)
-  const int ctas = a.r >= 128 ? ExpandCfg<32>::kCtas : ExpandCfg<16>::kCtas;
+  const int ctas = a.r >= 128 ? ExpandCfg<32>::kCtas
+                   : a.r >= 64 ? ExpandCfg<16>::kCtas
+                   : a.r >= 32 ? ExpandCfg<8>::kCtas
+                               : ExpandCfg<4>::kCtas;
   const long slots = static_cast<long>(num_sms()) * ctas;
   int max_groups = (a.M + kExpandMinRows - 1) / kExpandMinRows;
   int min_groups = (a.M + kExpandItemRows - 1) / kExpandItemRows;
