@@ -529,7 +529,8 @@ def run_ours(args, rank, world, local):
                           "roofline_us": round(max(t_hbm, t_tc) * 1e6, 1),
                           "frac": round(max(t_hbm, t_tc) / (ms_l / 1000), 4),
                           "peak_source": "measured bf16 burst x " + ("2 (FP8)" if fl == 0 else "6 (NVFP4)")
-                                         + "; measured copy bandwidth"})
+                                         + "; measured copy bandwidth",
+                          "kernels_per_projection": [kernels_per_call(fl, Ml, N, K, spec[5]) for _, K, N in plist]})
             del projs_l
             torch.cuda.empty_cache()
 
@@ -872,8 +873,8 @@ def run_profile_fused(args):
 
 def run_profile_large(args):
     """The 8B NVFP4 M = 512 layer's gate_up projection alone, for ncu: three
-    fused layer calls (shrink grid + wide-tile GEMM) on Zipf-indexed rank-64
-    adapters out of 128."""
+    fused layer calls (shrink grid, expand pass, wide-tile GEMM) on
+    Zipf-indexed rank-64 adapters out of 128."""
     import torch
 
     import precision_gemm_token_gb300 as E
