@@ -313,8 +313,9 @@ def test_standalone_shrink_then_dependent_gemm(fmt, M, K, N, r):
     assert torch.equal(outs[0], outs[1])
 
 
-def test_out_of_range_index_in_gemm():
-    p = make_projection(6, 512, 256, 3, 16, seed=12)
+@pytest.mark.parametrize("M,r", [(6, 16), (40, 64)])   # decode tile; wide tiles with the expand pass
+def test_out_of_range_index_in_gemm(M, r):
+    p = make_projection(M, 512, 256, 3, r, seed=12)
     idx = p.idx.clone()
     idx[2] = 5
     st = status_buf()

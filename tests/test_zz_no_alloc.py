@@ -42,7 +42,7 @@ def _noalloc(fmt, p, w, gx, Y, st, with_adapters=True):
 
 @pytest.mark.parametrize("fmt", [FP8, NVFP4], ids=["fp8", "nvfp4"])
 @pytest.mark.parametrize("M,K,N,L,r", [(1, 4096, 1024, 1, 64), (3, 2048, 4096, 2, 16), (33, 1024, 640, 5, 32),
-                                       (200, 1024, 1280, 7, 16)])
+                                       (200, 1024, 1280, 7, 16), (200, 1024, 1280, 7, 64)])
 def test_noalloc_matches_workspace_entry(fmt, M, K, N, L, r):
     """Two noalloc calls back to back on one stream, on two different batches
     (activations, indices and mask) through the same weights: each result is
