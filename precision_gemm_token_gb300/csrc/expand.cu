@@ -19,10 +19,11 @@
 // columns: the 16 B rows of every adapter run that they use stream through
 // the warp's own ring in shared memory with 16-byte asynchronous copies
 // issued one to three runs ahead (no CTA-wide barrier per run). Per run the
-// warp loads the A fragments of its B rows once, then per 8 tokens of the segment runs one bf16 m16n8k16 MMA per
-// k-step of 16 and per part of S, S being split into three bf16 parts
-// (hi + mid + lo == S exactly): every product is exact and the sum is
-// accumulated in fp32, the precision the epilogue's own term has.
+// warp loads the A fragments of its B rows once, then per 8 tokens of the
+// segment runs one bf16 m16n8k16 MMA per k-step of 16 and per part of S, S
+// being split into three bf16 parts (hi + mid + lo == S exactly): every
+// product is exact and the sum is accumulated in fp32, the precision the
+// epilogue's own term has.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -30,7 +31,7 @@ namespace epi {
 
 namespace {
 
-constexpr int kExpandThreads = 256;   // two per output column
+constexpr int kExpandThreads = 256;   // 8 warps of 16 output columns
 constexpr int kExpandRows = 32;       // sorted rows staged per round
 constexpr int kExpandMinRows = 16;    // smallest row range of a work item
 constexpr int kExpandItemRows = 256;  // largest row range of a work item
