@@ -14,8 +14,8 @@
 //
 // Work item: one weight tile of 128 output columns and a range of at most 256
 // adapter-sorted rows. The item's adapter per row is staged once and cut into
-// segments (runs of one adapter, also cut every 32 rows, where a round of S
-// rows is staged in shared memory). Each of the 8 warps owns 16 output
+// segments (runs of one adapter, also cut every 64 rows (32 at rank 128),
+// where a round of S rows is staged in shared memory). Each of the 8 warps owns 16 output
 // columns: the 16 B rows of every adapter run that they use stream through
 // the warp's own ring in shared memory with 16-byte asynchronous copies
 // issued one to three runs ahead (no CTA-wide barrier per run). Per run the
@@ -32,7 +32,6 @@ namespace epi {
 namespace {
 
 constexpr int kExpandThreads = 256;   // 8 warps of 16 output columns
-constexpr int kExpandRows = 32;       // sorted rows staged per round
 constexpr int kExpandMinRows = 16;    // smallest row range of a work item
 constexpr int kExpandItemRows = 256;  // largest row range of a work item
 constexpr int kExpandItemCost = 16;   // set-up of a work item, in rows' worth of time
@@ -50,12 +49,15 @@ struct ExpandCfg {
   static constexpr int kSwMask = kUnits - 1 < 7 ? kUnits - 1 : 7;
   static constexpr int kSlotBytes = 16 * kRowBytes;        // one warp's rows of a slice
   static constexpr int kDepth = R4 >= 16 ? 2 : 4;
-  static constexpr int kCtas = R4 >= 32 ? 2 : R4 >= 16 ? 4 : 3;   // resident CTAs per SM
+  static constexpr int kCtas = R4 >= 32 ? 2 : 3;            // resident CTAs per SM
   static constexpr int kRingBytes = 8 * kDepth * kSlotBytes;   // 8 warps
+  // sorted rows whose S is staged per round (rank 128: 32, so that the
+  // static shared memory stays within 48 KB)
+  static constexpr int kRows = R4 >= 32 ? 32 : 64;
   // S rows of a round as three bf16 planes (hi, mid, lo), rows padded by 16
   // bytes so that the 8 token rows of an MMA fragment fall into different banks
   static constexpr int kSRowBytes = kRowBytes + 16;
-  static constexpr int kSPlaneBytes = kExpandRows * kSRowBytes;
+  static constexpr int kSPlaneBytes = kRows * kSRowBytes;
 };
 
 struct ExpandParams {
@@ -142,14 +144,14 @@ __global__ void __launch_bounds__(kExpandThreads, ExpandCfg<R4>::kCtas)
     }
     __syncthreads();
     // segments: runs of one adapter (or of none), also cut where a round of
-    // kExpandRows rows starts; one B slice load per run with an adapter
+    // kRows rows starts; one B slice load per run with an adapter
     if (tid < 32) {
       int ns = 0, nl = 0;
       for (int base = 0; base < nrows; base += 32) {
         const int i = base + lane;
         const int l = i < nrows ? meta_l[i] : -1;
         const bool run = i < nrows && (i == 0 || meta_l[i - 1] != l);
-        const bool st = run || (i < nrows && i % kExpandRows == 0);
+        const bool st = run || (i < nrows && i % C::kRows == 0);
         const bool ld = run && l >= 0;
         const unsigned below = (1u << lane) - 1u;
         const unsigned smsk = __ballot_sync(0xffffffffu, st);
@@ -197,8 +199,8 @@ __global__ void __launch_bounds__(kExpandThreads, ExpandCfg<R4>::kCtas)
     uint32_t af[kKSteps][4];          // A fragments of the current adapter run
     int cur_j = -1;
     int k = 0;
-    for (int c0 = 0; c0 < nrows; c0 += kExpandRows) {
-      const int nr = min(kExpandRows, nrows - c0);
+    for (int c0 = 0; c0 < nrows; c0 += C::kRows) {
+      const int nr = min(C::kRows, nrows - c0);
       __syncthreads();   // the previous round's rows are consumed
       // S rows of the round's active tokens (partial sums added in part
       // order), split into the three bf16 planes
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(kExpandThreads, ExpandCfg<R4>::kCtas)
         // past the segment (other rows of the round, or none) are computed
         // but not stored.
         for (int t0 = i; t0 < jr; t0 += 8) {
-          const int t = min(t0 + g, kExpandRows - 1);
+          const int t = min(t0 + g, C::kRows - 1);
           float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
           for (int ks = 0; ks < kKSteps; ++ks)
