@@ -392,9 +392,11 @@ EPILORA_API int epilora_test_drop_shrink_results(int on);
  * whose S term grows with the number of K slices of the shrink (e.g. FP8,
  * r = 64: M up to 1175 at K = 4096); EPILORA_ERR_CUDA if the address lookup
  * fails.
- * Otherwise it enqueues what epilora_layer_forward enqueues (the scratch
- * starts zeroed when the library is loaded, which is what
- * epilora_layer_forward requires of a workspace's head).
+ * Otherwise it enqueues what epilora_layer_forward enqueues given a workspace
+ * of the whole scratch (the scratch starts zeroed when the library is
+ * loaded, which is what epilora_layer_forward requires of a workspace's
+ * head): batches of more than 32 tokens with rank >= 32 take the expand pass
+ * whenever epilora_layer_workspace_bytes fits the scratch.
  *
  * All calls on one device share the one scratch array: calls that overlap in
  * time (on different streams, or from host threads that do not order their
