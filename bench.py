@@ -874,7 +874,8 @@ def run_profile_fused(args):
 def run_profile_large(args):
     """The 8B NVFP4 M = 512 layer's gate_up projection alone, for ncu: three
     fused layer calls (shrink grid, expand pass, wide-tile GEMM) on
-    Zipf-indexed rank-64 adapters out of 128."""
+    Zipf-indexed rank-64 adapters out of 128; with --profile-large-base the
+    same calls without adapters (quantizer grid and base GEMM)."""
     import torch
 
     import precision_gemm_token_gb300 as E
@@ -893,11 +894,13 @@ def run_profile_large(args):
     ws = T.LayerWorkspace("cuda")
     Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    A, B = (None, None) if getattr(args, "profile_large_base", False) else (p.A, p.B)
     for _ in range(3):
-        T.layer_forward(p.X, w, p.A, p.B, p.idx, p.mask, x_global_scale=gx, workspace=ws, status=st, Y=Y)
+        T.layer_forward(p.X, w, A, B, p.idx, p.mask, x_global_scale=gx, workspace=ws, status=st, Y=Y)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    print(json.dumps({"profile": "8b_m512_nvfp4", "kernel": f"gate_up {K}->{N} M={M}", "ok": True}))
+    print(json.dumps({"profile": "8b_m512_nvfp4", "kernel": f"gate_up {K}->{N} M={M}",
+                      "adapters": A is not None, "ok": True}))
 
 
 def run_profile_wide(args):
@@ -944,6 +947,8 @@ def main():
     ap.add_argument("--profile-wide", action="store_true", help="run one wide-tile fused layer call alone (for ncu)")
     ap.add_argument("--profile-large", action="store_true",
                     help="run the 8B NVFP4 M=512 gate_up fused call alone (for ncu)")
+    ap.add_argument("--profile-large-base", action="store_true",
+                    help="the same calls without adapters (the base GEMM alone, for ncu)")
     ap.add_argument("--profile-fused", action="store_true",
                     help="run the workload's fused gate_up layer call alone (for ncu)")
     args = ap.parse_args()
@@ -958,7 +963,7 @@ def main():
     if args.profile_fused:
         run_profile_fused(args)
         return
-    if args.profile_large:
+    if args.profile_large or args.profile_large_base:
         run_profile_large(args)
         return
     rank, world, local = dist_setup()
